@@ -1,0 +1,379 @@
+"""Pins for the oracle: checks against what the pages and the mathematics fix.
+
+Each pin is a function of the oracle module ``O`` so that the same pin can be
+run against a copy of the oracle with a planted mistake (test_oracle_pins.py
+asserts that every planted mistake is caught by at least one pin).
+
+Nothing here retypes an oracle formula: pins use closed forms, hand-derived
+values, values printed on the pages (tests/golden), exact brute force in
+decimal arithmetic, finite differences, and independent library routines
+(torch fp64 autograd, scipy, numpy ufunc.at).
+"""
+from __future__ import annotations
+
+import math
+from decimal import Decimal, getcontext
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from conftest import read_golden
+
+IGN = -100
+
+
+def _rand_case(seed, T, H, V_real, Vp, ignore=(), bad=(), pad=8.0, scale=1.0):
+    rng = np.random.default_rng(seed)
+    h = rng.standard_normal((T, H)) * scale
+    W = rng.standard_normal((Vp, H)) * 0.5
+    if Vp > V_real:
+        W[V_real:] = pad
+    y = rng.integers(0, V_real, size=T)
+    for t in ignore:
+        y[t] = IGN
+    for t in bad:
+        y[t] = V_real + 3
+    return h, W, y
+
+
+# --------------------------------------------------------------------------
+# Padding and shard layout
+# --------------------------------------------------------------------------
+
+def pin_pad_vocab(O):
+    g = read_golden("padded_head_demo.txt")
+    assert O.pad_vocab_size(g["head_vocab"]) == g["head_vocab_padded"]
+    assert O.pad_vocab_size(g["vocab_real"]) == g["vocab_padded"]
+    # closed form: the least multiple of 64 that is >= v
+    for v in list(range(1, 300)) + [50000, 151936, 201088]:
+        p = O.pad_vocab_size(v)
+        assert p % 64 == 0 and v <= p < v + 64
+    assert O.vocab_aligned(64) and not O.vocab_aligned(g["vocab_real"])
+
+
+def pin_shards_tp_page(O):
+    g = read_golden("tp_embedding_shards.txt")
+    lo = O.shard_bounds(g["V"], g["ranks"])
+    assert np.all(np.diff(lo) == g["rows_per_rank"])
+    for k in (0, 1, 7):
+        a, b = g[f"rank{k}"]
+        assert lo[k] == a and lo[k + 1] - 1 == b
+    ids = np.array([0, 25135, 25136, 50271, 175952, 201087, 201088, -100])
+    valid, owner, local = O.ownership(ids, g["V"], g["V"], g["ranks"])
+    assert list(owner) == [0, 0, 1, 1, 7, 7, -1, -1]
+    assert list(local) == [0, 25135, 0, 25135, 0, 25135, -1, -1]
+
+
+def pin_shards_cover(O):
+    """Shards tile [0, Vp) contiguously; sizes are floor or ceil of Vp/S; an
+    even split agrees with numpy's array_split; every valid id has exactly one
+    owner and invalid ids none."""
+    for Vp in (64, 1024, 50048, 151936):
+        for S in (1, 2, 3, 4, 7, 8, 64):
+            lo = O.shard_bounds(Vp, S)
+            assert lo[0] == 0 and lo[-1] == Vp
+            sz = np.diff(lo)
+            assert set(sz.tolist()) <= {Vp // S, -(-Vp // S)}
+            if Vp % S == 0:
+                ref = [a[0] for a in np.array_split(np.arange(Vp), S)]
+                assert list(lo[:-1]) == ref
+    Vp, V_real = 1024, 1000
+    ids = np.concatenate([np.arange(-3, Vp + 3), [IGN, -(2 ** 31), 2 ** 40]])
+    for S in (1, 3, 4, 7, Vp):
+        valid, owner, local = O.ownership(ids, V_real, Vp, S)
+        lo = O.shard_bounds(Vp, S)
+        for i, v in enumerate(ids):
+            inside = [k for k in range(S) if lo[k] <= v < lo[k + 1]]
+            if 0 <= v < V_real:
+                assert valid[i] and owner[i] == inside[0] and local[i] == v - lo[inside[0]]
+            else:
+                assert not valid[i] and owner[i] == -1 and local[i] == -1
+
+
+# --------------------------------------------------------------------------
+# Embedding
+# --------------------------------------------------------------------------
+
+def pin_embedding_forward(O):
+    rng = np.random.default_rng(5)
+    Vp, V_real, H = 1024, 1000, 24
+    W = rng.standard_normal((Vp, H)).astype(np.float32)
+    W[V_real:] = 8.0
+    ids = np.concatenate([rng.integers(0, Vp, 200), [IGN, -1, Vp, Vp + 10, 999, 1000, 0]])
+    E = O.embed_forward(ids, W, V_real)
+    valid = (ids >= 0) & (ids < V_real)
+    # torch's own lookup on the valid ids; padded rows, padding and
+    # out-of-range ids give zero rows
+    ref = F.embedding(torch.from_numpy(np.where(valid, ids, 0)), torch.from_numpy(W)).numpy()
+    assert np.array_equal(E[valid], ref[valid])
+    assert np.all(E[~valid] == 0)
+    for S in (1, 2, 3, 4, 7, 8):
+        Es = O.embed_forward_by_shards(ids, W, V_real, Vp, S)
+        assert np.array_equal(Es, E.astype(np.float64))
+    # bf16 bit patterns are copied exactly
+    Wb = rng.integers(0, 2 ** 16, size=(Vp, H), dtype=np.uint16)
+    Eb = O.embed_forward(ids, Wb, V_real)
+    assert np.array_equal(Eb[valid], Wb[ids[valid]])
+
+
+def pin_embedding_backward(O):
+    rng = np.random.default_rng(6)
+    Vp, V_real, H, T = 256, 250, 16, 500
+    ids = rng.integers(-5, Vp + 5, size=T)
+    ids[:40] = 3                                   # a long run of one id
+    ids[40:45] = IGN
+    dE = rng.standard_normal((T, H))
+    dW = O.embed_backward(ids, dE, V_real, Vp)
+    ref = np.zeros((Vp, H))
+    keep = (ids >= 0) & (ids < V_real)
+    np.add.at(ref, ids[keep], dE[keep])
+    assert np.allclose(dW, ref, rtol=0, atol=1e-12)
+    ref_t = torch.zeros(Vp, H, dtype=torch.float64).index_add_(
+        0, torch.from_numpy(ids[keep]), torch.from_numpy(dE[keep]))
+    assert np.allclose(dW, ref_t.numpy(), rtol=0, atol=1e-12)
+    assert np.all(dW[V_real:] == 0)
+
+
+def pin_embedding_replay_order(O):
+    """Hand-derived fp32 results that fix the summation order.
+
+    1e8 has an fp32 spacing of 8, so adding 1.0 to it is lost while eight
+    ones summed first give 8.0, which is kept.
+    """
+    H = 1
+    big = np.float32(1e8)
+    vals = [big] + [np.float32(1.0)] * 15                  # t = 0..15, one id
+    dE = np.array(vals, dtype=np.float32).reshape(-1, 1)
+    ids = np.full(16, 5)
+    init = np.zeros((8, H), dtype=np.float32)
+    # one run of 16: every +1 is absorbed -> 1e8
+    r16 = O.embed_backward_replay_f32(ids, dE, 8, 16, init)
+    assert r16[5, 0] == np.float32(100000000.0)
+    # runs of 8: (1e8 + seven ones -> 1e8) + (eight ones -> 8) = 100000008
+    r8 = O.embed_backward_replay_f32(ids, dE, 8, 8, init)
+    assert r8[5, 0] == np.float32(100000008.0)
+    # runs of 4: 1e8, 4, 4, 4 added left to right; 1e8 + 4 is a tie that rounds
+    # to the even neighbour 1e8 each time (right to left would give 100000016)
+    r4 = O.embed_backward_replay_f32(ids, dE, 8, 4, init)
+    assert r4[5, 0] == np.float32(100000000.0)
+    # tokens ascending in t: the same values in reverse t order sum the ones first
+    r_rev = O.embed_backward_replay_f32(ids, dE[::-1].copy(), 8, 16, init)
+    assert r_rev[5, 0] == np.float32(100000016.0)          # 1e8 + 15 rounds to +16
+    # the total is added once to the existing row
+    init2 = init.copy(); init2[5, 0] = np.float32(3.0)
+    r = O.embed_backward_replay_f32(np.array([5]), np.array([[np.float32(2.0)]]), 8, 4, init2)
+    assert r[5, 0] == np.float32(5.0)
+    # other rows and invalid ids leave dW unchanged
+    r = O.embed_backward_replay_f32(np.array([IGN, 9, -1]), np.ones((3, 1), np.float32), 8, 4, init2)
+    assert np.array_equal(r, init2)
+
+
+def pin_embedding_replay_bound(O):
+    """The fp32 replay equals the exact sum within the sequential-summation
+    error bound n*u*sum|x|, and single-token rows are exact."""
+    rng = np.random.default_rng(7)
+    Vp, V_real, H, T = 300, 300, 8, 2000
+    ids = np.minimum(rng.zipf(1.3, size=T) - 1, V_real - 1)
+    dE = rng.standard_normal((T, H)).astype(np.float32)
+    init = rng.standard_normal((Vp, H)).astype(np.float32)
+    for chunk in (1, 4, 32, 4096):
+        got = O.embed_backward_replay_f32(ids, dE, V_real, chunk, init).astype(np.float64)
+        exact = init.astype(np.float64)
+        np.add.at(exact, ids, dE.astype(np.float64))
+        n = np.bincount(ids, minlength=Vp)[:, None] + 1
+        absum = np.abs(init.astype(np.float64)).copy()
+        np.add.at(absum, ids, np.abs(dE.astype(np.float64)))
+        u = 2.0 ** -24
+        assert np.all(np.abs(got - exact) <= n * u * absum * 1.01 + 1e-30)
+        single = np.bincount(ids, minlength=Vp) == 1
+        for v in np.nonzero(single)[0]:
+            t = int(np.nonzero(ids == v)[0][0])
+            assert np.array_equal(got[v].astype(np.float32), (init[v] + dE[t]).astype(np.float32))
+
+
+# --------------------------------------------------------------------------
+# Cross-entropy forward
+# --------------------------------------------------------------------------
+
+def pin_equal_logits(O):
+    """All-equal logits give loss = ln(V_real) exactly (up to rounding)."""
+    T, H, V_real, Vp = 64, 64, 1000, 1024
+    h = np.zeros((T, H))
+    rng = np.random.default_rng(1)
+    W = rng.standard_normal((Vp, H)) * 0.02
+    W[V_real:] = 8.0
+    y = rng.integers(0, V_real, T)
+    r = O.cross_entropy_forward(h, W, y, V_real)
+    assert abs(r["loss"] - math.log(1000)) < 1e-12
+    assert abs(math.log(1000) - 6.907755278982137) < 1e-15
+    # identical rows of W with any h: every logit of a row is the same value
+    W2 = np.tile(rng.standard_normal(H), (Vp, 1))
+    W2[V_real:] = 8.0
+    r2 = O.cross_entropy_forward(rng.standard_normal((T, H)), W2, y, V_real)
+    assert np.allclose(r2["token_loss"], math.log(V_real), rtol=0, atol=1e-11)
+
+
+def pin_normalisation(O):
+    h, W, y = _rand_case(2, 20, 16, 77, 128)
+    p = O.probabilities(h, W, 77, 128)
+    assert np.allclose(p[:, :77].sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert np.all(p[:, 77:] == 0.0)
+    # the assertion of section 7: padded mass below 1e-6
+    assert np.abs(p[:, 77:]).sum() < 1e-6
+
+
+def pin_padded_head_demo(O):
+    """Section 4 of the padding write-up: real-class mass 1.000 once masked."""
+    g = read_golden("padded_head_demo.txt")
+    V, Vp = g["vocab_real"], g["vocab_padded"]
+    rng = np.random.default_rng(0)
+    z = rng.standard_normal(Vp)
+    z[V:] = g["pad_logit"]
+    # logits chosen directly: H = Vp, W = identity, h = the logit row
+    h = z[None, :]
+    W = np.eye(Vp)
+    p = O.probabilities(h, W, V, Vp)
+    assert round(float(p[0, :V].sum()), 3) == g["masked_real_mass"]
+    assert p[0, V:].sum() == 0.0
+    # unmasked, the garbage would hold most of the mass (closed form)
+    unmasked_real = np.exp(z[:V]).sum() / np.exp(z).sum()
+    assert unmasked_real < 0.01
+
+
+def pin_bruteforce_decimal(O):
+    """Tiny problems: logits summed exactly and log-sum-exp evaluated in
+    60-digit decimal arithmetic."""
+    getcontext().prec = 60
+    for seed in range(4):
+        T, H, V_real, Vp = 3, 4, 7, 64
+        h, W, y = _rand_case(10 + seed, T, H, V_real, Vp, ignore=(2,) if seed % 2 else ())
+        r = O.cross_entropy_forward(h, W, y, V_real)
+        total, nv = Decimal(0), 0
+        for t in range(T):
+            zs = [sum(Decimal(float(h[t, j])) * Decimal(float(W[v, j])) for j in range(H))
+                  for v in range(V_real)]
+            lse = sum(z.exp() for z in zs).ln()
+            assert abs(float(lse) - r["lse"][t]) < 1e-13 * max(1.0, abs(float(lse)))
+            if y[t] != IGN:
+                total += lse - zs[y[t]]
+                nv += 1
+        assert abs(float(total / nv) - r["loss"]) < 1e-13
+
+
+def pin_torch_cross_entropy(O):
+    """torch's fp64 cross_entropy (padded logits at -inf, ignore_index=-100,
+    mean) and its autograd gradients, the library form of the padded head."""
+    for seed, (T, H, V_real, Vp, g) in enumerate([(16, 8, 50, 64, 1.0), (33, 12, 200, 256, 0.37),
+                                                   (5, 3, 64, 64, 2.0)]):
+        h, W, y = _rand_case(20 + seed, T, H, V_real, Vp, ignore=(1, 4))
+        ht = torch.tensor(h, requires_grad=True)
+        Wt = torch.tensor(W, requires_grad=True)
+        z = ht @ Wt.T
+        mask = torch.zeros(Vp, dtype=torch.float64)
+        mask[V_real:] = float("-inf")
+        loss = g * F.cross_entropy(z + mask, torch.tensor(y), ignore_index=IGN)
+        loss.backward()
+        r = O.cross_entropy_forward(h, W, y, V_real, g=g)
+        assert abs(r["loss"] - loss.item()) < 1e-12 * max(1, abs(loss.item()))
+        dH, dW = O.cross_entropy_backward(h, W, y, V_real, Vp, g=g)
+        assert np.allclose(dH, ht.grad.numpy(), rtol=0, atol=1e-12)
+        assert np.allclose(dW, Wt.grad.numpy(), rtol=0, atol=1e-12)
+        lse_ref = torch.logsumexp(z.detach()[:, :V_real], dim=1).numpy()
+        assert np.allclose(r["lse"], lse_ref, rtol=1e-14, atol=1e-14)
+
+
+def pin_shard_invariance(O):
+    """The sharded schedule equals the unsharded definition for any S, with
+    targets at shard edges, the maximum in another shard, and the padded tail."""
+    T, H, V_real, Vp = 24, 16, 1000, 1024
+    h, W, y = _rand_case(30, T, H, V_real, Vp, ignore=(3,))
+    y[:6] = [255, 256, 511, 512, 999, 0]
+    # rows 6..9 get a dominant logit at a column in another shard than y
+    for i, (yt, vs) in enumerate([(10, 519), (261, 779), (515, 17), (999, 0)]):
+        y[6 + i] = yt
+        h[6 + i] = 50 * W[vs] / np.linalg.norm(W[vs])
+    plain = O.cross_entropy_forward(h, W, y, V_real)
+    for S in (1, 2, 3, 4, 5, 6, 7, 8, Vp):
+        sh = O.cross_entropy_forward_sharded(h, W, y, V_real, Vp, S)
+        assert abs(sh["loss"] - plain["loss"]) <= 1e-12 * abs(plain["loss"])
+        assert np.allclose(sh["lse"], plain["lse"], rtol=1e-13, atol=0)
+        assert np.allclose(sh["z_target"], plain["z_target"], rtol=1e-13, atol=1e-13)
+    own, _gap = O.max_owner(h, W, V_real, Vp, 4)
+    tgt = O.target_owner(y, V_real, Vp, 4)
+    assert all(own[6 + i] != tgt[6 + i] for i in range(4))
+    z = h @ W[:V_real].T
+    assert list(z[6:10].argmax(axis=1)) == [519, 779, 17, 0]
+    sh4 = O.cross_entropy_forward_sharded(h, W, y, V_real, Vp, 4)
+    assert list(np.argmax(sh4["shard_max"], axis=1)[6:10]) == [2, 3, 0, 0]
+
+
+def pin_ignored_and_bad(O):
+    h, W, y = _rand_case(40, 12, 8, 90, 128, ignore=(0, 5), bad=(7,))
+    r = O.cross_entropy_forward(h, W, y, 90)
+    assert r["n_valid"] == 9
+    assert r["token_loss"][0] == 0 and r["token_loss"][5] == 0 and r["token_loss"][7] == 0
+    assert list(np.nonzero(r["bad"])[0]) == [7]
+    dH, dW = O.cross_entropy_backward(h, W, y, 90, 128)
+    assert np.all(dH[[0, 5, 7]] == 0)
+    # a bad target behaves exactly like an ignored one
+    y2 = y.copy(); y2[7] = IGN
+    dH2, dW2 = O.cross_entropy_backward(h, W, y2, 90, 128)
+    assert np.array_equal(dH, dH2) and np.array_equal(dW, dW2)
+    # no valid token at all: loss 0 and no gradient (reading R4)
+    yn = np.full(12, IGN)
+    assert O.cross_entropy_forward(h, W, yn, 90)["loss"] == 0.0
+    dHn, dWn = O.cross_entropy_backward(h, W, yn, 90, 128)
+    assert not dHn.any() and not dWn.any()
+
+
+# --------------------------------------------------------------------------
+# Cross-entropy backward
+# --------------------------------------------------------------------------
+
+def pin_finite_differences(O):
+    """Central differences of the fp64 loss against dH and dW."""
+    T, H, V_real, Vp, g = 3, 4, 7, 16, 1.7
+    h, W, y = _rand_case(50, T, H, V_real, Vp, ignore=(1,))
+    dH, dW = O.cross_entropy_backward(h, W, y, V_real, Vp, g=g)
+    eps = 1e-6
+
+    def L(hh, WW):
+        return O.cross_entropy_forward(hh, WW, y, V_real, g=g)["loss"]
+
+    for t in range(T):
+        for j in range(H):
+            e = np.zeros_like(h); e[t, j] = eps
+            fd = (L(h + e, W) - L(h - e, W)) / (2 * eps)
+            assert abs(fd - dH[t, j]) < 1e-7
+    for v in range(Vp):
+        for j in range(H):
+            e = np.zeros_like(W); e[v, j] = eps
+            fd = (L(h, W + e) - L(h, W - e)) / (2 * eps)
+            assert abs(fd - dW[v, j]) < 1e-7
+
+
+def pin_gradient_invariants(O):
+    T, H, V_real, Vp = 40, 16, 300, 320
+    h, W, y = _rand_case(60, T, H, V_real, Vp, ignore=(2, 9))
+    nv = O.n_valid(y, V_real)
+    G = O.logit_gradient(h, W, y, V_real, Vp, 1.0 / nv)
+    valid = y != IGN
+    assert np.allclose(G[valid].sum(axis=1), 0.0, atol=1e-15)
+    assert np.all(G[~valid] == 0) and np.all(G[:, V_real:] == 0)
+    dH, dW = O.cross_entropy_backward(h, W, y, V_real, Vp)
+    # sum over classes of dW_head = sum_t (sum_v G_tv) h_t = 0
+    assert np.allclose(dW.sum(axis=0), 0.0, atol=1e-13)
+    assert np.all(dW[V_real:] == 0)
+    # rows of dH computed alone agree with the full computation
+    part = O.hidden_gradient_rows(h[5:9], W, y[5:9], V_real, 1.0 / nv)
+    assert np.allclose(part, dH[5:9], rtol=0, atol=1e-15)
+
+
+ALL_PINS = [
+    pin_pad_vocab, pin_shards_tp_page, pin_shards_cover, pin_embedding_forward,
+    pin_embedding_backward, pin_embedding_replay_order, pin_embedding_replay_bound,
+    pin_equal_logits, pin_normalisation, pin_padded_head_demo, pin_bruteforce_decimal,
+    pin_torch_cross_entropy, pin_shard_invariance, pin_ignored_and_bad,
+    pin_finite_differences, pin_gradient_invariants,
+]

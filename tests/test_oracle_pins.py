@@ -1,0 +1,83 @@
+"""The oracle against its pins, and planted mistakes that the pins must catch.
+
+CPU only. The mutation tests plant a mistake in a fresh copy of the oracle's
+source (never in the CUDA path) and check that at least one pin fails.
+"""
+import os
+import types
+
+import pytest
+
+import oracle_pins as P
+from oracle import vce_oracle
+
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                          "oracle", "vce_oracle.py")
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(vce_oracle)
+
+
+def _mutant(old, new):
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) == 1, old
+    mod = types.ModuleType("vce_oracle_mutant")
+    exec(compile(src.replace(old, new), "vce_oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+MUTATIONS = {
+    # the max term dropped from log-sum-exp
+    "lse_drops_max": ("return M + np.log(np.exp(z - M[:, None]).sum(axis=1))",
+                      "return np.log(np.exp(z - M[:, None]).sum(axis=1))"),
+    # padded classes not excluded: the softmax runs over all Vp columns
+    "padded_classes_kept": ("z = logits(h, W, V_real)\n    lse = log_sum_exp(z)\n    valid, bad",
+                            "z = logits(h, W, W.shape[0])\n    lse = log_sum_exp(z)\n    valid, bad"),
+    # wrong sign of the target indicator
+    "onehot_sign": ("G[rows, y[rows]] -= 1.0", "G[rows, y[rows]] += 1.0"),
+    # the target indicator forgotten
+    "onehot_dropped": ("G[rows, y[rows]] -= 1.0", "pass"),
+    # averaged over all tokens instead of the valid ones
+    "mean_over_all": ("scale = g / nv if nv > 0 else 0.0",
+                      "scale = g / len(targets) if nv > 0 else 0.0"),
+    # transposed operand in dW_head
+    "dw_uses_W": ("dW[:V_real] = G[:, :V_real].T @ hf",
+                  "dW[:V_real] = G[:, :V_real].T @ Wf[:V_real][:, :hf.shape[1]][:hf.shape[0]]"),
+    # shard bounds computed as k * (Vp // S): the last rows lose their owner
+    "shard_floor_first": ("return np.array([(k * Vp) // S for k in range(S + 1)], dtype=np.int64)",
+                          "return np.array([k * (Vp // S) for k in range(S + 1)], dtype=np.int64)"),
+    # padded rows treated as valid ids
+    "valid_up_to_Vp": ("valid = (ids >= 0) & (ids < V_real)\n    owner",
+                       "valid = (ids >= 0) & (ids < Vp)\n    owner"),
+    # embedding of an invalid id not zeroed
+    "embed_no_mask": ("E[valid] = W[ids[valid]]", "E[:] = W[np.clip(ids, 0, W.shape[0] - 1)]"),
+    # local softmax per shard: each shard normalised against its own maximum
+    "local_max": ("s_k = np.stack([np.exp(b - M[:, None]).sum(axis=1) for b in blocks], axis=1)",
+                  "s_k = np.stack([np.exp(b - np.max(b, axis=1, keepdims=True)).sum(axis=1) "
+                  "for b in blocks], axis=1)"),
+    # run sums taken in reverse token order
+    "replay_reverse": ("for t in ts[c0:c0 + chunk]:", "for t in reversed(ts[c0:c0 + chunk]):"),
+    # run partials summed right to left
+    "replay_right_to_left": ("for c0 in range(0, len(ts), chunk):",
+                             "for c0 in reversed(range(0, len(ts), chunk)):"),
+    # repeated tokens overwrite instead of accumulating
+    "embed_bwd_overwrite": ("dW[v] += dEf[t]", "dW[v] = dEf[t]"),
+    # target logit taken from the wrong shard offset
+    "target_local_off": ("z_tgt[t] = blocks[owner[t]][t, local[t]]",
+                         "z_tgt[t] = blocks[owner[t]][t, max(local[t] - 1, 0)]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name):
+    old, new = MUTATIONS[name]
+    mod = _mutant(old, new)
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(mod)
+        except Exception:  # AssertionError, or a shape error the mistake causes
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake {name} passed every pin"
