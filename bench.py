@@ -1,0 +1,410 @@
+"""Benchmark of the vocabulary-sharded embedding + globally normalised
+cross-entropy step on one GB300 (or N independent replicas under torchrun).
+
+One step = embedding lookup of the step's token ids, loss forward, loss
+backward (dH and the tied dW), embedding backward into the same dW, on the
+Qwen3-like tied workload (T=8192, H=2048, V=151936, S=8, bf16). Inputs are
+seeded and synthetic and already resident in HBM when the timed region starts;
+W (622 MB) and the per-pass G chunks (256 MB) are larger than L2, so no extra
+flush is done between steps.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle instead
+(the slow fp64 definition, on the host cores, on a bounded token sample).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused vocab-CE fwd+bwd tokens/s & % BF16 TC peak; embed gather/bwd GB/s vs HBM"
+WORKLOAD = "qwen3_tied"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class Clocks:
+    """Samples nvidia-smi during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from vocab_embedding_cross_gb300 import _lib as vce
+    if not os.path.exists(vce.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    from vocab_embedding_cross_gb300 import device as D
+    from vocab_embedding_cross_gb300 import inputs as I
+
+    wl = I.WORKLOADS[args.workload]
+    # each replica draws its own batch (weak scaling); W is shared by seed
+    t_gen = time.time()
+    d = I.make_all(wl, ("W", "h", "targets", "ids", "dE"))
+    gen_s = time.time() - t_gen
+    T, H, Vp, V = wl.T, wl.H, wl.Vp, wl.V_real
+    p = vce.problem(T, H, Vp, V, wl.S, vce.VCE_BF16, tied=wl.tied)
+    W = D.to_device(d["W"])
+    h = D.to_device(d["h"])
+    ids = torch.from_numpy(d["ids"]).cuda()
+    y = torch.from_numpy(d["targets"]).cuda()
+    dE = D.to_device(d["dE"])
+    E = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    loss = torch.empty(1, device="cuda")
+    lse = torch.empty(T, device="cuda")
+    dH = torch.empty((T, H), device="cuda")
+    dW = torch.empty((Vp, H), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws_f = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD))
+    ws_b = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD))
+    ws_e = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_EMBED_BWD))
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def step():
+        if wl.tied:
+            dW.zero_()          # the tied gradient buffer starts each step at zero
+        vce.vce_embed_fwd(p, ids, W, E, dev_status=st, stream=sp)
+        vce.vce_loss_fwd(p, h, W, y, loss, lse, ws=ws_f, dev_status=st, stream=sp)
+        vce.vce_loss_bwd(p, h, W, y, lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp)
+        vce.vce_embed_bwd(p, ids, dE, dW, ws_e, dev_status=st, stream=sp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, vce.status_str(int(st.item()))
+
+    # ---- timed region: K steps, device resident ----
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    n0 = vce.vce_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    launches = vce.vce_launch_count() - n0
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+        ms = float(t.item())
+    value = world * T / (ms / 1e3)
+
+    # ---- per-launch timing (separate pass, events after every launch) ----
+    cap = 4096
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
+    handles = (ctypes.c_void_p * cap)(*[e.cuda_event for e in evs]) if hasattr(evs[0], "cuda_event") else None
+    per_kind = {}
+    if handles is not None:
+        for e in evs:
+            e.record(stream)            # materialise the events
+        torch.cuda.synchronize()
+        kinds = (ctypes.c_int32 * cap)()
+        count = (ctypes.c_int32 * 1)(0)
+        reps = max(3, min(args.steps, 10))
+        start = torch.cuda.Event(enable_timing=True)
+        vce.vce_set_launch_events(handles, kinds, cap, count)
+        start.record(stream)
+        for _ in range(reps):
+            step()
+        torch.cuda.synchronize()
+        vce.vce_set_launch_events(None, None, 0, None)
+        prev = start
+        for i in range(count[0]):
+            k = vce.KERNEL_KINDS[kinds[i]]
+            dt = prev.elapsed_time(evs[i])
+            tot, n = per_kind.get(k, (0.0, 0))
+            per_kind[k] = (tot + dt, n + 1)
+            prev = evs[i]
+        per_kind = {k: (tot / reps, n // reps) for k, (tot, n) in per_kind.items()}
+
+    # ---- roofline ----
+    peaks, peak_src = load_peaks()
+    vc = (vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD) - 256) // (T * 2)
+    flops = {"tc_fwd": 2.0 * T * H * V, "tc_grad": 2.0 * T * H * V, "tc_dh": 2.0 * T * H * V,
+             "tc_dw": 2.0 * T * H * V}
+    loss_kinds = ["tc_fwd", "tc_grad", "tc_dh", "tc_dw", "merge", "loss_mean", "count_valid"]
+    loss_ms = sum(per_kind.get(k, (0.0, 0))[0] for k in loss_kinds)
+    dom = max((k for k in flops if k in per_kind), key=lambda k: per_kind[k][0], default=None)
+    roofline = None
+    if dom is not None:
+        t_ms, n = per_kind[dom]
+        achieved = flops[dom] / (t_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "launches_per_step": n, "ms_per_step": round(t_ms, 4),
+                    "peak_kind": f"bf16_tflops_sustained ({peak_src})"}
+    credited = 6.0 * T * H * V
+    loss_tflops = credited / (loss_ms / 1e3) / 1e12 if loss_ms else None
+    valid = (d["ids"] >= 0) & (d["ids"] < V)
+    U = int(np.unique(d["ids"][valid]).size)
+    gather_bytes = 8 * T + U * H * 2 + T * H * 2
+    bwd_bytes = 8 * T + T * H * 2 + U * H * 8
+    emb = {}
+    if "embed_gather" in per_kind:
+        g_ms = per_kind["embed_gather"][0]
+        emb["gather_GBps"] = round(gather_bytes / (g_ms / 1e3) / 1e9, 1)
+        emb["gather_us"] = round(g_ms * 1e3, 2)
+    if "embed_reduce" in per_kind:
+        b_ms = per_kind["embed_reduce"][0] + per_kind.get("embed_sort", (0.0, 0))[0]
+        emb["bwd_GBps"] = round(bwd_bytes / (b_ms / 1e3) / 1e9, 1)
+        emb["bwd_us"] = round(b_ms * 1e3, 2)
+        emb["bwd_sort_us"] = round(per_kind.get("embed_sort", (0.0, 0))[0] * 1e3, 2)
+    emb["hbm_peak_GBps"] = peaks["hbm_gbs"]
+    for k in ("gather", "bwd"):
+        if f"{k}_GBps" in emb:
+            emb[f"{k}_frac"] = round(emb[f"{k}_GBps"] / peaks["hbm_gbs"], 4)
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = run_e2e(args, vce, D, d, p, W, E, loss, lse, dH, dW, st, ws_f, ws_b, ws_e, stream, wl)
+
+    # ---- CPU baseline (rank 0, N = 1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args, sample_tokens=args.cpu_sample)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; Zipf(1.1) token ids, RMS-normalised h, W ~ N(0, 0.02^2))",
+            "config": {"workload": f"{args.workload}: T={T} H={H} V_real={V} Vp={Vp} S={wl.S} tied={wl.tied}",
+                       "step": "embed_fwd + loss_fwd + loss_bwd + embed_bwd (+ tied dW zeroing)",
+                       "l2": "inputs larger than L2 (W 622 MB, G chunk per pass 256 MB); no extra flush",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline,
+            "loss_fwd_bwd": {"ms": round(loss_ms, 4), "credited_flops": credited,
+                             "credited_TFLOPs": round(loss_tflops, 1) if loss_tflops else None,
+                             "frac_of_burst": round(loss_tflops / peaks["bf16_tflops"], 4) if loss_tflops else None,
+                             "frac_of_sustained": round(loss_tflops / peaks["bf16_tflops_sustained"], 4)
+                             if loss_tflops else None,
+                             "executed_flops": 8.0 * T * H * V, "vc": int(vc)},
+            "embedding": emb,
+            "per_kernel_ms": {k: round(v[0], 4) for k, v in sorted(per_kind.items())},
+            "per_kernel_launches": {k: v[1] for k, v in sorted(per_kind.items())},
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "input_gen_s": round(gen_s, 1),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, vce, D, d, p, W, E, loss, lse, dH, dW, st, ws_f, ws_b, ws_e, stream, wl):
+    """Same step through the C ABI with the step's inputs (ids, targets, h, dE)
+    copied from pinned host buffers and the loss read back, every step."""
+    import torch
+    sp = stream.cuda_stream
+    host = {k: D.to_device(d[k], device="cpu") if k in ("h", "dE") else torch.from_numpy(d[k])
+            for k in ("ids", "targets", "h", "dE")}
+    host = {k: v.pin_memory() for k, v in host.items()}
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        if wl.tied:
+            dW.zero_()
+        vce.vce_embed_fwd(p, dev["ids"], W, E, dev_status=st, stream=sp)
+        vce.vce_loss_fwd(p, dev["h"], W, dev["targets"], loss, lse, ws=ws_f, dev_status=st, stream=sp)
+        vce.vce_loss_bwd(p, dev["h"], W, dev["targets"], lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp)
+        vce.vce_embed_bwd(p, dev["ids"], dev["dE"], dW, ws_e, dev_status=st, stream=sp)
+        loss_h.copy_(loss, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 2)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) / n
+    ms = e0.elapsed_time(e1) / n
+    return {"value": round(wl.T / (max(ms, wall * 1e3) / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4, "ms_per_step": round(max(ms, wall * 1e3), 4)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (bench's cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(args, sample_tokens):
+    """Runs the oracle in a child process with an explicit BLAS thread count."""
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores),
+               MKL_NUM_THREADS=str(cores))
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", args.workload,
+           "--cpu-sample", str(sample_tokens), "--steps", "1"]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    try:
+        out = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "sample": f"failed: {r.stderr[-300:]}"}
+    out["cores"] = cores
+    return out
+
+
+def oracle_child(args):
+    import numpy as np
+    from oracle import vce_oracle as O
+    from vocab_embedding_cross_gb300 import inputs as I
+
+    wl = I.WORKLOADS[args.workload]
+    d = I.make_all(wl, ("W", "h", "targets", "ids", "dE"))
+    n = min(args.cpu_sample, wl.T)
+    # a bounded sample of the workload: the first n tokens, full vocabulary and hidden size
+    h, y, ids, dE = d["h"][:n], d["targets"][:n], d["ids"][:n], d["dE"][:n]
+    times = []
+    for _ in range(max(1, args.steps)):
+        t0 = time.perf_counter()
+        O.embed_forward(ids, d["W"], wl.V_real)
+        O.cross_entropy_forward(h, d["W"], y, wl.V_real)
+        dH, dWh = O.cross_entropy_backward(h, d["W"], y, wl.V_real, wl.Vp)
+        dWe = O.embed_backward(ids, dE, wl.V_real, wl.Vp)
+        _ = dWh + dWe
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    print(json.dumps({"value": round(n / t, 3), "unit": "tokens/s", "kind": "oracle",
+                      "sample": f"first {n} of {wl.T} tokens of {args.workload}, full V={wl.V_real} and "
+                                f"H={wl.H}; embed fwd + loss fwd + loss bwd + embed bwd in fp64 numpy",
+                      "seconds": round(t, 3)}))
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0))
+    res = cpu_baseline(argparse.Namespace(workload=args.workload), sample_tokens=args.cpu_sample)
+    line = {"impl": "reference", "metric": METRIC, "value": res.get("value"), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": res.get("value"), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": res.get("sample")},
+            "e2e": {"value": res.get("value"), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--cpu-sample", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-child", action="store_true")
+    args = ap.parse_args()
+    if args.oracle_child:
+        oracle_child(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,224 @@
+/*
+ * libvocabce — vocabulary-sharded embedding lookup and globally normalised
+ * cross-entropy over a padded vocabulary, for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI. Every pointer argument except `p` is a DEVICE pointer owned by the
+ * caller, unless a comment says otherwise. The library allocates no device
+ * memory: scratch space is passed in as a caller-owned workspace whose size
+ * `vce_workspace_size` returns. The library keeps no state between calls
+ * apart from the wait limit set by `vce_set_wait_limit_ns` and a cache of
+ * device attributes.
+ *
+ * All calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ * NULL is the legacy default stream). The return value reports argument,
+ * shape, alignment and launch errors found on the host; nothing has been
+ * enqueued when it is not VCE_OK. Data errors found on the device are
+ * written to the optional `dev_status` word (int32, device memory, caller
+ * sets it to 0): the first error wins (atomic compare-and-swap from 0).
+ *
+ * Sources are cited by page title and section:
+ *  [VS]  "Vocabulary shards: look up locally and normalize globally",
+ *        paragraphs 1-5.
+ *  [PAD] "Training collapses when token embeddings are not padded to a
+ *        multiple of 64", sections 4-7.
+ *  [SPN] "Sequence-parallel normalization: shard tokens, retain their hidden
+ *        features", paragraph 3.
+ *  [TP]  "Tensor Parallelism (TP)", Component Sharding: Embedding
+ *        (VocabDimShardedEmbedding) and LM Head (ColumnParallelLinear).
+ */
+#ifndef VCE_H
+#define VCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vce_status {
+  VCE_OK = 0,
+  VCE_ERR_ARG = 1,          /* bad shape or argument (e.g. Vp not a multiple of 64) */
+  VCE_ERR_UNSUPPORTED = 2,  /* valid but unsupported: dtype, alignment, size limit */
+  VCE_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+  VCE_ERR_BAD_INDEX = 4,    /* device: a target outside [0,V_real) that is not ignore_index */
+  VCE_ERR_TIMEOUT = 5,      /* device: a bounded wait inside a kernel ran out */
+  VCE_ERR_WORKSPACE = 6     /* workspace missing, too small or misaligned */
+} vce_status;
+
+typedef enum vce_dtype {
+  VCE_F32 = 0,   /* fp32 storage and fp32 arithmetic (SIMT FMA) */
+  VCE_BF16 = 1   /* bf16 storage, fp32 accumulation on tcgen05 tensor cores */
+} vce_dtype;
+
+typedef enum vce_op {
+  VCE_OP_EMBED_FWD = 0,
+  VCE_OP_EMBED_BWD = 1,
+  VCE_OP_LOSS_FWD = 2,
+  VCE_OP_LOSS_BWD = 3
+} vce_op;
+
+/*
+ * One problem. Shapes:
+ *   h[T,H], W[Vp,H], E[T,H], dE[T,H]   row-major, element type `dtype`;
+ *   ids[T], targets[T]                 int64;
+ *   dW[Vp,H], dH[T,H]                  fp32, row-major;
+ *   lse[T], token_loss[T]              fp32;  owner maps int32.
+ * Rows of every 2-D tensor are contiguous with stride H elements; H*size(dtype)
+ * must be a multiple of 16 bytes and every 2-D tensor 16-byte aligned.
+ *
+ * Vocabulary layout [PAD s.5, s.7]: Vp is the padded vocabulary and must be a
+ * multiple of 64; classes [0, V_real) are real, rows [V_real, Vp) are padding
+ * and may hold any value (they are never read by the loss and never looked up).
+ * Shards [TP, VS p.1]: S logical shards on one GPU; shard k owns the contiguous
+ * rows [floor(k*Vp/S), floor((k+1)*Vp/S)). Any 1 <= S <= Vp is allowed.
+ *
+ * Limits: 0 <= T < 2^31, 1 <= H <= 65536, 64 <= Vp < 2^31, 1 <= V_real <= Vp.
+ * `reserved` must be 0.
+ */
+typedef struct vce_problem {
+  int64_t T;
+  int64_t H;
+  int64_t Vp;
+  int64_t V_real;
+  int64_t ignore_index;   /* target value meaning "no loss here"; the usual -100 */
+  int32_t S;
+  int32_t tied_weights;   /* 1: embedding and LM head share W and one fp32 dW */
+  int32_t dtype;          /* vce_dtype */
+  int32_t reserved;
+} vce_problem;
+
+/* Bytes of workspace the call `op` needs for problem `p` (0 if none, SIZE_MAX
+ * if the problem is invalid). The workspace must be 256-byte aligned. For
+ * VCE_OP_LOSS_BWD this is the recommended size; any size of at least
+ * vce_workspace_size_min(p, op) is accepted and a larger workspace lets the
+ * backward process more vocabulary columns per pass. */
+size_t vce_workspace_size(const vce_problem* p, int32_t op);
+size_t vce_workspace_size_min(const vce_problem* p, int32_t op);
+
+/*
+ * Masked embedding lookup [VS p.1-2; TP Embedding, prefill].
+ *   E[t,:] = W[ids[t],:]  if 0 <= ids[t] < V_real,   else 0.
+ * The ownership test is done before any index into W is formed; the row is
+ * owned by exactly one shard, so the sum over shards of the masked partial
+ * lookups is the owner's row and the result is an exact copy.
+ * Padding ids (ignore_index), negative ids, padded rows [V_real,Vp) and ids
+ * >= Vp all give zero rows; they are not errors.
+ * Optional outputs (NULL to skip): owner[t] = shard owning ids[t] (-1 if
+ * invalid); local[t] = ids[t] - floor(owner*Vp/S) (-1 if invalid).
+ * No workspace. `dev_status` is unused and may be NULL.
+ */
+vce_status vce_embed_fwd(const vce_problem* p, const int64_t* ids, const void* W,
+                         void* E, int32_t* owner, int32_t* local,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * Embedding backward [VS p.2: repeated tokens accumulate into the same owned
+ * row; tied weights combine all gradient contributions].
+ *   dW[v,:] += sum over t with ids[t] == v of dE[t,:]      for 0 <= v < V_real
+ * dW is fp32 and is always accumulated into (+=); rows with no valid id are
+ * not touched. Invalid ids (as in vce_embed_fwd) contribute nothing.
+ * Deterministic: valid (id, t) pairs are sorted ascending; the tokens of one
+ * id are cut into runs of vce_embed_bwd_chunk() consecutive tokens; each run
+ * is summed in fp32 from 0.0 in ascending t; the run sums are added left to
+ * right; the total is added to dW[v] with one fp32 rounding. Results are
+ * bit-identical run to run.
+ * Workspace: vce_workspace_size(p, VCE_OP_EMBED_BWD) bytes.
+ */
+vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* dE,
+                         float* dW, void* ws, size_t ws_bytes,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * Globally normalised cross-entropy, forward [VS p.3-5; PAD s.5; SPN p.3].
+ *   z[t,v] = <h_t, W_v> accumulated in fp32, for real classes v < V_real only
+ *   (padded classes are excluded, as if their logits were -inf);
+ *   lse[t] = log sum_v exp(z[t,v]);  token_loss[t] = lse[t] - z[t, y_t];
+ *   loss   = sum over valid t of token_loss[t] / N_valid   (0 if N_valid == 0).
+ * A target y_t is valid iff 0 <= y_t < V_real. y_t == ignore_index is ignored.
+ * Any other value is a data error: VCE_ERR_BAD_INDEX goes to dev_status and
+ * the token is treated as ignored.
+ * Each vocabulary tile's partial (max, sum of exp) and the target logit from
+ * its unique owning tile are merged on the GPU into one maximum and one
+ * denominator per token; the [T,Vp] logits are never written to memory.
+ * Outputs: loss[1] and lse[T] (kept for the backward) are required;
+ * token_loss[T] (0 for ignored tokens), target_owner[T] (shard owning y_t, -1
+ * if not valid) and max_owner[T] (shard holding the largest logit, lowest shard
+ * on ties) may be NULL. lse is written for every token.
+ * Workspace: vce_workspace_size(p, VCE_OP_LOSS_FWD) bytes.
+ */
+vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W,
+                        const int64_t* targets, float* loss, float* lse,
+                        float* token_loss, int32_t* target_owner, int32_t* max_owner,
+                        void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * Cross-entropy backward [VS p.4: gradient = probability - target indicator,
+ * times the loss scale; SPN p.3: averaged once over the valid tokens].
+ *   G[t,v] = (exp(z[t,v] - lse[t]) - [v == y_t]) * g / N_valid
+ * for valid t and real v, 0 elsewhere; z is recomputed tile by tile.
+ *   dH  = G W        (fp32, overwritten)
+ *   dW  = G^T h      rows [V_real,Vp) are 0:
+ *         tied_weights == 0: dW is overwritten;
+ *         tied_weights == 1: dW is accumulated into (+=), so that the embedding
+ *         backward and this call combine into one parameter gradient.
+ * lse must come from vce_loss_fwd on the same inputs. g is the upstream
+ * gradient of the scalar loss (1 for a plain mean).
+ * bf16: G is formed in bf16 for the two tensor-core GEMMs; fp32: all fp32.
+ * Workspace: at least vce_workspace_size_min(p, VCE_OP_LOSS_BWD) bytes; the
+ * vocabulary is processed in column chunks that fit the workspace.
+ */
+vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W,
+                        const int64_t* targets, const float* lse, float g,
+                        float* dH, float* dW, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, void* stream);
+
+/* Static string naming a status code. */
+const char* vce_status_str(vce_status s);
+
+/* The run length of the embedding backward's fixed summation order (tokens). */
+int32_t vce_embed_bwd_chunk(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t vce_version(void);
+
+/*
+ * Upper bound, in nanoseconds, on any single wait inside a kernel (pipeline
+ * barriers of the tensor-core kernels). When a wait runs out the kernel stops
+ * its work, writes VCE_ERR_TIMEOUT to dev_status (or to the workspace's status
+ * word when dev_status is NULL) and returns. Default 2e9 (2 s). Process-wide.
+ */
+void vce_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Self-test of the bounded wait: launches one block that waits on a pipeline
+ * barrier nothing will ever complete, bounded by `limit_ns`. The kernel gives
+ * up, writes VCE_ERR_TIMEOUT to dev_status and exits; the stream and context
+ * stay usable. Used by the failure-detection tests. No workspace.
+ */
+vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* stream);
+
+/*
+ * Launch accounting, for profilers and benchmarks (no counterpart on the
+ * pages). Every kernel the library launches increments a process-wide
+ * counter. While an event table is installed, each launch is also followed by
+ * cudaEventRecord(events[i]) on the launching stream and kinds[i] records which
+ * kernel it was (vce_kernel_kind); *count is the number of entries written.
+ * Launch i therefore runs between events[i-1] (or an event the caller records
+ * before the call) and events[i]. Pass events == NULL to uninstall. The table
+ * is host memory owned by the caller; events are cudaEvent_t handles.
+ */
+typedef enum vce_kernel_kind {
+  VCE_K_EMBED_GATHER = 0, VCE_K_EMBED_SORT = 1, VCE_K_EMBED_REDUCE = 2,
+  VCE_K_TC_FWD = 3, VCE_K_TC_GRAD = 4, VCE_K_TC_DH = 5, VCE_K_TC_DW = 6,
+  VCE_K_MERGE = 7, VCE_K_LOSS_MEAN = 8, VCE_K_COUNT_VALID = 9,
+  VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13
+} vce_kernel_kind;
+uint64_t vce_launch_count(void);
+void vce_set_launch_events(void** events, int32_t* kinds, int32_t capacity, int32_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VCE_H */

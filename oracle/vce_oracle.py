@@ -322,6 +322,22 @@ def hidden_gradient_rows(h_rows, W, targets_rows, V_real: int, scale: float,
     return (p * scale) @ _as_f64(W)[:V_real]
 
 
+def head_gradient_rows(h, W, targets, V_real: int, lse: np.ndarray, scale: float, rows,
+                       ignore_index: int = IGNORE_INDEX) -> np.ndarray:
+    """dW_head[v] = sum_t G[t, v] h_t for the given real classes v, from the
+    batch's lse (computed by this oracle) and scale = g / N_valid (P4)."""
+    y = np.asarray(targets, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    hf = _as_f64(h)
+    z = hf @ _as_f64(W)[rows].T
+    p = np.exp(z - np.asarray(lse, dtype=np.float64)[:, None])
+    valid, _ = target_status(y, V_real, ignore_index)
+    p[~valid] = 0.0
+    for j, v in enumerate(rows):
+        p[valid & (y == v), j] -= 1.0
+    return (p * scale).T @ hf
+
+
 def target_owner(targets, V_real: int, Vp: int, S: int,
                  ignore_index: int = IGNORE_INDEX) -> np.ndarray:
     """Shard that owns each valid target, -1 for ignored or bad ones (P3)."""

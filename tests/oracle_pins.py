@@ -368,6 +368,11 @@ def pin_gradient_invariants(O):
     # rows of dH computed alone agree with the full computation
     part = O.hidden_gradient_rows(h[5:9], W, y[5:9], V_real, 1.0 / nv)
     assert np.allclose(part, dH[5:9], rtol=0, atol=1e-15)
+    # rows of dW_head from the batch lse agree with the full computation
+    lse = O.cross_entropy_forward(h, W, y, V_real)["lse"]
+    rows = [0, y[0], y[1], V_real - 1]
+    part = O.head_gradient_rows(h, W, y, V_real, lse, 1.0 / nv, rows)
+    assert np.allclose(part, dW[rows], rtol=0, atol=1e-15)
 
 
 ALL_PINS = [

@@ -1,0 +1,112 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import os
+import re
+
+import pytest
+
+from vocab_embedding_cross_gb300 import _lib as vce
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(vce.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return vce.lib()
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^\s*[a-z_0-9]+\**\s+\**(vce_[a-z_0-9]+)\s*\(", src, re.M))
+    return sorted(names)
+
+
+def test_every_declared_symbol_exported(L):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert vce.status_str(s).startswith("VCE_")
+    assert vce.vce_embed_bwd_chunk() == 32
+    assert vce.vce_version() >= 100
+
+
+def P(**kw):
+    base = dict(T=64, H=64, Vp=1024, V_real=1000, S=4, dtype=vce.VCE_BF16)
+    base.update(kw)
+    return vce.problem(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Vp=1000), vce.VCE_ERR_ARG),            # not a multiple of 64
+    (dict(Vp=0), vce.VCE_ERR_ARG),
+    (dict(V_real=1025), vce.VCE_ERR_ARG),
+    (dict(V_real=0), vce.VCE_ERR_ARG),
+    (dict(S=0), vce.VCE_ERR_ARG),
+    (dict(S=1025), vce.VCE_ERR_ARG),
+    (dict(T=-1), vce.VCE_ERR_ARG),
+    (dict(H=0), vce.VCE_ERR_ARG),
+    (dict(H=4), vce.VCE_ERR_UNSUPPORTED),         # 8 bytes per bf16 row
+    (dict(dtype=7), vce.VCE_ERR_UNSUPPORTED),
+    (dict(T=1 << 31), vce.VCE_ERR_UNSUPPORTED),
+])
+def test_bad_problem_rejected_on_host(L, kw, code):
+    p = P(**kw)
+    assert vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD) == vce.SIZE_MAX
+    for fn, args in ((L.vce_embed_fwd, (None,) * 7), (L.vce_embed_bwd, (None, None, None, None, 0, None, None)),
+                     (L.vce_loss_fwd, (None,) * 9 + (0, None, None)),
+                     (L.vce_loss_bwd, (None, None, None, None, 1.0, None, None, None, 0, None, None))):
+        import ctypes
+        assert fn(ctypes.byref(p), *args) == code
+
+
+def test_null_pointers_rejected(L):
+    import ctypes
+    p = P()
+    assert L.vce_embed_fwd(ctypes.byref(p), None, None, None, None, None, None, None) == vce.VCE_ERR_ARG
+    assert L.vce_loss_fwd(ctypes.byref(p), None, None, None, None, None, None, None, None, None, 0, None,
+                          None) == vce.VCE_ERR_ARG
+    assert L.vce_wait_selftest(1000, None, None) == vce.VCE_ERR_ARG
+
+
+def test_misaligned_pointers_rejected(L):
+    import ctypes
+    p = P()
+    # 8-byte aligned but not 16-byte aligned matrices; never dereferenced
+    assert L.vce_embed_fwd(ctypes.byref(p), 0x1000, 0x1008, 0x2000, None, None, None, None) == \
+        vce.VCE_ERR_UNSUPPORTED
+
+
+def test_workspace_sizes(L):
+    p = P(T=8192, H=2048, Vp=151936, V_real=151936, S=8)
+    assert vce.vce_workspace_size(p, vce.VCE_OP_EMBED_FWD) == 0
+    fwd = vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD)
+    units = 8 * -(-(151936 // 8) // 2048)
+    assert fwd >= 8192 * units * 8 + 8192 * 4
+    mn = vce.vce_workspace_size_min(p, vce.VCE_OP_LOSS_BWD)
+    rec = vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD)
+    assert mn == 256 + 8192 * 256 * 2 and rec >= mn and (rec - 256) % (8192 * 256 * 2) == 0
+    assert vce.vce_workspace_size(p, vce.VCE_OP_EMBED_BWD) > 8192 * 16
+    # the embedding backward workspace holds keys, runs and run partial slots
+    p4 = P(T=16384, H=3072, Vp=201088, V_real=201088, S=8)
+    assert vce.vce_workspace_size(p4, vce.VCE_OP_EMBED_BWD) < 64 << 20
+
+
+def test_workspace_too_small_rejected_on_host(L):
+    import ctypes
+    p = P(T=64)
+    need = vce.vce_workspace_size(p, vce.VCE_OP_EMBED_BWD)
+    assert L.vce_embed_bwd(ctypes.byref(p), 0x1000, 0x2000, 0x3000, 0x4000, need - 1, None, None) == \
+        vce.VCE_ERR_WORKSPACE
+    assert L.vce_embed_bwd(ctypes.byref(p), 0x1000, 0x2000, 0x3000, 0x4010, need, None, None) == \
+        vce.VCE_ERR_WORKSPACE                      # misaligned workspace

@@ -1,0 +1,226 @@
+"""GPU parity of the globally normalised cross-entropy (forward and backward)
+against the fp64 oracle on the same seeded (bf16-rounded) inputs.
+
+Tolerances: fp32 problems 1e-5 relative for everything; bf16 problems (fp32
+accumulation on the tensor cores, G in bf16) loss and lse 1e-3 relative, dH
+and dW 2e-2 max-abs relative (max|gpu - ref| / max|ref| per tensor). Owner
+maps are compared exactly.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import vce_run as R
+from oracle import vce_oracle as O
+from vocab_embedding_cross_gb300 import device as D
+from vocab_embedding_cross_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": dict(loss=1e-5, lse=1e-5, grad=1e-5), "bf16": dict(loss=1e-3, lse=1e-3, grad=2e-2)}
+
+
+def _fwd_check(wl, d, tol, out=None):
+    h, W, y = d["h"], d["W"], d["targets"]
+    if out is None:
+        out = R.loss_fwd(wl, D.to_device(h), D.to_device(W), y)
+    ref = O.cross_entropy_forward(h, W, y, wl.V_real)
+    assert out["status"] == (R.vce.VCE_ERR_BAD_INDEX if ref["bad"].any() else 0)
+    assert R.rel(out["loss"], ref["loss"]) <= tol["loss"] or (ref["loss"] == 0 and out["loss"] == 0)
+    assert np.all(np.abs(out["lse"] - ref["lse"]) <= tol["lse"] * np.maximum(np.abs(ref["lse"]), 1.0))
+    assert R.max_abs_rel(out["token_loss"], ref["token_loss"]) <= tol["loss"]
+    assert np.array_equal(out["target_owner"], O.target_owner(y, wl.V_real, wl.Vp, wl.S).astype(np.int32))
+    own, gap = O.max_owner(h, W, wl.V_real, wl.Vp, wl.S)
+    clear = gap > 4 * tol["lse"] * np.maximum(1.0, np.abs(ref["lse"]))
+    assert np.array_equal(out["max_owner"][clear], own[clear].astype(np.int32))
+    return out, ref
+
+
+def _bwd_check(wl, d, out, tol, g=1.0):
+    h, W, y = d["h"], d["W"], d["targets"]
+    dH, dW, st = R.loss_bwd(wl, D.to_device(h), D.to_device(W), out["targets_d"], out["lse_d"], g=g,
+                            dW=torch.full((wl.Vp, wl.H), 0.0 if wl.tied else float("nan"),
+                                          dtype=torch.float32, device="cuda"))
+    rdH, rdW = O.cross_entropy_backward(h, W, y, wl.V_real, wl.Vp, g=g)
+    dH, dW = dH.cpu().numpy(), dW.cpu().numpy()
+    assert R.max_abs_rel(dH, rdH) <= tol["grad"]
+    assert R.max_abs_rel(dW, rdW) <= tol["grad"]
+    assert np.all(dW[wl.V_real:] == 0)
+    ign = ~((y >= 0) & (y < wl.V_real))
+    assert np.all(dH[ign] == 0)
+    return dH, dW
+
+
+def test_loss_tiny_f32():
+    """fp32, T=64, H=64, V_real=1000 -> 1024, S=4: boundary targets 255, 256,
+    511, 512, 999, maxima injected in other shards, garbage padded rows 8.0."""
+    wl = I.WORKLOADS["tiny_f32"]
+    d = I.make_all(wl, ("W", "h", "targets"))
+    out, ref = _fwd_check(wl, d, TOL["f32"])
+    # the injected maxima really sit in another shard than the target
+    assert np.all(out["max_owner"][5:9] != out["target_owner"][5:9])
+    _bwd_check(wl, d, out, TOL["f32"])
+    _bwd_check(wl, d, out, TOL["f32"], g=0.37)
+
+
+BF16_CASES = [
+    dict(T=300, H=192, V_real=1000, Vp=1024, S=3),     # ragged T, K and vocab
+    dict(T=1, H=64, V_real=50, Vp=64, S=1),
+    dict(T=129, H=256, V_real=4000, Vp=4032, S=7),
+    dict(T=64, H=128, V_real=700, Vp=1024, S=4),       # last shard only padding
+    dict(T=16, H=64, V_real=60, Vp=64, S=64),          # one row per shard
+    dict(T=520, H=1024, V_real=9000, Vp=9024, S=8, ignore_frac=0.3),
+]
+
+
+@pytest.mark.parametrize("case", BF16_CASES, ids=lambda c: "T{T}_H{H}_V{V_real}_S{S}".format(**c))
+def test_loss_bf16_cases(case):
+    wl = I.custom(dtype="bf16", seed=21, ignore_frac=case.pop("ignore_frac", 0.05), **case)
+    d = I.make_all(wl, ("W", "h", "targets"))
+    out, _ = _fwd_check(wl, d, TOL["bf16"])
+    _bwd_check(wl, d, out, TOL["bf16"])
+
+
+def test_loss_bf16_boundaries_and_injected_max():
+    """The tiny case's forced targets and injected maxima, in bf16 through the
+    tensor-core kernels."""
+    base = I.WORKLOADS["tiny_f32"]
+    wl = I.custom(T=64, H=64, V_real=1000, Vp=1024, S=4, dtype="bf16", seed=0, ignore_frac=0.1,
+                  forced_targets=base.forced_targets, injected=base.injected)
+    d = I.make_all(wl, ("W", "h", "targets"))
+    out, _ = _fwd_check(wl, d, TOL["bf16"])
+    assert np.all(out["max_owner"][5:9] != out["target_owner"][5:9])
+    _bwd_check(wl, d, out, TOL["bf16"])
+
+
+def test_loss_all_ignored():
+    wl = I.custom(T=200, H=64, V_real=500, Vp=512, S=2, dtype="bf16", seed=22)
+    d = I.make_all(wl, ("W", "h"))
+    d["targets"] = np.full(wl.T, -100, dtype=np.int64)
+    out = R.loss_fwd(wl, D.to_device(d["h"]), D.to_device(d["W"]), d["targets"])
+    assert out["loss"] == 0.0 and out["status"] == 0
+    assert np.all(out["token_loss"] == 0) and np.all(out["target_owner"] == -1)
+    dH, dW, st = R.loss_bwd(wl, D.to_device(d["h"]), D.to_device(d["W"]), out["targets_d"], out["lse_d"])
+    assert st == 0
+    assert not dH.any().item() and not dW.any().item()
+
+
+def test_loss_bad_target_flagged_and_ignored():
+    wl = I.custom(T=100, H=64, V_real=500, Vp=512, S=2, dtype="bf16", seed=23)
+    d = I.make_all(wl, ("W", "h", "targets"))
+    d["targets"][[3, 40]] = [505, -7]       # a padded class and a negative non-ignore value
+    out, ref = _fwd_check(wl, d, TOL["bf16"])
+    assert out["status"] == R.vce.VCE_ERR_BAD_INDEX
+    assert out["token_loss"][3] == 0 and out["target_owner"][40] == -1
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_loss_bwd_small_workspace_chunks(dtype):
+    """The smallest workspace (256 vocabulary columns per pass) gives the same
+    gradients as one large pass, within tolerance, and is run to run exact."""
+    wl = I.custom(T=200, H=128, V_real=3000, Vp=3008, S=5, dtype=dtype, seed=24, ignore_frac=0.1)
+    d = I.make_all(wl, ("W", "h", "targets"))
+    out, _ = _fwd_check(wl, d, TOL[dtype])
+    p = R.prob(wl)
+    nmin = R.vce.vce_workspace_size_min(p, R.vce.VCE_OP_LOSS_BWD)
+    h_d, W_d = D.to_device(d["h"]), D.to_device(d["W"])
+    dH1, dW1, _ = R.loss_bwd(wl, h_d, W_d, out["targets_d"], out["lse_d"], ws_bytes=nmin)
+    dH2, dW2, _ = R.loss_bwd(wl, h_d, W_d, out["targets_d"], out["lse_d"], ws_bytes=nmin)
+    assert torch.equal(dH1, dH2) and torch.equal(dW1, dW2)
+    rdH, rdW = O.cross_entropy_backward(d["h"], d["W"], d["targets"], wl.V_real, wl.Vp)
+    assert R.max_abs_rel(dH1.cpu().numpy(), rdH) <= TOL[dtype]["grad"]
+    assert R.max_abs_rel(dW1.cpu().numpy(), rdW) <= TOL[dtype]["grad"]
+    with pytest.raises(R.vce.VceError) as e:
+        R.loss_bwd(wl, h_d, W_d, out["targets_d"], out["lse_d"], ws_bytes=nmin - 256)
+    assert e.value.status == R.vce.VCE_ERR_WORKSPACE
+
+
+def test_tied_embedding_and_head_gradients_combine():
+    """Tied W: the head gradient is accumulated into dW and the embedding
+    backward adds its rows on top: dW = dW_head + dW_embed."""
+    wl = I.custom(T=256, H=128, V_real=1000, Vp=1024, S=4, dtype="bf16", seed=25, tied=True,
+                  ignore_frac=0.05)
+    d = I.make_all(wl, ("W", "h", "targets", "ids", "dE"))
+    dE = I.bf16_bits(I.bf16_to_f32(d["dE"]) * np.float32(1e-3))   # comparable magnitudes
+    out, _ = _fwd_check(wl, d, TOL["bf16"])
+    dW = torch.zeros((wl.Vp, wl.H), dtype=torch.float32, device="cuda")
+    R.loss_bwd(wl, D.to_device(d["h"]), D.to_device(d["W"]), out["targets_d"], out["lse_d"], dW=dW)
+    assert R.embed_bwd(wl, d["ids"], D.to_device(dE), dW) == 0
+    _, rdW_head = O.cross_entropy_backward(d["h"], d["W"], d["targets"], wl.V_real, wl.Vp)
+    ref = rdW_head + O.embed_backward(d["ids"], dE, wl.V_real, wl.Vp)
+    assert R.max_abs_rel(dW.cpu().numpy(), ref) <= TOL["bf16"]["grad"]
+    # tied accumulation: a second head backward adds the same amount again
+    before = dW.clone()
+    R.loss_bwd(wl, D.to_device(d["h"]), D.to_device(d["W"]), out["targets_d"], out["lse_d"], dW=dW)
+    assert R.max_abs_rel((dW - before).cpu().numpy(), rdW_head) <= TOL["bf16"]["grad"]
+
+
+def test_loss_gpt2_head_full():
+    """T=4096, H=1024, V_real=50000 -> 50048, S=8 (6256 rows per shard), 5%
+    ignored, untied: every lse, every token loss, all of dH and dW."""
+    wl = I.WORKLOADS["gpt2_head"]
+    d = I.make_all(wl, ("W", "h", "targets"))
+    out, _ = _fwd_check(wl, d, TOL["bf16"])
+    _bwd_check(wl, d, out, TOL["bf16"])
+
+
+def _oracle_rows_all(h, W, y, V_real, rows=256):
+    """The oracle's per-token quantities for every token, a block of rows at a time."""
+    lse = np.empty(h.shape[0])
+    tl = np.empty(h.shape[0])
+    for i in range(0, h.shape[0], rows):
+        r = O.cross_entropy_rows(h[i:i + rows], W, y[i:i + rows], V_real)
+        lse[i:i + rows] = r["lse"]
+        tl[i:i + rows] = r["token_loss"]
+    return lse, tl
+
+
+def _full_size_check(wl, with_dw_rows):
+    d = I.make_all(wl, ("W", "h", "targets"))
+    h, W, y = d["h"], d["W"], d["targets"]
+    h_d, W_d = D.to_device(h), D.to_device(W)
+    out = R.loss_fwd(wl, h_d, W_d, y)
+    assert out["status"] == 0
+    tol = TOL["bf16"]
+    rng = np.random.default_rng(0)
+    sample = np.unique(np.concatenate([rng.choice(wl.T, 48, replace=False), [0, wl.T - 1]]))
+    r = O.cross_entropy_rows(h[sample], W, y[sample], wl.V_real)
+    assert np.all(np.abs(out["lse"][sample] - r["lse"]) <= tol["lse"] * np.abs(r["lse"]))
+    assert R.max_abs_rel(out["token_loss"][sample], r["token_loss"]) <= tol["loss"]
+    nv = O.n_valid(y, wl.V_real)
+    dW = torch.zeros((wl.Vp, wl.H), dtype=torch.float32, device="cuda")
+    dH, dW, st = R.loss_bwd(wl, h_d, W_d, out["targets_d"], out["lse_d"], dW=dW)
+    assert st == 0
+    ref_dH = O.hidden_gradient_rows(h[sample], W, y[sample], wl.V_real, 1.0 / nv)
+    assert R.max_abs_rel(dH.cpu().numpy()[sample], ref_dH) <= tol["grad"]
+    if with_dw_rows:
+        t0 = time.time()
+        lse_all, tl_all = _oracle_rows_all(h, W, y, wl.V_real)
+        assert R.rel(out["loss"], tl_all.sum() / nv) <= tol["loss"]
+        assert np.all(np.abs(out["lse"] - lse_all) <= tol["lse"] * np.abs(lse_all))
+        # sampled rows of dW_head: most frequent targets, random classes, the last class
+        valid = (y >= 0) & (y < wl.V_real)
+        counts = np.bincount(y[valid], minlength=wl.V_real)
+        vs = np.unique(np.concatenate([np.argsort(-counts)[:8], rng.choice(wl.V_real, 8, replace=False),
+                                       [wl.V_real - 1]]))
+        ref_rows = O.head_gradient_rows(h, W, y, wl.V_real, lse_all, 1.0 / nv, vs)
+        got_rows = dW.index_select(0, torch.from_numpy(vs).cuda()).cpu().numpy()
+        assert R.max_abs_rel(got_rows, ref_rows) <= tol["grad"]
+        print(f"oracle over the full batch: {time.time() - t0:.1f}s")
+    # properties at any size: finite, padded rows zero
+    assert torch.isfinite(dW).all().item() and torch.isfinite(dH).all().item()
+    assert int((dW[wl.V_real:] != 0).sum().item()) == 0
+
+
+def test_loss_qwen3_full():
+    """T=8192, H=2048, V_real=151936, S=8, Zipf next-token targets: sampled lse,
+    token losses and dH rows; the exact loss, every lse and sampled dW rows
+    from the oracle's full-batch lse."""
+    _full_size_check(I.WORKLOADS["qwen3_tied"], with_dw_rows=True)
+
+
+def test_loss_gptoss_full():
+    """T=16384, H=3072, V_real=201088, S=8: sampled lse, token losses, dH rows."""
+    _full_size_check(I.WORKLOADS["gptoss_embed"], with_dw_rows=False)

@@ -1,0 +1,172 @@
+"""ctypes binding of libvocabce (include/vce.h). Argument marshalling only.
+
+Every function has the name of its C entry point and takes torch tensors (or
+None for optional pointers); the tensors' device pointers and the current CUDA
+stream are passed straight through. There is no fallback: if the shared
+library is missing this module raises on import of the binding.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_float, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libvocabce.so")
+
+VCE_OK, VCE_ERR_ARG, VCE_ERR_UNSUPPORTED, VCE_ERR_CUDA = 0, 1, 2, 3
+VCE_ERR_BAD_INDEX, VCE_ERR_TIMEOUT, VCE_ERR_WORKSPACE = 4, 5, 6
+VCE_F32, VCE_BF16 = 0, 1
+VCE_OP_EMBED_FWD, VCE_OP_EMBED_BWD, VCE_OP_LOSS_FWD, VCE_OP_LOSS_BWD = 0, 1, 2, 3
+SIZE_MAX = (1 << 64) - 1
+
+
+class VceProblem(ctypes.Structure):
+    _fields_ = [("T", c_int64), ("H", c_int64), ("Vp", c_int64), ("V_real", c_int64),
+                ("ignore_index", c_int64), ("S", c_int32), ("tied_weights", c_int32),
+                ("dtype", c_int32), ("reserved", c_int32)]
+
+
+class VceError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)}")
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libvocabce.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P = POINTER(VceProblem)
+        L.vce_workspace_size.argtypes = [P, c_int32]
+        L.vce_workspace_size.restype = c_size_t
+        L.vce_workspace_size_min.argtypes = [P, c_int32]
+        L.vce_workspace_size_min.restype = c_size_t
+        L.vce_embed_fwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+        L.vce_embed_fwd.restype = c_int32
+        L.vce_embed_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
+        L.vce_embed_bwd.restype = c_int32
+        L.vce_loss_fwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
+        L.vce_loss_fwd.restype = c_int32
+        L.vce_loss_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_void_p, c_void_p,
+                                   c_void_p, c_size_t, c_void_p, c_void_p]
+        L.vce_loss_bwd.restype = c_int32
+        L.vce_status_str.argtypes = [c_int32]
+        L.vce_status_str.restype = ctypes.c_char_p
+        L.vce_embed_bwd_chunk.argtypes = []
+        L.vce_embed_bwd_chunk.restype = c_int32
+        L.vce_version.argtypes = []
+        L.vce_version.restype = c_int32
+        L.vce_set_wait_limit_ns.argtypes = [c_uint64]
+        L.vce_set_wait_limit_ns.restype = None
+        L.vce_wait_selftest.argtypes = [c_uint64, c_void_p, c_void_p]
+        L.vce_wait_selftest.restype = c_int32
+        L.vce_launch_count.argtypes = []
+        L.vce_launch_count.restype = c_uint64
+        L.vce_set_launch_events.argtypes = [c_void_p, c_void_p, c_int32, c_void_p]
+        L.vce_set_launch_events.restype = None
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().vce_status_str(int(status)).decode()
+
+
+def problem(T: int, H: int, Vp: int, V_real: int, S: int, dtype: int, ignore_index: int = -100,
+            tied: bool = False) -> VceProblem:
+    return VceProblem(int(T), int(H), int(Vp), int(V_real), int(ignore_index), int(S), int(bool(tied)),
+                      int(dtype), 0)
+
+
+def _ptr(x, device=True) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if device and not x.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return int(stream)
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != VCE_OK:
+        raise VceError(status, where)
+
+
+def vce_workspace_size(p: VceProblem, op: int) -> int:
+    return int(lib().vce_workspace_size(ctypes.byref(p), op))
+
+
+def vce_workspace_size_min(p: VceProblem, op: int) -> int:
+    return int(lib().vce_workspace_size_min(ctypes.byref(p), op))
+
+
+def vce_embed_fwd(p, ids, W, E, owner=None, local=None, dev_status=None, stream=None) -> None:
+    _check(lib().vce_embed_fwd(ctypes.byref(p), _ptr(ids), _ptr(W), _ptr(E), _ptr(owner), _ptr(local),
+                               _ptr(dev_status), _stream(stream)), "vce_embed_fwd")
+
+
+def vce_embed_bwd(p, ids, dE, dW, ws, ws_bytes=None, dev_status=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().vce_embed_bwd(ctypes.byref(p), _ptr(ids), _ptr(dE), _ptr(dW), _ptr(ws), nb,
+                               _ptr(dev_status), _stream(stream)), "vce_embed_bwd")
+
+
+def vce_loss_fwd(p, h, W, targets, loss, lse, token_loss=None, target_owner=None, max_owner=None, ws=None,
+                 ws_bytes=None, dev_status=None, stream=None) -> None:
+    nb = (ws.numel() * ws.element_size() if ws is not None else 0) if ws_bytes is None else ws_bytes
+    _check(lib().vce_loss_fwd(ctypes.byref(p), _ptr(h), _ptr(W), _ptr(targets), _ptr(loss), _ptr(lse),
+                              _ptr(token_loss), _ptr(target_owner), _ptr(max_owner), _ptr(ws), nb,
+                              _ptr(dev_status), _stream(stream)), "vce_loss_fwd")
+
+
+def vce_loss_bwd(p, h, W, targets, lse, g, dH, dW, ws, ws_bytes=None, dev_status=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().vce_loss_bwd(ctypes.byref(p), _ptr(h), _ptr(W), _ptr(targets), _ptr(lse), float(g),
+                              _ptr(dH), _ptr(dW), _ptr(ws), nb, _ptr(dev_status), _stream(stream)),
+           "vce_loss_bwd")
+
+
+def vce_embed_bwd_chunk() -> int:
+    return int(lib().vce_embed_bwd_chunk())
+
+
+def vce_version() -> int:
+    return int(lib().vce_version())
+
+
+def vce_set_wait_limit_ns(ns: int) -> None:
+    lib().vce_set_wait_limit_ns(int(ns))
+
+
+def vce_wait_selftest(limit_ns: int, dev_status, stream=None) -> None:
+    _check(lib().vce_wait_selftest(int(limit_ns), _ptr(dev_status), _stream(stream)), "vce_wait_selftest")
+
+
+KERNEL_KINDS = ["embed_gather", "embed_sort", "embed_reduce", "tc_fwd", "tc_grad", "tc_dh", "tc_dw",
+                "merge", "loss_mean", "count_valid", "simt_fwd", "simt_grad", "sgemm", "wait_selftest"]
+
+
+def vce_launch_count() -> int:
+    return int(lib().vce_launch_count())
+
+
+def vce_set_launch_events(events, kinds, capacity: int, count) -> None:
+    """events: ctypes array of void* (cudaEvent_t); kinds, count: ctypes int32 arrays."""
+    lib().vce_set_launch_events(events, kinds, int(capacity), count)

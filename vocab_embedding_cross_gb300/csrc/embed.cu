@@ -1,0 +1,487 @@
+// Vocabulary-sharded embedding: masked lookup and deterministic backward.
+//
+// Forward ("Vocabulary shards: look up locally and normalize globally",
+// paragraph 1; "Tensor Parallelism (TP)", Embedding): the ownership test is
+// made on the global id before any row address is formed. A valid id is owned
+// by exactly one shard, so the sum of the S masked partial lookups is the
+// owner's row; on one GPU that sum is the row itself, copied with 16-byte
+// vector loads. Invalid ids (padding id, negatives, padded rows, >= Vp) give
+// zero rows.
+//
+// Backward (same page, paragraph 2: repeated tokens accumulate into the same
+// owned row): the valid (id, t) pairs are sorted (stable LSD radix sort on the
+// id, one CTA), the tokens of each id are cut into runs of kEmbedBwdChunk,
+// each run is summed in fp32 in ascending t, run sums are combined left to
+// right, and the total is added once into the fp32 row. The order is fixed,
+// so results are bit-identical from run to run.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace vce {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Forward gather: one warp per token row.
+// ---------------------------------------------------------------------------
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(kGatherWarps * 32)
+    embed_gather_kernel(const int64_t* __restrict__ ids, const uint4* __restrict__ W, uint4* __restrict__ E,
+                        int32_t* __restrict__ owner, int32_t* __restrict__ local, int64_t T, int64_t Vp,
+                        int64_t V_real, int32_t S, int row_vecs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kGatherWarps + warp;
+  if (t >= T) return;
+  const int64_t id = __ldg(ids + t);
+  const bool valid = (id >= 0) && (id < V_real);   // ownership test before indexing
+  if (lane == 0) {
+    int32_t k = -1, l = -1;
+    if (valid) {
+      k = shard_of(id, Vp, S);
+      l = static_cast<int32_t>(id - shard_lo(k, Vp, S));
+    }
+    if (owner) owner[t] = k;
+    if (local) local[t] = l;
+  }
+  uint4* dst = E + t * row_vecs;
+  if (!valid) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int i = lane; i < row_vecs; i += 32) dst[i] = z;
+    return;
+  }
+  const uint4* src = W + id * row_vecs;
+  int i = lane;
+  for (; i + 96 < row_vecs; i += 128) {
+    uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64), d = __ldg(src + i + 96);
+    dst[i] = a;
+    dst[i + 32] = b;
+    dst[i + 64] = c;
+    dst[i + 96] = d;
+  }
+  for (; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
+}
+
+// ---------------------------------------------------------------------------
+// Backward, step 1: one CTA sorts the valid (id, t) keys and builds the runs.
+// ---------------------------------------------------------------------------
+constexpr int kSortThreads = 1024;
+constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSortItems = 8;
+constexpr int kSortTile = kSortThreads * kSortItems;
+constexpr int kRadix = 256;
+
+struct RunDesc {
+  int32_t start, end;   // sorted positions [start, end)
+  int32_t id;
+  int32_t slot;         // partial slot (multi-run ids) or -1
+  int32_t mseg;         // index of the multi-run id, or -1
+  int32_t nruns;        // runs of this id
+  int32_t first_slot;   // slot of the id's first run
+  int32_t pad;
+};
+
+struct BwdLayout {
+  size_t hdr, keys_a, keys_b, seg_start, runs, counters, partials, total;
+  int64_t n_counters, n_slots;
+  int nh;
+};
+
+int cols_per_item(int esize) { return 128 * (16 / esize); }
+
+BwdLayout bwd_layout(const vce_problem& p) {
+  BwdLayout L{};
+  const int64_t T = p.T;
+  const int esize = p.dtype == VCE_BF16 ? 2 : 4;
+  L.nh = static_cast<int>(ceil_div(p.H, cols_per_item(esize)));
+  L.n_counters = (T / (kEmbedBwdChunk + 1) + 2) * L.nh;
+  L.n_slots = 2 * T / kEmbedBwdChunk + 2;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, kWsAlign);
+    return o;
+  };
+  L.hdr = take(64);
+  L.keys_a = take(sizeof(uint64_t) * (T + 1));
+  L.keys_b = take(sizeof(uint64_t) * (T + 1));
+  L.seg_start = take(sizeof(int32_t) * (T + 2));
+  L.runs = take(sizeof(RunDesc) * (T + 1));
+  L.counters = take(sizeof(int32_t) * L.n_counters);
+  L.partials = take(sizeof(float) * L.n_slots * p.H);
+  L.total = off;
+  return L;
+}
+
+// Block-wide exclusive scan of one int per thread (1024 threads).
+__device__ __forceinline__ int block_excl_scan(int v, int* sh_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = sh_warp[lane];
+    int s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    sh_warp[lane] = s - w;          // exclusive prefix of warp totals
+    if (lane == 31) sh_warp[32] = s;
+  }
+  __syncthreads();
+  const int res = sh_warp[warp] + x - v;
+  *total = sh_warp[32];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(kSortThreads, 1)
+    embed_sort_kernel(const int64_t* __restrict__ ids, int64_t T, int64_t V_real, int nh, int32_t* hdr,
+                      uint64_t* keys_a, uint64_t* keys_b, int32_t* seg_start, RunDesc* runs, int32_t* counters) {
+  __shared__ int sh_warp[33];
+  __shared__ int hist[kRadix];
+  __shared__ int carry[kRadix];
+  __shared__ int warp_cnt[kSortWarps][kRadix];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // Phase 0: stable compaction of the valid ids, key = (id << 32) | t.
+  int n = 0;
+  for (int64_t base = 0; base < T; base += kSortTile) {
+    int cnt = 0;
+    int64_t t0 = base + static_cast<int64_t>(tid) * kSortItems;
+#pragma unroll
+    for (int j = 0; j < kSortItems; ++j) {
+      int64_t t = t0 + j;
+      if (t < T) {
+        int64_t id = ids[t];
+        cnt += (id >= 0 && id < V_real) ? 1 : 0;
+      }
+    }
+    int tot;
+    int pos = n + block_excl_scan(cnt, sh_warp, &tot);
+#pragma unroll
+    for (int j = 0; j < kSortItems; ++j) {
+      int64_t t = t0 + j;
+      if (t < T) {
+        int64_t id = ids[t];
+        if (id >= 0 && id < V_real) keys_a[pos++] = (static_cast<uint64_t>(id) << 32) | static_cast<uint64_t>(t);
+      }
+    }
+    n += tot;
+  }
+  __syncthreads();
+
+  // Phase 1: LSD radix passes over the id bits (stable, so t stays ascending).
+  int idbits = 1;
+  while (idbits < 40 && (int64_t(1) << idbits) < V_real) ++idbits;
+  uint64_t* src = keys_a;
+  uint64_t* dst = keys_b;
+  for (int shift = 0; shift < idbits; shift += 8) {
+    const int sh = 32 + shift;
+    for (int i = tid; i < kRadix; i += kSortThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kSortThreads) atomicAdd(&hist[(src[i] >> sh) & 0xFF], 1);
+    __syncthreads();
+    {
+      int v = tid < kRadix ? hist[tid] : 0;
+      int tot;
+      int ex = block_excl_scan(v, sh_warp, &tot);
+      if (tid < kRadix) carry[tid] = ex;
+    }
+    __syncthreads();
+    for (int base = 0; base < n; base += kSortTile) {
+      for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&warp_cnt[0][0])[i] = 0;
+      __syncthreads();
+      uint64_t key[kSortItems];
+      int dig[kSortItems], rank[kSortItems];
+#pragma unroll
+      for (int j = 0; j < kSortItems; ++j) {
+        const int idx = base + warp * (32 * kSortItems) + j * 32 + lane;   // warp-striped
+        const bool ok = idx < n;
+        key[j] = ok ? src[idx] : 0ull;
+        const int d = ok ? static_cast<int>((key[j] >> sh) & 0xFF) : (kRadix + lane);
+        dig[j] = d;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        const int before = __popc(peers & ((1u << lane) - 1u));
+        int c0 = 0;
+        if (ok) c0 = warp_cnt[warp][d];
+        __syncwarp();
+        if (ok && before == 0) warp_cnt[warp][d] = c0 + __popc(peers);
+        __syncwarp();
+        rank[j] = c0 + before;
+      }
+      __syncthreads();
+      if (tid < kRadix) {
+        int s = carry[tid];
+        for (int w = 0; w < kSortWarps; ++w) {
+          int c = warp_cnt[w][tid];
+          warp_cnt[w][tid] = s;
+          s += c;
+        }
+        carry[tid] = s;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kSortItems; ++j) {
+        const int idx = base + warp * (32 * kSortItems) + j * 32 + lane;
+        if (idx < n) dst[warp_cnt[warp][dig[j]] + rank[j]] = key[j];
+      }
+      __syncthreads();
+    }
+    uint64_t* tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+
+  // Phase 2a: id boundaries in the sorted keys.
+  int nseg = 0;
+  for (int base = 0; base < n; base += kSortTile) {
+    int cnt = 0;
+    const int p0 = base + tid * kSortItems;
+#pragma unroll
+    for (int j = 0; j < kSortItems; ++j) {
+      const int q = p0 + j;
+      if (q < n && (q == 0 || (src[q] >> 32) != (src[q - 1] >> 32))) ++cnt;
+    }
+    int tot;
+    int s = nseg + block_excl_scan(cnt, sh_warp, &tot);
+#pragma unroll
+    for (int j = 0; j < kSortItems; ++j) {
+      const int q = p0 + j;
+      if (q < n && (q == 0 || (src[q] >> 32) != (src[q - 1] >> 32))) seg_start[s++] = q;
+    }
+    nseg += tot;
+  }
+  if (tid == 0) seg_start[nseg] = n;
+  __syncthreads();
+
+  // Phase 2b: runs of kEmbedBwdChunk tokens per id; slots for multi-run ids.
+  int run_base = 0, mseg_base = 0, slot_base = 0;
+  for (int base = 0; base < nseg; base += kSortThreads) {
+    const int s = base + tid;
+    int len = 0, nr = 0;
+    if (s < nseg) {
+      len = seg_start[s + 1] - seg_start[s];
+      nr = (len + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+    }
+    const int multi = nr > 1 ? 1 : 0;
+    int t_runs, t_mseg, t_slots;
+    const int r0 = run_base + block_excl_scan(nr, sh_warp, &t_runs);
+    const int m0 = mseg_base + block_excl_scan(multi, sh_warp, &t_mseg);
+    const int q0 = slot_base + block_excl_scan(multi ? nr : 0, sh_warp, &t_slots);
+    if (s < nseg) {
+      const int st = seg_start[s];
+      const int en = seg_start[s + 1];
+      const int id = static_cast<int>(src[st] >> 32);
+      for (int j = 0; j < nr; ++j) {
+        RunDesc r;
+        r.start = st + j * kEmbedBwdChunk;
+        r.end = min(en, st + (j + 1) * kEmbedBwdChunk);
+        r.id = id;
+        r.slot = multi ? q0 + j : -1;
+        r.mseg = multi ? m0 : -1;
+        r.nruns = nr;
+        r.first_slot = multi ? q0 : -1;
+        r.pad = 0;
+        runs[r0 + j] = r;
+      }
+      if (multi)
+        for (int hh = 0; hh < nh; ++hh) counters[m0 * nh + hh] = 0;
+    }
+    run_base += t_runs;
+    mseg_base += t_mseg;
+    slot_base += t_slots;
+  }
+  if (tid == 0) {
+    hdr[0] = n;
+    hdr[1] = run_base;
+    hdr[2] = nseg;
+    hdr[3] = mseg_base;
+    hdr[4] = slot_base;
+    hdr[5] = (src == keys_a) ? 0 : 1;   // which buffer holds the sorted keys
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward, step 2: persistent segmented reduction. Work item = (run, column
+// slice of 128 threads x 16 bytes).
+// ---------------------------------------------------------------------------
+template <typename TE>
+__device__ __forceinline__ void widen(const uint4& v, float (&o)[16 / sizeof(TE)]);
+template <>
+__device__ __forceinline__ void widen<uint16_t>(const uint4& v, float (&o)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __uint_as_float(w[i] << 16);
+    o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+template <>
+__device__ __forceinline__ void widen<float>(const uint4& v, float (&o)[4]) {
+  o[0] = __uint_as_float(v.x);
+  o[1] = __uint_as_float(v.y);
+  o[2] = __uint_as_float(v.z);
+  o[3] = __uint_as_float(v.w);
+}
+
+template <typename TE>
+__global__ void __launch_bounds__(128)
+    embed_reduce_kernel(const int32_t* __restrict__ hdr, const uint64_t* __restrict__ keys_a,
+                        const uint64_t* __restrict__ keys_b, const RunDesc* __restrict__ runs,
+                        const TE* __restrict__ dE, float* __restrict__ dW, float* partials, int32_t* counters,
+                        int H, int nh) {
+  constexpr int VEC = 16 / sizeof(TE);
+  constexpr int U = 8;   // rows loaded ahead of the sequential adds
+  __shared__ int s_last;
+  const uint64_t* keys = hdr[5] ? keys_b : keys_a;
+  const int n_items = hdr[1] * nh;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int r = item / nh, hs = item - r * nh;
+    const RunDesc rd = runs[r];
+    const int col = hs * 128 * VEC + static_cast<int>(threadIdx.x) * VEC;
+    const bool active = col < H;
+    float acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+    for (int p = rd.start; p < rd.end; p += U) {
+      uint4 v[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        v[k] = make_uint4(0, 0, 0, 0);
+        if (active && p + k < rd.end) {
+          const int64_t t = static_cast<int64_t>(keys[p + k] & 0xFFFFFFFFull);
+          v[k] = __ldg(reinterpret_cast<const uint4*>(dE + t * H + col));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        if (p + k < rd.end) {          // tokens in ascending t, one add each
+          float f[VEC];
+          widen<TE>(v[k], f);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[e] = acc[e] + f[e];
+        }
+      }
+    }
+    if (rd.slot < 0) {
+      if (active) {
+        float4* row = reinterpret_cast<float4*>(dW + static_cast<int64_t>(rd.id) * H + col);
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+          float4 w = row[q];
+          w.x = w.x + acc[4 * q + 0];
+          w.y = w.y + acc[4 * q + 1];
+          w.z = w.z + acc[4 * q + 2];
+          w.w = w.w + acc[4 * q + 3];
+          row[q] = w;
+        }
+      }
+    } else {
+      if (active) {
+        float4* slot = reinterpret_cast<float4*>(partials + static_cast<int64_t>(rd.slot) * H + col);
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q)
+          __stcg(slot + q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const int prev = atomicAdd(&counters[rd.mseg * nh + hs], 1);
+        s_last = (prev == rd.nruns - 1) ? 1 : 0;
+        __threadfence();
+      }
+      __syncthreads();
+      if (s_last && active) {
+        // Last run of this id to finish: add the run sums left to right.
+        float tot[VEC];
+        const float4* s0 = reinterpret_cast<const float4*>(partials + static_cast<int64_t>(rd.first_slot) * H + col);
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+          float4 a = __ldcg(s0 + q);
+          tot[4 * q] = a.x; tot[4 * q + 1] = a.y; tot[4 * q + 2] = a.z; tot[4 * q + 3] = a.w;
+        }
+        for (int j = 1; j < rd.nruns; ++j) {
+          const float4* sj =
+              reinterpret_cast<const float4*>(partials + static_cast<int64_t>(rd.first_slot + j) * H + col);
+#pragma unroll
+          for (int q = 0; q < VEC / 4; ++q) {
+            float4 a = __ldcg(sj + q);
+            tot[4 * q] = tot[4 * q] + a.x;
+            tot[4 * q + 1] = tot[4 * q + 1] + a.y;
+            tot[4 * q + 2] = tot[4 * q + 2] + a.z;
+            tot[4 * q + 3] = tot[4 * q + 3] + a.w;
+          }
+        }
+        float4* row = reinterpret_cast<float4*>(dW + static_cast<int64_t>(rd.id) * H + col);
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+          float4 w = row[q];
+          w.x = w.x + tot[4 * q + 0];
+          w.y = w.y + tot[4 * q + 1];
+          w.z = w.z + tot[4 * q + 2];
+          w.w = w.w + tot[4 * q + 3];
+          row[q] = w;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_embed_fwd(const vce_problem& p, const int64_t* ids, const void* W, void* E, int32_t* owner,
+                             int32_t* local, cudaStream_t st) {
+  if (p.T == 0) return cudaSuccess;
+  const int esize = p.dtype == VCE_BF16 ? 2 : 4;
+  const int row_vecs = static_cast<int>(p.H * esize / 16);
+  const int64_t blocks = ceil_div(p.T, kGatherWarps);
+  embed_gather_kernel<<<static_cast<unsigned>(blocks), kGatherWarps * 32, 0, st>>>(
+      ids, static_cast<const uint4*>(W), static_cast<uint4*>(E), owner, local, p.T, p.Vp, p.V_real, p.S,
+      row_vecs);
+  note_launch(VCE_K_EMBED_GATHER, st);
+  return cudaGetLastError();
+}
+
+size_t embed_bwd_ws_bytes(const vce_problem& p) { return bwd_layout(p).total; }
+
+cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const void* dE, float* dW, void* ws,
+                             int32_t* status, cudaStream_t st) {
+  (void)status;
+  if (p.T == 0) return cudaSuccess;
+  const BwdLayout L = bwd_layout(p);
+  char* b = static_cast<char*>(ws);
+  int32_t* hdr = reinterpret_cast<int32_t*>(b + L.hdr);
+  uint64_t* ka = reinterpret_cast<uint64_t*>(b + L.keys_a);
+  uint64_t* kb = reinterpret_cast<uint64_t*>(b + L.keys_b);
+  int32_t* seg = reinterpret_cast<int32_t*>(b + L.seg_start);
+  RunDesc* runs = reinterpret_cast<RunDesc*>(b + L.runs);
+  int32_t* counters = reinterpret_cast<int32_t*>(b + L.counters);
+  float* partials = reinterpret_cast<float*>(b + L.partials);
+  embed_sort_kernel<<<1, kSortThreads, 0, st>>>(ids, p.T, p.V_real, L.nh, hdr, ka, kb, seg, runs, counters);
+  note_launch(VCE_K_EMBED_SORT, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const DevInfo di = current_device_info();
+  const int grid = di.num_sms * 8;
+  if (p.dtype == VCE_BF16)
+    embed_reduce_kernel<uint16_t><<<grid, 128, 0, st>>>(hdr, ka, kb, runs, static_cast<const uint16_t*>(dE), dW,
+                                                        partials, counters, static_cast<int>(p.H), L.nh);
+  else
+    embed_reduce_kernel<float><<<grid, 128, 0, st>>>(hdr, ka, kb, runs, static_cast<const float*>(dE), dW,
+                                                     partials, counters, static_cast<int>(p.H), L.nh);
+  note_launch(VCE_K_EMBED_REDUCE, st);
+  return cudaGetLastError();
+}
+
+}  // namespace vce

@@ -1,0 +1,104 @@
+// Internal declarations shared by the translation units of libvocabce.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/vce.h"
+
+namespace vce {
+
+constexpr int kEmbedBwdChunk = 32;      // run length of the embedding backward's order
+constexpr int kTcUnitWidth = 2048;      // vocab columns per forward work unit (tensor cores)
+constexpr int kSimtUnitWidth = 256;     // vocab columns per forward work unit (fp32 SIMT)
+constexpr size_t kWsAlign = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Shard owning a row id in [0, Vp): the largest k with floor(k*Vp/S) <= id,
+// i.e. ceil((id+1)*S/Vp) - 1.
+__host__ __device__ inline int32_t shard_of(int64_t id, int64_t Vp, int32_t S) {
+  return static_cast<int32_t>(((id + 1) * static_cast<int64_t>(S) + Vp - 1) / Vp - 1);
+}
+__host__ __device__ inline int64_t shard_lo(int64_t k, int64_t Vp, int32_t S) { return (k * Vp) / S; }
+
+// Forward work units: each shard is cut into `ups` units of `uw` columns
+// (the last one of a shard may be shorter or empty).
+struct UnitGrid {
+  int32_t uw, ups, n_units;
+};
+inline UnitGrid unit_grid(const vce_problem& p, int uw) {
+  int64_t max_rows = ceil_div(p.Vp, p.S);
+  int32_t ups = static_cast<int32_t>(ceil_div(max_rows, uw));
+  if (ups < 1) ups = 1;
+  return UnitGrid{uw, ups, static_cast<int32_t>(ups * static_cast<int64_t>(p.S))};
+}
+
+// Device-side view of a problem (plain values, passed by value to kernels).
+struct ProbDev {
+  int32_t T, H, Vp, V_real, S;
+  int64_t ignore_index;
+};
+inline ProbDev prob_dev(const vce_problem& p) {
+  return ProbDev{static_cast<int32_t>(p.T), static_cast<int32_t>(p.H), static_cast<int32_t>(p.Vp),
+                 static_cast<int32_t>(p.V_real), p.S, p.ignore_index};
+}
+
+struct DevInfo {
+  int device = -1;
+  int num_sms = 0;
+};
+DevInfo current_device_info();
+uint64_t wait_limit_ns();
+// Called after every kernel launch: counts it and, when a table is installed,
+// records the next timing event on `st` (see vce_set_launch_events).
+void note_launch(int kind, cudaStream_t st);
+
+// Encodes a row-major 2-D tensor map (driver entry point fetched at run time).
+// rows x cols elements of `esize` bytes, row stride `ld` elements.
+bool make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t cols,
+                  uint64_t rows, uint64_t ld, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+
+// ---------------------------------------------------------------------------
+// Launchers. Each returns cudaSuccess or the launch error.
+// ---------------------------------------------------------------------------
+cudaError_t launch_embed_fwd(const vce_problem& p, const int64_t* ids, const void* W, void* E, int32_t* owner,
+                             int32_t* local, cudaStream_t st);
+
+size_t embed_bwd_ws_bytes(const vce_problem& p);
+cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const void* dE, float* dW, void* ws,
+                             int32_t* status, cudaStream_t st);
+
+// Merge of the forward partials into lse, per-token loss and the mean.
+cudaError_t launch_merge(const ProbDev& pd, const UnitGrid& ug, const int64_t* targets, const float2* part,
+                         const float* ztgt, float* lse, float* token_loss, int32_t* target_owner,
+                         int32_t* max_owner, float* block_sums, float* loss, int32_t* status, cudaStream_t st);
+int merge_blocks(int64_t T);
+cudaError_t launch_count_valid(const ProbDev& pd, const int64_t* targets, int32_t* n_valid, int32_t* status,
+                               cudaStream_t st);
+
+// fp32 SIMT path.
+cudaError_t launch_simt_fwd(const ProbDev& pd, const UnitGrid& ug, const float* h, const float* W,
+                            const int64_t* targets, float2* part, float* ztgt, cudaStream_t st);
+cudaError_t launch_simt_grad(const ProbDev& pd, const float* h, const float* W, const int64_t* targets,
+                             const float* lse, const int32_t* n_valid, float g, int v0, int vc, float* G,
+                             cudaStream_t st);
+// C[M,N] = beta*C + sum_k A(m,k) B(k,n), A(m,k) = A[m*sam + k*sak], B(k,n) = B[k*sbk + n*sbn],
+// C row-major with leading dimension ldc. beta is 0 or 1.
+cudaError_t launch_sgemm(int M, int N, int K, const float* A, int64_t sam, int64_t sak, const float* B,
+                         int64_t sbk, int64_t sbn, float* C, int64_t ldc, int beta, cudaStream_t st);
+
+// bf16 tensor-core path.
+cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* h, const void* W,
+                          const int64_t* targets, float2* part, float* ztgt, int32_t* status, cudaStream_t st);
+cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void* W, const int64_t* targets,
+                                const float* lse, const int32_t* n_valid, float g, int v0, int vc_act,
+                                void* G, int g_ld, float* dH, bool dH_accumulate, float* dW, bool dW_accumulate,
+                                int32_t* status, cudaStream_t st);
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t st);
+
+}  // namespace vce

@@ -1,0 +1,623 @@
+// bf16 cross-entropy on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// One persistent, warp-specialised kernel template serves the four
+// contractions of the loss ("Vocabulary shards: look up locally and normalize
+// globally", paragraphs 3-5):
+//   FWD   z = h W^T per (128-token block, work unit inside one shard): the
+//         epilogue keeps a running maximum and sum of exp per token over the
+//         unit's real columns (padded classes >= V_real never count) and picks
+//         the target logit from the one tile that owns it. Logits stay in TMEM.
+//   GRAD  z recomputed per 128 x 256 tile; the epilogue forms
+//         G = (exp(z - lse) - [v == y]) * g / N_valid in bf16 and stores it.
+//   DH    dH (+)= G W      (A = G K-major, B = W rows as an MN-major operand)
+//   DW    dW (+)= G^T h    (A = G^T and B = h, both MN-major operands)
+//
+// Roles (192 threads): warp 0 issues TMA loads into a 4-stage shared-memory
+// ring; warp 1 allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
+// and one lane issues tcgen05.mma; warps 2-5 drain TMEM with tcgen05.ld (warp
+// w reads TMEM lanes 32*(w%4)..+31, i.e. one token row per thread). Every wait
+// is bounded: on a timeout the CTA raises a shared abort flag, records
+// VCE_ERR_TIMEOUT, drains what it has in flight and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace vce {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr uint32_t kBBytes = BN * BK * 2;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kAtomBytes = 64 * 128;        // 64 rows of 128 B: one MN-major atom column
+constexpr uint32_t kStagingPerWarp = 2 * 4096;   // two 32-row x 128-B TMA store boxes
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum Mode : int { MODE_FWD = 0, MODE_GRAD = 1, MODE_DH = 2, MODE_DW = 3 };
+
+template <int MODE>
+struct Traits {
+  static constexpr uint32_t a_mn = (MODE == MODE_DW) ? 1u : 0u;
+  static constexpr uint32_t b_mn = (MODE == MODE_DH || MODE == MODE_DW) ? 1u : 0u;
+  static constexpr bool staging = MODE != MODE_FWD;
+  static constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn, b_mn);
+};
+
+template <int MODE>
+constexpr size_t smem_bytes() {
+  return 1024 + size_t(kStages) * kStageBytes + (Traits<MODE>::staging ? 4 * kStagingPerWarp : 0) + 256;
+}
+
+struct TcArgs {
+  ProbDev pd;
+  const int64_t* targets;
+  int n_items;
+  int n_mblk;
+  int n_nblk;
+  int num_kb;
+  UnitGrid ug;
+  float2* part;
+  float* ztgt;
+  const float* lse;
+  const int32_t* n_valid;
+  float g;
+  int v0;
+  int vc;
+  int out_row0;
+  int accumulate;
+  int32_t* status;
+  uint64_t limit_ns;
+};
+
+// Columns [vb, vlim) of forward work unit u, and its number of 256-wide tiles.
+struct UnitSpan {
+  int64_t vb, vlim;
+  int ntiles;
+};
+__device__ __forceinline__ UnitSpan unit_span(const TcArgs& a, int u) {
+  const int k = u / a.ug.ups, j = u - k * a.ug.ups;
+  const int64_t lo = shard_lo(k, a.pd.Vp, a.pd.S), hi = shard_lo(k + 1, a.pd.Vp, a.pd.S);
+  UnitSpan s;
+  s.vb = lo + static_cast<int64_t>(j) * a.ug.uw;
+  int64_t ve = s.vb + a.ug.uw;
+  if (ve > hi) ve = hi;
+  s.vlim = ve < a.pd.V_real ? ve : a.pd.V_real;
+  s.ntiles = s.vlim > s.vb ? static_cast<int>((s.vlim - s.vb + BN - 1) / BN) : 0;
+  return s;
+}
+
+template <int MODE>
+__device__ __forceinline__ int item_tiles(const TcArgs& a, int item) {
+  if constexpr (MODE == MODE_FWD) {
+    return unit_span(a, item / a.n_mblk).ntiles;
+  } else {
+    return 1;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void issue_loads(const TcArgs& a, const CUtensorMap* mA, const CUtensorMap* mB,
+                                            uint32_t sA, uint32_t sB, uint64_t* bar, int item, int tt, int kb) {
+  const int k0 = kb * BK;
+  if constexpr (MODE == MODE_FWD) {
+    const int m_blk = item % a.n_mblk;
+    const UnitSpan us = unit_span(a, item / a.n_mblk);
+    tma_load_2d(sA, mA, bar, k0, m_blk * BM);
+    tma_load_2d(sB, mB, bar, k0, static_cast<int32_t>(us.vb + static_cast<int64_t>(tt) * BN));
+  } else if constexpr (MODE == MODE_GRAD) {
+    const int m_blk = item % a.n_mblk, n_blk = item / a.n_mblk;
+    tma_load_2d(sA, mA, bar, k0, m_blk * BM);
+    tma_load_2d(sB, mB, bar, k0, a.v0 + n_blk * BN);
+  } else if constexpr (MODE == MODE_DH) {
+    const int n_blk = item % a.n_nblk, m_blk = item / a.n_nblk;
+    tma_load_2d(sA, mA, bar, k0, m_blk * BM);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tma_load_2d(sB + b * kAtomBytes, mB, bar, n_blk * BN + 64 * b, a.v0 + k0);
+  } else {
+    const int n_blk = item % a.n_nblk, m_blk = item / a.n_nblk;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) tma_load_2d(sA + b * kAtomBytes, mA, bar, m_blk * BM + 64 * b, k0);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tma_load_2d(sB + b * kAtomBytes, mB, bar, n_blk * BN + 64 * b, k0);
+  }
+}
+
+__device__ __forceinline__ float select32(const uint32_t (&x)[32], int idx) {
+  float r = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j == idx) r = __uint_as_float(x[j]);
+  return r;
+}
+
+// Writes one thread's 128-byte row into a 32-row staging box laid out with
+// the 128-byte swizzle a TMA store expects (16-byte chunk c of row r at
+// c ^ (r % 8)).
+__device__ __forceinline__ void stage_row(uint32_t box, int r, const uint32_t (&w)[32]) {
+  const uint32_t row = box + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t addr = row + ((static_cast<uint32_t>(c) ^ static_cast<uint32_t>(r & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * c]), "r"(w[4 * c + 1]),
+                 "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
+                 : "memory");
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_loss_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapOut, const TcArgs a) {
+  using Tr = Traits<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t stage0 = base;
+  const uint32_t staging0 = base + kStages * kStageBytes;
+  uint8_t* tail = gbase + kStages * kStageBytes + (Tr::staging ? 4 * kStagingPerWarp : 0);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tail);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 4);
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const WaitCtx wc{s_abort, a.status, a.limit_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_desc(&mapA);
+      tma_prefetch_desc(&mapB);
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_parity[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+        const int nt = item_tiles<MODE>(a, item);
+        for (int tt = 0; ok && tt < nt; ++tt) {
+          for (int kb = 0; kb < a.num_kb; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            const uint32_t sA = stage0 + stage * kStageBytes;
+            issue_loads<MODE>(a, &mapA, &mapB, sA, sA + kABytes, &full[stage], item, tt, kb);
+            last_parity[stage] = static_cast<int>(phase);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA's memory goes away.
+        const WaitCtx drain_wc{s_abort, nullptr, 100000000ull};
+        int dummy = 0;
+        for (int s = 0; s < kStages; ++s) {
+          if (last_parity[s] < 0) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&full[s], static_cast<uint32_t>(last_parity[s])) &&
+                 globaltimer_ns() - t0 < drain_wc.limit_ns)
+            ++dummy;
+        }
+        (void)dummy;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t tile_count = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+        const int nt = item_tiles<MODE>(a, item);
+        for (int tt = 0; ok && tt < nt; ++tt) {
+          const uint32_t acc = tile_count & 1u;
+          if (!mbar_wait(&tempty[acc], ((tile_count >> 1) & 1u) ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + acc * BN;
+          for (int kb = 0; kb < a.num_kb; ++kb) {
+            if (!mbar_wait(&full[stage], phase, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sA = stage0 + stage * kStageBytes;
+            const uint32_t sB = sA + kABytes;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              uint64_t ad, bd;
+              if constexpr (Tr::a_mn) {
+                ad = smem_desc_sw128(sA + kk * 2048u, kAtomBytes, 1024u);
+              } else {
+                ad = smem_desc_sw128(sA + kk * 32u, 16u, 1024u);
+              }
+              if constexpr (Tr::b_mn) {
+                bd = smem_desc_sw128(sB + kk * 2048u, kAtomBytes, 1024u);
+              } else {
+                bd = smem_desc_sw128(sB + kk * 32u, 16u, 1024u);
+              }
+              umma_f16(d, ad, bd, Tr::idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            issued = true;
+            umma_commit(&empty[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&tfull[acc]);
+          ++tile_count;
+        }
+      }
+      if (!ok && issued) {
+        // Wait for the MMAs in flight before TMEM is released.
+        umma_commit(drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 ----------------
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;      // row of the tile held by this thread
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t my_staging = staging0 + static_cast<uint32_t>(warp - 2) * kStagingPerWarp;
+    uint32_t box_count = 0;
+    uint32_t tile_count = 0;
+    bool ok = true;
+    float scale = 0.0f;
+    if constexpr (MODE == MODE_GRAD) {
+      const int nv = a.n_valid[0];
+      scale = nv > 0 ? a.g / static_cast<float>(nv) : 0.0f;
+    }
+    for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+      if constexpr (MODE == MODE_FWD) {
+        const int m_blk = item % a.n_mblk, u = item / a.n_mblk;
+        const UnitSpan us = unit_span(a, u);
+        const int t = m_blk * BM + r;
+        const bool row_ok = t < a.pd.T;
+        const int64_t y = row_ok ? a.targets[t] : -1;
+        float m_run = -INFINITY, s_run = 0.0f, zt = 0.0f;
+        bool have_zt = false;
+        for (int tt = 0; tt < us.ntiles; ++tt) {
+          const uint32_t acc = tile_count & 1u;
+          if (!mbar_wait(&tfull[acc], (tile_count >> 1) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int64_t vt0 = us.vb + static_cast<int64_t>(tt) * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t x[32];
+            tmem_ld_32x32b_x32(lane_base + acc * BN + c * 32, x);
+            tmem_ld_wait();
+            const int64_t vc0 = vt0 + c * 32;
+            int64_t nval64 = us.vlim - vc0;
+            const int nval = nval64 >= 32 ? 32 : (nval64 <= 0 ? 0 : static_cast<int>(nval64));
+            if (nval == 0) continue;
+            if (y >= vc0 && y < vc0 + nval) {
+              zt = select32(x, static_cast<int>(y - vc0));
+              have_zt = true;
+            }
+            float cm = -INFINITY;
+            if (nval == 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) cm = fmaxf(cm, __uint_as_float(x[j]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nval) cm = fmaxf(cm, __uint_as_float(x[j]));
+            }
+            const float mn = fmaxf(m_run, cm);
+            const float mL = mn * kLog2e;
+            float sum = 0.0f;
+            if (nval == 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) sum += ex2_approx(fmaf(__uint_as_float(x[j]), kLog2e, -mL));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nval) sum += ex2_approx(fmaf(__uint_as_float(x[j]), kLog2e, -mL));
+            }
+            s_run = s_run * ex2_approx((m_run - mn) * kLog2e) + sum;
+            m_run = mn;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
+          ++tile_count;
+        }
+        if (!ok) break;
+        if (row_ok) {
+          a.part[static_cast<int64_t>(t) * a.ug.n_units + u] = make_float2(m_run, s_run);
+          if (have_zt) a.ztgt[t] = zt;
+        }
+      } else {
+        int m_blk, n_blk, row0, col0;
+        if constexpr (MODE == MODE_GRAD) {
+          m_blk = item % a.n_mblk;
+          n_blk = item / a.n_mblk;
+          row0 = m_blk * BM;
+          col0 = n_blk * BN;   // chunk-local column
+        } else {
+          n_blk = item % a.n_nblk;
+          m_blk = item / a.n_nblk;
+          row0 = (MODE == MODE_DW ? a.out_row0 : 0) + m_blk * BM;
+          col0 = n_blk * BN;
+        }
+        const uint32_t acc = tile_count & 1u;
+        if (!mbar_wait(&tfull[acc], (tile_count >> 1) & 1u, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if constexpr (MODE == MODE_GRAD) {
+          const int t = m_blk * BM + r;
+          int64_t y = -1;
+          float lseL = 0.0f;
+          bool row_ok = false;
+          if (t < a.pd.T) {
+            y = a.targets[t];
+            row_ok = (y >= 0) && (y < a.pd.V_real);
+            lseL = a.lse[t] * kLog2e;
+          }
+          const int64_t vt0 = static_cast<int64_t>(a.v0) + col0;
+#pragma unroll 1
+          for (int b = 0; b < BN / 64; ++b) {
+            uint32_t w[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint32_t x[32];
+              tmem_ld_32x32b_x32(lane_base + acc * BN + b * 64 + half * 32, x);
+              tmem_ld_wait();
+              const int64_t vc0 = vt0 + b * 64 + half * 32;
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                float g0 = 0.0f, g1 = 0.0f;
+                if (row_ok) {
+                  const int64_t v = vc0 + j;
+                  if (v < a.pd.V_real) g0 = ex2_approx(fmaf(__uint_as_float(x[j]), kLog2e, -lseL)) * scale;
+                  if (v + 1 < a.pd.V_real) g1 = ex2_approx(fmaf(__uint_as_float(x[j + 1]), kLog2e, -lseL)) * scale;
+                  if (v == y) g0 -= scale;
+                  if (v + 1 == y) g1 -= scale;
+                }
+                w[half * 16 + j / 2] = pack_bf16x2(g0, g1);
+              }
+            }
+            if (b == BN / 64 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            const uint32_t box = my_staging + (box_count & 1u) * 4096u;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            stage_row(box, lane, w);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&mapOut, box, col0 + b * 64, row0 + q * 32);
+              bulk_commit();
+            }
+            ++box_count;
+          }
+        } else {
+#pragma unroll 1
+          for (int b = 0; b < BN / 32; ++b) {
+            uint32_t x[32];
+            tmem_ld_32x32b_x32(lane_base + acc * BN + b * 32, x);
+            tmem_ld_wait();
+            if (b == BN / 32 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            const uint32_t box = my_staging + (box_count & 1u) * 4096u;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            stage_row(box, lane, x);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (a.accumulate)
+                tma_reduce_add_2d(&mapOut, box, col0 + b * 32, row0 + q * 32);
+              else
+                tma_store_2d(&mapOut, box, col0 + b * 32, row0 + q * 32);
+              bulk_commit();
+            }
+            ++box_count;
+          }
+        }
+        ++tile_count;
+      }
+    }
+    if constexpr (Tr::staging) {
+      if (lane == 0) bulk_wait<0>();
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Bounded-wait self-test: one block waits on a barrier nothing completes.
+__global__ void wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtx wc{&abort_flag, status, limit_ns};
+    (void)mbar_wait(&bar, 0, wc);
+  }
+  __syncthreads();
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mO, const TcArgs& a,
+                        cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(tc_loss_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<MODE>()));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  if (a.n_items <= 0) return cudaSuccess;
+  const DevInfo di = current_device_info();
+  const int grid = a.n_items < di.num_sms ? a.n_items : di.num_sms;
+  tc_loss_kernel<MODE><<<grid, kThreads, smem_bytes<MODE>(), st>>>(mA, mB, mO, a);
+  note_launch(VCE_K_TC_FWD + MODE, st);
+  return cudaGetLastError();
+}
+
+TcArgs base_args(const vce_problem& p, const int64_t* targets, int32_t* status) {
+  TcArgs a{};
+  a.pd = prob_dev(p);
+  a.targets = targets;
+  a.status = status;
+  a.limit_ns = wait_limit_ns();
+  return a;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* h, const void* W,
+                          const int64_t* targets, float2* part, float* ztgt, int32_t* status, cudaStream_t st) {
+  CUtensorMap mh, mw;
+  if (!make_tmap_2d(&mh, h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, p.T, p.H, 64, BM, true) ||
+      !make_tmap_2d(&mw, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, p.V_real, p.H, 64, BN, true))
+    return cudaErrorInvalidValue;
+  TcArgs a = base_args(p, targets, status);
+  a.n_mblk = static_cast<int>(ceil_div(p.T, BM));
+  a.n_items = a.n_mblk * ug.n_units;
+  a.num_kb = static_cast<int>(ceil_div(p.H, BK));
+  a.ug = ug;
+  a.part = part;
+  a.ztgt = ztgt;
+  return launch_mode<MODE_FWD>(mh, mw, mh, a, st);
+}
+
+cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void* W, const int64_t* targets,
+                                const float* lse, const int32_t* n_valid, float g, int v0, int vc_act, void* G,
+                                int g_ld, float* dH, bool dH_accumulate, float* dW, bool dW_accumulate,
+                                int32_t* status, cudaStream_t st) {
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  cudaError_t e;
+  // GRAD: G[:, 0:vc_act] for vocabulary columns [v0, v0 + vc_act).
+  {
+    CUtensorMap mh, mw, mg;
+    if (!make_tmap_2d(&mh, h, BF, 2, p.H, p.T, p.H, 64, BM, true) ||
+        !make_tmap_2d(&mw, W, BF, 2, p.H, p.V_real, p.H, 64, BN, true) ||
+        !make_tmap_2d(&mg, G, BF, 2, vc_act, p.T, g_ld, 64, 32, true))
+      return cudaErrorInvalidValue;
+    TcArgs a = base_args(p, targets, status);
+    a.n_mblk = static_cast<int>(ceil_div(p.T, BM));
+    a.n_nblk = static_cast<int>(ceil_div(vc_act, BN));
+    a.n_items = a.n_mblk * a.n_nblk;
+    a.num_kb = static_cast<int>(ceil_div(p.H, BK));
+    a.lse = lse;
+    a.n_valid = n_valid;
+    a.g = g;
+    a.v0 = v0;
+    a.vc = vc_act;
+    if ((e = launch_mode<MODE_GRAD>(mh, mw, mg, a, st)) != cudaSuccess) return e;
+  }
+  // DH: dH (+)= G[:, 0:vc_act] W[v0:v0+vc_act, :]
+  {
+    CUtensorMap mg, mw, mo;
+    if (!make_tmap_2d(&mg, G, BF, 2, vc_act, p.T, g_ld, 64, BM, true) ||
+        !make_tmap_2d(&mw, W, BF, 2, p.H, p.V_real, p.H, 64, 64, true) ||
+        !make_tmap_2d(&mo, dH, F32, 4, p.H, p.T, p.H, 32, 32, true))
+      return cudaErrorInvalidValue;
+    TcArgs a = base_args(p, targets, status);
+    a.n_mblk = static_cast<int>(ceil_div(p.T, BM));
+    a.n_nblk = static_cast<int>(ceil_div(p.H, BN));
+    a.n_items = a.n_mblk * a.n_nblk;
+    a.num_kb = static_cast<int>(ceil_div(vc_act, BK));
+    a.v0 = v0;
+    a.accumulate = dH_accumulate ? 1 : 0;
+    if ((e = launch_mode<MODE_DH>(mg, mw, mo, a, st)) != cudaSuccess) return e;
+  }
+  // DW: dW[v0:v0+vc_act, :] (+)= G[:, 0:vc_act]^T h
+  {
+    CUtensorMap mg, mh, mo;
+    if (!make_tmap_2d(&mg, G, BF, 2, vc_act, p.T, g_ld, 64, 64, true) ||
+        !make_tmap_2d(&mh, h, BF, 2, p.H, p.T, p.H, 64, 64, true) ||
+        !make_tmap_2d(&mo, dW, F32, 4, p.H, static_cast<uint64_t>(v0) + vc_act, p.H, 32, 32, true))
+      return cudaErrorInvalidValue;
+    TcArgs a = base_args(p, targets, status);
+    a.n_mblk = static_cast<int>(ceil_div(vc_act, BM));
+    a.n_nblk = static_cast<int>(ceil_div(p.H, BN));
+    a.n_items = a.n_mblk * a.n_nblk;
+    a.num_kb = static_cast<int>(ceil_div(p.T, BK));
+    a.out_row0 = v0;
+    a.accumulate = dW_accumulate ? 1 : 0;
+    if ((e = launch_mode<MODE_DW>(mg, mh, mo, a, st)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  note_launch(VCE_K_WAIT_SELFTEST, st);
+  return cudaGetLastError();
+}
+
+}  // namespace vce

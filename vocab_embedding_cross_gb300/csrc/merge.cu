@@ -1,0 +1,190 @@
+// Merge of the forward partials into one maximum and one denominator per token.
+//
+// "Vocabulary shards: look up locally and normalize globally", paragraphs 3-4:
+// the loss needs the global maximum over the valid classes of every shard and
+// one global denominator; the target logit comes from its unique owner. The
+// forward kernels leave, for every (token, work unit) with a unit lying inside
+// one shard, the unit's maximum m_u and its sum s_u = sum exp(z - m_u). Here
+// they are combined with the rescaling rule
+//     (m, s) + (m', s') = (M, s*exp(m - M) + s'*exp(m' - M)),  M = max(m, m'),
+// which equals the page's "subtract the global maximum, sum, combine" schedule
+// (paragraph 4: fused implementations may use other reduction schedules).
+// The loss is then averaged once over the valid tokens ("Sequence-parallel
+// normalization", paragraph 3) with a fixed-order, deterministic reduction.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace vce {
+namespace {
+
+constexpr int kMergeWarps = 8;
+
+__device__ __forceinline__ void combine(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;
+    m = m2;
+  } else {
+    s = s + s2 * expf(m2 - m);
+  }
+}
+
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    merge_kernel(ProbDev pd, UnitGrid ug, const int64_t* __restrict__ targets, const float2* __restrict__ part,
+                 const float* __restrict__ ztgt, float* __restrict__ lse, float* __restrict__ token_loss,
+                 int32_t* __restrict__ target_owner, int32_t* __restrict__ max_owner, float* __restrict__ block_sums,
+                 int32_t* status) {
+  __shared__ float sh_loss[kMergeWarps];
+  __shared__ int sh_cnt[kMergeWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
+  float my_loss = 0.0f;
+  int my_cnt = 0;
+  if (t < pd.T) {
+    float m = -INFINITY, s = 0.0f, bm = -INFINITY;
+    int bu = 0x7FFFFFFF;
+    const float2* row = part + t * ug.n_units;
+    for (int u = lane; u < ug.n_units; u += 32) {
+      const float2 ms = row[u];
+      combine(m, s, ms.x, ms.y);
+      if (ms.x > bm) {          // units ascend with the lane, so the first maximum wins
+        bm = ms.x;
+        bu = u;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      const float bm2 = __shfl_xor_sync(0xffffffffu, bm, o);
+      const int bu2 = __shfl_xor_sync(0xffffffffu, bu, o);
+      // combine in lane order so every lane ends with the same bits
+      if ((lane & o) == 0) {
+        combine(m, s, m2, s2);
+      } else {
+        float mm = m2, ss = s2;
+        combine(mm, ss, m, s);
+        m = mm;
+        s = ss;
+      }
+      if (bm2 > bm || (bm2 == bm && bu2 < bu)) {
+        bm = bm2;
+        bu = bu2;
+      }
+    }
+    if (lane == 0) {
+      const float l = m + logf(s);
+      lse[t] = l;
+      const int64_t y = targets[t];
+      const bool valid = (y >= 0) && (y < pd.V_real);
+      if (!valid && y != pd.ignore_index && status) atomicCAS(status, 0, static_cast<int>(VCE_ERR_BAD_INDEX));
+      const float tl = valid ? (l - ztgt[t]) : 0.0f;
+      if (token_loss) token_loss[t] = tl;
+      if (target_owner) target_owner[t] = valid ? shard_of(y, pd.Vp, pd.S) : -1;
+      if (max_owner) max_owner[t] = (bu < ug.n_units) ? bu / ug.ups : -1;
+      my_loss = tl;
+      my_cnt = valid ? 1 : 0;
+    }
+  }
+  if (lane == 0) {
+    sh_loss[warp] = my_loss;
+    sh_cnt[warp] = my_cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 0.0f;
+    int c = 0;
+    for (int w = 0; w < kMergeWarps; ++w) {
+      a += sh_loss[w];
+      c += sh_cnt[w];
+    }
+    block_sums[2 * blockIdx.x] = a;
+    block_sums[2 * blockIdx.x + 1] = __int_as_float(c);
+  }
+}
+
+// One block: sum of the block partials in block order, then the mean.
+__global__ void __launch_bounds__(1024) loss_mean_kernel(const float* __restrict__ block_sums, int nblocks,
+                                                         float* __restrict__ loss) {
+  __shared__ double sh_a[1024];
+  __shared__ long long sh_c[1024];
+  double a = 0.0;
+  long long c = 0;
+  // contiguous block ranges per thread, then a fixed tree: deterministic
+  const int per = (nblocks + 1023) / 1024;
+  const int b0 = threadIdx.x * per;
+  for (int b = b0; b < min(nblocks, b0 + per); ++b) {
+    a += static_cast<double>(block_sums[2 * b]);
+    c += __float_as_int(block_sums[2 * b + 1]);
+  }
+  sh_a[threadIdx.x] = a;
+  sh_c[threadIdx.x] = c;
+  __syncthreads();
+  for (int o = 512; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      sh_a[threadIdx.x] += sh_a[threadIdx.x + o];
+      sh_c[threadIdx.x] += sh_c[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) loss[0] = sh_c[0] > 0 ? static_cast<float>(sh_a[0] / static_cast<double>(sh_c[0])) : 0.0f;
+}
+
+__global__ void __launch_bounds__(1024) count_valid_kernel(ProbDev pd, const int64_t* __restrict__ targets,
+                                                           int32_t* n_valid, int32_t* status) {
+  __shared__ int sh[32];
+  int c = 0;
+  bool bad = false;
+  for (int64_t t = threadIdx.x; t < pd.T; t += blockDim.x) {
+    const int64_t y = targets[t];
+    const bool v = (y >= 0) && (y < pd.V_real);
+    c += v ? 1 : 0;
+    bad |= (!v && y != pd.ignore_index);
+  }
+  if (bad && status) atomicCAS(status, 0, static_cast<int>(VCE_ERR_BAD_INDEX));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int s = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) s += sh[w];
+    n_valid[0] = s;
+  }
+}
+
+}  // namespace
+
+int merge_blocks(int64_t T) { return static_cast<int>(ceil_div(T, kMergeWarps)); }
+
+cudaError_t launch_merge(const ProbDev& pd, const UnitGrid& ug, const int64_t* targets, const float2* part,
+                         const float* ztgt, float* lse, float* token_loss, int32_t* target_owner,
+                         int32_t* max_owner, float* block_sums, float* loss, int32_t* status, cudaStream_t st) {
+  const int nb = merge_blocks(pd.T);
+  merge_kernel<<<nb, kMergeWarps * 32, 0, st>>>(pd, ug, targets, part, ztgt, lse, token_loss, target_owner,
+                                                 max_owner, block_sums, status);
+  note_launch(VCE_K_MERGE, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  loss_mean_kernel<<<1, 1024, 0, st>>>(block_sums, nb, loss);
+  note_launch(VCE_K_LOSS_MEAN, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_count_valid(const ProbDev& pd, const int64_t* targets, int32_t* n_valid, int32_t* status,
+                               cudaStream_t st) {
+  count_valid_kernel<<<1, 1024, 0, st>>>(pd, targets, n_valid, status);
+  note_launch(VCE_K_COUNT_VALID, st);
+  return cudaGetLastError();
+}
+
+}  // namespace vce

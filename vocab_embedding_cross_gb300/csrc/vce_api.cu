@@ -1,0 +1,316 @@
+// The C ABI of libvocabce: argument checks, workspace layout, tensor-map
+// encoding and the launch sequence of each call. No device memory is
+// allocated here; every buffer comes from the caller.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace vce {
+
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_ev_mu;
+void** g_ev = nullptr;
+int32_t* g_ev_kinds = nullptr;
+int32_t g_ev_cap = 0;
+int32_t* g_ev_count = nullptr;
+}  // namespace
+
+void note_launch(int kind, cudaStream_t st) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  if (g_ev && g_ev_count && *g_ev_count < g_ev_cap) {
+    const int i = (*g_ev_count)++;
+    if (g_ev_kinds) g_ev_kinds[i] = kind;
+    cudaEventRecord(static_cast<cudaEvent_t>(g_ev[i]), st);
+  }
+}
+
+DevInfo current_device_info() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return DevInfo{dev, 148};
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev[dev].device != dev) {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    g_dev[dev] = DevInfo{dev, sms > 0 ? sms : 148};
+  }
+  return g_dev[dev];
+}
+
+bool make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t cols,
+                  uint64_t rows, uint64_t ld, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode || cols == 0 || rows == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * static_cast<uint64_t>(esize)};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+int esize_of(const vce_problem& p) { return p.dtype == VCE_BF16 ? 2 : 4; }
+
+vce_status check_problem(const vce_problem* p) {
+  if (!p) return VCE_ERR_ARG;
+  if (p->reserved != 0) return VCE_ERR_ARG;
+  if (p->dtype != VCE_F32 && p->dtype != VCE_BF16) return VCE_ERR_UNSUPPORTED;
+  if (p->T < 0 || p->H < 1 || p->V_real < 1 || p->S < 1) return VCE_ERR_ARG;
+  if (p->Vp < 64 || p->Vp % 64 != 0) return VCE_ERR_ARG;   // the padded vocabulary must be 64-aligned
+  if (p->V_real > p->Vp || p->S > p->Vp) return VCE_ERR_ARG;
+  if (p->tied_weights != 0 && p->tied_weights != 1) return VCE_ERR_ARG;
+  if (p->T >= (int64_t(1) << 31) || p->Vp >= (int64_t(1) << 31) || p->H > 65536) return VCE_ERR_UNSUPPORTED;
+  if ((p->H * esize_of(*p)) % 16 != 0) return VCE_ERR_UNSUPPORTED;
+  return VCE_OK;
+}
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+vce_status cuda_status(cudaError_t e) { return e == cudaSuccess ? VCE_OK : VCE_ERR_CUDA; }
+
+// ----- workspace layouts -----
+struct FwdLayout {
+  size_t status, part, ztgt, block_sums, total;
+  UnitGrid ug;
+};
+FwdLayout fwd_layout(const vce_problem& p) {
+  FwdLayout L{};
+  L.ug = unit_grid(p, p.dtype == VCE_BF16 ? kTcUnitWidth : kSimtUnitWidth);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, kWsAlign);
+    return o;
+  };
+  L.status = take(16);
+  L.part = take(sizeof(float2) * static_cast<size_t>(p.T) * L.ug.n_units);
+  L.ztgt = take(sizeof(float) * static_cast<size_t>(p.T));
+  L.block_sums = take(sizeof(float) * 2 * static_cast<size_t>(merge_blocks(p.T)));
+  L.total = off;
+  return L;
+}
+
+constexpr size_t kBwdHeader = 256;   // status word, N_valid
+size_t g_esize(const vce_problem& p) { return p.dtype == VCE_BF16 ? 2 : 4; }
+int64_t vocab_cols_cap(const vce_problem& p) { return ceil_div(p.V_real, 256) * 256; }
+size_t bwd_bytes_for(const vce_problem& p, int64_t vc) {
+  return kBwdHeader + align_up(static_cast<size_t>(p.T) * static_cast<size_t>(vc) * g_esize(p), kWsAlign);
+}
+// Column chunk that fits the given workspace (multiple of 256), 0 if none.
+int64_t bwd_chunk_cols(const vce_problem& p, size_t ws_bytes) {
+  if (p.T == 0) return vocab_cols_cap(p);
+  if (ws_bytes < kBwdHeader) return 0;
+  int64_t vc = static_cast<int64_t>((ws_bytes - kBwdHeader) / (static_cast<size_t>(p.T) * g_esize(p)));
+  vc = vc / 256 * 256;
+  const int64_t cap = vocab_cols_cap(p);
+  return vc > cap ? cap : vc;
+}
+int64_t bwd_recommended_cols(const vce_problem& p) {
+  if (p.T == 0) return 256;
+  // about 256 MiB of G per pass
+  int64_t vc = static_cast<int64_t>((size_t(1) << 28) / (static_cast<size_t>(p.T) * g_esize(p)));
+  vc = vc / 256 * 256;
+  if (vc < 256) vc = 256;
+  const int64_t cap = vocab_cols_cap(p);
+  return vc > cap ? cap : vc;
+}
+
+}  // namespace
+}  // namespace vce
+
+using namespace vce;
+
+extern "C" {
+
+const char* vce_status_str(vce_status s) {
+  switch (s) {
+    case VCE_OK: return "VCE_OK";
+    case VCE_ERR_ARG: return "VCE_ERR_ARG: invalid argument or shape";
+    case VCE_ERR_UNSUPPORTED: return "VCE_ERR_UNSUPPORTED: unsupported dtype, alignment or size";
+    case VCE_ERR_CUDA: return "VCE_ERR_CUDA: CUDA call or launch failed";
+    case VCE_ERR_BAD_INDEX: return "VCE_ERR_BAD_INDEX: target outside [0, V_real) and not ignore_index";
+    case VCE_ERR_TIMEOUT: return "VCE_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+    case VCE_ERR_WORKSPACE: return "VCE_ERR_WORKSPACE: workspace missing, too small or misaligned";
+  }
+  return "unknown vce_status";
+}
+
+int32_t vce_embed_bwd_chunk(void) { return kEmbedBwdChunk; }
+uint64_t vce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+void vce_set_launch_events(void** events, int32_t* kinds, int32_t capacity, int32_t* count) {
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  g_ev = events;
+  g_ev_kinds = kinds;
+  g_ev_cap = events ? capacity : 0;
+  g_ev_count = count;
+}
+int32_t vce_version(void) { return 100; }
+void vce_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1, std::memory_order_relaxed); }
+
+size_t vce_workspace_size(const vce_problem* p, int32_t op) {
+  if (check_problem(p) != VCE_OK) return SIZE_MAX;
+  switch (op) {
+    case VCE_OP_EMBED_FWD: return 0;
+    case VCE_OP_EMBED_BWD: return embed_bwd_ws_bytes(*p);
+    case VCE_OP_LOSS_FWD: return fwd_layout(*p).total;
+    case VCE_OP_LOSS_BWD: return bwd_bytes_for(*p, bwd_recommended_cols(*p));
+  }
+  return SIZE_MAX;
+}
+
+size_t vce_workspace_size_min(const vce_problem* p, int32_t op) {
+  if (check_problem(p) != VCE_OK) return SIZE_MAX;
+  if (op == VCE_OP_LOSS_BWD) return bwd_bytes_for(*p, p->T == 0 ? 0 : 256);
+  return vce_workspace_size(p, op);
+}
+
+vce_status vce_embed_fwd(const vce_problem* p, const int64_t* ids, const void* W, void* E, int32_t* owner,
+                         int32_t* local, int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (p->T == 0) return VCE_OK;
+  if (!ids || !W || !E) return VCE_ERR_ARG;
+  if (!aligned(ids, 8) || !aligned(W, 16) || !aligned(E, 16) || !aligned(owner, 4) || !aligned(local, 4))
+    return VCE_ERR_UNSUPPORTED;
+  return cuda_status(launch_embed_fwd(*p, ids, W, E, owner, local, static_cast<cudaStream_t>(stream)));
+}
+
+vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* dE, float* dW, void* ws,
+                         size_t ws_bytes, int32_t* dev_status, void* stream) {
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (p->T == 0) return VCE_OK;
+  if (!ids || !dE || !dW) return VCE_ERR_ARG;
+  if (!aligned(ids, 8) || !aligned(dE, 16) || !aligned(dW, 16)) return VCE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < embed_bwd_ws_bytes(*p)) return VCE_ERR_WORKSPACE;
+  return cuda_status(launch_embed_bwd(*p, ids, dE, dW, ws, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W, const int64_t* targets, float* loss,
+                        float* lse, float* token_loss, int32_t* target_owner, int32_t* max_owner, void* ws,
+                        size_t ws_bytes, int32_t* dev_status, void* stream) {
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (!loss) return VCE_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p->T == 0) return cuda_status(cudaMemsetAsync(loss, 0, sizeof(float), st));
+  if (!h || !W || !targets || !lse) return VCE_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(W, 16) || !aligned(targets, 8) || !aligned(loss, 4) || !aligned(lse, 4) ||
+      !aligned(token_loss, 4) || !aligned(target_owner, 4) || !aligned(max_owner, 4))
+    return VCE_ERR_UNSUPPORTED;
+  const FwdLayout L = fwd_layout(*p);
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < L.total) return VCE_ERR_WORKSPACE;
+  char* b = static_cast<char*>(ws);
+  int32_t* status = dev_status;
+  if (!status) {
+    status = reinterpret_cast<int32_t*>(b + L.status);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return VCE_ERR_CUDA;
+  }
+  float2* part = reinterpret_cast<float2*>(b + L.part);
+  float* ztgt = reinterpret_cast<float*>(b + L.ztgt);
+  float* bsum = reinterpret_cast<float*>(b + L.block_sums);
+  const ProbDev pd = prob_dev(*p);
+  cudaError_t e;
+  if (p->dtype == VCE_BF16)
+    e = launch_tc_fwd(*p, L.ug, h, W, targets, part, ztgt, status, st);
+  else
+    e = launch_simt_fwd(pd, L.ug, static_cast<const float*>(h), static_cast<const float*>(W), targets, part, ztgt,
+                        st);
+  if (e != cudaSuccess) return VCE_ERR_CUDA;
+  return cuda_status(
+      launch_merge(pd, L.ug, targets, part, ztgt, lse, token_loss, target_owner, max_owner, bsum, loss, status, st));
+}
+
+vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, const int64_t* targets,
+                        const float* lse, float g, float* dH, float* dW, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, void* stream) {
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (!dW) return VCE_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t row_bytes = static_cast<size_t>(p->H) * sizeof(float);
+  if (p->T == 0) {
+    if (!p->tied_weights) return cuda_status(cudaMemsetAsync(dW, 0, row_bytes * p->Vp, st));
+    return VCE_OK;
+  }
+  if (!h || !W || !targets || !lse || !dH) return VCE_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(W, 16) || !aligned(targets, 8) || !aligned(lse, 4) || !aligned(dH, 16) ||
+      !aligned(dW, 16))
+    return VCE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, kWsAlign)) return VCE_ERR_WORKSPACE;
+  const int64_t vc = bwd_chunk_cols(*p, ws_bytes);
+  if (vc < 256) return VCE_ERR_WORKSPACE;
+  char* b = static_cast<char*>(ws);
+  int32_t* status = dev_status;
+  int32_t* n_valid = reinterpret_cast<int32_t*>(b + 16);
+  if (!status) {
+    status = reinterpret_cast<int32_t*>(b);
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return VCE_ERR_CUDA;
+  }
+  void* G = b + kBwdHeader;
+  const ProbDev pd = prob_dev(*p);
+  if (launch_count_valid(pd, targets, n_valid, status, st) != cudaSuccess) return VCE_ERR_CUDA;
+  if (!p->tied_weights && p->Vp > p->V_real) {
+    if (cudaMemsetAsync(dW + static_cast<size_t>(p->V_real) * p->H, 0, row_bytes * (p->Vp - p->V_real), st) !=
+        cudaSuccess)
+      return VCE_ERR_CUDA;
+  }
+  for (int64_t c0 = 0; c0 < p->V_real; c0 += vc) {
+    const int vc_act = static_cast<int>((p->V_real - c0) < vc ? (p->V_real - c0) : vc);
+    cudaError_t e;
+    if (p->dtype == VCE_BF16) {
+      e = launch_tc_bwd_chunk(*p, h, W, targets, lse, n_valid, g, static_cast<int>(c0), vc_act, G,
+                              static_cast<int>(vc), dH, c0 > 0, dW, p->tied_weights != 0, status, st);
+    } else {
+      float* Gf = static_cast<float*>(G);
+      const float* hf = static_cast<const float*>(h);
+      const float* Wf = static_cast<const float*>(W);
+      e = launch_simt_grad(pd, hf, Wf, targets, lse, n_valid, g, static_cast<int>(c0), vc_act, Gf, st);
+      if (e == cudaSuccess)   // dH (+)= G W[c0:c0+vc_act]
+        e = launch_sgemm(pd.T, pd.H, vc_act, Gf, vc_act, 1, Wf + c0 * p->H, p->H, 1, dH, p->H, c0 > 0 ? 1 : 0, st);
+      if (e == cudaSuccess)   // dW[c0:c0+vc_act] (+)= G^T h
+        e = launch_sgemm(vc_act, pd.H, pd.T, Gf, 1, vc_act, hf, p->H, 1, dW + c0 * p->H, p->H,
+                         p->tied_weights ? 1 : 0, st);
+    }
+    if (e != cudaSuccess) return VCE_ERR_CUDA;
+  }
+  return VCE_OK;
+}
+
+vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* stream) {
+  if (!dev_status) return VCE_ERR_ARG;
+  return cuda_status(launch_wait_selftest(limit_ns, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

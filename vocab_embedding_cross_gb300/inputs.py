@@ -199,8 +199,9 @@ def make_ids(wl: Workload) -> np.ndarray:
     oor = pos[n_pad:n_pad + n_oor]
     ids[oor[: len(oor) // 2]] = rng.integers(wl.Vp, wl.Vp + 1000, size=len(oor) // 2)
     ids[oor[len(oor) // 2:]] = rng.integers(-1000, -1, size=len(oor) - len(oor) // 2)
-    if n_padrow:
-        ids[pos[n_pad + n_oor:n_pad + n_oor + n_padrow]] = rng.integers(wl.V_real, wl.Vp, size=n_padrow)
+    padrow_pos = pos[n_pad + n_oor:n_pad + n_oor + n_padrow]
+    if len(padrow_pos):
+        ids[padrow_pos] = rng.integers(wl.V_real, wl.Vp, size=len(padrow_pos))
     if T >= 16:
         rep = pos[-min(8, T // 8):]
         ids[rep] = 7
