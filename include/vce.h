@@ -176,6 +176,10 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W,
 /* Static string naming a status code. */
 const char* vce_status_str(vce_status s);
 
+/* Name and text of the CUDA error behind the calling thread's last
+ * VCE_ERR_CUDA ("" if none); static storage, valid until the next call. */
+const char* vce_last_error(void);
+
 /* The run length of the embedding backward's fixed summation order (tokens). */
 int32_t vce_embed_bwd_chunk(void);
 

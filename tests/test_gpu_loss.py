@@ -166,7 +166,7 @@ def test_loss_gpt2_head_full():
     _bwd_check(wl, d, out, TOL["bf16"])
 
 
-def _oracle_rows_all(h, W, y, V_real, rows=256):
+def _oracle_rows_all(h, W, y, V_real, rows=1024):
     """The oracle's per-token quantities for every token, a block of rows at a time."""
     lse = np.empty(h.shape[0])
     tl = np.empty(h.shape[0])

@@ -31,7 +31,10 @@ class VceProblem(ctypes.Structure):
 class VceError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_str(status)}")
+        detail = ""
+        if status == VCE_ERR_CUDA:
+            detail = " (" + lib().vce_last_error().decode() + ")"
+        super().__init__(f"{where}: {status_str(status)}{detail}")
 
 
 _lib = None
@@ -69,6 +72,8 @@ def lib():
         L.vce_set_wait_limit_ns.restype = None
         L.vce_wait_selftest.argtypes = [c_uint64, c_void_p, c_void_p]
         L.vce_wait_selftest.restype = c_int32
+        L.vce_last_error.argtypes = []
+        L.vce_last_error.restype = ctypes.c_char_p
         L.vce_launch_count.argtypes = []
         L.vce_launch_count.restype = c_uint64
         L.vce_set_launch_events.argtypes = [c_void_p, c_void_p, c_int32, c_void_p]

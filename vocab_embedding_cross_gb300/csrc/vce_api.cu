@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -96,7 +97,13 @@ vce_status check_problem(const vce_problem* p) {
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-vce_status cuda_status(cudaError_t e) { return e == cudaSuccess ? VCE_OK : VCE_ERR_CUDA; }
+thread_local char g_last_err[256] = "";
+vce_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return VCE_OK;
+  snprintf(g_last_err, sizeof(g_last_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  cudaGetLastError();
+  return VCE_ERR_CUDA;
+}
 
 // ----- workspace layouts -----
 struct FwdLayout {
@@ -166,6 +173,7 @@ const char* vce_status_str(vce_status s) {
 }
 
 int32_t vce_embed_bwd_chunk(void) { return kEmbedBwdChunk; }
+const char* vce_last_error(void) { return g_last_err; }
 uint64_t vce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 void vce_set_launch_events(void** events, int32_t* kinds, int32_t capacity, int32_t* count) {
   std::lock_guard<std::mutex> lk(g_ev_mu);
@@ -235,7 +243,7 @@ vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W, cons
   int32_t* status = dev_status;
   if (!status) {
     status = reinterpret_cast<int32_t*>(b + L.status);
-    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return VCE_ERR_CUDA;
+    if (cudaError_t me = cudaMemsetAsync(status, 0, sizeof(int32_t), st)) return cuda_status(me);
   }
   float2* part = reinterpret_cast<float2*>(b + L.part);
   float* ztgt = reinterpret_cast<float*>(b + L.ztgt);
@@ -247,7 +255,7 @@ vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W, cons
   else
     e = launch_simt_fwd(pd, L.ug, static_cast<const float*>(h), static_cast<const float*>(W), targets, part, ztgt,
                         st);
-  if (e != cudaSuccess) return VCE_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(
       launch_merge(pd, L.ug, targets, part, ztgt, lse, token_loss, target_owner, max_owner, bsum, loss, status, st));
 }
@@ -276,11 +284,11 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
   int32_t* n_valid = reinterpret_cast<int32_t*>(b + 16);
   if (!status) {
     status = reinterpret_cast<int32_t*>(b);
-    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return VCE_ERR_CUDA;
+    if (cudaError_t me = cudaMemsetAsync(status, 0, sizeof(int32_t), st)) return cuda_status(me);
   }
   void* G = b + kBwdHeader;
   const ProbDev pd = prob_dev(*p);
-  if (launch_count_valid(pd, targets, n_valid, status, st) != cudaSuccess) return VCE_ERR_CUDA;
+  if (cudaError_t ce = launch_count_valid(pd, targets, n_valid, status, st)) return cuda_status(ce);
   if (!p->tied_weights && p->Vp > p->V_real) {
     if (cudaMemsetAsync(dW + static_cast<size_t>(p->V_real) * p->H, 0, row_bytes * (p->Vp - p->V_real), st) !=
         cudaSuccess)
@@ -303,7 +311,7 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
         e = launch_sgemm(vc_act, pd.H, pd.T, Gf, 1, vc_act, hf, p->H, 1, dW + c0 * p->H, p->H,
                          p->tied_weights ? 1 : 0, st);
     }
-    if (e != cudaSuccess) return VCE_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
   }
   return VCE_OK;
 }
