@@ -139,13 +139,16 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
 
-    def step():
-        if wl.tied:
-            dW.zero_()          # the tied gradient buffer starts each step at zero
+    def step_ops():
         vce.vce_embed_fwd(p, ids, W, E, dev_status=st, stream=sp)
         vce.vce_loss_fwd(p, h, W, y, loss, lse, ws=ws_f, dev_status=st, stream=sp)
         vce.vce_loss_bwd(p, h, W, y, lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp)
         vce.vce_embed_bwd(p, ids, dE, dW, ws_e, dev_status=st, stream=sp)
+
+    def step():
+        if wl.tied:
+            dW.zero_()          # the tied gradient buffer starts each step at zero
+        step_ops()
 
     for _ in range(args.warmup):
         step()
@@ -178,32 +181,22 @@ def run_ours(args):
     value = world * T / (ms / 1e3)
 
     # ---- per-launch timing (separate pass, events after every launch) ----
-    cap = 4096
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
-    handles = (ctypes.c_void_p * cap)(*[e.cuda_event for e in evs]) if hasattr(evs[0], "cuda_event") else None
+    # A spin kernel first holds the stream so that every launch below is queued
+    # before the GPU reaches it: the intervals then contain no host gaps. The
+    # tied dW is not re-zeroed here (that memset is not one of our launches).
+    cap = 8192
     per_kind = {}
-    if handles is not None:
-        for e in evs:
-            e.record(stream)            # materialise the events
-        torch.cuda.synchronize()
-        kinds = (ctypes.c_int32 * cap)()
-        count = (ctypes.c_int32 * 1)(0)
-        reps = max(3, min(args.steps, 10))
-        start = torch.cuda.Event(enable_timing=True)
-        vce.vce_set_launch_events(handles, kinds, cap, count)
-        start.record(stream)
-        for _ in range(reps):
-            step()
-        torch.cuda.synchronize()
-        vce.vce_set_launch_events(None, None, 0, None)
-        prev = start
-        for i in range(count[0]):
-            k = vce.KERNEL_KINDS[kinds[i]]
-            dt = prev.elapsed_time(evs[i])
-            tot, n = per_kind.get(k, (0.0, 0))
-            per_kind[k] = (tot + dt, n + 1)
-            prev = evs[i]
-        per_kind = {k: (tot / reps, n // reps) for k, (tot, n) in per_kind.items()}
+    reps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)
+    vce.vce_profile_begin(cap, stream=sp)
+    for _ in range(reps):
+        step_ops()
+    prof = vce.vce_profile_end(cap)
+    for k, dt in prof:
+        tot, n = per_kind.get(k, (0.0, 0))
+        per_kind[k] = (tot + dt, n + 1)
+    per_kind = {k: (tot / reps, n // reps) for k, (tot, n) in per_kind.items()}
 
     # ---- roofline ----
     peaks, peak_src = load_peaks()

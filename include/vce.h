@@ -205,12 +205,18 @@ vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* strea
 /*
  * Launch accounting, for profilers and benchmarks (no counterpart on the
  * pages). Every kernel the library launches increments a process-wide
- * counter. While an event table is installed, each launch is also followed by
- * cudaEventRecord(events[i]) on the launching stream and kinds[i] records which
- * kernel it was (vce_kernel_kind); *count is the number of entries written.
- * Launch i therefore runs between events[i-1] (or an event the caller records
- * before the call) and events[i]. Pass events == NULL to uninstall. The table
- * is host memory owned by the caller; events are cudaEvent_t handles.
+ * counter (vce_launch_count).
+ *
+ * Per-launch timing: vce_profile_begin(capacity, stream) creates `capacity`
+ * timing events (host-side CUDA event objects, no device memory) and records
+ * a start event on `stream`. Until vce_profile_end, every kernel launch made by
+ * the library records the next event on its own stream right after itself.
+ * vce_profile_end waits for the last recorded event, writes for each launch i
+ * its vce_kernel_kind and the milliseconds between event i-1 (the start event
+ * for i = 0) and event i, destroys the events and returns the number of
+ * launches recorded (at most `capacity`, -1 on error). Launches on one stream
+ * run back to back, so each interval is that launch's duration including its
+ * launch gap. Process-wide; not for concurrent callers.
  */
 typedef enum vce_kernel_kind {
   VCE_K_EMBED_GATHER = 0, VCE_K_EMBED_SORT = 1, VCE_K_EMBED_REDUCE = 2,
@@ -219,7 +225,8 @@ typedef enum vce_kernel_kind {
   VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13
 } vce_kernel_kind;
 uint64_t vce_launch_count(void);
-void vce_set_launch_events(void** events, int32_t* kinds, int32_t capacity, int32_t* count);
+vce_status vce_profile_begin(int32_t capacity, void* stream);
+int32_t vce_profile_end(float* ms, int32_t* kinds, int32_t capacity);
 
 #ifdef __cplusplus
 }

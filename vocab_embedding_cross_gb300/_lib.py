@@ -76,8 +76,10 @@ def lib():
         L.vce_last_error.restype = ctypes.c_char_p
         L.vce_launch_count.argtypes = []
         L.vce_launch_count.restype = c_uint64
-        L.vce_set_launch_events.argtypes = [c_void_p, c_void_p, c_int32, c_void_p]
-        L.vce_set_launch_events.restype = None
+        L.vce_profile_begin.argtypes = [c_int32, c_void_p]
+        L.vce_profile_begin.restype = c_int32
+        L.vce_profile_end.argtypes = [c_void_p, c_void_p, c_int32]
+        L.vce_profile_end.restype = c_int32
         _lib = L
     return _lib
 
@@ -172,6 +174,15 @@ def vce_launch_count() -> int:
     return int(lib().vce_launch_count())
 
 
-def vce_set_launch_events(events, kinds, capacity: int, count) -> None:
-    """events: ctypes array of void* (cudaEvent_t); kinds, count: ctypes int32 arrays."""
-    lib().vce_set_launch_events(events, kinds, int(capacity), count)
+def vce_profile_begin(capacity: int, stream=None) -> None:
+    _check(lib().vce_profile_begin(int(capacity), _stream(stream)), "vce_profile_begin")
+
+
+def vce_profile_end(capacity: int):
+    """[(kernel kind name, milliseconds)] for each launch since vce_profile_begin."""
+    ms = (ctypes.c_float * capacity)()
+    kinds = (ctypes.c_int32 * capacity)()
+    n = lib().vce_profile_end(ms, kinds, int(capacity))
+    if n < 0:
+        raise VceError(VCE_ERR_CUDA, "vce_profile_end")
+    return [(KERNEL_KINDS[kinds[i]], float(ms[i])) for i in range(n)]

@@ -27,20 +27,35 @@ uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed
 
 namespace {
 std::atomic<uint64_t> g_launches{0};
-std::mutex g_ev_mu;
-void** g_ev = nullptr;
-int32_t* g_ev_kinds = nullptr;
-int32_t g_ev_cap = 0;
-int32_t* g_ev_count = nullptr;
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+cudaEvent_t g_prof_start = nullptr;
+cudaEvent_t* g_prof_ev = nullptr;
+int32_t* g_prof_kind = nullptr;
+int32_t g_prof_cap = 0;
+int32_t g_prof_n = 0;
+
+void prof_release() {
+  for (int i = 0; i < g_prof_cap; ++i)
+    if (g_prof_ev[i]) cudaEventDestroy(g_prof_ev[i]);
+  if (g_prof_start) cudaEventDestroy(g_prof_start);
+  delete[] g_prof_ev;
+  delete[] g_prof_kind;
+  g_prof_ev = nullptr;
+  g_prof_kind = nullptr;
+  g_prof_start = nullptr;
+  g_prof_cap = g_prof_n = 0;
+  g_prof_on = false;
+}
 }  // namespace
 
 void note_launch(int kind, cudaStream_t st) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  std::lock_guard<std::mutex> lk(g_ev_mu);
-  if (g_ev && g_ev_count && *g_ev_count < g_ev_cap) {
-    const int i = (*g_ev_count)++;
-    if (g_ev_kinds) g_ev_kinds[i] = kind;
-    cudaEventRecord(static_cast<cudaEvent_t>(g_ev[i]), st);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof_on && g_prof_n < g_prof_cap) {
+    g_prof_kind[g_prof_n] = kind;
+    cudaEventRecord(g_prof_ev[g_prof_n], st);
+    ++g_prof_n;
   }
 }
 
@@ -175,12 +190,43 @@ const char* vce_status_str(vce_status s) {
 int32_t vce_embed_bwd_chunk(void) { return kEmbedBwdChunk; }
 const char* vce_last_error(void) { return g_last_err; }
 uint64_t vce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
-void vce_set_launch_events(void** events, int32_t* kinds, int32_t capacity, int32_t* count) {
-  std::lock_guard<std::mutex> lk(g_ev_mu);
-  g_ev = events;
-  g_ev_kinds = kinds;
-  g_ev_cap = events ? capacity : 0;
-  g_ev_count = count;
+vce_status vce_profile_begin(int32_t capacity, void* stream) {
+  if (capacity < 1 || capacity > (1 << 20)) return VCE_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof_on) prof_release();
+  g_prof_ev = new cudaEvent_t[capacity]();
+  g_prof_kind = new int32_t[capacity]();
+  g_prof_cap = capacity;
+  g_prof_n = 0;
+  cudaError_t e = cudaEventCreate(&g_prof_start);
+  for (int i = 0; e == cudaSuccess && i < capacity; ++i) e = cudaEventCreate(&g_prof_ev[i]);
+  if (e == cudaSuccess) e = cudaEventRecord(g_prof_start, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    prof_release();
+    return cuda_status(e);
+  }
+  g_prof_on = true;
+  return VCE_OK;
+}
+
+int32_t vce_profile_end(float* ms, int32_t* kinds, int32_t capacity) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return -1;
+  const int n = g_prof_n;
+  int32_t out = n < capacity ? n : capacity;
+  if (n > 0 && cudaEventSynchronize(g_prof_ev[n - 1]) != cudaSuccess) out = -1;
+  for (int i = 0; out >= 0 && i < out; ++i) {
+    float t = 0.0f;
+    if (cudaEventElapsedTime(&t, i == 0 ? g_prof_start : g_prof_ev[i - 1], g_prof_ev[i]) != cudaSuccess) {
+      out = -1;
+      break;
+    }
+    if (ms) ms[i] = t;
+    if (kinds) kinds[i] = g_prof_kind[i];
+  }
+  prof_release();
+  cudaGetLastError();
+  return out;
 }
 int32_t vce_version(void) { return 100; }
 void vce_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1, std::memory_order_relaxed); }
