@@ -103,30 +103,48 @@ __device__ __forceinline__ int item_tiles(const TcArgs& a, int item) {
   }
 }
 
+// Tile origin: am = first row of A's M range, bn = first index of B's N range
+// (a vocabulary row for FWD/GRAD, an H column for DH/DW). Computed once per
+// tile so that the producer's per-K-block work is only the TMA issue.
+struct TileCoord {
+  int32_t am, bn;
+};
 template <int MODE>
-__device__ __forceinline__ void issue_loads(const TcArgs& a, const CUtensorMap* mA, const CUtensorMap* mB,
-                                            uint32_t sA, uint32_t sB, uint64_t* bar, int item, int tt, int kb) {
-  const int k0 = kb * BK;
+__device__ __forceinline__ TileCoord tile_coord(const TcArgs& a, int item, int tt) {
+  TileCoord c;
   if constexpr (MODE == MODE_FWD) {
     const int m_blk = item % a.n_mblk;
     const UnitSpan us = unit_span(a, item / a.n_mblk);
-    tma_load_2d(sA, mA, bar, k0, m_blk * BM);
-    tma_load_2d(sB, mB, bar, k0, static_cast<int32_t>(us.vb + static_cast<int64_t>(tt) * BN));
+    c.am = m_blk * BM;
+    c.bn = static_cast<int32_t>(us.vb + static_cast<int64_t>(tt) * BN);
   } else if constexpr (MODE == MODE_GRAD) {
     const int m_blk = item % a.n_mblk, n_blk = item / a.n_mblk;
-    tma_load_2d(sA, mA, bar, k0, m_blk * BM);
-    tma_load_2d(sB, mB, bar, k0, a.v0 + n_blk * BN);
-  } else if constexpr (MODE == MODE_DH) {
-    const int n_blk = item % a.n_nblk, m_blk = item / a.n_nblk;
-    tma_load_2d(sA, mA, bar, k0, m_blk * BM);
-#pragma unroll
-    for (int b = 0; b < 4; ++b) tma_load_2d(sB + b * kAtomBytes, mB, bar, n_blk * BN + 64 * b, a.v0 + k0);
+    c.am = m_blk * BM;
+    c.bn = a.v0 + n_blk * BN;
   } else {
     const int n_blk = item % a.n_nblk, m_blk = item / a.n_nblk;
+    c.am = m_blk * BM;
+    c.bn = n_blk * BN;
+  }
+  return c;
+}
+
+template <int MODE>
+__device__ __forceinline__ void issue_loads(const TcArgs& a, const CUtensorMap* mA, const CUtensorMap* mB,
+                                            uint32_t sA, uint32_t sB, uint64_t* bar, TileCoord c, int kb) {
+  const int k0 = kb * BK;
+  if constexpr (MODE == MODE_FWD || MODE == MODE_GRAD) {
+    tma_load_2d(sA, mA, bar, k0, c.am);
+    tma_load_2d(sB, mB, bar, k0, c.bn);
+  } else if constexpr (MODE == MODE_DH) {
+    tma_load_2d(sA, mA, bar, k0, c.am);
 #pragma unroll
-    for (int b = 0; b < 2; ++b) tma_load_2d(sA + b * kAtomBytes, mA, bar, m_blk * BM + 64 * b, k0);
+    for (int b = 0; b < 4; ++b) tma_load_2d(sB + b * kAtomBytes, mB, bar, c.bn + 64 * b, a.v0 + k0);
+  } else {
 #pragma unroll
-    for (int b = 0; b < 4; ++b) tma_load_2d(sB + b * kAtomBytes, mB, bar, n_blk * BN + 64 * b, k0);
+    for (int b = 0; b < 2; ++b) tma_load_2d(sA + b * kAtomBytes, mA, bar, c.am + 64 * b, k0);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tma_load_2d(sB + b * kAtomBytes, mB, bar, c.bn + 64 * b, k0);
   }
 }
 
@@ -210,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
         const int nt = item_tiles<MODE>(a, item);
         for (int tt = 0; ok && tt < nt; ++tt) {
+          const TileCoord tc = tile_coord<MODE>(a, item, tt);
           for (int kb = 0; kb < a.num_kb; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
               ok = false;
@@ -217,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive_expect_tx(&full[stage], kStageBytes);
             const uint32_t sA = stage0 + stage * kStageBytes;
-            issue_loads<MODE>(a, &mapA, &mapB, sA, sA + kABytes, &full[stage], item, tt, kb);
+            issue_loads<MODE>(a, &mapA, &mapB, sA, sA + kABytes, &full[stage], tc, kb);
             last_parity[stage] = static_cast<int>(phase);
             if (++stage == kStages) {
               stage = 0;
