@@ -173,6 +173,31 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W,
                         float* dH, float* dW, void* ws, size_t ws_bytes,
                         int32_t* dev_status, void* stream);
 
+/*
+ * Loss forward without a caller workspace. The method's pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory (a plugin inside a framework that owns all device memory and hands it
+ * only inputs and outputs, or a hot path that must not call cudaMalloc).
+ * Computes exactly what vce_loss_fwd computes, with the same kernels and the
+ * same arguments minus the workspace. Its scratch is a fixed array of
+ * vce_loss_fwd_noalloc_max_scratch() bytes (16 MiB) in the library's own
+ * device memory, held on every GPU that loads the library until the process
+ * exits; a problem whose forward workspace (vce_workspace_size(p,
+ * VCE_OP_LOSS_FWD)) is larger returns VCE_ERR_WORKSPACE before anything is
+ * enqueued. No device memory is allocated by the call.
+ * The first call on a device looks up the array's device address for that
+ * device (the device must be current); make that first call before any stream
+ * capture. All calls share the one array: calls that may overlap on the GPU
+ * (different streams without ordering, or different host threads) race on it
+ * and must not be used. When dev_status is NULL the status word inside the
+ * array is cleared at the start of each call.
+ */
+vce_status vce_loss_fwd_noalloc(const vce_problem* p, const void* h, const void* W,
+                                const int64_t* targets, float* loss, float* lse,
+                                float* token_loss, int32_t* target_owner, int32_t* max_owner,
+                                int32_t* dev_status, void* stream);
+size_t vce_loss_fwd_noalloc_max_scratch(void);
+
 /* Static string naming a status code. */
 const char* vce_status_str(vce_status s);
 

@@ -72,6 +72,11 @@ def lib():
         L.vce_set_wait_limit_ns.restype = None
         L.vce_wait_selftest.argtypes = [c_uint64, c_void_p, c_void_p]
         L.vce_wait_selftest.restype = c_int32
+        L.vce_loss_fwd_noalloc.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                           c_void_p, c_void_p, c_void_p, c_void_p]
+        L.vce_loss_fwd_noalloc.restype = c_int32
+        L.vce_loss_fwd_noalloc_max_scratch.argtypes = []
+        L.vce_loss_fwd_noalloc_max_scratch.restype = c_size_t
         L.vce_last_error.argtypes = []
         L.vce_last_error.restype = ctypes.c_char_p
         L.vce_launch_count.argtypes = []
@@ -186,3 +191,15 @@ def vce_profile_end(capacity: int):
     if n < 0:
         raise VceError(VCE_ERR_CUDA, "vce_profile_end")
     return [(KERNEL_KINDS[kinds[i]], float(ms[i])) for i in range(n)]
+
+
+def vce_loss_fwd_noalloc(p, h, W, targets, loss, lse, token_loss=None, target_owner=None, max_owner=None,
+                         dev_status=None, stream=None) -> None:
+    """vce_loss_fwd with the library's fixed internal scratch instead of a workspace."""
+    _check(lib().vce_loss_fwd_noalloc(ctypes.byref(p), _ptr(h), _ptr(W), _ptr(targets), _ptr(loss), _ptr(lse),
+                                      _ptr(token_loss), _ptr(target_owner), _ptr(max_owner), _ptr(dev_status),
+                                      _stream(stream)), "vce_loss_fwd_noalloc")
+
+
+def vce_loss_fwd_noalloc_max_scratch() -> int:
+    return int(lib().vce_loss_fwd_noalloc_max_scratch())
