@@ -134,7 +134,10 @@ def run_ours(args):
     dW = torch.empty((Vp, H), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws_f = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD))
-    ws_b = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD))
+    ws_b_bytes = vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD)
+    if args.bwd_cols:
+        ws_b_bytes = 256 + T * 2 * args.bwd_cols
+    ws_b = D.workspace(ws_b_bytes)
     ws_e = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_EMBED_BWD))
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -200,7 +203,7 @@ def run_ours(args):
 
     # ---- roofline ----
     peaks, peak_src = load_peaks()
-    vc = (vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD) - 256) // (T * 2)
+    vc = min((ws_b_bytes - 256) // (T * 2), -(-V // 256) * 256)
     flops = {"tc_fwd": 2.0 * T * H * V, "tc_grad": 2.0 * T * H * V, "tc_dh": 2.0 * T * H * V,
              "tc_dw": 2.0 * T * H * V}
     loss_kinds = ["tc_fwd", "tc_grad", "tc_dh", "tc_dw", "merge", "loss_mean", "count_valid"]
@@ -388,6 +391,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--cpu-sample", type=int, default=128)
+    ap.add_argument("--bwd-cols", type=int, default=0,
+                    help="vocabulary columns per backward pass (sizes the workspace); 0 = library default")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-child", action="store_true")
     args = ap.parse_args()

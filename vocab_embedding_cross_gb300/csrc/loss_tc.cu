@@ -3,21 +3,30 @@
 // One persistent, warp-specialised kernel template serves the four
 // contractions of the loss ("Vocabulary shards: look up locally and normalize
 // globally", paragraphs 3-5):
-//   FWD   z = h W^T per (128-token block, work unit inside one shard): the
+//   FWD   z = h W^T per (256-token block, work unit inside one shard): the
 //         epilogue keeps a running maximum and sum of exp per token over the
 //         unit's real columns (padded classes >= V_real never count) and picks
 //         the target logit from the one tile that owns it. Logits stay in TMEM.
-//   GRAD  z recomputed per 128 x 256 tile; the epilogue forms
+//   GRAD  z recomputed per 256 x 256 tile; the epilogue forms
 //         G = (exp(z - lse) - [v == y]) * g / N_valid in bf16 and stores it.
 //   DH    dH (+)= G W      (A = G K-major, B = W rows as an MN-major operand)
 //   DW    dW (+)= G^T h    (A = G^T and B = h, both MN-major operands)
 //
-// Roles (192 threads): warp 0 issues TMA loads into a 4-stage shared-memory
-// ring; warp 1 allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
-// and one lane issues tcgen05.mma; warps 2-5 drain TMEM with tcgen05.ld (warp
-// w reads TMEM lanes 32*(w%4)..+31, i.e. one token row per thread). Every wait
-// is bounded: on a timeout the CTA raises a shared abort flag, records
-// VCE_ERR_TIMEOUT, drains what it has in flight and returns.
+// Two CTAs on two SMs form a cluster and share each MMA (tcgen05 cta_group::2,
+// M = 256, N = 256, K = 16): each CTA loads 128 rows of A and half of B's N
+// range into its own shared memory, and each CTA's TMEM receives its 128 rows
+// of the 256 x 256 fp32 tile. Per SM this halves the B traffic through shared
+// memory compared with a 128 x 256 single-SM tile.
+//
+// Roles (320 threads per CTA): warp 0 issues TMA loads into a ring of stages;
+// their completion is counted on the even CTA's barrier. Warp 1 allocates 512
+// TMEM columns (two accumulators) in both CTAs; in the even CTA one lane issues
+// the MMAs and commits to the barriers of both CTAs. Warps 2-9 of both CTAs
+// drain their own TMEM (warp w reads lanes 32*(w%4)..+31, one token row per
+// thread, and one 128-column half of the tile) with software-pipelined TMEM
+// loads, and release the accumulator to the even CTA. Every wait is bounded:
+// on a timeout the CTA raises its abort flag, records VCE_ERR_TIMEOUT, drains
+// what it has in flight and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -30,14 +39,18 @@
 namespace vce {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
-constexpr uint32_t kABytes = BM * BK * 2;
-constexpr uint32_t kBBytes = BN * BK * 2;
+constexpr int BM = 128;          // A rows per CTA
+constexpr int BMP = 256;         // A rows per CTA pair (the MMA's M)
+constexpr int BN = 256;          // the MMA's N (tile columns)
+constexpr int BNH = 128;         // N rows of B held by each CTA
+constexpr int BK = 64;
+constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter, one per 128-column half
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer warp, MMA warp, epilogue warps
+constexpr uint32_t kABytes = BM * BK * 2;    // 16 KB
+constexpr uint32_t kBBytes = BNH * BK * 2;   // 16 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kAtomBytes = 64 * 128;        // 64 rows of 128 B: one MN-major atom column
-constexpr uint32_t kStagingPerWarp = 2 * 4096;   // two 32-row x 128-B TMA store boxes
+constexpr uint32_t kStagingPerWarp = 4096;       // one 32-row x 128-B TMA store box
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -48,12 +61,14 @@ struct Traits {
   static constexpr uint32_t a_mn = (MODE == MODE_DW) ? 1u : 0u;
   static constexpr uint32_t b_mn = (MODE == MODE_DH || MODE == MODE_DW) ? 1u : 0u;
   static constexpr bool staging = MODE != MODE_FWD;
-  static constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn, b_mn);
+  static constexpr int stages = 6;
+  static constexpr uint32_t idesc = idesc_bf16_f32(BMP, BN, a_mn, b_mn);
 };
 
 template <int MODE>
 constexpr size_t smem_bytes() {
-  return 1024 + size_t(kStages) * kStageBytes + (Traits<MODE>::staging ? 4 * kStagingPerWarp : 0) + 256;
+  return 1024 + size_t(Traits<MODE>::stages) * kStageBytes +
+         (Traits<MODE>::staging ? kEpiWarps * kStagingPerWarp : 0) + 256 + (MODE == MODE_FWD ? 2048 : 0);
 }
 
 struct TcArgs {
@@ -103,48 +118,48 @@ __device__ __forceinline__ int item_tiles(const TcArgs& a, int item) {
   }
 }
 
-// Tile origin: am = first row of A's M range, bn = first index of B's N range
-// (a vocabulary row for FWD/GRAD, an H column for DH/DW). Computed once per
-// tile so that the producer's per-K-block work is only the TMA issue.
+// This CTA's tile origin: am = first of its 128 rows of A's M range, bn =
+// first of its 128 indices of B's N range (a vocabulary row for FWD/GRAD, an
+// H column for DH/DW). Computed once per tile.
 struct TileCoord {
   int32_t am, bn;
 };
 template <int MODE>
-__device__ __forceinline__ TileCoord tile_coord(const TcArgs& a, int item, int tt) {
+__device__ __forceinline__ TileCoord tile_coord(const TcArgs& a, int item, int tt, int rank) {
   TileCoord c;
   if constexpr (MODE == MODE_FWD) {
     const int m_blk = item % a.n_mblk;
     const UnitSpan us = unit_span(a, item / a.n_mblk);
-    c.am = m_blk * BM;
-    c.bn = static_cast<int32_t>(us.vb + static_cast<int64_t>(tt) * BN);
+    c.am = m_blk * BMP + rank * BM;
+    c.bn = static_cast<int32_t>(us.vb + static_cast<int64_t>(tt) * BN) + rank * BNH;
   } else if constexpr (MODE == MODE_GRAD) {
     const int m_blk = item % a.n_mblk, n_blk = item / a.n_mblk;
-    c.am = m_blk * BM;
-    c.bn = a.v0 + n_blk * BN;
+    c.am = m_blk * BMP + rank * BM;
+    c.bn = a.v0 + n_blk * BN + rank * BNH;
   } else {
     const int n_blk = item % a.n_nblk, m_blk = item / a.n_nblk;
-    c.am = m_blk * BM;
-    c.bn = n_blk * BN;
+    c.am = m_blk * BMP + rank * BM;
+    c.bn = n_blk * BN + rank * BNH;
   }
   return c;
 }
 
 template <int MODE>
 __device__ __forceinline__ void issue_loads(const TcArgs& a, const CUtensorMap* mA, const CUtensorMap* mB,
-                                            uint32_t sA, uint32_t sB, uint64_t* bar, TileCoord c, int kb) {
+                                            uint32_t sA, uint32_t sB, uint32_t bar, TileCoord c, int kb) {
   const int k0 = kb * BK;
   if constexpr (MODE == MODE_FWD || MODE == MODE_GRAD) {
-    tma_load_2d(sA, mA, bar, k0, c.am);
-    tma_load_2d(sB, mB, bar, k0, c.bn);
+    tma_load_2d_pair(sA, mA, bar, k0, c.am);
+    tma_load_2d_pair(sB, mB, bar, k0, c.bn);
   } else if constexpr (MODE == MODE_DH) {
-    tma_load_2d(sA, mA, bar, k0, c.am);
+    tma_load_2d_pair(sA, mA, bar, k0, c.am);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) tma_load_2d(sB + b * kAtomBytes, mB, bar, c.bn + 64 * b, a.v0 + k0);
+    for (int b = 0; b < 2; ++b) tma_load_2d_pair(sB + b * kAtomBytes, mB, bar, c.bn + 64 * b, a.v0 + k0);
   } else {
 #pragma unroll
-    for (int b = 0; b < 2; ++b) tma_load_2d(sA + b * kAtomBytes, mA, bar, c.am + 64 * b, k0);
+    for (int b = 0; b < 2; ++b) tma_load_2d_pair(sA + b * kAtomBytes, mA, bar, c.am + 64 * b, k0);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) tma_load_2d(sB + b * kAtomBytes, mB, bar, c.bn + 64 * b, k0);
+    for (int b = 0; b < 2; ++b) tma_load_2d_pair(sB + b * kAtomBytes, mB, bar, c.bn + 64 * b, k0);
   }
 }
 
@@ -170,53 +185,72 @@ __device__ __forceinline__ void stage_row(uint32_t box, int r, const uint32_t (&
   }
 }
 
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_loss_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapOut, const TcArgs a) {
   using Tr = Traits<MODE>;
+  constexpr int kStages = Tr::stages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t stage0 = base;
   const uint32_t staging0 = base + kStages * kStageBytes;
-  uint8_t* tail = gbase + kStages * kStageBytes + (Tr::staging ? 4 * kStagingPerWarp : 0);
+  uint8_t* tail = gbase + kStages * kStageBytes + (Tr::staging ? kEpiWarps * kStagingPerWarp : 0);
   uint64_t* full = reinterpret_cast<uint64_t*>(tail);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* comb_full = drain + 1;     // forward: half-row partial handoff per lane quarter
+  uint64_t* comb_empty = comb_full + 4;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(comb_empty + 4);
   int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
+  float4* comb = reinterpret_cast<float4*>(tail + 256);   // [4 quarters][32 lanes], forward only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int first_item = static_cast<int>(cluster_id_x());
+  const int item_step = static_cast<int>(cluster_count_x());
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&full[s], 1);     // the even CTA's expect_tx; bytes from both CTAs
+      mbar_init(&empty[s], 1);    // one multicast commit per use
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], 4);
+      mbar_init(&tempty[s], 2 * kEpiWarps);   // every epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&comb_full[s], 1);
+      mbar_init(&comb_empty[s], 1);
+    }
     *s_abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(s_tmem, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(s_tmem, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const WaitCtx wc{s_abort, a.status, a.limit_ns};
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (both CTAs) ----------------
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB);
       int stage = 0;
@@ -224,19 +258,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_parity[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
-      bool ok = true;
-      for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+      bool ok = true, issued = false;
+      for (int item = first_item; ok && item < a.n_items; item += item_step) {
         const int nt = item_tiles<MODE>(a, item);
         for (int tt = 0; ok && tt < nt; ++tt) {
-          const TileCoord tc = tile_coord<MODE>(a, item, tt);
+          const TileCoord tc = tile_coord<MODE>(a, item, tt, static_cast<int>(rank));
           for (int kb = 0; kb < a.num_kb; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
+            if (!mbar_wait_cl(&empty[stage], phase ^ 1u, wc)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
             const uint32_t sA = stage0 + stage * kStageBytes;
-            issue_loads<MODE>(a, &mapA, &mapB, sA, sA + kABytes, &full[stage], tc, kb);
+            issue_loads<MODE>(a, &mapA, &mapB, sA, sA + kABytes, full_leader, tc, kb);
+            issued = true;
             last_parity[stage] = static_cast<int>(phase);
             if (++stage == kStages) {
               stage = 0;
@@ -245,40 +281,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && issued) {
         // Let the copies already issued land before the CTA's memory goes away.
-        const WaitCtx drain_wc{s_abort, nullptr, 100000000ull};
-        int dummy = 0;
-        for (int s = 0; s < kStages; ++s) {
-          if (last_parity[s] < 0) continue;
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&full[s], static_cast<uint32_t>(last_parity[s])) &&
-                 globaltimer_ns() - t0 < drain_wc.limit_ns)
-            ++dummy;
+        const uint64_t t0 = globaltimer_ns();
+        if (leader) {
+          for (int s = 0; s < kStages; ++s) {
+            if (last_parity[s] < 0) continue;
+            while (!mbar_try_wait_cluster(&full[s], static_cast<uint32_t>(last_parity[s])) &&
+                   globaltimer_ns() - t0 < 100000000ull) {
+            }
+          }
+        } else {
+          while (globaltimer_ns() - t0 < 2000000ull) {
+          }
         }
-        (void)dummy;
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (even CTA) ----------------
       int stage = 0;
       uint32_t phase = 0;
       uint32_t tile_count = 0;
       bool ok = true;
       bool issued = false;
-      for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+      for (int item = first_item; ok && item < a.n_items; item += item_step) {
         const int nt = item_tiles<MODE>(a, item);
         for (int tt = 0; ok && tt < nt; ++tt) {
           const uint32_t acc = tile_count & 1u;
-          if (!mbar_wait(&tempty[acc], ((tile_count >> 1) & 1u) ^ 1u, wc)) {
+          if (!mbar_wait_cl(&tempty[acc], ((tile_count >> 1) & 1u) ^ 1u, wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d = tmem + acc * BN;
           for (int kb = 0; kb < a.num_kb; ++kb) {
-            if (!mbar_wait(&full[stage], phase, wc)) {
+            if (!mbar_wait_cl(&full[stage], phase, wc)) {
               ok = false;
               break;
             }
@@ -298,126 +336,197 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else {
                 bd = smem_desc_sw128(sB + kk * 32u, 16u, 1024u);
               }
-              umma_f16(d, ad, bd, Tr::idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_f16_pair(d, ad, bd, Tr::idesc, (kb | kk) != 0 ? 1u : 0u);
             }
             issued = true;
-            umma_commit(&empty[stage]);
+            umma_commit_pair_mc(&empty[stage], 0x3);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit(&tfull[acc]);
+          umma_commit_pair_mc(&tfull[acc], 0x3);
           ++tile_count;
         }
       }
       if (!ok && issued) {
         // Wait for the MMAs in flight before TMEM is released.
-        umma_commit(drain);
+        umma_commit_pair(drain);
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 100000000ull) {
         }
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5 ----------------
-    const int q = warp & 3;           // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;      // row of the tile held by this thread
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t my_staging = staging0 + static_cast<uint32_t>(warp - 2) * kStagingPerWarp;
-    uint32_t box_count = 0;
+    // ---------------- epilogue: warps 2..9 of both CTAs ----------------
+    // Warps e and e+4 (e = warp - 2) share TMEM lane quarter warp % 4; warp e
+    // takes tile columns [128 * (e / 4), +128).
+    const int e = warp - 2;
+    const int q = warp & 3;
+    const int half = e >> 2;
+    const int pq = e & 3;
+    const int r = q * 32 + lane;      // row of this CTA's half tile held by this thread
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(half * 128);
+    const uint32_t my_staging = staging0 + static_cast<uint32_t>(e) * kStagingPerWarp;
+    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
     uint32_t tile_count = 0;
+    uint32_t items_done = 0;
     bool ok = true;
     float scale = 0.0f;
     if constexpr (MODE == MODE_GRAD) {
       const int nv = a.n_valid[0];
       scale = nv > 0 ? a.g / static_cast<float>(nv) : 0.0f;
     }
-    for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+    auto release = [&](uint32_t acc) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+    };
+    // One 32-row x 128-byte TMA store (or reduce-add) from this warp's staging box.
+    auto store_box = [&](const uint32_t (&w)[32], int col, int row) {
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
+      stage_row(my_staging, lane, w);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (MODE != MODE_GRAD && a.accumulate)
+          tma_reduce_add_2d(&mapOut, my_staging, col, row);
+        else
+          tma_store_2d(&mapOut, my_staging, col, row);
+        bulk_commit();
+      }
+    };
+    for (int item = first_item; ok && item < a.n_items; item += item_step) {
       if constexpr (MODE == MODE_FWD) {
         const int m_blk = item % a.n_mblk, u = item / a.n_mblk;
         const UnitSpan us = unit_span(a, u);
-        const int t = m_blk * BM + r;
+        const int t = m_blk * BMP + static_cast<int>(rank) * BM + r;
         const bool row_ok = t < a.pd.T;
         const int64_t y = row_ok ? a.targets[t] : -1;
         float m_run = -INFINITY, s_run = 0.0f, zt = 0.0f;
         bool have_zt = false;
+        // Online maximum and sum of exp over one 32-column chunk of real columns.
+        auto chunk = [&](const uint32_t (&x)[32], int64_t vc0) {
+          const int64_t nval64 = us.vlim - vc0;
+          const int nval = nval64 >= 32 ? 32 : (nval64 <= 0 ? 0 : static_cast<int>(nval64));
+          if (nval == 0) return;
+          if (y >= vc0 && y < vc0 + nval) {
+            zt = select32(x, static_cast<int>(y - vc0));
+            have_zt = true;
+          }
+          float cm = -INFINITY;
+          if (nval == 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cm = fmaxf(cm, __uint_as_float(x[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nval) cm = fmaxf(cm, __uint_as_float(x[j]));
+          }
+          const float mn = fmaxf(m_run, cm);
+          const float mL = mn * kLog2e;
+          float s0 = 0.0f, s1 = 0.0f;
+          if (nval == 32) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              s0 += ex2_approx(fmaf(__uint_as_float(x[j]), kLog2e, -mL));
+              s1 += ex2_approx(fmaf(__uint_as_float(x[j + 1]), kLog2e, -mL));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nval) s0 += ex2_approx(fmaf(__uint_as_float(x[j]), kLog2e, -mL));
+          }
+          s_run = s_run * ex2_approx((m_run - mn) * kLog2e) + (s0 + s1);
+          m_run = mn;
+        };
         for (int tt = 0; tt < us.ntiles; ++tt) {
           const uint32_t acc = tile_count & 1u;
-          if (!mbar_wait(&tfull[acc], (tile_count >> 1) & 1u, wc)) {
+          if (!mbar_wait_cl(&tfull[acc], (tile_count >> 1) & 1u, wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int64_t vt0 = us.vb + static_cast<int64_t>(tt) * BN;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t x[32];
-            tmem_ld_32x32b_x32(lane_base + acc * BN + c * 32, x);
-            tmem_ld_wait();
-            const int64_t vc0 = vt0 + c * 32;
-            int64_t nval64 = us.vlim - vc0;
-            const int nval = nval64 >= 32 ? 32 : (nval64 <= 0 ? 0 : static_cast<int>(nval64));
-            if (nval == 0) continue;
-            if (y >= vc0 && y < vc0 + nval) {
-              zt = select32(x, static_cast<int>(y - vc0));
-              have_zt = true;
-            }
-            float cm = -INFINITY;
-            if (nval == 32) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) cm = fmaxf(cm, __uint_as_float(x[j]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < nval) cm = fmaxf(cm, __uint_as_float(x[j]));
-            }
-            const float mn = fmaxf(m_run, cm);
-            const float mL = mn * kLog2e;
-            float sum = 0.0f;
-            if (nval == 32) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) sum += ex2_approx(fmaf(__uint_as_float(x[j]), kLog2e, -mL));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < nval) sum += ex2_approx(fmaf(__uint_as_float(x[j]), kLog2e, -mL));
-            }
-            s_run = s_run * ex2_approx((m_run - mn) * kLog2e) + sum;
-            m_run = mn;
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[acc]);
+          const int64_t vc = us.vb + static_cast<int64_t>(tt) * BN + half * 128;
+          const uint32_t ta = lane_base + acc * BN;
+          uint32_t xa[32], xb[32];
+          tmem_ld_32x32b_x32(ta, xa);
+          tmem_ld_wait();
+          reg_fence(xa);
+          tmem_ld_32x32b_x32(ta + 32, xb);
+          chunk(xa, vc);
+          tmem_ld_wait();
+          reg_fence(xb);
+          tmem_ld_32x32b_x32(ta + 64, xa);
+          chunk(xb, vc + 32);
+          tmem_ld_wait();
+          reg_fence(xa);
+          tmem_ld_32x32b_x32(ta + 96, xb);
+          chunk(xa, vc + 64);
+          tmem_ld_wait();
+          reg_fence(xb);
+          release(acc);
+          chunk(xb, vc + 96);
           ++tile_count;
         }
         if (!ok) break;
-        if (row_ok) {
-          a.part[static_cast<int64_t>(t) * a.ug.n_units + u] = make_float2(m_run, s_run);
-          if (have_zt) a.ztgt[t] = zt;
+        // Join the two half-row partials of the warps sharing this lane quarter.
+        if (half == 1) {
+          if (!mbar_wait(&comb_empty[pq], (items_done & 1u) ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          comb[pq * 32 + lane] = make_float4(m_run, s_run, zt, have_zt ? 1.0f : 0.0f);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_full[pq]);
+        } else {
+          if (!mbar_wait(&comb_full[pq], items_done & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          const float4 o = comb[pq * 32 + lane];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_empty[pq]);
+          const float M = fmaxf(m_run, o.x);
+          float S = 0.0f;
+          if (M != -INFINITY)
+            S = s_run * ex2_approx((m_run - M) * kLog2e) + o.y * ex2_approx((o.x - M) * kLog2e);
+          if (!have_zt && o.w != 0.0f) {
+            zt = o.z;
+            have_zt = true;
+          }
+          if (row_ok) {
+            a.part[static_cast<int64_t>(t) * a.ug.n_units + u] = make_float2(M, S);
+            if (have_zt) a.ztgt[t] = zt;
+          }
         }
+        ++items_done;
       } else {
         int m_blk, n_blk, row0, col0;
         if constexpr (MODE == MODE_GRAD) {
           m_blk = item % a.n_mblk;
           n_blk = item / a.n_mblk;
-          row0 = m_blk * BM;
-          col0 = n_blk * BN;   // chunk-local column
+          row0 = m_blk * BMP + static_cast<int>(rank) * BM;
+          col0 = n_blk * BN + half * 128;   // chunk-local column of this warp's half
         } else {
           n_blk = item % a.n_nblk;
           m_blk = item / a.n_nblk;
-          row0 = (MODE == MODE_DW ? a.out_row0 : 0) + m_blk * BM;
-          col0 = n_blk * BN;
+          row0 = (MODE == MODE_DW ? a.out_row0 : 0) + m_blk * BMP + static_cast<int>(rank) * BM;
+          col0 = n_blk * BN + half * 128;
         }
+        const int orow = row0 + q * 32;
         const uint32_t acc = tile_count & 1u;
-        if (!mbar_wait(&tfull[acc], (tile_count >> 1) & 1u, wc)) {
+        if (!mbar_wait_cl(&tfull[acc], (tile_count >> 1) & 1u, wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t ta = lane_base + acc * BN;
         if constexpr (MODE == MODE_GRAD) {
-          const int t = m_blk * BM + r;
+          const int t = m_blk * BMP + static_cast<int>(rank) * BM + r;
           int64_t y = -1;
           float lseL = 0.0f;
           bool row_ok = false;
@@ -428,85 +537,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int64_t vt0 = static_cast<int64_t>(a.v0) + col0;
 #pragma unroll 1
-          for (int b = 0; b < BN / 64; ++b) {
-            uint32_t w[32];
+          for (int bb = 0; bb < 2; ++bb) {
+            uint32_t x0[32], x1[32], w[32];
+            tmem_ld_32x32b_x32(ta + bb * 64, x0);
+            tmem_ld_32x32b_x32(ta + bb * 64 + 32, x1);
+            tmem_ld_wait();
+            reg_fence(x0);
+            reg_fence(x1);
+            if (bb == 1) release(acc);
+            const int64_t vc0 = vt0 + bb * 64;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint32_t x[32];
-              tmem_ld_32x32b_x32(lane_base + acc * BN + b * 64 + half * 32, x);
-              tmem_ld_wait();
-              const int64_t vc0 = vt0 + b * 64 + half * 32;
-#pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                float g0 = 0.0f, g1 = 0.0f;
-                if (row_ok) {
-                  const int64_t v = vc0 + j;
-                  if (v < a.pd.V_real) g0 = ex2_approx(fmaf(__uint_as_float(x[j]), kLog2e, -lseL)) * scale;
-                  if (v + 1 < a.pd.V_real) g1 = ex2_approx(fmaf(__uint_as_float(x[j + 1]), kLog2e, -lseL)) * scale;
-                  if (v == y) g0 -= scale;
-                  if (v + 1 == y) g1 -= scale;
-                }
-                w[half * 16 + j / 2] = pack_bf16x2(g0, g1);
+            for (int j = 0; j < 64; j += 2) {
+              const uint32_t xa = j < 32 ? x0[j] : x1[j - 32];
+              const uint32_t xb = j < 32 ? x0[j + 1] : x1[j - 31];
+              float g0 = 0.0f, g1 = 0.0f;
+              if (row_ok) {
+                const int64_t v = vc0 + j;
+                if (v < a.pd.V_real) g0 = ex2_approx(fmaf(__uint_as_float(xa), kLog2e, -lseL)) * scale;
+                if (v + 1 < a.pd.V_real) g1 = ex2_approx(fmaf(__uint_as_float(xb), kLog2e, -lseL)) * scale;
+                if (v == y) g0 -= scale;
+                if (v + 1 == y) g1 -= scale;
               }
+              w[j / 2] = pack_bf16x2(g0, g1);
             }
-            if (b == BN / 64 - 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&tempty[acc]);
-            }
-            const uint32_t box = my_staging + (box_count & 1u) * 4096u;
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-            stage_row(box, lane, w);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&mapOut, box, col0 + b * 64, row0 + q * 32);
-              bulk_commit();
-            }
-            ++box_count;
+            store_box(w, col0 + bb * 64, orow);
           }
         } else {
-#pragma unroll 1
-          for (int b = 0; b < BN / 32; ++b) {
-            uint32_t x[32];
-            tmem_ld_32x32b_x32(lane_base + acc * BN + b * 32, x);
-            tmem_ld_wait();
-            if (b == BN / 32 - 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&tempty[acc]);
-            }
-            const uint32_t box = my_staging + (box_count & 1u) * 4096u;
-            if (lane == 0) bulk_wait_read<1>();
-            __syncwarp();
-            stage_row(box, lane, x);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              if (a.accumulate)
-                tma_reduce_add_2d(&mapOut, box, col0 + b * 32, row0 + q * 32);
-              else
-                tma_store_2d(&mapOut, box, col0 + b * 32, row0 + q * 32);
-              bulk_commit();
-            }
-            ++box_count;
-          }
+          uint32_t xa[32], xb[32];
+          tmem_ld_32x32b_x32(ta, xa);
+          tmem_ld_wait();
+          reg_fence(xa);
+          tmem_ld_32x32b_x32(ta + 32, xb);
+          store_box(xa, col0, orow);
+          tmem_ld_wait();
+          reg_fence(xb);
+          tmem_ld_32x32b_x32(ta + 64, xa);
+          store_box(xb, col0 + 32, orow);
+          tmem_ld_wait();
+          reg_fence(xa);
+          tmem_ld_32x32b_x32(ta + 96, xb);
+          store_box(xa, col0 + 64, orow);
+          tmem_ld_wait();
+          reg_fence(xb);
+          release(acc);
+          store_box(xb, col0 + 96, orow);
         }
         ++tile_count;
       }
     }
     if constexpr (Tr::staging) {
       if (lane == 0) bulk_wait<0>();
-      __syncwarp();
     }
   }
 
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();   // the peer's TMEM and shared memory stay live until the pair is done
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -528,6 +618,24 @@ __global__ void wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
 }
 
 template <int MODE>
+int max_clusters(int num_sms) {
+  static int cached = -1;
+  if (cached < 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<MODE>();
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_loss_kernel<MODE>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms / 2;
+    }
+    cached = n;
+  }
+  return cached;
+}
+
+template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mO, const TcArgs& a,
                         cudaStream_t st) {
   static bool configured = false;
@@ -539,8 +647,9 @@ cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
   }
   if (a.n_items <= 0) return cudaSuccess;
   const DevInfo di = current_device_info();
-  const int grid = a.n_items < di.num_sms ? a.n_items : di.num_sms;
-  tc_loss_kernel<MODE><<<grid, kThreads, smem_bytes<MODE>(), st>>>(mA, mB, mO, a);
+  const int mc = max_clusters<MODE>(di.num_sms);
+  const int clusters = a.n_items < mc ? a.n_items : mc;
+  tc_loss_kernel<MODE><<<2 * clusters, kThreads, smem_bytes<MODE>(), st>>>(mA, mB, mO, a);
   note_launch(VCE_K_TC_FWD + MODE, st);
   return cudaGetLastError();
 }
@@ -560,10 +669,10 @@ cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* 
                           const int64_t* targets, float2* part, float* ztgt, int32_t* status, cudaStream_t st) {
   CUtensorMap mh, mw;
   if (!make_tmap_2d(&mh, h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, p.T, p.H, 64, BM, true) ||
-      !make_tmap_2d(&mw, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, p.V_real, p.H, 64, BN, true))
+      !make_tmap_2d(&mw, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, p.V_real, p.H, 64, BNH, true))
     return cudaErrorInvalidValue;
   TcArgs a = base_args(p, targets, status);
-  a.n_mblk = static_cast<int>(ceil_div(p.T, BM));
+  a.n_mblk = static_cast<int>(ceil_div(p.T, BMP));
   a.n_items = a.n_mblk * ug.n_units;
   a.num_kb = static_cast<int>(ceil_div(p.H, BK));
   a.ug = ug;
@@ -583,11 +692,11 @@ cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void*
   {
     CUtensorMap mh, mw, mg;
     if (!make_tmap_2d(&mh, h, BF, 2, p.H, p.T, p.H, 64, BM, true) ||
-        !make_tmap_2d(&mw, W, BF, 2, p.H, p.V_real, p.H, 64, BN, true) ||
+        !make_tmap_2d(&mw, W, BF, 2, p.H, p.V_real, p.H, 64, BNH, true) ||
         !make_tmap_2d(&mg, G, BF, 2, vc_act, p.T, g_ld, 64, 32, true))
       return cudaErrorInvalidValue;
     TcArgs a = base_args(p, targets, status);
-    a.n_mblk = static_cast<int>(ceil_div(p.T, BM));
+    a.n_mblk = static_cast<int>(ceil_div(p.T, BMP));
     a.n_nblk = static_cast<int>(ceil_div(vc_act, BN));
     a.n_items = a.n_mblk * a.n_nblk;
     a.num_kb = static_cast<int>(ceil_div(p.H, BK));
@@ -606,7 +715,7 @@ cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void*
         !make_tmap_2d(&mo, dH, F32, 4, p.H, p.T, p.H, 32, 32, true))
       return cudaErrorInvalidValue;
     TcArgs a = base_args(p, targets, status);
-    a.n_mblk = static_cast<int>(ceil_div(p.T, BM));
+    a.n_mblk = static_cast<int>(ceil_div(p.T, BMP));
     a.n_nblk = static_cast<int>(ceil_div(p.H, BN));
     a.n_items = a.n_mblk * a.n_nblk;
     a.num_kb = static_cast<int>(ceil_div(vc_act, BK));
@@ -622,7 +731,7 @@ cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void*
         !make_tmap_2d(&mo, dW, F32, 4, p.H, static_cast<uint64_t>(v0) + vc_act, p.H, 32, 32, true))
       return cudaErrorInvalidValue;
     TcArgs a = base_args(p, targets, status);
-    a.n_mblk = static_cast<int>(ceil_div(vc_act, BM));
+    a.n_mblk = static_cast<int>(ceil_div(vc_act, BMP));
     a.n_nblk = static_cast<int>(ceil_div(p.H, BN));
     a.n_items = a.n_mblk * a.n_nblk;
     a.num_kb = static_cast<int>(ceil_div(p.T, BK));

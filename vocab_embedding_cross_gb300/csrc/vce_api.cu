@@ -159,12 +159,16 @@ int64_t bwd_chunk_cols(const vce_problem& p, size_t ws_bytes) {
 }
 int64_t bwd_recommended_cols(const vce_problem& p) {
   if (p.T == 0) return 256;
-  // about 256 MiB of G per pass
-  int64_t vc = static_cast<int64_t>((size_t(1) << 28) / (static_cast<size_t>(p.T) * g_esize(p)));
-  vc = vc / 256 * 256;
-  if (vc < 256) vc = 256;
-  const int64_t cap = vocab_cols_cap(p);
-  return vc > cap ? cap : vc;
+  // Fewest passes with at most 1.5 GiB of G per pass, the columns split evenly
+  // between the passes (each pass costs three launches and a pipeline fill).
+  const size_t per_col = static_cast<size_t>(p.T) * g_esize(p);
+  const size_t cap_bytes = size_t(3) << 29;
+  const int64_t cols = vocab_cols_cap(p);
+  int64_t max_cols = static_cast<int64_t>(cap_bytes / per_col) / 256 * 256;
+  if (max_cols < 256) max_cols = 256;
+  const int64_t passes = ceil_div(cols, max_cols);
+  int64_t vc = ceil_div(ceil_div(cols, passes), 256) * 256;
+  return vc > cols ? cols : vc;
 }
 
 }  // namespace
