@@ -135,8 +135,8 @@ def run_ours(args):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws_f = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD))
     ws_b_bytes = vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD)
-    if args.bwd_cols:
-        ws_b_bytes = 256 + T * 2 * args.bwd_cols
+    if args.bwd_cols:   # G chunk of that many columns plus the dH K-part partials
+        ws_b_bytes = 256 + T * 2 * args.bwd_cols + (0 if args.no_dh_split else 8 * (-(-T // 256) * 256) * H * 4)
     ws_b = D.workspace(ws_b_bytes)
     ws_e = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_EMBED_BWD))
     stream = torch.cuda.current_stream()
@@ -203,10 +203,11 @@ def run_ours(args):
 
     # ---- roofline ----
     peaks, peak_src = load_peaks()
-    vc = min((ws_b_bytes - 256) // (T * 2), -(-V // 256) * 256)
+    dh_part = 0 if args.no_dh_split else 8 * (-(-T // 256) * 256) * H * 4
+    vc = min((ws_b_bytes - 256 - dh_part) // (T * 2), -(-V // 256) * 256)
     flops = {"tc_fwd": 2.0 * T * H * V, "tc_grad": 2.0 * T * H * V, "tc_dh": 2.0 * T * H * V,
              "tc_dw": 2.0 * T * H * V}
-    loss_kinds = ["tc_fwd", "tc_grad", "tc_dh", "tc_dw", "merge", "loss_mean", "count_valid"]
+    loss_kinds = ["tc_fwd", "tc_grad", "tc_dh", "tc_dw", "dh_reduce", "merge", "loss_mean", "count_valid"]
     loss_ms = sum(per_kind.get(k, (0.0, 0))[0] for k in loss_kinds)
     dom = max((k for k in flops if k in per_kind), key=lambda k: per_kind[k][0], default=None)
     roofline = None
@@ -391,6 +392,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--cpu-sample", type=int, default=128)
+    ap.add_argument("--no-dh-split", action="store_true", help="with --bwd-cols: no room for dH K parts")
     ap.add_argument("--bwd-cols", type=int, default=0,
                     help="vocabulary columns per backward pass (sizes the workspace); 0 = library default")
     ap.add_argument("--no-cpu-baseline", action="store_true")

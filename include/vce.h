@@ -247,7 +247,8 @@ typedef enum vce_kernel_kind {
   VCE_K_EMBED_GATHER = 0, VCE_K_EMBED_SORT = 1, VCE_K_EMBED_REDUCE = 2,
   VCE_K_TC_FWD = 3, VCE_K_TC_GRAD = 4, VCE_K_TC_DH = 5, VCE_K_TC_DW = 6,
   VCE_K_MERGE = 7, VCE_K_LOSS_MEAN = 8, VCE_K_COUNT_VALID = 9,
-  VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13
+  VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13,
+  VCE_K_DH_REDUCE = 14
 } vce_kernel_kind;
 uint64_t vce_launch_count(void);
 vce_status vce_profile_begin(int32_t capacity, void* stream);

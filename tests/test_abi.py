@@ -95,7 +95,7 @@ def test_workspace_sizes(L):
     assert fwd >= 8192 * units * 8 + 8192 * 4
     mn = vce.vce_workspace_size_min(p, vce.VCE_OP_LOSS_BWD)
     rec = vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD)
-    assert mn == 256 + 8192 * 256 * 2 and rec >= mn and (rec - 256) % (8192 * 256 * 2) == 0
+    assert mn == 256 + 8192 * 256 * 2 and rec > mn
     assert vce.vce_workspace_size(p, vce.VCE_OP_EMBED_BWD) > 8192 * 16
     # the embedding backward workspace holds keys, runs and run partial slots
     p4 = P(T=16384, H=3072, Vp=201088, V_real=201088, S=8)

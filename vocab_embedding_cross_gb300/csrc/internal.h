@@ -97,7 +97,11 @@ cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* 
 cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void* W, const int64_t* targets,
                                 const float* lse, const int32_t* n_valid, float g, int v0, int vc_act,
                                 void* G, int g_ld, float* dH, bool dH_accumulate, float* dW, bool dW_accumulate,
-                                int32_t* status, cudaStream_t st);
+                                float* dh_part, int dh_parts, int32_t* status, cudaStream_t st);
+// Number of K parts for the dH GEMM of one column chunk (fills the waves of
+// the persistent grid); at most kMaxDhParts.
+constexpr int kMaxDhParts = 8;
+int tc_dh_parts(const vce_problem& p, int vc_act);
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t st);
 

@@ -88,6 +88,9 @@ struct TcArgs {
   int vc;
   int out_row0;
   int accumulate;
+  int ksplit;    // DH: the K range (vocabulary columns) is cut into ksplit parts
+  int kb_per;    // DH: K blocks per part
+  int t_pad;     // DH with ksplit > 1: rows per partial buffer
   int32_t* status;
   uint64_t limit_ns;
 };
@@ -137,11 +140,28 @@ __device__ __forceinline__ TileCoord tile_coord(const TcArgs& a, int item, int t
     c.am = m_blk * BMP + rank * BM;
     c.bn = a.v0 + n_blk * BN + rank * BNH;
   } else {
-    const int n_blk = item % a.n_nblk, m_blk = item / a.n_nblk;
+    const int n_blk = item % a.n_nblk, m_blk = (item / a.n_nblk) / a.ksplit;
     c.am = m_blk * BMP + rank * BM;
     c.bn = n_blk * BN + rank * BNH;
   }
   return c;
+}
+
+// K blocks [kb0, kb1) of an item: all of K, except for DH cut into parts
+// (item = (m_blk * ksplit + part) * n_nblk + n_blk).
+struct KRange {
+  int kb0, kb1;
+};
+template <int MODE>
+__device__ __forceinline__ KRange item_krange(const TcArgs& a, int item) {
+  if constexpr (MODE == MODE_DH) {
+    const int part = (item / a.n_nblk) % a.ksplit;
+    const int kb0 = part * a.kb_per;
+    const int kb1 = kb0 + a.kb_per < a.num_kb ? kb0 + a.kb_per : a.num_kb;
+    return KRange{kb0, kb1};
+  } else {
+    return KRange{0, a.num_kb};
+  }
 }
 
 template <int MODE>
@@ -263,7 +283,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int nt = item_tiles<MODE>(a, item);
         for (int tt = 0; ok && tt < nt; ++tt) {
           const TileCoord tc = tile_coord<MODE>(a, item, tt, static_cast<int>(rank));
-          for (int kb = 0; kb < a.num_kb; ++kb) {
+          const KRange kr = item_krange<MODE>(a, item);
+          for (int kb = kr.kb0; kb < kr.kb1; ++kb) {
             if (!mbar_wait_cl(&empty[stage], phase ^ 1u, wc)) {
               ok = false;
               break;
@@ -315,7 +336,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem + acc * BN;
-          for (int kb = 0; kb < a.num_kb; ++kb) {
+          const KRange kr = item_krange<MODE>(a, item);
+          for (int kb = kr.kb0; kb < kr.kb1; ++kb) {
             if (!mbar_wait_cl(&full[stage], phase, wc)) {
               ok = false;
               break;
@@ -336,7 +358,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               } else {
                 bd = smem_desc_sw128(sB + kk * 32u, 16u, 1024u);
               }
-              umma_f16_pair(d, ad, bd, Tr::idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_f16_pair(d, ad, bd, Tr::idesc, (kb != kr.kb0 || kk != 0) ? 1u : 0u);
             }
             issued = true;
             umma_commit_pair_mc(&empty[stage], 0x3);
@@ -513,8 +535,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           col0 = n_blk * BN + half * 128;   // chunk-local column of this warp's half
         } else {
           n_blk = item % a.n_nblk;
-          m_blk = item / a.n_nblk;
-          row0 = (MODE == MODE_DW ? a.out_row0 : 0) + m_blk * BMP + static_cast<int>(rank) * BM;
+          m_blk = (item / a.n_nblk) / a.ksplit;
+          const int part = (item / a.n_nblk) % a.ksplit;   // DH: partial buffer of this K part
+          row0 = (MODE == MODE_DW ? a.out_row0 : part * a.t_pad) + m_blk * BMP + static_cast<int>(rank) * BM;
           col0 = n_blk * BN + half * 128;
         }
         const int orow = row0 + q * 32;
@@ -660,10 +683,51 @@ TcArgs base_args(const vce_problem& p, const int64_t* targets, int32_t* status) 
   a.targets = targets;
   a.status = status;
   a.limit_ns = wait_limit_ns();
+  a.ksplit = 1;
   return a;
 }
 
+// dH = (accumulate ? dH : 0) + P[0] + P[1] + ... in this order (deterministic).
+__global__ void __launch_bounds__(256) dh_reduce_kernel(const float4* __restrict__ P, int nparts, int64_t part_stride4,
+                                                        float4* __restrict__ dH, int64_t n4, int accumulate) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 s = accumulate ? dH[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < nparts; ++k) {
+      const float4 v = __ldcs(P + k * part_stride4 + i);
+      s.x = s.x + v.x;
+      s.y = s.y + v.y;
+      s.z = s.z + v.z;
+      s.w = s.w + v.w;
+    }
+    dH[i] = s;
+  }
+}
+
 }  // namespace
+
+int tc_dh_parts(const vce_problem& p, int vc_act) {
+  const DevInfo di = current_device_info();
+  const int clusters = max_clusters<MODE_DH>(di.num_sms);
+  const int tiles = static_cast<int>(ceil_div(p.T, BMP) * ceil_div(p.H, BN));
+  const int kb = static_cast<int>(ceil_div(vc_act, BK));
+  // Fewest parts whose tile count fills the clusters' waves to >= 95%, each
+  // part keeping at least 32 K blocks.
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= kMaxDhParts; ++s) {
+    if (s > 1 && kb / s < 32) break;
+    const int items = tiles * s;
+    const int waves = (items + clusters - 1) / clusters;
+    const double eff = static_cast<double>(items) / (static_cast<double>(waves) * clusters);
+    if (eff > best_eff + 1e-9) {
+      best = s;
+      best_eff = eff;
+    }
+    if (eff >= 0.95) break;
+  }
+  return best;
+}
 
 cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* h, const void* W,
                           const int64_t* targets, float2* part, float* ztgt, int32_t* status, cudaStream_t st) {
@@ -684,7 +748,7 @@ cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* 
 cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void* W, const int64_t* targets,
                                 const float* lse, const int32_t* n_valid, float g, int v0, int vc_act, void* G,
                                 int g_ld, float* dH, bool dH_accumulate, float* dW, bool dW_accumulate,
-                                int32_t* status, cudaStream_t st) {
+                                float* dh_part, int dh_parts, int32_t* status, cudaStream_t st) {
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   cudaError_t e;
@@ -707,21 +771,40 @@ cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void*
     a.vc = vc_act;
     if ((e = launch_mode<MODE_GRAD>(mh, mw, mg, a, st)) != cudaSuccess) return e;
   }
-  // DH: dH (+)= G[:, 0:vc_act] W[v0:v0+vc_act, :]
+  // DH: dH (+)= G[:, 0:vc_act] W[v0:v0+vc_act, :]. With dh_parts > 1 the K
+  // range is cut into parts that write fp32 partials (row blocks of t_pad rows
+  // in dh_part), added to dH in part order by dh_reduce_kernel.
   {
+    const int parts = dh_part ? dh_parts : 1;
+    const int t_pad = static_cast<int>(ceil_div(p.T, BMP) * BMP);
     CUtensorMap mg, mw, mo;
+    const bool ok_out = parts > 1
+                            ? make_tmap_2d(&mo, dh_part, F32, 4, p.H, static_cast<uint64_t>(parts) * t_pad, p.H, 32,
+                                           32, true)
+                            : make_tmap_2d(&mo, dH, F32, 4, p.H, p.T, p.H, 32, 32, true);
     if (!make_tmap_2d(&mg, G, BF, 2, vc_act, p.T, g_ld, 64, BM, true) ||
-        !make_tmap_2d(&mw, W, BF, 2, p.H, p.V_real, p.H, 64, 64, true) ||
-        !make_tmap_2d(&mo, dH, F32, 4, p.H, p.T, p.H, 32, 32, true))
+        !make_tmap_2d(&mw, W, BF, 2, p.H, p.V_real, p.H, 64, 64, true) || !ok_out)
       return cudaErrorInvalidValue;
     TcArgs a = base_args(p, targets, status);
     a.n_mblk = static_cast<int>(ceil_div(p.T, BMP));
     a.n_nblk = static_cast<int>(ceil_div(p.H, BN));
-    a.n_items = a.n_mblk * a.n_nblk;
     a.num_kb = static_cast<int>(ceil_div(vc_act, BK));
+    a.ksplit = parts;
+    a.kb_per = static_cast<int>(ceil_div(a.num_kb, parts));
+    a.t_pad = t_pad;
+    a.n_items = a.n_mblk * parts * a.n_nblk;
     a.v0 = v0;
-    a.accumulate = dH_accumulate ? 1 : 0;
+    a.accumulate = (parts == 1 && dH_accumulate) ? 1 : 0;
     if ((e = launch_mode<MODE_DH>(mg, mw, mo, a, st)) != cudaSuccess) return e;
+    if (parts > 1) {
+      const int64_t n4 = p.T * p.H / 4;
+      const int64_t stride4 = static_cast<int64_t>(t_pad) * p.H / 4;
+      const DevInfo di = current_device_info();
+      dh_reduce_kernel<<<di.num_sms * 8, 256, 0, st>>>(reinterpret_cast<const float4*>(dh_part), parts, stride4,
+                                                       reinterpret_cast<float4*>(dH), n4, dH_accumulate ? 1 : 0);
+      note_launch(VCE_K_DH_REDUCE, st);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   // DW: dW[v0:v0+vc_act, :] (+)= G[:, 0:vc_act]^T h
   {

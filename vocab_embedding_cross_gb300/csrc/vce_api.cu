@@ -170,6 +170,14 @@ int64_t bwd_recommended_cols(const vce_problem& p) {
   int64_t vc = ceil_div(ceil_div(cols, passes), 256) * 256;
   return vc > cols ? cols : vc;
 }
+// fp32 partials of the dH GEMM's K parts (bf16 path): kMaxDhParts buffers of
+// T rounded up to 256 rows.
+size_t dh_part_bytes(const vce_problem& p) {
+  if (p.dtype != VCE_BF16 || p.T == 0) return 0;
+  return align_up(static_cast<size_t>(kMaxDhParts) * static_cast<size_t>(ceil_div(p.T, 256) * 256) *
+                      static_cast<size_t>(p.H) * sizeof(float),
+                  kWsAlign);
+}
 
 }  // namespace
 }  // namespace vce
@@ -241,7 +249,7 @@ size_t vce_workspace_size(const vce_problem* p, int32_t op) {
     case VCE_OP_EMBED_FWD: return 0;
     case VCE_OP_EMBED_BWD: return embed_bwd_ws_bytes(*p);
     case VCE_OP_LOSS_FWD: return fwd_layout(*p).total;
-    case VCE_OP_LOSS_BWD: return bwd_bytes_for(*p, bwd_recommended_cols(*p));
+    case VCE_OP_LOSS_BWD: return bwd_bytes_for(*p, bwd_recommended_cols(*p)) + dh_part_bytes(*p);
   }
   return SIZE_MAX;
 }
@@ -327,7 +335,10 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
       !aligned(dW, 16))
     return VCE_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, kWsAlign)) return VCE_ERR_WORKSPACE;
-  const int64_t vc = bwd_chunk_cols(*p, ws_bytes);
+  // Layout: header | dH K-part partials (when the workspace has room) | G chunk.
+  const size_t part_bytes = dh_part_bytes(*p);
+  const bool use_parts = part_bytes > 0 && ws_bytes >= bwd_bytes_for(*p, 256) + part_bytes;
+  const int64_t vc = bwd_chunk_cols(*p, use_parts ? ws_bytes - part_bytes : ws_bytes);
   if (vc < 256) return VCE_ERR_WORKSPACE;
   char* b = static_cast<char*>(ws);
   int32_t* status = dev_status;
@@ -336,7 +347,8 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
     status = reinterpret_cast<int32_t*>(b);
     if (cudaError_t me = cudaMemsetAsync(status, 0, sizeof(int32_t), st)) return cuda_status(me);
   }
-  void* G = b + kBwdHeader;
+  float* dh_part = use_parts ? reinterpret_cast<float*>(b + kBwdHeader) : nullptr;
+  void* G = b + kBwdHeader + (use_parts ? part_bytes : 0);
   const ProbDev pd = prob_dev(*p);
   if (cudaError_t ce = launch_count_valid(pd, targets, n_valid, status, st)) return cuda_status(ce);
   if (!p->tied_weights && p->Vp > p->V_real) {
@@ -348,8 +360,10 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
     const int vc_act = static_cast<int>((p->V_real - c0) < vc ? (p->V_real - c0) : vc);
     cudaError_t e;
     if (p->dtype == VCE_BF16) {
+      const int parts = dh_part ? tc_dh_parts(*p, vc_act) : 1;
       e = launch_tc_bwd_chunk(*p, h, W, targets, lse, n_valid, g, static_cast<int>(c0), vc_act, G,
-                              static_cast<int>(vc), dH, c0 > 0, dW, p->tied_weights != 0, status, st);
+                              static_cast<int>(vc), dH, c0 > 0, dW, p->tied_weights != 0, dh_part, parts, status,
+                              st);
     } else {
       float* Gf = static_cast<float*>(G);
       const float* hf = static_cast<const float*>(h);
