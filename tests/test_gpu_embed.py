@@ -149,3 +149,16 @@ def test_embed_bwd_gptoss_full_deterministic():
         R.vce.vce_embed_bwd(p, ids_d, dE_d, dW_d, ws)
         torch.cuda.synchronize()
         assert torch.equal(dW_d.view(torch.int32), first.view(torch.int32))
+
+
+@pytest.mark.parametrize("T,V_real,Vp", [(20000, 1000, 1024),      # more tokens than the shared-memory sort holds
+                                         (5000, 1048000, 1048064)])  # id and t need more than 32 bits together
+def test_embed_bwd_workspace_sort_path(T, V_real, Vp):
+    wl = I.custom(T=T, H=64, V_real=V_real, Vp=Vp, S=8, dtype="bf16", seed=16, pad_id_frac=0.05, oor_id_frac=0.05)
+    d = I.make_all(wl, ("ids", "dE"))
+    ids = d["ids"].copy()
+    ids[: T // 4] = V_real - 1                 # one heavy id across many runs
+    rng = np.random.default_rng(8)
+    ids = rng.permutation(ids)
+    dW0 = np.zeros((wl.Vp, wl.H), np.float32)
+    _check_bwd(wl, ids, d["dE"], dW0)

@@ -66,12 +66,19 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
 
 // ---------------------------------------------------------------------------
 // Backward, step 1: one CTA sorts the valid (id, t) keys and builds the runs.
+// Two variants: keys in shared memory (T <= 16384 and id, t packed in 32 bits)
+// and keys in the workspace (any size, 64-bit keys). Both leave the sorted
+// token indices in `tsorted` and the run descriptors in `runs`.
 // ---------------------------------------------------------------------------
 constexpr int kSortThreads = 1024;
 constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kSortItems = 8;
 constexpr int kSortTile = kSortThreads * kSortItems;
 constexpr int kRadix = 256;
+constexpr int kSmemSortMax = 16384;                       // keys the shared-memory variant holds
+constexpr int kSmemItems = kSmemSortMax / kSortThreads;   // 16 keys per thread
+constexpr size_t kSmemSortBytes =
+    2 * kSmemSortMax * sizeof(uint32_t) + kSortWarps * kRadix * sizeof(int) + 64 * sizeof(int);
 
 struct RunDesc {
   int32_t start, end;   // sorted positions [start, end)
@@ -84,7 +91,7 @@ struct RunDesc {
 };
 
 struct BwdLayout {
-  size_t hdr, keys_a, keys_b, seg_start, runs, counters, partials, total;
+  size_t hdr, keys_a, keys_b, seg_start, tsorted, runs, counters, partials, total;
   int64_t n_counters, n_slots;
   int nh;
 };
@@ -108,11 +115,18 @@ BwdLayout bwd_layout(const vce_problem& p) {
   L.keys_a = take(sizeof(uint64_t) * (T + 1));
   L.keys_b = take(sizeof(uint64_t) * (T + 1));
   L.seg_start = take(sizeof(int32_t) * (T + 2));
+  L.tsorted = take(sizeof(int32_t) * (T + 1));
   L.runs = take(sizeof(RunDesc) * (T + 1));
   L.counters = take(sizeof(int32_t) * L.n_counters);
   L.partials = take(sizeof(float) * L.n_slots * p.H);
   L.total = off;
   return L;
+}
+
+int bit_width(int64_t x) {   // bits needed for values in [0, x)
+  int b = 1;
+  while (b < 62 && (int64_t(1) << b) < x) ++b;
+  return b;
 }
 
 // Block-wide exclusive scan of one int per thread (1024 threads).
@@ -144,9 +158,186 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sh_warp, int* total) 
   return res;
 }
 
+// Runs of kEmbedBwdChunk tokens for the segments [s0, s0 + per_thread) of one
+// thread (all threads together cover [0, nseg) in order); slots for multi-run
+// ids. seg[s] is the sorted position where segment s starts (segment s ends at
+// seg[s + 1], the last one at n); id_of(s) gives its id.
+template <typename IdOf>
+__device__ __forceinline__ void build_runs(const int* seg, int nseg, int n, int per_thread, int nh, IdOf id_of,
+                                           int* sh_warp, int32_t* hdr, RunDesc* runs, int32_t* counters) {
+  const int s0 = threadIdx.x * per_thread;
+  int my_runs = 0, my_multi = 0, my_slots = 0;
+  for (int j = 0; j < per_thread; ++j) {
+    const int s = s0 + j;
+    if (s < nseg) {
+      const int en = s + 1 < nseg ? seg[s + 1] : n;
+      const int nr = (en - seg[s] + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+      my_runs += nr;
+      if (nr > 1) {
+        my_multi += 1;
+        my_slots += nr;
+      }
+    }
+  }
+  int t_runs, t_multi, t_slots;
+  int r0 = block_excl_scan(my_runs, sh_warp, &t_runs);
+  int m0 = block_excl_scan(my_multi, sh_warp, &t_multi);
+  int q0 = block_excl_scan(my_slots, sh_warp, &t_slots);
+  for (int j = 0; j < per_thread; ++j) {
+    const int s = s0 + j;
+    if (s >= nseg) break;
+    const int st = seg[s], en = s + 1 < nseg ? seg[s + 1] : n;
+    const int nr = (en - st + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+    const bool multi = nr > 1;
+    const int id = id_of(s);
+    for (int k = 0; k < nr; ++k) {
+      RunDesc r;
+      r.start = st + k * kEmbedBwdChunk;
+      r.end = min(en, st + (k + 1) * kEmbedBwdChunk);
+      r.id = id;
+      r.slot = multi ? q0 + k : -1;
+      r.mseg = multi ? m0 : -1;
+      r.nruns = nr;
+      r.first_slot = multi ? q0 : -1;
+      r.pad = 0;
+      runs[r0 + k] = r;
+    }
+    if (multi) {
+      for (int hh = 0; hh < nh; ++hh) counters[m0 * nh + hh] = 0;
+      m0 += 1;
+      q0 += nr;
+    }
+    r0 += nr;
+  }
+  if (threadIdx.x == 0) {
+    hdr[1] = t_runs;
+    hdr[3] = t_multi;
+    hdr[4] = t_slots;
+  }
+}
+
+// Shared-memory variant: keys (id << tbits) | t in 32 bits, T <= kSmemSortMax.
+__global__ void __launch_bounds__(kSortThreads, 1)
+    embed_sort_smem_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int idbits, int nh,
+                           int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
+  extern __shared__ __align__(16) uint32_t smem_keys[];
+  uint32_t* ka = smem_keys;
+  uint32_t* kb = smem_keys + kSmemSortMax;
+  int* wcnt = reinterpret_cast<int*>(smem_keys + 2 * kSmemSortMax);
+  int* sh_warp = wcnt + kSortWarps * kRadix;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // Phase 0: stable compaction of the valid ids (tokens blocked 16 per thread).
+  int64_t idv[kSmemItems];
+  int cnt = 0;
+  const int t0 = tid * kSmemItems;
+#pragma unroll
+  for (int j = 0; j < kSmemItems; ++j) {
+    const int t = t0 + j;
+    idv[j] = t < T ? ids[t] : -1;
+    cnt += (idv[j] >= 0 && idv[j] < V_real) ? 1 : 0;
+  }
+  int n;
+  int pos = block_excl_scan(cnt, sh_warp, &n);
+#pragma unroll
+  for (int j = 0; j < kSmemItems; ++j)
+    if (idv[j] >= 0 && idv[j] < V_real)
+      ka[pos++] = (static_cast<uint32_t>(idv[j]) << tbits) | static_cast<uint32_t>(t0 + j);
+  __syncthreads();
+
+  // Phase 1: stable LSD radix passes over the id bits; each warp owns a
+  // contiguous slice of the keys, ranked 32 at a time in order.
+  const int slice = ((n + kSortWarps - 1) / kSortWarps + 31) / 32 * 32;
+  const int steps = slice / 32;
+  uint32_t* src = ka;
+  uint32_t* dst = kb;
+  for (int shift = tbits; shift < tbits + idbits; shift += 8) {
+    for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) wcnt[i] = 0;
+    __syncthreads();
+    uint32_t key[kSmemItems];
+    int dig[kSmemItems], rank[kSmemItems];
+#pragma unroll
+    for (int j = 0; j < kSmemItems; ++j) {
+      const int idx = warp * slice + j * 32 + lane;
+      const bool ok = j < steps && idx < n;
+      key[j] = ok ? src[idx] : 0u;
+      const int d = ok ? static_cast<int>((key[j] >> shift) & 0xFFu) : (kRadix + lane);
+      dig[j] = d;
+      rank[j] = 0;
+      if (j < steps) {
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        const int before = __popc(peers & ((1u << lane) - 1u));
+        int c0 = 0;
+        if (ok) c0 = wcnt[warp * kRadix + d];
+        __syncwarp();
+        if (ok && before == 0) wcnt[warp * kRadix + d] = c0 + __popc(peers);
+        __syncwarp();
+        rank[j] = c0 + before;
+      }
+    }
+    __syncthreads();
+    {
+      int tot = 0;
+      if (tid < kRadix)
+        for (int w = 0; w < kSortWarps; ++w) tot += wcnt[w * kRadix + tid];
+      int all;
+      int s = block_excl_scan(tid < kRadix ? tot : 0, sh_warp, &all);
+      if (tid < kRadix) {
+        for (int w = 0; w < kSortWarps; ++w) {
+          const int c = wcnt[w * kRadix + tid];
+          wcnt[w * kRadix + tid] = s;
+          s += c;
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kSmemItems; ++j) {
+      const int idx = warp * slice + j * 32 + lane;
+      if (j < steps && idx < n) dst[wcnt[warp * kRadix + dig[j]] + rank[j]] = key[j];
+    }
+    __syncthreads();
+    uint32_t* tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+
+  // Phase 2: segment starts (positions blocked 16 per thread) into the free
+  // key buffer, at most n <= kSmemSortMax entries.
+  const uint32_t tmask = (1u << tbits) - 1u;
+  int* seg = reinterpret_cast<int*>(dst);
+  int heads = 0;
+  const int p0 = tid * kSmemItems;
+#pragma unroll
+  for (int j = 0; j < kSmemItems; ++j) {
+    const int q = p0 + j;
+    if (q < n) {
+      tsorted[q] = static_cast<int32_t>(src[q] & tmask);
+      if (q == 0 || (src[q] >> tbits) != (src[q - 1] >> tbits)) ++heads;
+    }
+  }
+  int nseg;
+  int sidx = block_excl_scan(heads, sh_warp, &nseg);
+#pragma unroll
+  for (int j = 0; j < kSmemItems; ++j) {
+    const int q = p0 + j;
+    if (q < n && (q == 0 || (src[q] >> tbits) != (src[q - 1] >> tbits))) seg[sidx++] = q;
+  }
+  __syncthreads();
+  const uint32_t* sorted = src;
+  auto id_of = [&](int sg) { return static_cast<int>(sorted[seg[sg]] >> tbits); };
+  build_runs(seg, nseg, n, kSmemItems, nh, id_of, sh_warp, hdr, runs, counters);
+  if (tid == 0) {
+    hdr[0] = n;
+    hdr[2] = nseg;
+  }
+}
+
+// Workspace variant: 64-bit keys (id << 32) | t, any T.
 __global__ void __launch_bounds__(kSortThreads, 1)
     embed_sort_kernel(const int64_t* __restrict__ ids, int64_t T, int64_t V_real, int nh, int32_t* hdr,
-                      uint64_t* keys_a, uint64_t* keys_b, int32_t* seg_start, RunDesc* runs, int32_t* counters) {
+                      uint64_t* keys_a, uint64_t* keys_b, int32_t* seg_start, int32_t* tsorted, RunDesc* runs,
+                      int32_t* counters) {
   __shared__ int sh_warp[33];
   __shared__ int hist[kRadix];
   __shared__ int carry[kRadix];
@@ -242,72 +433,40 @@ __global__ void __launch_bounds__(kSortThreads, 1)
     dst = tmp;
   }
 
-  // Phase 2a: id boundaries in the sorted keys.
+  // Phase 2a: id boundaries in the sorted keys; sorted token indices.
   int nseg = 0;
+  int32_t* seg_ids = reinterpret_cast<int32_t*>(dst);   // the free key buffer
   for (int base = 0; base < n; base += kSortTile) {
     int cnt = 0;
     const int p0 = base + tid * kSortItems;
 #pragma unroll
     for (int j = 0; j < kSortItems; ++j) {
       const int q = p0 + j;
-      if (q < n && (q == 0 || (src[q] >> 32) != (src[q - 1] >> 32))) ++cnt;
+      if (q < n) {
+        tsorted[q] = static_cast<int32_t>(src[q] & 0xFFFFFFFFull);
+        if (q == 0 || (src[q] >> 32) != (src[q - 1] >> 32)) ++cnt;
+      }
     }
     int tot;
     int s = nseg + block_excl_scan(cnt, sh_warp, &tot);
 #pragma unroll
     for (int j = 0; j < kSortItems; ++j) {
       const int q = p0 + j;
-      if (q < n && (q == 0 || (src[q] >> 32) != (src[q - 1] >> 32))) seg_start[s++] = q;
+      if (q < n && (q == 0 || (src[q] >> 32) != (src[q - 1] >> 32))) {
+        seg_start[s] = q;
+        seg_ids[s] = static_cast<int32_t>(src[q] >> 32);
+        ++s;
+      }
     }
     nseg += tot;
   }
-  if (tid == 0) seg_start[nseg] = n;
   __syncthreads();
-
-  // Phase 2b: runs of kEmbedBwdChunk tokens per id; slots for multi-run ids.
-  int run_base = 0, mseg_base = 0, slot_base = 0;
-  for (int base = 0; base < nseg; base += kSortThreads) {
-    const int s = base + tid;
-    int len = 0, nr = 0;
-    if (s < nseg) {
-      len = seg_start[s + 1] - seg_start[s];
-      nr = (len + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
-    }
-    const int multi = nr > 1 ? 1 : 0;
-    int t_runs, t_mseg, t_slots;
-    const int r0 = run_base + block_excl_scan(nr, sh_warp, &t_runs);
-    const int m0 = mseg_base + block_excl_scan(multi, sh_warp, &t_mseg);
-    const int q0 = slot_base + block_excl_scan(multi ? nr : 0, sh_warp, &t_slots);
-    if (s < nseg) {
-      const int st = seg_start[s];
-      const int en = seg_start[s + 1];
-      const int id = static_cast<int>(src[st] >> 32);
-      for (int j = 0; j < nr; ++j) {
-        RunDesc r;
-        r.start = st + j * kEmbedBwdChunk;
-        r.end = min(en, st + (j + 1) * kEmbedBwdChunk);
-        r.id = id;
-        r.slot = multi ? q0 + j : -1;
-        r.mseg = multi ? m0 : -1;
-        r.nruns = nr;
-        r.first_slot = multi ? q0 : -1;
-        r.pad = 0;
-        runs[r0 + j] = r;
-      }
-      if (multi)
-        for (int hh = 0; hh < nh; ++hh) counters[m0 * nh + hh] = 0;
-    }
-    run_base += t_runs;
-    mseg_base += t_mseg;
-    slot_base += t_slots;
-  }
+  auto id_of = [&](int sg) { return static_cast<int>(seg_ids[sg]); };
+  build_runs(seg_start, nseg, n, (nseg + kSortThreads - 1) / kSortThreads, nh, id_of, sh_warp, hdr, runs,
+             counters);
   if (tid == 0) {
     hdr[0] = n;
-    hdr[1] = run_base;
     hdr[2] = nseg;
-    hdr[3] = mseg_base;
-    hdr[4] = slot_base;
-    hdr[5] = (src == keys_a) ? 0 : 1;   // which buffer holds the sorted keys
   }
 }
 
@@ -336,36 +495,43 @@ __device__ __forceinline__ void widen<float>(const uint4& v, float (&o)[4]) {
 
 template <typename TE>
 __global__ void __launch_bounds__(128)
-    embed_reduce_kernel(const int32_t* __restrict__ hdr, const uint64_t* __restrict__ keys_a,
-                        const uint64_t* __restrict__ keys_b, const RunDesc* __restrict__ runs,
-                        const TE* __restrict__ dE, float* __restrict__ dW, float* partials, int32_t* counters,
-                        int H, int nh) {
+    embed_reduce_kernel(const int32_t* __restrict__ hdr, const int32_t* __restrict__ tsorted,
+                        const RunDesc* __restrict__ runs, const TE* __restrict__ dE, float* __restrict__ dW,
+                        float* partials, int32_t* counters, int H, int nh) {
   constexpr int VEC = 16 / sizeof(TE);
+  constexpr int NQ = VEC / 4;
   constexpr int U = 8;   // rows loaded ahead of the sequential adds
   __shared__ int s_last;
-  const uint64_t* keys = hdr[5] ? keys_b : keys_a;
+  const int lane = threadIdx.x & 31;
   const int n_items = hdr[1] * nh;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int r = item / nh, hs = item - r * nh;
     const RunDesc rd = runs[r];
+    const int len = rd.end - rd.start;   // <= 32
     const int col = hs * 128 * VEC + static_cast<int>(threadIdx.x) * VEC;
     const bool active = col < H;
+    // the run's token indices, one per lane, broadcast below
+    const int my_t = lane < len ? tsorted[rd.start + lane] : 0;
+    float4* row = reinterpret_cast<float4*>(dW + static_cast<int64_t>(rd.id) * H + col);
+    float4 w[NQ];
+    if (rd.slot < 0 && active) {   // single-run id: fetch the row now, add once the sum is ready
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) w[q] = row[q];
+    }
     float acc[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
-    for (int p = rd.start; p < rd.end; p += U) {
+    for (int p = 0; p < len; p += U) {
       uint4 v[U];
 #pragma unroll
       for (int k = 0; k < U; ++k) {
+        const int t = __shfl_sync(0xffffffffu, my_t, (p + k) & 31);
         v[k] = make_uint4(0, 0, 0, 0);
-        if (active && p + k < rd.end) {
-          const int64_t t = static_cast<int64_t>(keys[p + k] & 0xFFFFFFFFull);
-          v[k] = __ldg(reinterpret_cast<const uint4*>(dE + t * H + col));
-        }
+        if (active && p + k < len) v[k] = __ldg(reinterpret_cast<const uint4*>(dE + static_cast<int64_t>(t) * H + col));
       }
 #pragma unroll
       for (int k = 0; k < U; ++k) {
-        if (p + k < rd.end) {          // tokens in ascending t, one add each
+        if (p + k < len) {          // tokens in ascending t, one add each
           float f[VEC];
           widen<TE>(v[k], f);
 #pragma unroll
@@ -375,22 +541,20 @@ __global__ void __launch_bounds__(128)
     }
     if (rd.slot < 0) {
       if (active) {
-        float4* row = reinterpret_cast<float4*>(dW + static_cast<int64_t>(rd.id) * H + col);
 #pragma unroll
-        for (int q = 0; q < VEC / 4; ++q) {
-          float4 w = row[q];
-          w.x = w.x + acc[4 * q + 0];
-          w.y = w.y + acc[4 * q + 1];
-          w.z = w.z + acc[4 * q + 2];
-          w.w = w.w + acc[4 * q + 3];
-          row[q] = w;
+        for (int q = 0; q < NQ; ++q) {
+          w[q].x = w[q].x + acc[4 * q + 0];
+          w[q].y = w[q].y + acc[4 * q + 1];
+          w[q].z = w[q].z + acc[4 * q + 2];
+          w[q].w = w[q].w + acc[4 * q + 3];
+          row[q] = w[q];
         }
       }
     } else {
       if (active) {
         float4* slot = reinterpret_cast<float4*>(partials + static_cast<int64_t>(rd.slot) * H + col);
 #pragma unroll
-        for (int q = 0; q < VEC / 4; ++q)
+        for (int q = 0; q < NQ; ++q)
           __stcg(slot + q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
       }
       __threadfence();
@@ -406,7 +570,7 @@ __global__ void __launch_bounds__(128)
         float tot[VEC];
         const float4* s0 = reinterpret_cast<const float4*>(partials + static_cast<int64_t>(rd.first_slot) * H + col);
 #pragma unroll
-        for (int q = 0; q < VEC / 4; ++q) {
+        for (int q = 0; q < NQ; ++q) {
           float4 a = __ldcg(s0 + q);
           tot[4 * q] = a.x; tot[4 * q + 1] = a.y; tot[4 * q + 2] = a.z; tot[4 * q + 3] = a.w;
         }
@@ -414,7 +578,7 @@ __global__ void __launch_bounds__(128)
           const float4* sj =
               reinterpret_cast<const float4*>(partials + static_cast<int64_t>(rd.first_slot + j) * H + col);
 #pragma unroll
-          for (int q = 0; q < VEC / 4; ++q) {
+          for (int q = 0; q < NQ; ++q) {
             float4 a = __ldcg(sj + q);
             tot[4 * q] = tot[4 * q] + a.x;
             tot[4 * q + 1] = tot[4 * q + 1] + a.y;
@@ -422,15 +586,14 @@ __global__ void __launch_bounds__(128)
             tot[4 * q + 3] = tot[4 * q + 3] + a.w;
           }
         }
-        float4* row = reinterpret_cast<float4*>(dW + static_cast<int64_t>(rd.id) * H + col);
 #pragma unroll
-        for (int q = 0; q < VEC / 4; ++q) {
-          float4 w = row[q];
-          w.x = w.x + tot[4 * q + 0];
-          w.y = w.y + tot[4 * q + 1];
-          w.z = w.z + tot[4 * q + 2];
-          w.w = w.w + tot[4 * q + 3];
-          row[q] = w;
+        for (int q = 0; q < NQ; ++q) {
+          float4 x = row[q];
+          x.x = x.x + tot[4 * q + 0];
+          x.y = x.y + tot[4 * q + 1];
+          x.z = x.z + tot[4 * q + 2];
+          x.w = x.w + tot[4 * q + 3];
+          row[q] = x;
         }
       }
       __syncthreads();
@@ -465,20 +628,36 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   uint64_t* ka = reinterpret_cast<uint64_t*>(b + L.keys_a);
   uint64_t* kb = reinterpret_cast<uint64_t*>(b + L.keys_b);
   int32_t* seg = reinterpret_cast<int32_t*>(b + L.seg_start);
+  int32_t* tsorted = reinterpret_cast<int32_t*>(b + L.tsorted);
   RunDesc* runs = reinterpret_cast<RunDesc*>(b + L.runs);
   int32_t* counters = reinterpret_cast<int32_t*>(b + L.counters);
   float* partials = reinterpret_cast<float*>(b + L.partials);
-  embed_sort_kernel<<<1, kSortThreads, 0, st>>>(ids, p.T, p.V_real, L.nh, hdr, ka, kb, seg, runs, counters);
+  const int tbits = bit_width(p.T);
+  const int idbits = bit_width(p.V_real);
+  if (p.T <= kSmemSortMax && tbits + idbits <= 32) {
+    static bool configured = false;
+    if (!configured) {
+      cudaError_t e = cudaFuncSetAttribute(embed_sort_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kSmemSortBytes));
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    embed_sort_smem_kernel<<<1, kSortThreads, kSmemSortBytes, st>>>(ids, static_cast<int>(p.T), p.V_real, tbits,
+                                                                    idbits, L.nh, hdr, tsorted, runs, counters);
+  } else {
+    embed_sort_kernel<<<1, kSortThreads, 0, st>>>(ids, p.T, p.V_real, L.nh, hdr, ka, kb, seg, tsorted, runs,
+                                                  counters);
+  }
   note_launch(VCE_K_EMBED_SORT, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const DevInfo di = current_device_info();
   const int grid = di.num_sms * 8;
   if (p.dtype == VCE_BF16)
-    embed_reduce_kernel<uint16_t><<<grid, 128, 0, st>>>(hdr, ka, kb, runs, static_cast<const uint16_t*>(dE), dW,
+    embed_reduce_kernel<uint16_t><<<grid, 128, 0, st>>>(hdr, tsorted, runs, static_cast<const uint16_t*>(dE), dW,
                                                         partials, counters, static_cast<int>(p.H), L.nh);
   else
-    embed_reduce_kernel<float><<<grid, 128, 0, st>>>(hdr, ka, kb, runs, static_cast<const float*>(dE), dW,
+    embed_reduce_kernel<float><<<grid, 128, 0, st>>>(hdr, tsorted, runs, static_cast<const float*>(dE), dW,
                                                      partials, counters, static_cast<int>(p.H), L.nh);
   note_launch(VCE_K_EMBED_REDUCE, st);
   return cudaGetLastError();
