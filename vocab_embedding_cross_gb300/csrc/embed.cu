@@ -77,8 +77,11 @@ constexpr int kSortTile = kSortThreads * kSortItems;
 constexpr int kRadix = 256;
 constexpr int kSmemSortMax = 16384;                       // keys the shared-memory variant holds
 constexpr int kSmemItems = kSmemSortMax / kSortThreads;   // 16 keys per thread
-constexpr size_t kSmemSortBytes =
-    2 * kSmemSortMax * sizeof(uint32_t) + kSortWarps * kRadix * sizeof(int) + 64 * sizeof(int);
+// Shared-memory arrays are padded by one word per 32 (index i at i + i/32), so
+// that each thread's 16 consecutive entries fall in distinct banks across a warp.
+__host__ __device__ constexpr int pad32(int i) { return i + (i >> 5); }
+constexpr size_t kSmemSortBytes = 2 * pad32(kSmemSortMax) * sizeof(uint32_t) +
+                                  pad32(16 * kSortThreads) * sizeof(int) + 64 * sizeof(int);
 
 struct RunDesc {
   int32_t start, end;   // sorted positions [start, end)
@@ -162,16 +165,16 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sh_warp, int* total) 
 // thread (all threads together cover [0, nseg) in order); slots for multi-run
 // ids. seg[s] is the sorted position where segment s starts (segment s ends at
 // seg[s + 1], the last one at n); id_of(s) gives its id.
-template <typename IdOf>
-__device__ __forceinline__ void build_runs(const int* seg, int nseg, int n, int per_thread, int nh, IdOf id_of,
+template <typename SegAt, typename IdOf>
+__device__ __forceinline__ void build_runs(SegAt seg, int nseg, int n, int per_thread, int nh, IdOf id_of,
                                            int* sh_warp, int32_t* hdr, RunDesc* runs, int32_t* counters) {
   const int s0 = threadIdx.x * per_thread;
   int my_runs = 0, my_multi = 0, my_slots = 0;
   for (int j = 0; j < per_thread; ++j) {
     const int s = s0 + j;
     if (s < nseg) {
-      const int en = s + 1 < nseg ? seg[s + 1] : n;
-      const int nr = (en - seg[s] + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+      const int en = s + 1 < nseg ? seg(s + 1) : n;
+      const int nr = (en - seg(s) + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
       my_runs += nr;
       if (nr > 1) {
         my_multi += 1;
@@ -186,7 +189,7 @@ __device__ __forceinline__ void build_runs(const int* seg, int nseg, int n, int 
   for (int j = 0; j < per_thread; ++j) {
     const int s = s0 + j;
     if (s >= nseg) break;
-    const int st = seg[s], en = s + 1 < nseg ? seg[s + 1] : n;
+    const int st = seg(s), en = s + 1 < nseg ? seg(s + 1) : n;
     const int nr = (en - st + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
     const bool multi = nr > 1;
     const int id = id_of(s);
@@ -222,114 +225,175 @@ __global__ void __launch_bounds__(kSortThreads, 1)
                            int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
   extern __shared__ __align__(16) uint32_t smem_keys[];
   uint32_t* ka = smem_keys;
-  uint32_t* kb = smem_keys + kSmemSortMax;
-  int* wcnt = reinterpret_cast<int*>(smem_keys + 2 * kSmemSortMax);
-  int* sh_warp = wcnt + kSortWarps * kRadix;
+  uint32_t* kb = smem_keys + pad32(kSmemSortMax);
+  int* ctab = reinterpret_cast<int*>(smem_keys + 2 * pad32(kSmemSortMax));   // [16 digits][1024 threads]
+  int* sh_warp = ctab + pad32(16 * kSortThreads);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
 
-  // Phase 0: stable compaction of the valid ids (tokens blocked 16 per thread).
-  int64_t idv[kSmemItems];
-  int cnt = 0;
-  const int t0 = tid * kSmemItems;
-#pragma unroll
-  for (int j = 0; j < kSmemItems; ++j) {
-    const int t = t0 + j;
-    idv[j] = t < T ? ids[t] : -1;
-    cnt += (idv[j] >= 0 && idv[j] < V_real) ? 1 : 0;
+  // Phase 0: stable compaction of the valid ids. Warp w reads its contiguous
+  // block of tokens 32 at a time (coalesced); ballots give the order.
+  const int tpw = ((T + kSortWarps - 1) / kSortWarps + 31) / 32 * 32;   // tokens per warp, <= 512
+  int wcount = 0;
+  for (int j = 0; j < tpw / 32; ++j) {
+    const int t = warp * tpw + j * 32 + lane;
+    const int64_t id = t < T ? ids[t] : -1;
+    wcount += __popc(__ballot_sync(0xffffffffu, id >= 0 && id < V_real));
   }
-  int n;
-  int pos = block_excl_scan(cnt, sh_warp, &n);
-#pragma unroll
-  for (int j = 0; j < kSmemItems; ++j)
-    if (idv[j] >= 0 && idv[j] < V_real)
-      ka[pos++] = (static_cast<uint32_t>(idv[j]) << tbits) | static_cast<uint32_t>(t0 + j);
+  if (lane == 0) sh_warp[warp] = wcount;
+  __syncthreads();
+  int wbase = 0, n = 0;
+  for (int w = 0; w < kSortWarps; ++w) {
+    const int c = sh_warp[w];
+    wbase += w < warp ? c : 0;
+    n += c;
+  }
+  __syncthreads();
+  for (int j = 0; j < tpw / 32; ++j) {
+    const int t = warp * tpw + j * 32 + lane;
+    const int64_t id = t < T ? ids[t] : -1;
+    const bool ok = id >= 0 && id < V_real;
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    if (ok) ka[pad32(wbase + __popc(bal & lt_mask))] = (static_cast<uint32_t>(id) << tbits) | static_cast<uint32_t>(t);
+    wbase += __popc(bal);
+  }
   __syncthreads();
 
-  // Phase 1: stable LSD radix passes over the id bits; each warp owns a
-  // contiguous slice of the keys, ranked 32 at a time in order.
-  const int slice = ((n + kSortWarps - 1) / kSortWarps + 31) / 32 * 32;
-  const int steps = slice / 32;
+  // Phase 1: stable LSD radix passes over the id bits, 4 bits per pass. Thread
+  // tid owns kpt consecutive keys and ranks them with its own shared-memory
+  // counter per digit; the table of counters (digit-major, thread-minor) is
+  // scanned once per pass, which gives every key its stable destination.
+  const int kpt = (n + kSortThreads - 1) / kSortThreads;   // keys per thread, <= 16
+  const int k0 = tid * kpt;
   uint32_t* src = ka;
   uint32_t* dst = kb;
-  for (int shift = tbits; shift < tbits + idbits; shift += 8) {
-    for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) wcnt[i] = 0;
-    __syncthreads();
+  for (int shift = tbits; shift < tbits + idbits; shift += 4) {
     uint32_t key[kSmemItems];
-    int dig[kSmemItems], rank[kSmemItems];
+    uint32_t lrw[kSmemItems / 4] = {};   // byte j%4 of word j/4: rank among this thread's keys of that digit
+#pragma unroll
+    for (int b = 0; b < 16; ++b) ctab[pad32(b * kSortThreads + tid)] = 0;
 #pragma unroll
     for (int j = 0; j < kSmemItems; ++j) {
-      const int idx = warp * slice + j * 32 + lane;
-      const bool ok = j < steps && idx < n;
-      key[j] = ok ? src[idx] : 0u;
-      const int d = ok ? static_cast<int>((key[j] >> shift) & 0xFFu) : (kRadix + lane);
-      dig[j] = d;
-      rank[j] = 0;
-      if (j < steps) {
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
-        const int before = __popc(peers & ((1u << lane) - 1u));
-        int c0 = 0;
-        if (ok) c0 = wcnt[warp * kRadix + d];
-        __syncwarp();
-        if (ok && before == 0) wcnt[warp * kRadix + d] = c0 + __popc(peers);
-        __syncwarp();
-        rank[j] = c0 + before;
+      const bool ok = j < kpt && k0 + j < n;
+      key[j] = ok ? src[pad32(k0 + j)] : 0u;
+      if (ok) {
+        int* c = &ctab[pad32(static_cast<int>((key[j] >> shift) & 15u) * kSortThreads + tid)];
+        const int v = *c;
+        *c = v + 1;
+        lrw[j >> 2] |= static_cast<uint32_t>(v) << ((j & 3) * 8);
       }
     }
     __syncthreads();
     {
-      int tot = 0;
-      if (tid < kRadix)
-        for (int w = 0; w < kSortWarps; ++w) tot += wcnt[w * kRadix + tid];
+      int v[16];
+      int sum = 0;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        v[k] = ctab[pad32(tid * 16 + k)];
+        sum += v[k];
+      }
       int all;
-      int s = block_excl_scan(tid < kRadix ? tot : 0, sh_warp, &all);
-      if (tid < kRadix) {
-        for (int w = 0; w < kSortWarps; ++w) {
-          const int c = wcnt[w * kRadix + tid];
-          wcnt[w * kRadix + tid] = s;
-          s += c;
-        }
+      int run = block_excl_scan(sum, sh_warp, &all);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        ctab[pad32(tid * 16 + k)] = run;
+        run += v[k];
       }
     }
     __syncthreads();
 #pragma unroll
-    for (int j = 0; j < kSmemItems; ++j) {
-      const int idx = warp * slice + j * 32 + lane;
-      if (j < steps && idx < n) dst[wcnt[warp * kRadix + dig[j]] + rank[j]] = key[j];
-    }
+    for (int j = 0; j < kSmemItems; ++j)
+      if (j < kpt && k0 + j < n)
+        dst[pad32(ctab[pad32(static_cast<int>((key[j] >> shift) & 15u) * kSortThreads + tid)] +
+                  static_cast<int>((lrw[j >> 2] >> ((j & 3) * 8)) & 0xFFu))] = key[j];
     __syncthreads();
     uint32_t* tmp = src;
     src = dst;
     dst = tmp;
   }
 
-  // Phase 2: segment starts (positions blocked 16 per thread) into the free
-  // key buffer, at most n <= kSmemSortMax entries.
+  // Phase 2: sorted token indices to global memory; segment starts into the
+  // free key buffer (seg), one entry per distinct id, at most n <= 16384.
   const uint32_t tmask = (1u << tbits) - 1u;
   int* seg = reinterpret_cast<int*>(dst);
   int heads = 0;
-  const int p0 = tid * kSmemItems;
-#pragma unroll
-  for (int j = 0; j < kSmemItems; ++j) {
-    const int q = p0 + j;
+  for (int j = 0; j < kpt; ++j) {
+    const int q = k0 + j;
     if (q < n) {
-      tsorted[q] = static_cast<int32_t>(src[q] & tmask);
-      if (q == 0 || (src[q] >> tbits) != (src[q - 1] >> tbits)) ++heads;
+      tsorted[q] = static_cast<int32_t>(src[pad32(q)] & tmask);
+      if (q == 0 || (src[pad32(q)] >> tbits) != (src[pad32(q - 1)] >> tbits)) ++heads;
     }
   }
   int nseg;
   int sidx = block_excl_scan(heads, sh_warp, &nseg);
-#pragma unroll
-  for (int j = 0; j < kSmemItems; ++j) {
-    const int q = p0 + j;
-    if (q < n && (q == 0 || (src[q] >> tbits) != (src[q - 1] >> tbits))) seg[sidx++] = q;
+  for (int j = 0; j < kpt; ++j) {
+    const int q = k0 + j;
+    if (q < n && (q == 0 || (src[pad32(q)] >> tbits) != (src[pad32(q - 1)] >> tbits))) seg[pad32(sidx++)] = q;
   }
   __syncthreads();
-  const uint32_t* sorted = src;
-  auto id_of = [&](int sg) { return static_cast<int>(sorted[seg[sg]] >> tbits); };
-  build_runs(seg, nseg, n, kSmemItems, nh, id_of, sh_warp, hdr, runs, counters);
+
+  // Phase 3: runs of kEmbedBwdChunk tokens. Per segment s: nr runs; packed
+  // prefix rb[s] = (runs before s) << 16 | (multi-run segments before s) in
+  // ctab. Then each run is written by one thread, which finds its segment by
+  // binary search.
+  auto seg_end = [&](int sg) { return sg + 1 < nseg ? seg[pad32(sg + 1)] : n; };
+  const int spt = (nseg + kSortThreads - 1) / kSortThreads;   // segments per thread, <= 16
+  const int s0 = tid * spt;
+  int packed = 0;
+  for (int j = 0; j < spt; ++j) {
+    const int sg = s0 + j;
+    if (sg < nseg) {
+      const int nr = (seg_end(sg) - seg[pad32(sg)] + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+      packed += (nr << 16) | (nr > 1 ? 1 : 0);
+    }
+  }
+  int tot_packed;
+  int pre = block_excl_scan(packed, sh_warp, &tot_packed);
+  for (int j = 0; j < spt; ++j) {
+    const int sg = s0 + j;
+    if (sg < nseg) {
+      ctab[pad32(sg)] = pre;
+      const int nr = (seg_end(sg) - seg[pad32(sg)] + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+      pre += (nr << 16) | (nr > 1 ? 1 : 0);
+    }
+  }
+  __syncthreads();
+  const int n_runs = tot_packed >> 16, n_multi = tot_packed & 0xFFFF;
+  for (int r = tid; r < n_runs; r += kSortThreads) {
+    int lo = 0, hi = nseg - 1;   // largest sg with runs-before(sg) <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((ctab[pad32(mid)] >> 16) <= r)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int sg = lo;
+    const int rb = ctab[pad32(sg)] >> 16, mb = ctab[pad32(sg)] & 0xFFFF;
+    const int st = seg[pad32(sg)], en = seg_end(sg);
+    const int nr = (en - st + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+    const int k = r - rb;
+    const bool multi = nr > 1;
+    const int q0 = rb - (sg - mb);   // slots used by the multi-run segments before sg
+    RunDesc rd;
+    rd.start = st + k * kEmbedBwdChunk;
+    rd.end = min(en, rd.start + kEmbedBwdChunk);
+    rd.id = static_cast<int32_t>(src[pad32(st)] >> tbits);
+    rd.slot = multi ? q0 + k : -1;
+    rd.mseg = multi ? mb : -1;
+    rd.nruns = nr;
+    rd.first_slot = multi ? q0 : -1;
+    rd.pad = 0;
+    runs[r] = rd;
+    if (multi && k == 0)
+      for (int hh = 0; hh < nh; ++hh) counters[mb * nh + hh] = 0;
+  }
   if (tid == 0) {
     hdr[0] = n;
+    hdr[1] = n_runs;
     hdr[2] = nseg;
+    hdr[3] = n_multi;
+    hdr[4] = (tot_packed >> 16) - (nseg - n_multi);
   }
 }
 
@@ -462,7 +526,8 @@ __global__ void __launch_bounds__(kSortThreads, 1)
   }
   __syncthreads();
   auto id_of = [&](int sg) { return static_cast<int>(seg_ids[sg]); };
-  build_runs(seg_start, nseg, n, (nseg + kSortThreads - 1) / kSortThreads, nh, id_of, sh_warp, hdr, runs,
+  auto seg_at = [&](int sg) { return seg_start[sg]; };
+  build_runs(seg_at, nseg, n, (nseg + kSortThreads - 1) / kSortThreads, nh, id_of, sh_warp, hdr, runs,
              counters);
   if (tid == 0) {
     hdr[0] = n;
