@@ -338,6 +338,57 @@ def head_gradient_rows(h, W, targets, V_real: int, lse: np.ndarray, scale: float
     return (p * scale).T @ hf
 
 
+# ---------------------------------------------------------------------------
+# Sampled softmax ("Sampled Softmax with Over-Tokenized Transformer", Setup:
+# the loss_fn listing scores this GPU's targets plus random negatives, P
+# tokens in all, and takes the cross-entropy at each target's position in
+# that candidate list; no correction for the sampling is applied)
+# ---------------------------------------------------------------------------
+
+def sampled_candidates(targets, V_real: int, P: int, draws, ignore_index: int = IGNORE_INDEX):
+    """The candidate list and each target's position in it.
+
+    Reading: the distinct valid targets in ascending order, then negatives
+    taken in draw order from `draws` (distinct uniform draws from [0, V_real),
+    the random numbers of the method), skipping any that is a target, until P
+    entries. Ignored or bad targets keep ignore_index as position.
+    """
+    y = np.asarray(targets, dtype=np.int64)
+    valid, _ = target_status(y, V_real, ignore_index)
+    uniq = np.unique(y[valid])
+    if uniq.size > P:
+        raise ValueError("more distinct targets than candidates")
+    taken = set(uniq.tolist())
+    negs = []
+    for d in np.asarray(draws, dtype=np.int64):
+        if len(negs) == P - uniq.size:
+            break
+        if int(d) not in taken:
+            negs.append(int(d))
+    if len(negs) < P - uniq.size:
+        raise ValueError("not enough draws to fill the candidate list")
+    cand = np.concatenate([uniq, np.array(negs, dtype=np.int64)])
+    pos = np.full(y.shape, ignore_index, dtype=np.int64)
+    pos[valid] = np.searchsorted(uniq, y[valid])
+    return cand, pos, int(uniq.size)
+
+
+def sampled_cross_entropy(h, W, targets, V_real: int, Vp: int, cand, pos, g: float = 1.0,
+                          ignore_index: int = IGNORE_INDEX):
+    """Cross-entropy over the P candidate classes only (logits h W[cand]^T),
+    its gradient with respect to h, and the gradient of the full W, which is
+    non-zero only on the candidate rows."""
+    cand = np.asarray(cand, dtype=np.int64)
+    P = cand.size
+    Wc = _as_f64(W)[cand]
+    fwd = cross_entropy_forward(h, Wc, pos, P, ignore_index, g=g)
+    dH, dWc = cross_entropy_backward(h, Wc, pos, P, P, ignore_index, g=g)
+    dW = np.zeros((Vp, Wc.shape[1]), dtype=np.float64)
+    dW[cand] += dWc
+    fwd.update(dH=dH, dW=dW, dW_cand=dWc)
+    return fwd
+
+
 def target_owner(targets, V_real: int, Vp: int, S: int,
                  ignore_index: int = IGNORE_INDEX) -> np.ndarray:
     """Shard that owns each valid target, -1 for ignored or bad ones (P3)."""

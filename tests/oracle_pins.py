@@ -375,10 +375,56 @@ def pin_gradient_invariants(O):
     assert np.allclose(part, dW[rows], rtol=0, atol=1e-15)
 
 
+def pin_sampled_candidates(O):
+    """Candidate list: sorted distinct targets (numpy's unique), then draws in
+    order that are not targets; positions point back at each target."""
+    rng = np.random.default_rng(70)
+    V, P, T = 500, 160, 120
+    y = rng.integers(0, V, T)
+    y[:5] = IGN
+    y[5:40] = 7                               # repeats
+    draws = rng.permutation(V)
+    cand, pos, nu = O.sampled_candidates(y, V, P, draws)
+    uniq = np.unique(y[y != IGN])
+    assert nu == uniq.size and np.array_equal(cand[:nu], uniq)
+    assert cand.size == P and np.unique(cand).size == P
+    negs = cand[nu:]
+    assert not np.isin(negs, uniq).any()
+    order = [int(np.nonzero(draws == v)[0][0]) for v in negs]
+    assert order == sorted(order)
+    expected_first = [d for d in draws if d not in set(uniq.tolist())][:P - nu]
+    assert list(negs) == expected_first
+    valid = y != IGN
+    assert np.array_equal(cand[pos[valid]], y[valid]) and np.all(pos[~valid] == IGN)
+
+
+def pin_sampled_full_set_is_full_softmax(O):
+    """With every class a candidate (P = V_real), the sampled loss is the full
+    loss and its gradients the full gradients (the candidate order only
+    permutes the classes)."""
+    T, H, V = 30, 8, 40
+    h, W, y = _rand_case(71, T, H, V, 64, ignore=(3,))
+    draws = np.random.default_rng(72).permutation(V)
+    cand, pos, _ = O.sampled_candidates(y, V, V, draws)
+    r = O.sampled_cross_entropy(h, W, y, V, 64, cand, pos)
+    full = O.cross_entropy_forward(h, W, y, V)
+    dH, dW = O.cross_entropy_backward(h, W, y, V, 64)
+    assert abs(r["loss"] - full["loss"]) < 1e-12
+    assert np.allclose(r["dH"], dH, atol=1e-14) and np.allclose(r["dW"], dW, atol=1e-14)
+    # a smaller candidate list: torch's cross-entropy on the gathered logits
+    y2 = np.where(y == IGN, IGN, y % 10)      # at most 10 distinct targets
+    cand, pos, nu = O.sampled_candidates(y2, V, 16, draws)
+    assert nu <= 10
+    z = torch.tensor(h) @ torch.tensor(W)[torch.tensor(cand)].T
+    ref = F.cross_entropy(z, torch.tensor(pos), ignore_index=IGN).item()
+    assert abs(O.sampled_cross_entropy(h, W, y2, V, 64, cand, pos)["loss"] - ref) < 1e-12
+
+
 ALL_PINS = [
     pin_pad_vocab, pin_shards_tp_page, pin_shards_cover, pin_embedding_forward,
     pin_embedding_backward, pin_embedding_replay_order, pin_embedding_replay_bound,
     pin_equal_logits, pin_normalisation, pin_padded_head_demo, pin_bruteforce_decimal,
     pin_torch_cross_entropy, pin_shard_invariance, pin_ignored_and_bad,
-    pin_finite_differences, pin_gradient_invariants,
+    pin_finite_differences, pin_gradient_invariants, pin_sampled_candidates,
+    pin_sampled_full_set_is_full_softmax,
 ]

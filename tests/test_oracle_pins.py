@@ -64,6 +64,12 @@ MUTATIONS = {
                              "for c0 in reversed(range(0, len(ts), chunk)):"),
     # repeated tokens overwrite instead of accumulating
     "embed_bwd_overwrite": ("dW[v] += dEf[t]", "dW[v] = dEf[t]"),
+    # negatives taken in sorted order instead of draw order
+    "sampled_sorted_negatives": ("    for d in np.asarray(draws, dtype=np.int64):",
+                                 "    for d in np.sort(np.asarray(draws, dtype=np.int64)):"),
+    # target positions off by one in the candidate list
+    "sampled_pos_shift": ("    pos[valid] = np.searchsorted(uniq, y[valid])",
+                          "    pos[valid] = np.searchsorted(uniq, y[valid], side='right')"),
     # target logit taken from the wrong shard offset
     "target_local_off": ("z_tgt[t] = blocks[owner[t]][t, local[t]]",
                          "z_tgt[t] = blocks[owner[t]][t, max(local[t] - 1, 0)]"),

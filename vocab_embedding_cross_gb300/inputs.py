@@ -78,7 +78,20 @@ WORKLOADS: Dict[str, Workload] = {
                              Vp=201088, S=8, dtype="bf16", tied=False, seed=3,
                              pad_fill=None, token_dist="zipf", h_kind="rmsnorm",
                              pad_id_frac=0.02, oor_id_frac=0.01),
+    # Sampled softmax over P = 8192 candidates of the Qwen3 vocabulary.
+    "sampled": Workload("sampled", T=16384, H=2048, V_real=151936, Vp=151936, S=8,
+                        dtype="bf16", tied=False, seed=4, pad_fill=None,
+                        token_dist="zipf", h_kind="rmsnorm"),
 }
+
+SAMPLED_P = 8192   # candidates of the sampled-softmax workload
+
+
+def make_negative_draws(wl: Workload, n: int) -> np.ndarray:
+    """Uniform draws without replacement from [0, V_real), in draw order: the
+    random numbers the sampled softmax consumes for its negatives."""
+    rng = _rng(wl, "cand")
+    return rng.permutation(wl.V_real)[:n].astype(np.int64)
 
 
 def custom(name: str = "custom", **kw) -> Workload:
