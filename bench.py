@@ -243,6 +243,9 @@ def run_ours(args):
     # ---- end to end through the C ABI with host buffers ----
     e2e = run_e2e(args, vce, D, d, p, W, E, loss, lse, dH, dW, st, ws_f, ws_b, ws_e, stream, wl)
 
+    # ---- sampled-softmax variant, against the full-vocabulary loss ----
+    sampled = run_sampled(args, vce, D, I, stream, peaks, full_loss_tok_s=T / (loss_ms / 1e3) if loss_ms else None)
+
     # ---- CPU baseline (rank 0, N = 1 only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -266,6 +269,7 @@ def run_ours(args):
                              if loss_tflops else None,
                              "executed_flops": 8.0 * T * H * V, "vc": int(vc)},
             "embedding": emb,
+            "sampled_softmax": sampled,
             "per_kernel_ms": {k: round(v[0], 4) for k, v in sorted(per_kind.items())},
             "per_kernel_launches": {k: v[1] for k, v in sorted(per_kind.items())},
             "gpu_launches": int(launches),
@@ -277,6 +281,71 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_sampled(args, vce, D, I, stream, peaks, full_loss_tok_s):
+    """The sampled-softmax loss step (T=16384, H=2048, V=151936, P=8192
+    candidates: candidate list, gather of W[cand], cross-entropy over the
+    candidates forward and backward, scatter of dW into the candidate rows),
+    one vce_sampled_loss call per step, device resident, timed like the main
+    step; compared with the full-vocabulary loss fwd+bwd of the main workload."""
+    import torch
+    wl = I.WORKLOADS["sampled"]
+    P = I.SAMPLED_P
+    d = I.make_all(wl, ("W", "h", "targets"))
+    T, H = wl.T, wl.H
+    p = vce.problem(T, H, wl.Vp, wl.V_real, wl.S, vce.VCE_BF16)
+    W, h = D.to_device(d["W"]), D.to_device(d["h"])
+    y = torch.from_numpy(d["targets"]).cuda()
+    draws = torch.from_numpy(I.make_negative_draws(wl, P)).cuda()
+    loss = torch.empty(1, device="cuda")
+    dH = torch.empty((T, H), device="cuda")
+    dW = torch.zeros((wl.Vp, H), device="cuda")
+    cand = torch.empty(P, dtype=torch.int64, device="cuda")
+    pos = torch.empty(T, dtype=torch.int64, device="cuda")
+    nu = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = D.workspace(vce.vce_sampled_workspace_size(p, P))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = stream.cuda_stream
+
+    def step():
+        vce.vce_sampled_loss(p, h, W, y, draws, P, 1.0, loss, None, dH, dW, cand, pos, nu, ws, dev_status=st,
+                             stream=sp)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, vce.status_str(int(st.item()))
+    n = max(5, args.steps // 2)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    torch.cuda._sleep(100_000_000)
+    vce.vce_profile_begin(1024, stream=sp)
+    for _ in range(3):
+        step()
+    per = {}
+    for k, dt in vce.vce_profile_end(1024):
+        per[k] = per.get(k, 0.0) + dt / 3
+    tok_s = T / (ms / 1e3)
+    credited = 6.0 * T * H * P
+    out = {"workload": f"sampled: T={T} H={H} V={wl.V_real} P={P} S={wl.S} untied, Zipf(1.1) targets",
+           "step": "vce_sampled_loss (candidates + gather + CE fwd/bwd over P + dW scatter)",
+           "tokens_per_s": round(tok_s, 1), "ms_per_step": round(ms, 4), "steps": n,
+           "n_unique_targets": int(nu.item()),
+           "credited_TFLOPs": round(credited / (ms / 1e3) / 1e12, 1),
+           "frac_of_burst": round(credited / (ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+           "per_kernel_ms": {k: round(v, 4) for k, v in sorted(per.items())},
+           "full_vocab_loss_tokens_per_s": round(full_loss_tok_s, 1) if full_loss_tok_s else None,
+           "speedup_vs_full_vocab_loss": round(tok_s / full_loss_tok_s, 3) if full_loss_tok_s else None}
+    del W, h, dW, dH, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, vce, D, d, p, W, E, loss, lse, dH, dW, st, ws_f, ws_b, ws_e, stream, wl):

@@ -55,7 +55,8 @@ typedef enum vce_op {
   VCE_OP_EMBED_FWD = 0,
   VCE_OP_EMBED_BWD = 1,
   VCE_OP_LOSS_FWD = 2,
-  VCE_OP_LOSS_BWD = 3
+  VCE_OP_LOSS_BWD = 3,
+  VCE_OP_SAMPLED_CANDIDATES = 4
 } vce_op;
 
 /*
@@ -174,6 +175,59 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W,
                         int32_t* dev_status, void* stream);
 
 /*
+ * Candidate list of a sampled softmax ["Sampled Softmax with Over-Tokenized
+ * Transformer", Setup: the loss scores the batch's targets plus random
+ * negatives, P tokens in all, at each target's position in that list].
+ *   cand[0 .. U)  the distinct valid targets (0 <= y < V_real), ascending;
+ *   cand[U .. P)  the entries of `draws` that are not targets, in draw order;
+ *   pos[t]        index of targets[t] in cand, or ignore_index when the target
+ *                 is ignored or invalid;  *n_unique = U.
+ * `draws` (device, n_draws int64) are the method's random numbers: distinct
+ * values drawn uniformly from [0, V_real) (e.g. a prefix of a random
+ * permutation); entries outside [0, V_real) are skipped. Uses p->T, p->V_real
+ * and p->ignore_index. cand[P], pos[T] int64 and n_unique (one int32) are
+ * device outputs. Data errors go to dev_status: a target that is neither
+ * valid nor ignore_index -> VCE_ERR_BAD_INDEX (treated as ignored); U > P or
+ * too few usable draws -> VCE_ERR_ARG; the unfilled entries of cand are then
+ * -1 (and, when U > P, every entry of cand is -1 and every pos ignore_index).
+ * Workspace: vce_workspace_size(p, VCE_OP_SAMPLED_CANDIDATES) bytes.
+ */
+vce_status vce_sampled_candidates(const vce_problem* p, const int64_t* targets, const int64_t* draws,
+                                  int64_t n_draws, int64_t P, int64_t* cand, int64_t* pos,
+                                  int32_t* n_unique, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                  void* stream);
+
+/*
+ * Sampled-softmax loss, forward and backward in one call ["Sampled Softmax
+ * with Over-Tokenized Transformer", Setup and its loss listing: the head's
+ * logits are taken over W[cand] only and the cross-entropy is taken at
+ * position_in(cand, target)]. In order, on `stream`:
+ *   1. vce_sampled_candidates  -> cand[P], pos[T], *n_unique
+ *   2. Wc = W[cand]            (vce_embed_fwd with T = P, ids = cand; a [P, H]
+ *                               table in the workspace, padded to 64 rows)
+ *   3. the globally normalised cross-entropy over the P candidate columns
+ *      (vce_loss_fwd with Vp = P rounded up to 64, V_real = P, S = 1,
+ *      targets = pos) -> *loss (mean over valid tokens), lse[T]
+ *   4. its backward (vce_loss_bwd, untied) -> dH[T,H] overwritten, and the
+ *      candidate rows' gradient dWc[P,H] in the workspace
+ *   5. dW[cand[i], :] += dWc[i, :] (vce_embed_bwd of an fp32 problem with
+ *      T = P, ids = cand); rows of dW that are not candidates are untouched.
+ * p describes the full problem (T, H, Vp, V_real, S, dtype, ignore_index; its
+ * tied_weights is ignored: dW is always accumulated into). h[T,H] and W[Vp,H]
+ * in p->dtype, dW[Vp,H] fp32, g the upstream gradient of the mean loss.
+ * lse may be NULL (kept in the workspace). Statuses and data errors as for the
+ * five steps; dev_status collects the first data error of any of them.
+ * Workspace: vce_sampled_workspace_size(p, P) bytes recommended; less is
+ * accepted down to the size that lets the backward run in 256-column chunks.
+ */
+size_t vce_sampled_workspace_size(const vce_problem* p, int64_t P);
+vce_status vce_sampled_loss(const vce_problem* p, const void* h, const void* W, const int64_t* targets,
+                            const int64_t* draws, int64_t n_draws, int64_t P, float g, float* loss,
+                            float* lse, float* dH, float* dW, int64_t* cand, int64_t* pos,
+                            int32_t* n_unique, void* ws, size_t ws_bytes, int32_t* dev_status,
+                            void* stream);
+
+/*
  * Loss forward without a caller workspace. The method's pages have no
  * counterpart to this call; it exists for callers that cannot allocate device
  * memory (a plugin inside a framework that owns all device memory and hands it
@@ -248,7 +302,7 @@ typedef enum vce_kernel_kind {
   VCE_K_TC_FWD = 3, VCE_K_TC_GRAD = 4, VCE_K_TC_DH = 5, VCE_K_TC_DW = 6,
   VCE_K_MERGE = 7, VCE_K_LOSS_MEAN = 8, VCE_K_COUNT_VALID = 9,
   VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13,
-  VCE_K_DH_REDUCE = 14
+  VCE_K_DH_REDUCE = 14, VCE_K_SAMPLED_CAND = 15
 } vce_kernel_kind;
 uint64_t vce_launch_count(void);
 vce_status vce_profile_begin(int32_t capacity, void* stream);

@@ -110,3 +110,21 @@ def test_workspace_too_small_rejected_on_host(L):
         vce.VCE_ERR_WORKSPACE
     assert L.vce_embed_bwd(ctypes.byref(p), 0x1000, 0x2000, 0x3000, 0x4010, need, None, None) == \
         vce.VCE_ERR_WORKSPACE                      # misaligned workspace
+
+
+def test_sampled_candidates_rejected_on_host(L):
+    import ctypes
+    p = P(dtype=vce.VCE_F32)
+    ws_need = vce.vce_workspace_size(p, vce.VCE_OP_SAMPLED_CANDIDATES)
+    assert 1000 + 4 * 1000 <= ws_need < vce.SIZE_MAX
+    fake = 1 << 20   # never dereferenced: every case below fails validation first
+    call = L.vce_sampled_candidates
+    assert call(ctypes.byref(p), fake, fake, 10, 0, fake, fake, fake, fake, ws_need, None, None) == vce.VCE_ERR_ARG
+    assert call(ctypes.byref(p), fake, fake, 10, 1001, fake, fake, fake, fake, ws_need, None,
+                None) == vce.VCE_ERR_ARG
+    assert call(ctypes.byref(p), None, fake, 10, 100, fake, fake, fake, fake, ws_need, None,
+                None) == vce.VCE_ERR_ARG
+    assert call(ctypes.byref(p), fake, fake, 10, 100, fake, fake, fake, fake, ws_need - 1, None,
+                None) == vce.VCE_ERR_WORKSPACE
+    assert call(ctypes.byref(p), fake, fake, 10, 100, fake, fake, fake, None, ws_need, None,
+                None) == vce.VCE_ERR_WORKSPACE

@@ -19,6 +19,7 @@ VCE_OK, VCE_ERR_ARG, VCE_ERR_UNSUPPORTED, VCE_ERR_CUDA = 0, 1, 2, 3
 VCE_ERR_BAD_INDEX, VCE_ERR_TIMEOUT, VCE_ERR_WORKSPACE = 4, 5, 6
 VCE_F32, VCE_BF16 = 0, 1
 VCE_OP_EMBED_FWD, VCE_OP_EMBED_BWD, VCE_OP_LOSS_FWD, VCE_OP_LOSS_BWD = 0, 1, 2, 3
+VCE_OP_SAMPLED_CANDIDATES = 4
 SIZE_MAX = (1 << 64) - 1
 
 
@@ -62,6 +63,15 @@ def lib():
         L.vce_loss_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_void_p, c_void_p,
                                    c_void_p, c_size_t, c_void_p, c_void_p]
         L.vce_loss_bwd.restype = c_int32
+        L.vce_sampled_candidates.argtypes = [P, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p,
+                                             c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
+        L.vce_sampled_candidates.restype = c_int32
+        L.vce_sampled_workspace_size.argtypes = [P, c_int64]
+        L.vce_sampled_workspace_size.restype = c_size_t
+        L.vce_sampled_loss.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_float,
+                                       c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                       c_void_p, c_size_t, c_void_p, c_void_p]
+        L.vce_sampled_loss.restype = c_int32
         L.vce_status_str.argtypes = [c_int32]
         L.vce_status_str.restype = ctypes.c_char_p
         L.vce_embed_bwd_chunk.argtypes = []
@@ -155,6 +165,29 @@ def vce_loss_bwd(p, h, W, targets, lse, g, dH, dW, ws, ws_bytes=None, dev_status
            "vce_loss_bwd")
 
 
+def vce_sampled_candidates(p, targets, draws, P, cand, pos, n_unique, ws, ws_bytes=None, dev_status=None,
+                           stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    n_draws = 0 if draws is None else draws.numel()
+    _check(lib().vce_sampled_candidates(ctypes.byref(p), _ptr(targets), _ptr(draws), int(n_draws), int(P),
+                                        _ptr(cand), _ptr(pos), _ptr(n_unique), _ptr(ws), nb, _ptr(dev_status),
+                                        _stream(stream)), "vce_sampled_candidates")
+
+
+def vce_sampled_workspace_size(p: VceProblem, P: int) -> int:
+    return int(lib().vce_sampled_workspace_size(ctypes.byref(p), int(P)))
+
+
+def vce_sampled_loss(p, h, W, targets, draws, P, g, loss, lse, dH, dW, cand, pos, n_unique, ws, ws_bytes=None,
+                     dev_status=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    n_draws = 0 if draws is None else draws.numel()
+    _check(lib().vce_sampled_loss(ctypes.byref(p), _ptr(h), _ptr(W), _ptr(targets), _ptr(draws), int(n_draws),
+                                  int(P), float(g), _ptr(loss), _ptr(lse), _ptr(dH), _ptr(dW), _ptr(cand),
+                                  _ptr(pos), _ptr(n_unique), _ptr(ws), nb, _ptr(dev_status), _stream(stream)),
+           "vce_sampled_loss")
+
+
 def vce_embed_bwd_chunk() -> int:
     return int(lib().vce_embed_bwd_chunk())
 
@@ -173,7 +206,7 @@ def vce_wait_selftest(limit_ns: int, dev_status, stream=None) -> None:
 
 KERNEL_KINDS = ["embed_gather", "embed_sort", "embed_reduce", "tc_fwd", "tc_grad", "tc_dh", "tc_dw",
                 "merge", "loss_mean", "count_valid", "simt_fwd", "simt_grad", "sgemm", "wait_selftest",
-                "dh_reduce"]
+                "dh_reduce", "sampled_cand"]
 
 
 def vce_launch_count() -> int:

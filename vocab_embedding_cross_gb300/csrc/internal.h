@@ -105,4 +105,10 @@ int tc_dh_parts(const vce_problem& p, int vc_act);
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t st);
 
+// Sampled-softmax candidate list.
+size_t sampled_ws_bytes(const vce_problem& p);
+cudaError_t launch_sampled_candidates(const vce_problem& p, const int64_t* targets, const int64_t* draws,
+                                      int64_t n_draws, int64_t P, int64_t* cand, int64_t* pos, int32_t* n_unique,
+                                      void* ws, int32_t* status, cudaStream_t st);
+
 }  // namespace vce

@@ -179,6 +179,53 @@ size_t dh_part_bytes(const vce_problem& p) {
                   kWsAlign);
 }
 
+// ----- sampled softmax: the sub-problems and the workspace layout -----
+// Candidate table: P rows, padded to a multiple of 64 for the loss kernels.
+int64_t cand_rows(int64_t P) { return ceil_div(P, 64) * 64; }
+// Gather W[cand] (and scatter into dW): T = P ids into the full table.
+vce_problem sampled_table_problem(const vce_problem& p, int64_t P, int32_t dtype) {
+  vce_problem q = p;
+  q.T = P;
+  q.dtype = dtype;
+  q.tied_weights = 0;
+  return q;
+}
+// Cross-entropy over the candidate columns: one dense table, no vocabulary shards.
+vce_problem sampled_loss_problem(const vce_problem& p, int64_t P) {
+  vce_problem q = p;
+  q.Vp = cand_rows(P);
+  q.V_real = P;
+  q.S = 1;
+  q.tied_weights = 0;
+  return q;
+}
+struct SampledLayout {
+  size_t Wc, dWc, lse, loss, scratch, scratch_min, total, total_min;
+};
+// Wc[Pc,H] | dWc[Pc,H] fp32 | lse[T] | loss | scratch shared by the steps,
+// which run one after the other on the caller's stream.
+SampledLayout sampled_layout(const vce_problem& p, int64_t P) {
+  SampledLayout L{};
+  const vce_problem pl = sampled_loss_problem(p, P);
+  const vce_problem pe = sampled_table_problem(p, P, VCE_F32);
+  const size_t rows = static_cast<size_t>(cand_rows(P)), H = static_cast<size_t>(p.H);
+  L.Wc = 0;
+  L.dWc = align_up(rows * H * esize_of(p), kWsAlign);
+  L.lse = L.dWc + align_up(rows * H * sizeof(float), kWsAlign);
+  L.loss = L.lse + align_up(sizeof(float) * static_cast<size_t>(p.T), kWsAlign);
+  L.scratch = L.loss + kWsAlign;
+  size_t common = sampled_ws_bytes(p);
+  common = common > fwd_layout(pl).total ? common : fwd_layout(pl).total;
+  common = common > embed_bwd_ws_bytes(pe) ? common : embed_bwd_ws_bytes(pe);
+  const size_t bwd_min = bwd_bytes_for(pl, pl.T == 0 ? 0 : 256);
+  const size_t bwd_rec = bwd_bytes_for(pl, bwd_recommended_cols(pl)) + dh_part_bytes(pl);
+  L.scratch_min = common > bwd_min ? common : bwd_min;
+  const size_t rec = common > bwd_rec ? common : bwd_rec;
+  L.total = L.scratch + rec;
+  L.total_min = L.scratch + L.scratch_min;
+  return L;
+}
+
 }  // namespace
 }  // namespace vce
 
@@ -250,6 +297,7 @@ size_t vce_workspace_size(const vce_problem* p, int32_t op) {
     case VCE_OP_EMBED_BWD: return embed_bwd_ws_bytes(*p);
     case VCE_OP_LOSS_FWD: return fwd_layout(*p).total;
     case VCE_OP_LOSS_BWD: return bwd_bytes_for(*p, bwd_recommended_cols(*p)) + dh_part_bytes(*p);
+    case VCE_OP_SAMPLED_CANDIDATES: return sampled_ws_bytes(*p);
   }
   return SIZE_MAX;
 }
@@ -378,6 +426,70 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
     if (e != cudaSuccess) return cuda_status(e);
   }
   return VCE_OK;
+}
+
+vce_status vce_sampled_candidates(const vce_problem* p, const int64_t* targets, const int64_t* draws,
+                                  int64_t n_draws, int64_t P, int64_t* cand, int64_t* pos, int32_t* n_unique,
+                                  void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (P < 1 || P > p->V_real || n_draws < 0) return VCE_ERR_ARG;
+  if (!cand || !n_unique || (p->T > 0 && (!targets || !pos)) || (n_draws > 0 && !draws)) return VCE_ERR_ARG;
+  if (!aligned(targets, 8) || !aligned(draws, 8) || !aligned(cand, 8) || !aligned(pos, 8) || !aligned(n_unique, 4))
+    return VCE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < sampled_ws_bytes(*p)) return VCE_ERR_WORKSPACE;
+  return cuda_status(launch_sampled_candidates(*p, targets, draws, n_draws, P, cand, pos, n_unique, ws, dev_status,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+size_t vce_sampled_workspace_size(const vce_problem* p, int64_t P) {
+  if (check_problem(p) != VCE_OK || P < 1 || P > p->V_real) return SIZE_MAX;
+  return sampled_layout(*p, P).total;
+}
+
+vce_status vce_sampled_loss(const vce_problem* p, const void* h, const void* W, const int64_t* targets,
+                            const int64_t* draws, int64_t n_draws, int64_t P, float g, float* loss, float* lse,
+                            float* dH, float* dW, int64_t* cand, int64_t* pos, int32_t* n_unique, void* ws,
+                            size_t ws_bytes, int32_t* dev_status, void* stream) {
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (P < 1 || P > p->V_real || n_draws < 0) return VCE_ERR_ARG;
+  if (!W || !dW || !cand || !n_unique || !loss || (n_draws > 0 && !draws)) return VCE_ERR_ARG;
+  if (p->T > 0 && (!h || !targets || !dH || !pos)) return VCE_ERR_ARG;
+  if (!aligned(dW, 16) || !aligned(loss, 4) || !aligned(lse, 4)) return VCE_ERR_UNSUPPORTED;
+  const SampledLayout L = sampled_layout(*p, P);
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < L.total_min) return VCE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* b = static_cast<char*>(ws);
+  void* Wc = b + L.Wc;
+  float* dWc = reinterpret_cast<float*>(b + L.dWc);
+  float* lse_c = lse ? lse : reinterpret_cast<float*>(b + L.lse);
+  void* scratch = b + L.scratch;
+  const size_t scratch_bytes = ws_bytes - L.scratch;
+  const vce_problem pg = sampled_table_problem(*p, P, p->dtype);
+  const vce_problem pl = sampled_loss_problem(*p, P);
+  const vce_problem pe = sampled_table_problem(*p, P, VCE_F32);
+  // 1. candidate list and each target's position in it
+  s = vce_sampled_candidates(p, targets, draws, n_draws, P, cand, pos, n_unique, scratch, scratch_bytes, dev_status,
+                             stream);
+  if (s != VCE_OK) return s;
+  // 2. Wc = W[cand]; the padding rows of the table are zero
+  const size_t row_bytes = static_cast<size_t>(p->H) * esize_of(*p);
+  if (pl.Vp > P) {
+    if (cudaError_t me = cudaMemsetAsync(static_cast<char*>(Wc) + P * row_bytes, 0, (pl.Vp - P) * row_bytes, st))
+      return cuda_status(me);
+  }
+  s = vce_embed_fwd(&pg, cand, W, Wc, nullptr, nullptr, dev_status, stream);
+  if (s != VCE_OK) return s;
+  // 3. cross-entropy over the candidate columns, targets remapped to positions
+  s = vce_loss_fwd(&pl, h, Wc, pos, loss, lse_c, nullptr, nullptr, nullptr, scratch, scratch_bytes, dev_status,
+                   stream);
+  if (s != VCE_OK) return s;
+  // 4. dH and the candidate rows' gradient dWc (overwritten)
+  s = vce_loss_bwd(&pl, h, Wc, pos, lse_c, g, dH, dWc, scratch, scratch_bytes, dev_status, stream);
+  if (s != VCE_OK) return s;
+  // 5. dW[cand[i]] += dWc[i]: the deterministic embedding backward in fp32
+  return vce_embed_bwd(&pe, cand, dWc, dW, scratch, scratch_bytes, dev_status, stream);
 }
 
 vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* stream) {
