@@ -1,0 +1,100 @@
+"""Small, self-contained invocations of the library for a profiler.
+
+    python -m vocab_embedding_cross_gb300.profile_case loss    [--tokens T] [--iters N]
+    python -m vocab_embedding_cross_gb300.profile_case embed   [--workload NAME] [--iters N]
+    python -m vocab_embedding_cross_gb300.profile_case sampled [--tokens T] [--iters N]
+
+`loss` runs the loss forward and backward (tied dW) on the Qwen3-like shapes
+(H=2048, V=151936, S=8) with T tokens; `embed` runs the embedding lookup and
+its backward on a named workload; `sampled` runs vce_sampled_loss (P=8192) with
+T tokens. Inputs are the seeded synthetic ones of `inputs.py`. Each case checks
+the device status word and exits non-zero on any error, so that a profiler is
+only pointed at a command that has already run cleanly.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import torch
+
+from . import _lib as vce
+from . import device as D
+from . import inputs as I
+
+
+def _loss(args):
+    wl = I.with_T(I.WORKLOADS["qwen3_tied"], args.tokens)
+    d = I.make_all(wl, ("W", "h", "targets"))
+    p = vce.problem(wl.T, wl.H, wl.Vp, wl.V_real, wl.S, vce.VCE_BF16, tied=True)
+    W, h = D.to_device(d["W"]), D.to_device(d["h"])
+    y = torch.from_numpy(d["targets"]).cuda()
+    loss = torch.empty(1, device="cuda")
+    lse = torch.empty(wl.T, device="cuda")
+    dH = torch.empty((wl.T, wl.H), device="cuda")
+    dW = torch.zeros((wl.Vp, wl.H), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws_f = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD))
+    ws_b = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD))
+    for _ in range(args.iters):
+        vce.vce_loss_fwd(p, h, W, y, loss, lse, ws=ws_f, dev_status=st)
+        vce.vce_loss_bwd(p, h, W, y, lse, 1.0, dH, dW, ws_b, dev_status=st)
+    torch.cuda.synchronize()
+    return int(st.item()), f"loss {loss.item():.6f}"
+
+
+def _embed(args):
+    wl = I.WORKLOADS[args.workload]
+    d = I.make_all(wl, ("W", "ids", "dE"))
+    p = vce.problem(wl.T, wl.H, wl.Vp, wl.V_real, wl.S, vce.VCE_BF16 if wl.dtype == "bf16" else vce.VCE_F32,
+                    tied=wl.tied)
+    W = D.to_device(d["W"])
+    ids = torch.from_numpy(d["ids"]).cuda()
+    dE = D.to_device(d["dE"])
+    E = torch.empty((wl.T, wl.H), dtype=W.dtype, device="cuda")
+    dW = torch.zeros((wl.Vp, wl.H), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_EMBED_BWD))
+    for _ in range(args.iters):
+        vce.vce_embed_fwd(p, ids, W, E, dev_status=st)
+        vce.vce_embed_bwd(p, ids, dE, dW, ws, dev_status=st)
+    torch.cuda.synchronize()
+    return int(st.item()), "embedding ok"
+
+
+def _sampled(args):
+    wl = I.with_T(I.WORKLOADS["sampled"], args.tokens)
+    P = I.SAMPLED_P
+    d = I.make_all(wl, ("W", "h", "targets"))
+    p = vce.problem(wl.T, wl.H, wl.Vp, wl.V_real, wl.S, vce.VCE_BF16)
+    W, h = D.to_device(d["W"]), D.to_device(d["h"])
+    y = torch.from_numpy(d["targets"]).cuda()
+    draws = torch.from_numpy(I.make_negative_draws(wl, P)).cuda()
+    loss = torch.empty(1, device="cuda")
+    dH = torch.empty((wl.T, wl.H), device="cuda")
+    dW = torch.zeros((wl.Vp, wl.H), device="cuda")
+    cand = torch.empty(P, dtype=torch.int64, device="cuda")
+    pos = torch.empty(wl.T, dtype=torch.int64, device="cuda")
+    nu = torch.empty(1, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = D.workspace(vce.vce_sampled_workspace_size(p, P))
+    for _ in range(args.iters):
+        vce.vce_sampled_loss(p, h, W, y, draws, P, 1.0, loss, None, dH, dW, cand, pos, nu, ws, dev_status=st)
+    torch.cuda.synchronize()
+    return int(st.item()), f"loss {loss.item():.6f}, {int(nu.item())} distinct targets"
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("case", choices=["loss", "embed", "sampled"])
+    ap.add_argument("--tokens", type=int, default=2048)
+    ap.add_argument("--workload", default="qwen3_tied")
+    ap.add_argument("--iters", type=int, default=2)
+    args = ap.parse_args(argv)
+    status, msg = {"loss": _loss, "embed": _embed, "sampled": _sampled}[args.case](args)
+    print(f"{args.case}: status {status} ({vce.status_str(status)}); {msg}")
+    return 0 if status == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
