@@ -182,9 +182,10 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W,
  *   cand[U .. P)  the entries of `draws` that are not targets, in draw order;
  *   pos[t]        index of targets[t] in cand, or ignore_index when the target
  *                 is ignored or invalid;  *n_unique = U.
- * `draws` (device, n_draws int64) are the method's random numbers: distinct
- * values drawn uniformly from [0, V_real) (e.g. a prefix of a random
- * permutation); entries outside [0, V_real) are skipped. Uses p->T, p->V_real
+ * `draws` (device, n_draws int64) are the method's random numbers, uniform
+ * over [0, V_real) (e.g. a prefix of a random permutation). Negatives are
+ * drawn without replacement: a draw that is a target, repeats an earlier
+ * negative or lies outside [0, V_real) is skipped, so cand holds distinct ids. Uses p->T, p->V_real
  * and p->ignore_index. cand[P], pos[T] int64 and n_unique (one int32) are
  * device outputs. Data errors go to dev_status: a target that is neither
  * valid nor ignore_index -> VCE_ERR_BAD_INDEX (treated as ignored); U > P or
@@ -210,8 +211,9 @@ vce_status vce_sampled_candidates(const vce_problem* p, const int64_t* targets, 
  *      targets = pos) -> *loss (mean over valid tokens), lse[T]
  *   4. its backward (vce_loss_bwd, untied) -> dH[T,H] overwritten, and the
  *      candidate rows' gradient dWc[P,H] in the workspace
- *   5. dW[cand[i], :] += dWc[i, :] (vce_embed_bwd of an fp32 problem with
- *      T = P, ids = cand); rows of dW that are not candidates are untouched.
+ *   5. dW[cand[i], :] += dWc[i, :], one fp32 addition per element (the
+ *      candidates are distinct); rows of dW that are not candidates, and
+ *      entries of cand that are -1, are untouched.
  * p describes the full problem (T, H, Vp, V_real, S, dtype, ignore_index; its
  * tied_weights is ignored: dW is always accumulated into). h[T,H] and W[Vp,H]
  * in p->dtype, dW[Vp,H] fp32, g the upstream gradient of the mean loss.
@@ -302,7 +304,7 @@ typedef enum vce_kernel_kind {
   VCE_K_TC_FWD = 3, VCE_K_TC_GRAD = 4, VCE_K_TC_DH = 5, VCE_K_TC_DW = 6,
   VCE_K_MERGE = 7, VCE_K_LOSS_MEAN = 8, VCE_K_COUNT_VALID = 9,
   VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13,
-  VCE_K_DH_REDUCE = 14, VCE_K_SAMPLED_CAND = 15
+  VCE_K_DH_REDUCE = 14, VCE_K_SAMPLED_CAND = 15, VCE_K_SAMPLED_SCATTER = 16
 } vce_kernel_kind;
 uint64_t vce_launch_count(void);
 vce_status vce_profile_begin(int32_t capacity, void* stream);

@@ -349,9 +349,12 @@ def sampled_candidates(targets, V_real: int, P: int, draws, ignore_index: int = 
     """The candidate list and each target's position in it.
 
     Reading: the distinct valid targets in ascending order, then negatives
-    taken in draw order from `draws` (distinct uniform draws from [0, V_real),
-    the random numbers of the method), skipping any that is a target, until P
-    entries. Ignored or bad targets keep ignore_index as position.
+    taken in draw order from `draws` (uniform draws from [0, V_real), the
+    random numbers of the method) until P entries. Negatives are drawn
+    without replacement, so a draw is skipped when it is a target, when it
+    repeats an earlier negative, or when it lies outside [0, V_real); every
+    class then appears at most once and a target's position is well defined.
+    Ignored or bad targets keep ignore_index as position.
     """
     y = np.asarray(targets, dtype=np.int64)
     valid, _ = target_status(y, V_real, ignore_index)
@@ -363,8 +366,10 @@ def sampled_candidates(targets, V_real: int, P: int, draws, ignore_index: int = 
     for d in np.asarray(draws, dtype=np.int64):
         if len(negs) == P - uniq.size:
             break
-        if int(d) not in taken:
-            negs.append(int(d))
+        d = int(d)
+        if 0 <= d < V_real and d not in taken:
+            negs.append(d)
+            taken.add(d)
     if len(negs) < P - uniq.size:
         raise ValueError("not enough draws to fill the candidate list")
     cand = np.concatenate([uniq, np.array(negs, dtype=np.int64)])

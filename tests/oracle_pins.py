@@ -396,6 +396,11 @@ def pin_sampled_candidates(O):
     assert list(negs) == expected_first
     valid = y != IGN
     assert np.array_equal(cand[pos[valid]], y[valid]) and np.all(pos[~valid] == IGN)
+    # draws with repeats and values outside the vocabulary, worked by hand:
+    # targets {2, 5}; draws 5 (a target), 9, -1 (outside), 9 (repeat), 500
+    # (outside), 3, 2 (a target), 7 -> negatives 9, 3, 7
+    cand, pos, nu = O.sampled_candidates([5, 2, IGN, 5], V, 5, [5, 9, -1, 9, 500, 3, 2, 7, 8])
+    assert list(cand) == [2, 5, 9, 3, 7] and nu == 2 and list(pos) == [1, 0, IGN, 1]
 
 
 def pin_sampled_full_set_is_full_softmax(O):

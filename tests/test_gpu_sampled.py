@@ -87,10 +87,28 @@ def test_candidates_skip_out_of_range_draws_and_flag_bad_targets():
     draws = I.make_negative_draws(wl, wl.V_real)
     noisy = np.insert(draws, [0, 10, 10, 500], [-1, 1000, 5000, -100]).astype(np.int64)
     cand, pos, nu, st = _candidates(wl, y, noisy, 256)
-    rc, rp, rnu = O.sampled_candidates(y, wl.V_real, 256, draws)
+    rc, rp, rnu = O.sampled_candidates(y, wl.V_real, 256, noisy)
     assert st == R.vce.VCE_ERR_BAD_INDEX
     assert nu == rnu and np.array_equal(cand, rc) and np.array_equal(pos, rp)
+    assert np.array_equal(rc, O.sampled_candidates(y, wl.V_real, 256, draws)[0])
     assert pos[5] == -100 and pos[6] == -100
+
+
+@pytest.mark.parametrize("P", [400, 900])
+def test_candidates_repeated_draws(P):
+    """Draws with replacement (repeats inside one round of 1024 draws and
+    across rounds): each class is taken once, at its first draw."""
+    wl = _small()
+    y = I.make_targets(wl)
+    rng = np.random.default_rng(31)
+    draws = rng.integers(0, wl.V_real, size=6000).astype(np.int64)
+    draws[1500:1600] = draws[100:200]              # repeats of an earlier round
+    draws[2100:2110] = 17                          # one value ten times in a round
+    cand, pos, nu, st = _candidates(wl, y, draws, P)
+    rc, rp, rnu = O.sampled_candidates(y, wl.V_real, P, draws)
+    assert st == 0
+    assert nu == rnu and np.array_equal(cand, rc) and np.array_equal(pos, rp)
+    assert np.unique(cand).size == P
 
 
 def test_candidates_data_errors():

@@ -67,6 +67,9 @@ MUTATIONS = {
     # negatives taken in sorted order instead of draw order
     "sampled_sorted_negatives": ("    for d in np.asarray(draws, dtype=np.int64):",
                                  "    for d in np.sort(np.asarray(draws, dtype=np.int64)):"),
+    # a repeated draw taken twice as a negative
+    "sampled_repeats_kept": ("            negs.append(d)\n            taken.add(d)",
+                             "            negs.append(d)"),
     # target positions off by one in the candidate list
     "sampled_pos_shift": ("    pos[valid] = np.searchsorted(uniq, y[valid])",
                           "    pos[valid] = np.searchsorted(uniq, y[valid], side='right')"),

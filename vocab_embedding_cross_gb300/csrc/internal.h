@@ -11,7 +11,7 @@
 namespace vce {
 
 constexpr int kEmbedBwdChunk = 32;      // run length of the embedding backward's order
-constexpr int kTcUnitWidth = 2048;      // vocab columns per forward work unit (tensor cores)
+constexpr int kTcUnitWidth = 2048;      // widest forward work unit (tensor cores), in vocab columns
 constexpr int kSimtUnitWidth = 256;     // vocab columns per forward work unit (fp32 SIMT)
 constexpr size_t kWsAlign = 256;
 
@@ -102,6 +102,9 @@ cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void*
 // the persistent grid); at most kMaxDhParts.
 constexpr int kMaxDhParts = 8;
 int tc_dh_parts(const vce_problem& p, int vc_act);
+// Forward unit width (a multiple of 256, at most kTcUnitWidth) that balances
+// the persistent grid's waves for this problem on the current device.
+int tc_unit_width(const vce_problem& p);
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t st);
 
@@ -110,5 +113,8 @@ size_t sampled_ws_bytes(const vce_problem& p);
 cudaError_t launch_sampled_candidates(const vce_problem& p, const int64_t* targets, const int64_t* draws,
                                       int64_t n_draws, int64_t P, int64_t* cand, int64_t* pos, int32_t* n_unique,
                                       void* ws, int32_t* status, cudaStream_t st);
+// dW[cand[i], :] += dWc[i, :] for the distinct candidates (rows with cand < 0 skipped).
+cudaError_t launch_sampled_scatter(const int64_t* cand, int64_t P, const vce_problem& p, const float* dWc, float* dW,
+                                   cudaStream_t st);
 
 }  // namespace vce

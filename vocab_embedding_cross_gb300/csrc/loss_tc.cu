@@ -32,6 +32,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <vector>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -705,6 +706,47 @@ __global__ void __launch_bounds__(256) dh_reduce_kernel(const float4* __restrict
 }
 
 }  // namespace
+
+int tc_unit_width(const vce_problem& p) {
+  // The persistent grid takes items in strides of the cluster count; pick the
+  // widest unit (fewest partials to merge) whose heaviest cluster carries no
+  // more than 1% over the best width's, counting 256-column tiles per item.
+  const DevInfo di = current_device_info();
+  const int64_t clusters = di.num_sms >= 2 ? di.num_sms / 2 : 1;
+  const int64_t n_mblk = ceil_div(p.T, BMP);
+  if (n_mblk == 0) return kTcUnitWidth;
+  struct Memo {
+    int64_t T, Vp, V_real, clusters;
+    int32_t S, uw;
+  };
+  thread_local Memo memo{-1, -1, -1, -1, -1, 0};
+  if (memo.T == p.T && memo.Vp == p.Vp && memo.V_real == p.V_real && memo.S == p.S && memo.clusters == clusters)
+    return memo.uw;
+  int best_uw = kTcUnitWidth;
+  int64_t best_load = -1;
+  std::vector<int64_t> load;
+  for (int uw = kTcUnitWidth; uw >= 512; uw -= BN) {
+    const UnitGrid ug = unit_grid(p, uw);
+    load.assign(static_cast<size_t>(clusters), 0);
+    for (int64_t u = 0; u < ug.n_units; ++u) {
+      const int64_t k = u / ug.ups, j = u - k * ug.ups;
+      const int64_t lo = shard_lo(k, p.Vp, p.S), hi = shard_lo(k + 1, p.Vp, p.S);
+      const int64_t vb = lo + j * uw;
+      int64_t ve = vb + uw < hi ? vb + uw : hi;
+      if (ve > p.V_real) ve = p.V_real;
+      const int64_t tiles = ve > vb ? ceil_div(ve - vb, BN) : 0;
+      for (int64_t m = 0; m < n_mblk; ++m) load[static_cast<size_t>((u * n_mblk + m) % clusters)] += tiles;
+    }
+    int64_t mx = 0;
+    for (int64_t v : load) mx = v > mx ? v : mx;
+    if (best_load < 0 || mx * 100 < best_load * 99) {
+      best_uw = uw;
+      best_load = mx;
+    }
+  }
+  memo = Memo{p.T, p.Vp, p.V_real, clusters, p.S, best_uw};
+  return best_uw;
+}
 
 int tc_dh_parts(const vce_problem& p, int vc_act) {
   const DevInfo di = current_device_info();

@@ -52,7 +52,7 @@ struct Layout {
 };
 Layout layout(const vce_problem& p) {
   Layout L{};
-  L.ug = unit_grid(p, p.dtype == VCE_BF16 ? kTcUnitWidth : kSimtUnitWidth);
+  L.ug = unit_grid(p, p.dtype == VCE_BF16 ? tc_unit_width(p) : kSimtUnitWidth);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;

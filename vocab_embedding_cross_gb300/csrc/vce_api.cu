@@ -127,7 +127,7 @@ struct FwdLayout {
 };
 FwdLayout fwd_layout(const vce_problem& p) {
   FwdLayout L{};
-  L.ug = unit_grid(p, p.dtype == VCE_BF16 ? kTcUnitWidth : kSimtUnitWidth);
+  L.ug = unit_grid(p, p.dtype == VCE_BF16 ? tc_unit_width(p) : kSimtUnitWidth);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -207,7 +207,6 @@ struct SampledLayout {
 SampledLayout sampled_layout(const vce_problem& p, int64_t P) {
   SampledLayout L{};
   const vce_problem pl = sampled_loss_problem(p, P);
-  const vce_problem pe = sampled_table_problem(p, P, VCE_F32);
   const size_t rows = static_cast<size_t>(cand_rows(P)), H = static_cast<size_t>(p.H);
   L.Wc = 0;
   L.dWc = align_up(rows * H * esize_of(p), kWsAlign);
@@ -216,7 +215,6 @@ SampledLayout sampled_layout(const vce_problem& p, int64_t P) {
   L.scratch = L.loss + kWsAlign;
   size_t common = sampled_ws_bytes(p);
   common = common > fwd_layout(pl).total ? common : fwd_layout(pl).total;
-  common = common > embed_bwd_ws_bytes(pe) ? common : embed_bwd_ws_bytes(pe);
   const size_t bwd_min = bwd_bytes_for(pl, pl.T == 0 ? 0 : 256);
   const size_t bwd_rec = bwd_bytes_for(pl, bwd_recommended_cols(pl)) + dh_part_bytes(pl);
   L.scratch_min = common > bwd_min ? common : bwd_min;
@@ -468,7 +466,6 @@ vce_status vce_sampled_loss(const vce_problem* p, const void* h, const void* W, 
   const size_t scratch_bytes = ws_bytes - L.scratch;
   const vce_problem pg = sampled_table_problem(*p, P, p->dtype);
   const vce_problem pl = sampled_loss_problem(*p, P);
-  const vce_problem pe = sampled_table_problem(*p, P, VCE_F32);
   // 1. candidate list and each target's position in it
   s = vce_sampled_candidates(p, targets, draws, n_draws, P, cand, pos, n_unique, scratch, scratch_bytes, dev_status,
                              stream);
@@ -488,8 +485,8 @@ vce_status vce_sampled_loss(const vce_problem* p, const void* h, const void* W, 
   // 4. dH and the candidate rows' gradient dWc (overwritten)
   s = vce_loss_bwd(&pl, h, Wc, pos, lse_c, g, dH, dWc, scratch, scratch_bytes, dev_status, stream);
   if (s != VCE_OK) return s;
-  // 5. dW[cand[i]] += dWc[i]: the deterministic embedding backward in fp32
-  return vce_embed_bwd(&pe, cand, dWc, dW, scratch, scratch_bytes, dev_status, stream);
+  // 5. dW[cand[i]] += dWc[i]: the candidates are distinct, one addition per element
+  return cuda_status(launch_sampled_scatter(cand, P, *p, dWc, dW, st));
 }
 
 vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* stream) {
