@@ -75,7 +75,8 @@ typedef enum vce_op {
  * rows [floor(k*Vp/S), floor((k+1)*Vp/S)). Any 1 <= S <= Vp is allowed.
  *
  * Limits: 0 <= T < 2^31, 1 <= H <= 65536, 64 <= Vp < 2^31, 1 <= V_real <= Vp.
- * `reserved` must be 0.
+ * `flags` is 0 or a combination of the vce_flag bits below (other bits are
+ * rejected with VCE_ERR_ARG).
  */
 typedef struct vce_problem {
   int64_t T;
@@ -86,8 +87,17 @@ typedef struct vce_problem {
   int32_t S;
   int32_t tied_weights;   /* 1: embedding and LM head share W and one fp32 dW */
   int32_t dtype;          /* vce_dtype */
-  int32_t reserved;
+  int32_t flags;          /* vce_flag bits */
 } vce_problem;
+
+typedef enum vce_flag {
+  /* vce_loss_bwd: add G W into dH instead of overwriting it. Lets a second
+   * loss term on the same hidden states (the OT-H head of "Sampled Softmax with
+   * Over-Tokenized Transformer", Setup: a second head on h[:-1] predicting
+   * tokens[2:] at weight 0.1) accumulate its gradient into the first one's dH:
+   * pass dH itself with T-1 rows and g = 0.1. */
+  VCE_FLAG_ACCUMULATE_DH = 1
+} vce_flag;
 
 /* Bytes of workspace the call `op` needs for problem `p` (0 if none, SIZE_MAX
  * if the problem is invalid). The workspace must be 256-byte aligned. For
@@ -158,7 +168,7 @@ vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W,
  * times the loss scale; SPN p.3: averaged once over the valid tokens].
  *   G[t,v] = (exp(z[t,v] - lse[t]) - [v == y_t]) * g / N_valid
  * for valid t and real v, 0 elsewhere; z is recomputed tile by tile.
- *   dH  = G W        (fp32, overwritten)
+ *   dH  = G W        (fp32, overwritten; added into with VCE_FLAG_ACCUMULATE_DH)
  *   dW  = G^T h      rows [V_real,Vp) are 0:
  *         tied_weights == 0: dW is overwritten;
  *         tied_weights == 1: dW is accumulated into (+=), so that the embedding
@@ -209,7 +219,8 @@ vce_status vce_sampled_candidates(const vce_problem* p, const int64_t* targets, 
  *   3. the globally normalised cross-entropy over the P candidate columns
  *      (vce_loss_fwd with Vp = P rounded up to 64, V_real = P, S = 1,
  *      targets = pos) -> *loss (mean over valid tokens), lse[T]
- *   4. its backward (vce_loss_bwd, untied) -> dH[T,H] overwritten, and the
+ *   4. its backward (vce_loss_bwd, untied) -> dH[T,H] overwritten (added
+ *      into when p->flags has VCE_FLAG_ACCUMULATE_DH), and the
  *      candidate rows' gradient dWc[P,H] in the workspace
  *   5. dW[cand[i], :] += dWc[i, :], one fp32 addition per element (the
  *      candidates are distinct); rows of dW that are not candidates, and

@@ -394,6 +394,34 @@ def sampled_cross_entropy(h, W, targets, V_real: int, Vp: int, cand, pos, g: flo
     return fwd
 
 
+def oth_loss(h, W, W2, tokens, V_real: int, Vp: int, weight: float = 0.1,
+             ignore_index: int = IGNORE_INDEX):
+    """OT-H: the next-token cross-entropy of the head W plus `weight` times the
+    cross-entropy of a second head W2 that predicts the token two positions
+    ahead ("Sampled Softmax with Over-Tokenized Transformer", Setup and its
+    loss listing: the second head reads h[:-1] and is scored on tokens[2:]).
+
+    tokens holds T+1 ids; h[t] is the hidden state at input position t (the
+    input is tokens[:-1]), so head one is scored on tokens[1:]. Each term is
+    averaged over its own valid tokens. Returns the total loss, both terms, dH
+    (head two's gradient lands on rows [0, T-1)), dW and dW2.
+    """
+    tok = np.asarray(tokens, dtype=np.int64)
+    T = np.asarray(h).shape[0]
+    if tok.size != T + 1:
+        raise ValueError("tokens must hold T+1 ids")
+    y1, y2 = tok[1:], tok[2:]
+    main = cross_entropy_forward(h, W, y1, V_real, ignore_index)
+    dH, dW = cross_entropy_backward(h, W, y1, V_real, Vp, ignore_index)
+    if T > 1:
+        aux = cross_entropy_forward(h[:T - 1], W2, y2, V_real, ignore_index)["loss"]
+        dH2, dW2 = cross_entropy_backward(h[:T - 1], W2, y2, V_real, Vp, ignore_index, g=weight)
+        dH[:T - 1] += dH2
+    else:
+        aux, dW2 = 0.0, np.zeros((Vp, np.asarray(h).shape[1]))
+    return dict(loss=main["loss"] + weight * aux, main=main["loss"], aux=aux, dH=dH, dW=dW, dW2=dW2)
+
+
 def target_owner(targets, V_real: int, Vp: int, S: int,
                  ignore_index: int = IGNORE_INDEX) -> np.ndarray:
     """Shard that owns each valid target, -1 for ignored or bad ones (P3)."""

@@ -425,11 +425,52 @@ def pin_sampled_full_set_is_full_softmax(O):
     assert abs(O.sampled_cross_entropy(h, W, y2, V, 64, cand, pos)["loss"] - ref) < 1e-12
 
 
+def pin_oth_head(O):
+    """OT-H: the second head is scored on the token two positions ahead of each
+    input position, at weight 0.1."""
+    V, H = 8, 8
+    tokens = np.array([0, 1, 2, 3, 4, 5, 6, 7], dtype=np.int64)   # T + 1 = 8
+    T = tokens.size - 1
+    h = 50.0 * np.eye(H)[tokens[:-1]]               # h[t] encodes the input token at t
+    W = np.zeros((V, H))                             # head one: equal logits, loss ln V
+    W2 = np.zeros((V, H))
+    for v in range(2, V):
+        W2[v, v - 2] = 1.0                           # head two: logit 50 for class tokens[t] + 2
+    r = O.oth_loss(h, W, W2, tokens, V, V)
+    assert abs(r["main"] - np.log(V)) < 1e-12
+    # aligned on tokens[2:], head two is right at every position (loss ~ 7 e^-50)
+    assert r["aux"] < 1e-18
+    assert abs(r["loss"] - (np.log(V) + 0.1 * r["aux"])) < 1e-15
+    # with equal logits in head two as well, the total is 1.1 ln V
+    r0 = O.oth_loss(h, W, np.zeros((V, H)), tokens, V, V)
+    assert abs(r0["loss"] - 1.1 * np.log(V)) < 1e-12
+    # gradients: finite differences of the total loss in h, which also sees the
+    # row T-1 that head two never reads
+    rng = np.random.default_rng(80)
+    h = rng.standard_normal((T, H))
+    W = rng.standard_normal((V, H)) * 0.3
+    W2 = rng.standard_normal((V, H)) * 0.3
+    tokens = rng.integers(0, V, T + 1)
+    tokens[3] = IGN
+    r = O.oth_loss(h, W, W2, tokens, V, V)
+    eps = 1e-6
+    for (i, j) in [(0, 0), (2, 5), (T - 2, 1), (T - 1, 3)]:
+        hp, hm = h.copy(), h.copy()
+        hp[i, j] += eps
+        hm[i, j] -= eps
+        fd = (O.oth_loss(hp, W, W2, tokens, V, V)["loss"] - O.oth_loss(hm, W, W2, tokens, V, V)["loss"]) / (2 * eps)
+        assert abs(fd - r["dH"][i, j]) < 1e-8
+    # head two's weight gradient: torch autograd of 0.1 * CE(h[:-1] W2^T, tokens[2:])
+    W2t = torch.tensor(W2, requires_grad=True)
+    (0.1 * F.cross_entropy(torch.tensor(h[:-1]) @ W2t.T, torch.tensor(tokens[2:]), ignore_index=IGN)).backward()
+    assert np.allclose(r["dW2"], W2t.grad.numpy(), atol=1e-14)
+
+
 ALL_PINS = [
     pin_pad_vocab, pin_shards_tp_page, pin_shards_cover, pin_embedding_forward,
     pin_embedding_backward, pin_embedding_replay_order, pin_embedding_replay_bound,
     pin_equal_logits, pin_normalisation, pin_padded_head_demo, pin_bruteforce_decimal,
     pin_torch_cross_entropy, pin_shard_invariance, pin_ignored_and_bad,
     pin_finite_differences, pin_gradient_invariants, pin_sampled_candidates,
-    pin_sampled_full_set_is_full_softmax,
+    pin_sampled_full_set_is_full_softmax, pin_oth_head,
 ]

@@ -70,6 +70,10 @@ MUTATIONS = {
     # a repeated draw taken twice as a negative
     "sampled_repeats_kept": ("            negs.append(d)\n            taken.add(d)",
                              "            negs.append(d)"),
+    # OT-H's second head scored on the next token instead of two ahead
+    "oth_shift_one": ("    y1, y2 = tok[1:], tok[2:]", "    y1, y2 = tok[1:], tok[1:-1]"),
+    # OT-H's weight left off the second head's gradient
+    "oth_unweighted_grad": ("V_real, Vp, ignore_index, g=weight)", "V_real, Vp, ignore_index)"),
     # target positions off by one in the candidate list
     "sampled_pos_shift": ("    pos[valid] = np.searchsorted(uniq, y[valid])",
                           "    pos[valid] = np.searchsorted(uniq, y[valid], side='right')"),

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(HERE, "libvocabce.so")
 VCE_OK, VCE_ERR_ARG, VCE_ERR_UNSUPPORTED, VCE_ERR_CUDA = 0, 1, 2, 3
 VCE_ERR_BAD_INDEX, VCE_ERR_TIMEOUT, VCE_ERR_WORKSPACE = 4, 5, 6
 VCE_F32, VCE_BF16 = 0, 1
+VCE_FLAG_ACCUMULATE_DH = 1
 VCE_OP_EMBED_FWD, VCE_OP_EMBED_BWD, VCE_OP_LOSS_FWD, VCE_OP_LOSS_BWD = 0, 1, 2, 3
 VCE_OP_SAMPLED_CANDIDATES = 4
 SIZE_MAX = (1 << 64) - 1
@@ -26,7 +27,7 @@ SIZE_MAX = (1 << 64) - 1
 class VceProblem(ctypes.Structure):
     _fields_ = [("T", c_int64), ("H", c_int64), ("Vp", c_int64), ("V_real", c_int64),
                 ("ignore_index", c_int64), ("S", c_int32), ("tied_weights", c_int32),
-                ("dtype", c_int32), ("reserved", c_int32)]
+                ("dtype", c_int32), ("flags", c_int32)]
 
 
 class VceError(RuntimeError):
@@ -104,9 +105,9 @@ def status_str(status: int) -> str:
 
 
 def problem(T: int, H: int, Vp: int, V_real: int, S: int, dtype: int, ignore_index: int = -100,
-            tied: bool = False) -> VceProblem:
+            tied: bool = False, flags: int = 0) -> VceProblem:
     return VceProblem(int(T), int(H), int(Vp), int(V_real), int(ignore_index), int(S), int(bool(tied)),
-                      int(dtype), 0)
+                      int(dtype), int(flags))
 
 
 def _ptr(x, device=True) -> Optional[int]:

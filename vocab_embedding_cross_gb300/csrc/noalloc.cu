@@ -82,7 +82,7 @@ vce_status vce_loss_fwd_noalloc(const vce_problem* p, const void* h, const void*
                                 float* loss, float* lse, float* token_loss, int32_t* target_owner,
                                 int32_t* max_owner, int32_t* dev_status, void* stream) {
   // Same argument rules as vce_loss_fwd.
-  if (!p || p->reserved != 0) return VCE_ERR_ARG;
+  if (!p || (p->flags & ~VCE_FLAG_ACCUMULATE_DH) != 0) return VCE_ERR_ARG;
   if (p->dtype != VCE_F32 && p->dtype != VCE_BF16) return VCE_ERR_UNSUPPORTED;
   if (p->T < 0 || p->H < 1 || p->V_real < 1 || p->S < 1 || p->Vp < 64 || p->Vp % 64 != 0 ||
       p->V_real > p->Vp || p->S > p->Vp || (p->tied_weights != 0 && p->tied_weights != 1))

@@ -99,7 +99,7 @@ int esize_of(const vce_problem& p) { return p.dtype == VCE_BF16 ? 2 : 4; }
 
 vce_status check_problem(const vce_problem* p) {
   if (!p) return VCE_ERR_ARG;
-  if (p->reserved != 0) return VCE_ERR_ARG;
+  if ((p->flags & ~VCE_FLAG_ACCUMULATE_DH) != 0) return VCE_ERR_ARG;
   if (p->dtype != VCE_F32 && p->dtype != VCE_BF16) return VCE_ERR_UNSUPPORTED;
   if (p->T < 0 || p->H < 1 || p->V_real < 1 || p->S < 1) return VCE_ERR_ARG;
   if (p->Vp < 64 || p->Vp % 64 != 0) return VCE_ERR_ARG;   // the padded vocabulary must be 64-aligned
@@ -402,21 +402,23 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
         cudaSuccess)
       return VCE_ERR_CUDA;
   }
+  const bool acc_dh = (p->flags & VCE_FLAG_ACCUMULATE_DH) != 0;
   for (int64_t c0 = 0; c0 < p->V_real; c0 += vc) {
     const int vc_act = static_cast<int>((p->V_real - c0) < vc ? (p->V_real - c0) : vc);
     cudaError_t e;
     if (p->dtype == VCE_BF16) {
       const int parts = dh_part ? tc_dh_parts(*p, vc_act) : 1;
       e = launch_tc_bwd_chunk(*p, h, W, targets, lse, n_valid, g, static_cast<int>(c0), vc_act, G,
-                              static_cast<int>(vc), dH, c0 > 0, dW, p->tied_weights != 0, dh_part, parts, status,
-                              st);
+                              static_cast<int>(vc), dH, c0 > 0 || acc_dh, dW, p->tied_weights != 0, dh_part, parts,
+                              status, st);
     } else {
       float* Gf = static_cast<float*>(G);
       const float* hf = static_cast<const float*>(h);
       const float* Wf = static_cast<const float*>(W);
       e = launch_simt_grad(pd, hf, Wf, targets, lse, n_valid, g, static_cast<int>(c0), vc_act, Gf, st);
       if (e == cudaSuccess)   // dH (+)= G W[c0:c0+vc_act]
-        e = launch_sgemm(pd.T, pd.H, vc_act, Gf, vc_act, 1, Wf + c0 * p->H, p->H, 1, dH, p->H, c0 > 0 ? 1 : 0, st);
+        e = launch_sgemm(pd.T, pd.H, vc_act, Gf, vc_act, 1, Wf + c0 * p->H, p->H, 1, dH, p->H,
+                         (c0 > 0 || acc_dh) ? 1 : 0, st);
       if (e == cudaSuccess)   // dW[c0:c0+vc_act] (+)= G^T h
         e = launch_sgemm(vc_act, pd.H, pd.T, Gf, 1, vc_act, hf, p->H, 1, dW + c0 * p->H, p->H,
                          p->tied_weights ? 1 : 0, st);
