@@ -243,6 +243,9 @@ def run_ours(args):
     # ---- end to end through the C ABI with host buffers ----
     e2e = run_e2e(args, vce, D, d, p, W, E, loss, lse, dH, dW, st, ws_f, ws_b, ws_e, stream, wl)
 
+    # ---- greedy argmax over the same head (decoding), device resident ----
+    greedy = run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks)
+
     # ---- sampled-softmax variant, against the full-vocabulary loss ----
     sampled = run_sampled(args, vce, D, I, stream, peaks, full_loss_tok_s=T / (loss_ms / 1e3) if loss_ms else None)
 
@@ -270,6 +273,7 @@ def run_ours(args):
                              "executed_flops": 8.0 * T * H * V, "vc": int(vc)},
             "embedding": emb,
             "sampled_softmax": sampled,
+            "greedy_argmax": greedy,
             "per_kernel_ms": {k: round(v[0], 4) for k, v in sorted(per_kind.items())},
             "per_kernel_launches": {k: v[1] for k, v in sorted(per_kind.items())},
             "gpu_launches": int(launches),
@@ -281,6 +285,32 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks):
+    """vce_greedy_argmax on the main workload's h and W (T tokens, all V
+    classes, S shards): tokens/s and the logit GEMM's TFLOP/s (2*T*H*V)."""
+    import torch
+    arg = torch.empty(T, dtype=torch.int64, device="cuda")
+    ws = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_GREEDY_ARGMAX))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = stream.cuda_stream
+    for _ in range(3):
+        vce.vce_greedy_argmax(p, h, W, arg, ws=ws, dev_status=st, stream=sp)
+    torch.cuda.synchronize()
+    n = max(5, args.steps // 4)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        vce.vce_greedy_argmax(p, h, W, arg, ws=ws, dev_status=st, stream=sp)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, vce.status_str(int(st.item()))
+    ms = e0.elapsed_time(e1) / n
+    tf = 2.0 * T * H * V / (ms / 1e3) / 1e12
+    return {"tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_call": round(ms, 4), "calls": n,
+            "TFLOPs": round(tf, 1), "frac_of_burst": round(tf / peaks["bf16_tflops"], 4)}
 
 
 def run_sampled(args, vce, D, I, stream, peaks, full_loss_tok_s):

@@ -56,7 +56,8 @@ typedef enum vce_op {
   VCE_OP_EMBED_BWD = 1,
   VCE_OP_LOSS_FWD = 2,
   VCE_OP_LOSS_BWD = 3,
-  VCE_OP_SAMPLED_CANDIDATES = 4
+  VCE_OP_SAMPLED_CANDIDATES = 4,
+  VCE_OP_GREEDY_ARGMAX = 5
 } vce_op;
 
 /*
@@ -241,6 +242,23 @@ vce_status vce_sampled_loss(const vce_problem* p, const void* h, const void* W, 
                             void* stream);
 
 /*
+ * Greedy decoding over the sharded head ["Tensor Parallelism (TP)", on-device
+ * sampling: the sampler finds the global argmax across the TP-sharded logits
+ * without gathering them; "Vocabulary shards ...", paragraph 3: maxima are
+ * taken over valid entries only]. For every token t, with z = h W^T:
+ *   argmax[t]    = the lowest v in [0, V_real) with z_tv = max_u z_tu (int64);
+ *   max_logit[t] = that logit (fp32; optional);
+ *   owner[t]     = the shard owning argmax[t] (int32; optional).
+ * Padded classes [V_real, Vp) never win. Each shard's work units report their
+ * (max, lowest column); the pairs are merged on the GPU. No targets, no loss.
+ * Uses p->T, H, Vp, V_real, S and dtype. argmax must not be NULL when T > 0.
+ * Workspace: vce_workspace_size(p, VCE_OP_GREEDY_ARGMAX) bytes.
+ */
+vce_status vce_greedy_argmax(const vce_problem* p, const void* h, const void* W, int64_t* argmax,
+                             float* max_logit, int32_t* owner, void* ws, size_t ws_bytes,
+                             int32_t* dev_status, void* stream);
+
+/*
  * Loss forward without a caller workspace. The method's pages have no
  * counterpart to this call; it exists for callers that cannot allocate device
  * memory (a plugin inside a framework that owns all device memory and hands it
@@ -315,7 +333,8 @@ typedef enum vce_kernel_kind {
   VCE_K_TC_FWD = 3, VCE_K_TC_GRAD = 4, VCE_K_TC_DH = 5, VCE_K_TC_DW = 6,
   VCE_K_MERGE = 7, VCE_K_LOSS_MEAN = 8, VCE_K_COUNT_VALID = 9,
   VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13,
-  VCE_K_DH_REDUCE = 14, VCE_K_SAMPLED_CAND = 15, VCE_K_SAMPLED_SCATTER = 16
+  VCE_K_DH_REDUCE = 14, VCE_K_SAMPLED_CAND = 15, VCE_K_SAMPLED_SCATTER = 16,
+  VCE_K_TC_ARGMAX = 17, VCE_K_ARGMAX_MERGE = 18, VCE_K_SIMT_ARGMAX = 19
 } vce_kernel_kind;
 uint64_t vce_launch_count(void);
 vce_status vce_profile_begin(int32_t capacity, void* stream);

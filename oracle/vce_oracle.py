@@ -422,6 +422,37 @@ def oth_loss(h, W, W2, tokens, V_real: int, Vp: int, weight: float = 0.1,
     return dict(loss=main["loss"] + weight * aux, main=main["loss"], aux=aux, dH=dH, dW=dW, dW2=dW2)
 
 
+def greedy_argmax(h, W, V_real: int):
+    """Greedy decoding over the head: for each token the lowest class holding
+    the largest real logit, and that logit ("Tensor Parallelism (TP)",
+    on-device sampling; padded classes take no part, P3)."""
+    z = logits(h, W, V_real)
+    arg = z.argmax(axis=1).astype(np.int64)           # first occurrence: the lowest class
+    return arg, z[np.arange(z.shape[0]), arg]
+
+
+def greedy_argmax_sharded(h, W, V_real: int, Vp: int, S: int):
+    """The sharded schedule: every shard reports the largest logit over its
+    valid rows and the lowest row holding it; the shards' pairs are then
+    merged (largest value, lowest class on a tie) without gathering logits."""
+    hf, Wf = _as_f64(h), _as_f64(W)
+    T = hf.shape[0]
+    lo = shard_bounds(Vp, S)
+    best = np.full(T, -np.inf)
+    arg = np.full(T, -1, dtype=np.int64)
+    for k in range(S):
+        hi = min(lo[k + 1], V_real)
+        if hi <= lo[k]:
+            continue                                   # a shard of padding only
+        zk = hf @ Wf[lo[k]:hi].T
+        a_k = zk.argmax(axis=1)
+        m_k = zk[np.arange(T), a_k]
+        take = m_k > best                              # shards ascend: ties keep the lower one
+        best[take] = m_k[take]
+        arg[take] = lo[k] + a_k[take]
+    return arg, best
+
+
 def target_owner(targets, V_real: int, Vp: int, S: int,
                  ignore_index: int = IGNORE_INDEX) -> np.ndarray:
     """Shard that owns each valid target, -1 for ignored or bad ones (P3)."""

@@ -466,11 +466,49 @@ def pin_oth_head(O):
     assert np.allclose(r["dW2"], W2t.grad.numpy(), atol=1e-14)
 
 
+def pin_greedy_argmax(O):
+    """Greedy argmax: a constructed head whose answer is known, ties to the
+    lowest class, padded rows never chosen, the sharded schedule equal to the
+    plain one for every S, and brute force by plain loops."""
+    rng = np.random.default_rng(90)
+    V, H, Vp = 40, 48, 64
+    Q, _ = np.linalg.qr(rng.standard_normal((H, H)))
+    W = np.zeros((Vp, H))
+    W[:V] = Q[:V]                                    # orthonormal rows: z_v = 10 * [v == v*]
+    W[V:] = 8.0                                      # padding rows with large logits
+    want = np.array([0, 7, 39, 16, 23, 31], dtype=np.int64)
+    h = 10.0 * W[want]
+    arg, m = O.greedy_argmax(h, W, V)
+    assert np.array_equal(arg, want) and np.allclose(m, 10.0, atol=1e-12)
+    # a duplicate of row 23 at row 35 (another shard for S = 4): the lower class wins
+    W2 = W.copy()
+    W2[35] = W2[23]
+    arg, _ = O.greedy_argmax(10.0 * W2[[23, 35]], W2, V)
+    assert list(arg) == [23, 23]
+    for S in (1, 2, 3, 4, 5, 8, Vp):
+        a_s, m_s = O.greedy_argmax_sharded(10.0 * W2[[23, 35, 7]], W2, V, Vp, S)
+        assert list(a_s) == [23, 23, 7] and np.allclose(m_s, 10.0, atol=1e-12)
+    # random heads: plain loops over classes (strict >, so the first maximum stays)
+    h = rng.standard_normal((9, H))
+    Wr = rng.standard_normal((Vp, H))
+    arg, m = O.greedy_argmax(h, Wr, V)
+    for t in range(9):
+        bv, bc = -np.inf, -1
+        for v in range(V):
+            zv = sum(float(h[t, j]) * float(Wr[v, j]) for j in range(H))
+            if zv > bv:
+                bv, bc = zv, v
+        assert bc == arg[t] and abs(bv - m[t]) < 1e-12
+    for S in (1, 3, 7, 64):
+        a_s, _ = O.greedy_argmax_sharded(h, Wr, V, Vp, S)
+        assert np.array_equal(a_s, arg)
+
+
 ALL_PINS = [
     pin_pad_vocab, pin_shards_tp_page, pin_shards_cover, pin_embedding_forward,
     pin_embedding_backward, pin_embedding_replay_order, pin_embedding_replay_bound,
     pin_equal_logits, pin_normalisation, pin_padded_head_demo, pin_bruteforce_decimal,
     pin_torch_cross_entropy, pin_shard_invariance, pin_ignored_and_bad,
     pin_finite_differences, pin_gradient_invariants, pin_sampled_candidates,
-    pin_sampled_full_set_is_full_softmax, pin_oth_head,
+    pin_sampled_full_set_is_full_softmax, pin_oth_head, pin_greedy_argmax,
 ]

@@ -74,6 +74,14 @@ MUTATIONS = {
     "oth_shift_one": ("    y1, y2 = tok[1:], tok[2:]", "    y1, y2 = tok[1:], tok[1:-1]"),
     # OT-H's weight left off the second head's gradient
     "oth_unweighted_grad": ("V_real, Vp, ignore_index, g=weight)", "V_real, Vp, ignore_index)"),
+    # greedy argmax: ties to the highest class
+    "argmax_ties_high": ("    arg = z.argmax(axis=1).astype(np.int64)",
+                         "    arg = (z.shape[1] - 1 - z[:, ::-1].argmax(axis=1)).astype(np.int64)"),
+    # greedy argmax over the padded classes too
+    "argmax_padded": ("    z = logits(h, W, V_real)\n    arg = z.argmax(axis=1).astype(np.int64)",
+                      "    z = logits(h, W, W.shape[0])\n    arg = z.argmax(axis=1).astype(np.int64)"),
+    # sharded argmax: a later shard wins ties
+    "argmax_shard_tie_late": ("        take = m_k > best", "        take = m_k >= best"),
     # target positions off by one in the candidate list
     "sampled_pos_shift": ("    pos[valid] = np.searchsorted(uniq, y[valid])",
                           "    pos[valid] = np.searchsorted(uniq, y[valid], side='right')"),

@@ -21,6 +21,7 @@ VCE_F32, VCE_BF16 = 0, 1
 VCE_FLAG_ACCUMULATE_DH = 1
 VCE_OP_EMBED_FWD, VCE_OP_EMBED_BWD, VCE_OP_LOSS_FWD, VCE_OP_LOSS_BWD = 0, 1, 2, 3
 VCE_OP_SAMPLED_CANDIDATES = 4
+VCE_OP_GREEDY_ARGMAX = 5
 SIZE_MAX = (1 << 64) - 1
 
 
@@ -67,6 +68,9 @@ def lib():
         L.vce_sampled_candidates.argtypes = [P, c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
         L.vce_sampled_candidates.restype = c_int32
+        L.vce_greedy_argmax.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                        c_void_p, c_void_p]
+        L.vce_greedy_argmax.restype = c_int32
         L.vce_sampled_workspace_size.argtypes = [P, c_int64]
         L.vce_sampled_workspace_size.restype = c_size_t
         L.vce_sampled_loss.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_float,
@@ -189,6 +193,13 @@ def vce_sampled_loss(p, h, W, targets, draws, P, g, loss, lse, dH, dW, cand, pos
            "vce_sampled_loss")
 
 
+def vce_greedy_argmax(p, h, W, argmax, max_logit=None, owner=None, ws=None, ws_bytes=None, dev_status=None,
+                      stream=None) -> None:
+    nb = (ws.numel() * ws.element_size() if ws is not None else 0) if ws_bytes is None else ws_bytes
+    _check(lib().vce_greedy_argmax(ctypes.byref(p), _ptr(h), _ptr(W), _ptr(argmax), _ptr(max_logit), _ptr(owner),
+                                   _ptr(ws), nb, _ptr(dev_status), _stream(stream)), "vce_greedy_argmax")
+
+
 def vce_embed_bwd_chunk() -> int:
     return int(lib().vce_embed_bwd_chunk())
 
@@ -207,7 +218,7 @@ def vce_wait_selftest(limit_ns: int, dev_status, stream=None) -> None:
 
 KERNEL_KINDS = ["embed_gather", "embed_sort", "embed_reduce", "tc_fwd", "tc_grad", "tc_dh", "tc_dw",
                 "merge", "loss_mean", "count_valid", "simt_fwd", "simt_grad", "sgemm", "wait_selftest",
-                "dh_reduce", "sampled_cand", "sampled_scatter"]
+                "dh_reduce", "sampled_cand", "sampled_scatter", "tc_argmax", "argmax_merge", "simt_argmax"]
 
 
 def vce_launch_count() -> int:

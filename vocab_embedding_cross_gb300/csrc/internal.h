@@ -79,10 +79,15 @@ cudaError_t launch_merge(const ProbDev& pd, const UnitGrid& ug, const int64_t* t
 int merge_blocks(int64_t T);
 cudaError_t launch_count_valid(const ProbDev& pd, const int64_t* targets, int32_t* n_valid, int32_t* status,
                                cudaStream_t st);
+// Greedy argmax: merge of the units' (max, column) partials (column stored as the float's bits).
+cudaError_t launch_argmax_merge(const ProbDev& pd, const UnitGrid& ug, const float2* part, int64_t* argmax,
+                                float* max_logit, int32_t* owner, cudaStream_t st);
 
 // fp32 SIMT path.
 cudaError_t launch_simt_fwd(const ProbDev& pd, const UnitGrid& ug, const float* h, const float* W,
                             const int64_t* targets, float2* part, float* ztgt, cudaStream_t st);
+cudaError_t launch_simt_argmax(const ProbDev& pd, const UnitGrid& ug, const float* h, const float* W, float2* part,
+                               cudaStream_t st);
 cudaError_t launch_simt_grad(const ProbDev& pd, const float* h, const float* W, const int64_t* targets,
                              const float* lse, const int32_t* n_valid, float g, int v0, int vc, float* G,
                              cudaStream_t st);
@@ -94,6 +99,8 @@ cudaError_t launch_sgemm(int M, int N, int K, const float* A, int64_t sam, int64
 // bf16 tensor-core path.
 cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* h, const void* W,
                           const int64_t* targets, float2* part, float* ztgt, int32_t* status, cudaStream_t st);
+cudaError_t launch_tc_argmax(const vce_problem& p, const UnitGrid& ug, const void* h, const void* W, float2* part,
+                             int32_t* status, cudaStream_t st);
 cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void* W, const int64_t* targets,
                                 const float* lse, const int32_t* n_valid, float g, int v0, int vc_act,
                                 void* G, int g_ld, float* dH, bool dH_accumulate, float* dW, bool dW_accumulate,

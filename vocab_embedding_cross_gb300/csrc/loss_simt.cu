@@ -128,6 +128,72 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(ProbDev pd, UnitGrid ug, 
   }
 }
 
+// (max, argmax) pair reduction over the 16 lanes holding one row: larger
+// value first, lower column on a tie (columns < 0 mean "none").
+__device__ __forceinline__ void hargmax16(float& v, int32_t& c) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int32_t c2 = __shfl_xor_sync(0xffffffffu, c, o);
+    if (c2 >= 0 && (c < 0 || v2 > v || (v2 == v && c2 < c))) {
+      v = v2;
+      c = c2;
+    }
+  }
+}
+
+// grid (ceil(T/64), n_units): largest real logit of one unit and its lowest
+// column, for 64 tokens (greedy decoding over the sharded head).
+__global__ void __launch_bounds__(256) simt_argmax_kernel(ProbDev pd, UnitGrid ug, const float* __restrict__ h,
+                                                          const float* __restrict__ W, float2* __restrict__ part) {
+  __shared__ float hs[TK][TM + 4];
+  __shared__ float ws[TK][TN + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.x * TM;
+  const int u = blockIdx.y;
+  const int k_sh = u / ug.ups, j_u = u - k_sh * ug.ups;
+  const int64_t lo = shard_lo(k_sh, pd.Vp, pd.S), hi = shard_lo(k_sh + 1, pd.Vp, pd.S);
+  const int64_t vb = lo + static_cast<int64_t>(j_u) * ug.uw;
+  const int64_t ve = vb + ug.uw < hi ? vb + ug.uw : hi;
+  const int64_t vlim = ve < pd.V_real ? ve : pd.V_real;
+  float m_run[4];
+  int32_t c_run[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m_run[i] = -INFINITY;
+    c_run[i] = -1;
+  }
+  for (int64_t vt0 = vb; vt0 < vlim; vt0 += TN) {
+    float acc[4][4];
+    z_tile(h, W, pd.T, pd.H, m0, vt0, vlim, acc, hs, ws);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float bv = -INFINITY;
+      int32_t bc = -1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t v = vt0 + 4 * tx + j;
+        if (v < vlim && (bc < 0 || acc[i][j] > bv)) {
+          bv = acc[i][j];
+          bc = static_cast<int32_t>(v);
+        }
+      }
+      hargmax16(bv, bc);
+      if (bc >= 0 && (c_run[i] < 0 || bv > m_run[i])) {   // later tiles hold higher columns
+        m_run[i] = bv;
+        c_run[i] = bc;
+      }
+    }
+  }
+  if (tx == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = m0 + 4 * ty + i;
+      if (r < pd.T) part[static_cast<int64_t>(r) * ug.n_units + u] = make_float2(m_run[i], __int_as_float(c_run[i]));
+    }
+  }
+}
+
 // grid (ceil(T/64), ceil(vc/64)): G[t, v - v0] = (exp(z - lse) - [v == y]) * g / N_valid.
 __global__ void __launch_bounds__(256) simt_grad_kernel(ProbDev pd, const float* __restrict__ h,
                                                         const float* __restrict__ W,
@@ -230,6 +296,14 @@ cudaError_t launch_simt_fwd(const ProbDev& pd, const UnitGrid& ug, const float* 
   dim3 grid(static_cast<unsigned>(ceil_div(pd.T, TM)), static_cast<unsigned>(ug.n_units));
   simt_fwd_kernel<<<grid, 256, 0, st>>>(pd, ug, h, W, targets, part, ztgt);
   note_launch(VCE_K_SIMT_FWD, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_simt_argmax(const ProbDev& pd, const UnitGrid& ug, const float* h, const float* W, float2* part,
+                               cudaStream_t st) {
+  dim3 grid(static_cast<unsigned>(ceil_div(pd.T, TM)), static_cast<unsigned>(ug.n_units));
+  simt_argmax_kernel<<<grid, 256, 0, st>>>(pd, ug, h, W, part);
+  note_launch(VCE_K_SIMT_ARGMAX, st);
   return cudaGetLastError();
 }
 

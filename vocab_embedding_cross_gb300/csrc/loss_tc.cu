@@ -55,13 +55,16 @@ constexpr uint32_t kStagingPerWarp = 4096;       // one 32-row x 128-B TMA store
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum Mode : int { MODE_FWD = 0, MODE_GRAD = 1, MODE_DH = 2, MODE_DW = 3 };
+enum Mode : int { MODE_FWD = 0, MODE_GRAD = 1, MODE_DH = 2, MODE_DW = 3, MODE_ARGMAX = 4 };
+// FWD and ARGMAX share the logit GEMM and its work items; they differ in the epilogue.
+template <int MODE>
+constexpr bool kFwdLike = MODE == MODE_FWD || MODE == MODE_ARGMAX;
 
 template <int MODE>
 struct Traits {
   static constexpr uint32_t a_mn = (MODE == MODE_DW) ? 1u : 0u;
   static constexpr uint32_t b_mn = (MODE == MODE_DH || MODE == MODE_DW) ? 1u : 0u;
-  static constexpr bool staging = MODE != MODE_FWD;
+  static constexpr bool staging = !kFwdLike<MODE>;
   static constexpr int stages = 6;
   static constexpr uint32_t idesc = idesc_bf16_f32(BMP, BN, a_mn, b_mn);
 };
@@ -69,7 +72,7 @@ struct Traits {
 template <int MODE>
 constexpr size_t smem_bytes() {
   return 1024 + size_t(Traits<MODE>::stages) * kStageBytes +
-         (Traits<MODE>::staging ? kEpiWarps * kStagingPerWarp : 0) + 256 + (MODE == MODE_FWD ? 2048 : 0);
+         (Traits<MODE>::staging ? kEpiWarps * kStagingPerWarp : 0) + 256 + (kFwdLike<MODE> ? 2048 : 0);
 }
 
 struct TcArgs {
@@ -115,7 +118,7 @@ __device__ __forceinline__ UnitSpan unit_span(const TcArgs& a, int u) {
 
 template <int MODE>
 __device__ __forceinline__ int item_tiles(const TcArgs& a, int item) {
-  if constexpr (MODE == MODE_FWD) {
+  if constexpr (kFwdLike<MODE>) {
     return unit_span(a, item / a.n_mblk).ntiles;
   } else {
     return 1;
@@ -131,7 +134,7 @@ struct TileCoord {
 template <int MODE>
 __device__ __forceinline__ TileCoord tile_coord(const TcArgs& a, int item, int tt, int rank) {
   TileCoord c;
-  if constexpr (MODE == MODE_FWD) {
+  if constexpr (kFwdLike<MODE>) {
     const int m_blk = item % a.n_mblk;
     const UnitSpan us = unit_span(a, item / a.n_mblk);
     c.am = m_blk * BMP + rank * BM;
@@ -169,7 +172,7 @@ template <int MODE>
 __device__ __forceinline__ void issue_loads(const TcArgs& a, const CUtensorMap* mA, const CUtensorMap* mB,
                                             uint32_t sA, uint32_t sB, uint32_t bar, TileCoord c, int kb) {
   const int k0 = kb * BK;
-  if constexpr (MODE == MODE_FWD || MODE == MODE_GRAD) {
+  if constexpr (kFwdLike<MODE> || MODE == MODE_GRAD) {
     tma_load_2d_pair(sA, mA, bar, k0, c.am);
     tma_load_2d_pair(sB, mB, bar, k0, c.bn);
   } else if constexpr (MODE == MODE_DH) {
@@ -423,7 +426,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     };
     for (int item = first_item; ok && item < a.n_items; item += item_step) {
-      if constexpr (MODE == MODE_FWD) {
+      if constexpr (MODE == MODE_ARGMAX) {
+        const int m_blk = item % a.n_mblk, u = item / a.n_mblk;
+        const UnitSpan us = unit_span(a, u);
+        const int t = m_blk * BMP + static_cast<int>(rank) * BM + r;
+        float m_run = -INFINITY;
+        int32_t i_run = -1;
+        // Largest real logit of one 32-column chunk; strict > keeps the lowest column.
+        auto chunk = [&](const uint32_t (&x)[32], int64_t vc0) {
+          const int64_t nval64 = us.vlim - vc0;
+          const int nval = nval64 >= 32 ? 32 : (nval64 <= 0 ? 0 : static_cast<int>(nval64));
+          float best = -INFINITY;
+          int bj = -1;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float v = __uint_as_float(x[j]);
+            if (j < nval && v > best) {
+              best = v;
+              bj = j;
+            }
+          }
+          if (bj >= 0 && best > m_run) {
+            m_run = best;
+            i_run = static_cast<int32_t>(vc0) + bj;
+          }
+        };
+        for (int tt = 0; tt < us.ntiles; ++tt) {
+          const uint32_t acc = tile_count & 1u;
+          if (!mbar_wait_cl(&tfull[acc], (tile_count >> 1) & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int64_t vc = us.vb + static_cast<int64_t>(tt) * BN + half * 128;
+          const uint32_t ta = lane_base + acc * BN;
+          uint32_t xa[32], xb[32];
+          tmem_ld_32x32b_x32(ta, xa);
+          tmem_ld_wait();
+          reg_fence(xa);
+          tmem_ld_32x32b_x32(ta + 32, xb);
+          chunk(xa, vc);
+          tmem_ld_wait();
+          reg_fence(xb);
+          tmem_ld_32x32b_x32(ta + 64, xa);
+          chunk(xb, vc + 32);
+          tmem_ld_wait();
+          reg_fence(xa);
+          tmem_ld_32x32b_x32(ta + 96, xb);
+          chunk(xa, vc + 64);
+          tmem_ld_wait();
+          reg_fence(xb);
+          release(acc);
+          chunk(xb, vc + 96);
+          ++tile_count;
+        }
+        if (!ok) break;
+        // Join the two column halves: the larger logit, the lower column on a tie.
+        if (half == 1) {
+          if (!mbar_wait(&comb_empty[pq], (items_done & 1u) ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          comb[pq * 32 + lane] = make_float4(m_run, __int_as_float(i_run), 0.0f, 0.0f);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_full[pq]);
+        } else {
+          if (!mbar_wait(&comb_full[pq], items_done & 1u, wc)) {
+            ok = false;
+            break;
+          }
+          const float4 o = comb[pq * 32 + lane];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_empty[pq]);
+          const int32_t oi = __float_as_int(o.y);
+          if (oi >= 0 && (i_run < 0 || o.x > m_run || (o.x == m_run && oi < i_run))) {
+            m_run = o.x;
+            i_run = oi;
+          }
+          if (t < a.pd.T) a.part[static_cast<int64_t>(t) * a.ug.n_units + u] = make_float2(m_run, __int_as_float(i_run));
+        }
+        ++items_done;
+      } else if constexpr (MODE == MODE_FWD) {
         const int m_blk = item % a.n_mblk, u = item / a.n_mblk;
         const UnitSpan us = unit_span(a, u);
         const int t = m_blk * BMP + static_cast<int>(rank) * BM + r;
@@ -674,7 +757,7 @@ cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
   const int mc = max_clusters<MODE>(di.num_sms);
   const int clusters = a.n_items < mc ? a.n_items : mc;
   tc_loss_kernel<MODE><<<2 * clusters, kThreads, smem_bytes<MODE>(), st>>>(mA, mB, mO, a);
-  note_launch(VCE_K_TC_FWD + MODE, st);
+  note_launch(MODE == MODE_ARGMAX ? VCE_K_TC_ARGMAX : VCE_K_TC_FWD + MODE, st);
   return cudaGetLastError();
 }
 
@@ -785,6 +868,21 @@ cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* 
   a.part = part;
   a.ztgt = ztgt;
   return launch_mode<MODE_FWD>(mh, mw, mh, a, st);
+}
+
+cudaError_t launch_tc_argmax(const vce_problem& p, const UnitGrid& ug, const void* h, const void* W, float2* part,
+                             int32_t* status, cudaStream_t st) {
+  CUtensorMap mh, mw;
+  if (!make_tmap_2d(&mh, h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, p.T, p.H, 64, BM, true) ||
+      !make_tmap_2d(&mw, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, p.V_real, p.H, 64, BNH, true))
+    return cudaErrorInvalidValue;
+  TcArgs a = base_args(p, nullptr, status);
+  a.n_mblk = static_cast<int>(ceil_div(p.T, BMP));
+  a.n_items = a.n_mblk * ug.n_units;
+  a.num_kb = static_cast<int>(ceil_div(p.H, BK));
+  a.ug = ug;
+  a.part = part;
+  return launch_mode<MODE_ARGMAX>(mh, mw, mh, a, st);
 }
 
 cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void* W, const int64_t* targets,

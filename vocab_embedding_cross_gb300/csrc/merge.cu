@@ -162,9 +162,53 @@ __global__ void __launch_bounds__(1024) count_valid_kernel(ProbDev pd, const int
   }
 }
 
+// Greedy decoding: the units' (max, column) pairs of one token are merged to
+// the global maximum and its lowest column; the owner is the shard of that
+// column ("Tensor Parallelism (TP)", on-device sampling: the argmax is found
+// across the sharded logits without gathering them).
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    argmax_merge_kernel(ProbDev pd, UnitGrid ug, const float2* __restrict__ part, int64_t* __restrict__ argmax,
+                        float* __restrict__ max_logit, int32_t* __restrict__ owner) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
+  if (t >= pd.T) return;
+  float m = -INFINITY;
+  int32_t c = -1;
+  const float2* row = part + t * ug.n_units;
+  for (int u = lane; u < ug.n_units; u += 32) {
+    const float2 mc = row[u];
+    const int32_t c2 = __float_as_int(mc.y);
+    if (c2 >= 0 && (c < 0 || mc.x > m || (mc.x == m && c2 < c))) {
+      m = mc.x;
+      c = c2;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const int32_t c2 = __shfl_xor_sync(0xffffffffu, c, o);
+    if (c2 >= 0 && (c < 0 || m2 > m || (m2 == m && c2 < c))) {
+      m = m2;
+      c = c2;
+    }
+  }
+  if (lane == 0) {
+    argmax[t] = c;
+    if (max_logit) max_logit[t] = m;
+    if (owner) owner[t] = c >= 0 ? shard_of(c, pd.Vp, pd.S) : -1;
+  }
+}
+
 }  // namespace
 
 int merge_blocks(int64_t T) { return static_cast<int>(ceil_div(T, kMergeWarps)); }
+
+cudaError_t launch_argmax_merge(const ProbDev& pd, const UnitGrid& ug, const float2* part, int64_t* argmax,
+                                float* max_logit, int32_t* owner, cudaStream_t st) {
+  argmax_merge_kernel<<<merge_blocks(pd.T), kMergeWarps * 32, 0, st>>>(pd, ug, part, argmax, max_logit, owner);
+  note_launch(VCE_K_ARGMAX_MERGE, st);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const ProbDev& pd, const UnitGrid& ug, const int64_t* targets, const float2* part,
                          const float* ztgt, float* lse, float* token_loss, int32_t* target_owner,

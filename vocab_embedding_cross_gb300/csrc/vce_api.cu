@@ -142,6 +142,12 @@ FwdLayout fwd_layout(const vce_problem& p) {
   return L;
 }
 
+// Greedy argmax: one (max, column) pair per (token, unit).
+size_t argmax_ws_bytes(const vce_problem& p) {
+  const UnitGrid ug = unit_grid(p, p.dtype == VCE_BF16 ? tc_unit_width(p) : kSimtUnitWidth);
+  return align_up(sizeof(float2) * static_cast<size_t>(p.T) * ug.n_units, kWsAlign) + kWsAlign;
+}
+
 constexpr size_t kBwdHeader = 256;   // status word, N_valid
 size_t g_esize(const vce_problem& p) { return p.dtype == VCE_BF16 ? 2 : 4; }
 int64_t vocab_cols_cap(const vce_problem& p) { return ceil_div(p.V_real, 256) * 256; }
@@ -296,6 +302,7 @@ size_t vce_workspace_size(const vce_problem* p, int32_t op) {
     case VCE_OP_LOSS_FWD: return fwd_layout(*p).total;
     case VCE_OP_LOSS_BWD: return bwd_bytes_for(*p, bwd_recommended_cols(*p)) + dh_part_bytes(*p);
     case VCE_OP_SAMPLED_CANDIDATES: return sampled_ws_bytes(*p);
+    case VCE_OP_GREEDY_ARGMAX: return argmax_ws_bytes(*p);
   }
   return SIZE_MAX;
 }
@@ -489,6 +496,34 @@ vce_status vce_sampled_loss(const vce_problem* p, const void* h, const void* W, 
   if (s != VCE_OK) return s;
   // 5. dW[cand[i]] += dWc[i]: the candidates are distinct, one addition per element
   return cuda_status(launch_sampled_scatter(cand, P, *p, dWc, dW, st));
+}
+
+vce_status vce_greedy_argmax(const vce_problem* p, const void* h, const void* W, int64_t* argmax,
+                             float* max_logit, int32_t* owner, void* ws, size_t ws_bytes, int32_t* dev_status,
+                             void* stream) {
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (p->T == 0) return VCE_OK;
+  if (!h || !W || !argmax) return VCE_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(W, 16) || !aligned(argmax, 8) || !aligned(max_logit, 4) || !aligned(owner, 4))
+    return VCE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < argmax_ws_bytes(*p)) return VCE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const UnitGrid ug = unit_grid(*p, p->dtype == VCE_BF16 ? tc_unit_width(*p) : kSimtUnitWidth);
+  const ProbDev pd = prob_dev(*p);
+  char* b = static_cast<char*>(ws);
+  int32_t* status = dev_status;
+  if (!status) {
+    status = reinterpret_cast<int32_t*>(b);
+    if (cudaError_t me = cudaMemsetAsync(status, 0, sizeof(int32_t), st)) return cuda_status(me);
+  }
+  float2* part = reinterpret_cast<float2*>(b + kWsAlign);
+  cudaError_t e = p->dtype == VCE_BF16
+                      ? launch_tc_argmax(*p, ug, h, W, part, status, st)
+                      : launch_simt_argmax(pd, ug, static_cast<const float*>(h), static_cast<const float*>(W), part,
+                                           st);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_argmax_merge(pd, ug, part, argmax, max_logit, owner, st));
 }
 
 vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* stream) {
