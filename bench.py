@@ -246,6 +246,9 @@ def run_ours(args):
     # ---- greedy argmax over the same head (decoding), device resident ----
     greedy = run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks)
 
+    # ---- hashed n-gram input embeddings on the same ids ----
+    ngram = run_ngram(args, vce, D, I, wl, d, p, W, dE, stream, peaks)
+
     # ---- sampled-softmax variant, against the full-vocabulary loss ----
     sampled = run_sampled(args, vce, D, I, stream, peaks, full_loss_tok_s=T / (loss_ms / 1e3) if loss_ms else None)
 
@@ -274,6 +277,7 @@ def run_ours(args):
             "embedding": emb,
             "sampled_softmax": sampled,
             "greedy_argmax": greedy,
+            "ngram_embedding": ngram,
             "per_kernel_ms": {k: round(v[0], 4) for k, v in sorted(per_kind.items())},
             "per_kernel_launches": {k: v[1] for k, v in sorted(per_kind.items())},
             "gpu_launches": int(launches),
@@ -311,6 +315,60 @@ def run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks):
     tf = 2.0 * T * H * V / (ms / 1e3) / 1e12
     return {"tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_call": round(ms, 4), "calls": n,
             "TFLOPs": round(tf, 1), "frac_of_burst": round(tf / peaks["bf16_tflops"], 4)}
+
+
+def run_ngram(args, vce, D, I, wl, d, p, W, dE, stream, peaks):
+    """vce_ngram_embed_fwd / _bwd on the main workload's ids (4 sequences of
+    2048) with two hashed tables of 2^18 rows: time per call and GB/s of the
+    algorithmic bytes (ids, distinct rows read, E written; dE read once per
+    table, touched rows read-modify-written in fp32)."""
+    import torch
+    M, L = I.NGRAM_ROWS, I.NGRAM_SEQ_LEN
+    T, H = wl.T, wl.H
+    T2 = D.to_device(I.make_ngram_table(wl, 2, M))
+    T3 = D.to_device(I.make_ngram_table(wl, 3, M))
+    ids = torch.from_numpy(d["ids"]).cuda()
+    E = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    dW = torch.zeros((wl.Vp, H), device="cuda")
+    dT2 = torch.zeros((M, H), device="cuda")
+    dT3 = torch.zeros((M, H), device="cuda")
+    ws = D.workspace(vce.vce_ngram_workspace_size(p))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = stream.cuda_stream
+    idx = torch.empty(T, dtype=torch.int64, device="cuda")
+    uniq = []
+    for n, Mn in ((1, wl.V_real), (2, M), (3, M)):
+        vce.vce_ngram_hash(ids, n, wl.V_real, Mn, idx, seq_len=L, stream=sp)
+        uniq.append(int(torch.unique(idx[idx >= 0]).numel()))
+    fwd_bytes = 8 * T + sum(uniq) * H * 2 + T * H * 2
+    bwd_bytes = 8 * T + 3 * T * H * 2 + sum(uniq) * H * 8
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    n = max(10, args.steps)
+    f_ms = timed(lambda: vce.vce_ngram_embed_fwd(p, ids, W, T2, M, T3, M, E, seq_len=L, dev_status=st, stream=sp), n)
+    b_ms = timed(lambda: vce.vce_ngram_embed_bwd(p, ids, dE, dW, dT2, M, dT3, M, ws, seq_len=L, dev_status=st,
+                                                 stream=sp), n)
+    assert int(st.item()) == 0, vce.status_str(int(st.item()))
+    del T2, T3, dT2, dT3, dW, ws
+    torch.cuda.empty_cache()
+    return {"workload": f"ids of {wl.name} (T={T}, sequences of {L}), H={H}, tables V={wl.V_real}, 2^18, 2^18",
+            "distinct_rows": uniq, "fwd_us": round(f_ms * 1e3, 2),
+            "fwd_GBps": round(fwd_bytes / (f_ms / 1e3) / 1e9, 1),
+            "fwd_frac": round(fwd_bytes / (f_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "bwd_us": round(b_ms * 1e3, 2), "bwd_GBps": round(bwd_bytes / (b_ms / 1e3) / 1e9, 1),
+            "bwd_frac": round(bwd_bytes / (b_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
 
 
 def run_sampled(args, vce, D, I, stream, peaks, full_loss_tok_s):

@@ -259,6 +259,48 @@ vce_status vce_greedy_argmax(const vce_problem* p, const void* h, const void* W,
                              int32_t* dev_status, void* stream);
 
 /*
+ * Hashed n-gram input embeddings ["Sampled Softmax with Over-Tokenized
+ * Transformer", Setup and its loss listing: each input token's embedding gains
+ * the hashed 2-gram and 3-gram embeddings that end at it].
+ * The n-gram ending at token t of the input ids x is (x[t-n+1], ..., x[t]); its
+ * row in a table of M rows is the n-gram read as a base-V number (x[t] the
+ * lowest digit) mod M:
+ *     idx_n(t) = (x[t] + x[t-1]*V + ... + x[t-n+1]*V^(n-1)) mod M,   V = V_real.
+ * A token with fewer than n-1 earlier tokens in its sequence (the ids are
+ * sequences of seq_len tokens laid end to end; seq_len = 0: one sequence), or
+ * whose n-gram holds an id outside [0, V_real), has no n-gram: index -1.
+ *
+ * vce_ngram_hash: out[t] = idx_n(t) (int64, device) for n >= 1, 1 <= M < 2^31,
+ * 1 <= V < 2^31.
+ */
+vce_status vce_ngram_hash(const int64_t* ids, int64_t T, int32_t n, int64_t V, int64_t M, int64_t seq_len,
+                          int64_t* out, void* stream);
+
+/*
+ * E[t] = W[x_t] + T2[idx_2(t)] + T3[idx_3(t)], summed in fp32 in that order (a
+ * missing term, an invalid id or an absent n-gram, reads as +0) and rounded
+ * once to p->dtype (round to nearest even). W[Vp,H], T2[M2,H], T3[M3,H] and
+ * E[T,H] in p->dtype, 16-byte aligned. M2 = 0 (T2 NULL) or M3 = 0 (T3 NULL)
+ * leaves that table out. Uses p->T, H, V_real, dtype; ids are the input ids.
+ */
+vce_status vce_ngram_embed_fwd(const vce_problem* p, const int64_t* ids, const void* W, const void* T2,
+                               int64_t M2, const void* T3, int64_t M3, int64_t seq_len, void* E,
+                               int32_t* dev_status, void* stream);
+
+/*
+ * Backward of vce_ngram_embed_fwd: dW[x_t] += dE[t], dT2[idx_2(t)] += dE[t],
+ * dT3[idx_3(t)] += dE[t] (fp32 tables, accumulated into), each with the
+ * deterministic order of vce_embed_bwd (sorted (row, t), runs of 32 tokens
+ * summed in fp32, run sums left to right, one rounding into the row), so the
+ * results are bit-identical from run to run. dT2 / dT3 may be NULL when M2 /
+ * M3 is 0. Workspace: vce_ngram_workspace_size(p) bytes.
+ */
+size_t vce_ngram_workspace_size(const vce_problem* p);
+vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const void* dE, float* dW, float* dT2,
+                               int64_t M2, float* dT3, int64_t M3, int64_t seq_len, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, void* stream);
+
+/*
  * Loss forward without a caller workspace. The method's pages have no
  * counterpart to this call; it exists for callers that cannot allocate device
  * memory (a plugin inside a framework that owns all device memory and hands it
@@ -334,7 +376,8 @@ typedef enum vce_kernel_kind {
   VCE_K_MERGE = 7, VCE_K_LOSS_MEAN = 8, VCE_K_COUNT_VALID = 9,
   VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13,
   VCE_K_DH_REDUCE = 14, VCE_K_SAMPLED_CAND = 15, VCE_K_SAMPLED_SCATTER = 16,
-  VCE_K_TC_ARGMAX = 17, VCE_K_ARGMAX_MERGE = 18, VCE_K_SIMT_ARGMAX = 19
+  VCE_K_TC_ARGMAX = 17, VCE_K_ARGMAX_MERGE = 18, VCE_K_SIMT_ARGMAX = 19,
+  VCE_K_NGRAM_HASH = 20, VCE_K_NGRAM_FWD = 21
 } vce_kernel_kind;
 uint64_t vce_launch_count(void);
 vce_status vce_profile_begin(int32_t capacity, void* stream);

@@ -52,6 +52,83 @@ IGNORE_INDEX = -100
 
 
 # ---------------------------------------------------------------------------
+# Hashed n-gram input embeddings ("Sampled Softmax with Over-Tokenized
+# Transformer", Setup and its loss listing)
+# ---------------------------------------------------------------------------
+
+def ngram_index(ids, n: int, V: int, M: int, seq_len: int = 0) -> np.ndarray:
+    """Row of the hashed n-gram that ends at each token, -1 where there is none.
+
+    Reading (the pages name hashed 2-gram and 3-gram tables but no hash): the
+    n-gram (x[t-n+1], ..., x[t]) is read as a number in base V with x[t] the
+    lowest digit, and reduced mod the table's M rows. A token with fewer than
+    n-1 earlier tokens in its sequence (sequences of seq_len tokens laid end to
+    end; 0 means one sequence), or whose n-gram holds an id outside [0, V),
+    has no n-gram. Exact Python integers, one token at a time.
+    """
+    x = [int(v) for v in np.asarray(ids, dtype=np.int64)]
+    out = np.full(len(x), -1, dtype=np.int64)
+    if M <= 0:
+        return out
+    for t in range(len(x)):
+        pos = t % seq_len if seq_len > 0 else t
+        if pos < n - 1:
+            continue
+        gram = x[t - n + 1:t + 1]
+        if any(v < 0 or v >= V for v in gram):
+            continue
+        value = sum(v * V ** j for j, v in enumerate(reversed(gram)))
+        out[t] = value % M
+    return out
+
+
+def _rows_f32(table, idx: np.ndarray, H: int) -> np.ndarray:
+    """fp32 values of the rows idx of a stored table; +0 rows where idx < 0."""
+    out = np.zeros((idx.shape[0], H), dtype=np.float32)
+    ok = idx >= 0
+    if table is not None and ok.any():
+        rows = np.asarray(table)[idx[ok]]
+        if rows.dtype == np.uint16:
+            rows = (rows.astype(np.uint32) << np.uint32(16)).view(np.float32)
+        out[ok] = rows.astype(np.float32)
+    return out
+
+
+def _round_bf16_bits(x32: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest, ties to even (finite values)."""
+    u = np.ascontiguousarray(x32, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)).astype(np.uint16)
+
+
+def ngram_embed_forward(ids, W, T2, T3, V_real: int, M2: int, M3: int, seq_len: int = 0) -> np.ndarray:
+    """E[t] = W[x_t] + T2[idx_2(t)] + T3[idx_3(t)] (the listing's embed plus the
+    two n-gram embeddings), summed in fp32 in that order from +0 with a missing
+    term read as +0, then rounded once to the tables' storage type (bf16 bit
+    patterns when W is stored as uint16). Reading: one fp32 sum and one
+    rounding, the plainest way to add three stored rows."""
+    x = np.asarray(ids, dtype=np.int64)
+    H = np.asarray(W).shape[1]
+    i1 = np.where((x >= 0) & (x < V_real), x, -1)
+    i2 = ngram_index(x, 2, V_real, M2, seq_len)
+    i3 = ngram_index(x, 3, V_real, M3, seq_len)
+    acc = np.zeros((x.shape[0], H), dtype=np.float32)
+    acc = acc + _rows_f32(W, i1, H)
+    acc = acc + _rows_f32(T2, i2, H)
+    acc = acc + _rows_f32(T3, i3, H)
+    return _round_bf16_bits(acc) if np.asarray(W).dtype == np.uint16 else acc
+
+
+def ngram_embed_backward(ids, dE, V_real: int, Vp: int, M2: int, M3: int, seq_len: int = 0):
+    """fp64 gradients of the three tables: dW[x_t], dT2[idx_2(t)] and
+    dT3[idx_3(t)] each receive dE[t] (P2's accumulation, table by table)."""
+    x = np.asarray(ids, dtype=np.int64)
+    dW = embed_backward(x, dE, V_real, Vp)
+    dT2 = embed_backward(ngram_index(x, 2, V_real, M2, seq_len), dE, M2, M2) if M2 > 0 else None
+    dT3 = embed_backward(ngram_index(x, 3, V_real, M3, seq_len), dE, M3, M3) if M3 > 0 else None
+    return dW, dT2, dT3
+
+
+# ---------------------------------------------------------------------------
 # Vocabulary padding and shard layout
 # ---------------------------------------------------------------------------
 

@@ -504,11 +504,77 @@ def pin_greedy_argmax(O):
         assert np.array_equal(a_s, arg)
 
 
+def pin_ngram_hash(O):
+    """The n-gram row index: hand-worked in base 10, sequence starts, invalid
+    ids, and base-V digits recovered exactly when M = V^n."""
+    x = [1, 2, 3, 4]
+    assert list(O.ngram_index(x, 2, 10, 1000)) == [-1, 12, 23, 34]
+    assert list(O.ngram_index(x, 3, 10, 1000)) == [-1, -1, 123, 234]
+    assert list(O.ngram_index(x, 2, 10, 7)) == [-1, 5, 2, 6]        # 12, 23, 34 mod 7
+    assert list(O.ngram_index(x, 3, 10, 7)) == [-1, -1, 4, 3]       # 123, 234 mod 7
+    assert list(O.ngram_index(x, 1, 10, 1000)) == [1, 2, 3, 4]
+    # two sequences of 2 tokens: no n-gram crosses the boundary
+    assert list(O.ngram_index(x, 2, 10, 1000, seq_len=2)) == [-1, 12, -1, 34]
+    assert list(O.ngram_index(x, 3, 10, 1000, seq_len=2)) == [-1, -1, -1, -1]
+    # an invalid id removes every n-gram that contains it
+    assert list(O.ngram_index([1, IGN, 3, 4], 2, 10, 1000)) == [-1, -1, -1, 34]
+    assert list(O.ngram_index([1, 2, 10, 4, 5], 3, 10, 1000)) == [-1, -1, -1, -1, -1]
+    # M = V^3: the index is the n-gram itself, written in base V
+    V = 151936
+    rng = np.random.default_rng(95)
+    y = rng.integers(0, V, 50)
+    idx = O.ngram_index(y, 3, V, V ** 3)
+    for t in range(2, 50):
+        a, r = divmod(int(idx[t]), V * V)
+        b, c = divmod(r, V)
+        assert (a, b, c) == (y[t - 2], y[t - 1], y[t])
+    # reduced mod M exactly (Python integers, no overflow)
+    big = O.ngram_index([V - 1] * 3, 3, V, 1 << 19)
+    assert big[2] == (V ** 3 - 1) % (1 << 19)
+
+
+def pin_ngram_embedding(O):
+    """E = W[x] + T2[idx_2] + T3[idx_3]: exact on integer-valued fp32 tables,
+    one round-to-nearest-even to bf16 (hand-worked ties), and the tables'
+    gradients against np.add.at."""
+    V, H, M2, M3 = 10, 4, 7, 11
+    W = (100.0 * np.arange(V)[:, None] * np.ones((1, H))).astype(np.float32)
+    T2 = (10.0 * np.arange(M2)[:, None] * np.ones((1, H))).astype(np.float32)
+    T3 = (1.0 * np.arange(M3)[:, None] * np.ones((1, H))).astype(np.float32)
+    x = np.array([1, 2, 3, IGN, 4, 5, 6], dtype=np.int64)
+    E = O.ngram_embed_forward(x, W, T2, T3, V, M2, M3)
+    i2 = O.ngram_index(x, 2, V, M2)
+    i3 = O.ngram_index(x, 3, V, M3)
+    want = (100.0 * np.where((x >= 0) & (x < V), x, 0) + 10.0 * np.maximum(i2, 0) + np.maximum(i3, 0))
+    assert np.array_equal(E[:, 0], want.astype(np.float32))
+    assert list(i2) == [-1, 12 % 7, 23 % 7, -1, -1, 45 % 7, 56 % 7]
+    # bf16: 1 + 2^-8 rounds to 1 (a tie, to the even neighbour); 1 + 2^-8 + 2^-7
+    # = 1 + 1.5 * 2^-7 rounds up to 1 + 2^-6 (the even neighbour of 1 + 2^-7)
+    Wb = np.full((V, 2), 0x3F80, dtype=np.uint16)          # 1.0
+    T2b = np.full((M2, 2), 0x3B80, dtype=np.uint16)        # 2^-8
+    T3b = np.full((M3, 2), 0x3C00, dtype=np.uint16)        # 2^-7
+    Eb = O.ngram_embed_forward(np.array([1, 2, 3]), Wb, T2b, T3b, V, M2, M3)
+    assert list(Eb[:, 0]) == [0x3F80, 0x3F80, 0x3F82]
+    # gradients: the three tables against np.add.at
+    rng = np.random.default_rng(96)
+    x = rng.integers(0, V, 40)
+    x[[5, 17]] = IGN
+    dE = rng.standard_normal((40, H))
+    dW, dT2, dT3 = O.ngram_embed_backward(x, dE, V, 16, M2, M3, seq_len=8)
+    for table, idx, rows in ((dW, np.where((x >= 0) & (x < V), x, -1), 16),
+                             (dT2, O.ngram_index(x, 2, V, M2, 8), M2), (dT3, O.ngram_index(x, 3, V, M3, 8), M3)):
+        ref = np.zeros((rows, H))
+        ok = idx >= 0
+        np.add.at(ref, idx[ok], dE[ok])
+        assert np.allclose(table, ref, rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_pad_vocab, pin_shards_tp_page, pin_shards_cover, pin_embedding_forward,
     pin_embedding_backward, pin_embedding_replay_order, pin_embedding_replay_bound,
     pin_equal_logits, pin_normalisation, pin_padded_head_demo, pin_bruteforce_decimal,
     pin_torch_cross_entropy, pin_shard_invariance, pin_ignored_and_bad,
     pin_finite_differences, pin_gradient_invariants, pin_sampled_candidates,
-    pin_sampled_full_set_is_full_softmax, pin_oth_head, pin_greedy_argmax,
+    pin_sampled_full_set_is_full_softmax, pin_oth_head, pin_greedy_argmax, pin_ngram_hash,
+    pin_ngram_embedding,
 ]

@@ -82,6 +82,18 @@ MUTATIONS = {
                       "    z = logits(h, W, W.shape[0])\n    arg = z.argmax(axis=1).astype(np.int64)"),
     # sharded argmax: a later shard wins ties
     "argmax_shard_tie_late": ("        take = m_k > best", "        take = m_k >= best"),
+    # n-gram read with the newest token as the highest digit
+    "ngram_digit_order": ("        value = sum(v * V ** j for j, v in enumerate(reversed(gram)))",
+                          "        value = sum(v * V ** j for j, v in enumerate(gram))"),
+    # n-grams running across the start of a sequence
+    "ngram_crosses_sequences": ("        pos = t % seq_len if seq_len > 0 else t\n        if pos < n - 1:",
+                                "        pos = t\n        if pos < n - 1:"),
+    # an n-gram with an invalid id still looked up
+    "ngram_keeps_invalid": ("        if any(v < 0 or v >= V for v in gram):\n            continue",
+                            "        if False:\n            continue"),
+    # bf16 rounding by truncation
+    "ngram_truncates": ("    return ((u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16))",
+                        "    return ((u) >> np.uint64(16))"),
     # target positions off by one in the candidate list
     "sampled_pos_shift": ("    pos[valid] = np.searchsorted(uniq, y[valid])",
                           "    pos[valid] = np.searchsorted(uniq, y[valid], side='right')"),

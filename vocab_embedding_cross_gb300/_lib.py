@@ -71,6 +71,16 @@ def lib():
         L.vce_greedy_argmax.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                                         c_void_p, c_void_p]
         L.vce_greedy_argmax.restype = c_int32
+        L.vce_ngram_hash.argtypes = [c_void_p, c_int64, c_int32, c_int64, c_int64, c_int64, c_void_p, c_void_p]
+        L.vce_ngram_hash.restype = c_int32
+        L.vce_ngram_embed_fwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64, c_int64,
+                                          c_void_p, c_void_p, c_void_p]
+        L.vce_ngram_embed_fwd.restype = c_int32
+        L.vce_ngram_workspace_size.argtypes = [P]
+        L.vce_ngram_workspace_size.restype = c_size_t
+        L.vce_ngram_embed_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
+                                          c_int64, c_void_p, c_size_t, c_void_p, c_void_p]
+        L.vce_ngram_embed_bwd.restype = c_int32
         L.vce_sampled_workspace_size.argtypes = [P, c_int64]
         L.vce_sampled_workspace_size.restype = c_size_t
         L.vce_sampled_loss.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_float,
@@ -200,6 +210,29 @@ def vce_greedy_argmax(p, h, W, argmax, max_logit=None, owner=None, ws=None, ws_b
                                    _ptr(ws), nb, _ptr(dev_status), _stream(stream)), "vce_greedy_argmax")
 
 
+def vce_ngram_hash(ids, n, V, M, out, seq_len=0, stream=None) -> None:
+    _check(lib().vce_ngram_hash(_ptr(ids), int(ids.numel()), int(n), int(V), int(M), int(seq_len), _ptr(out),
+                                _stream(stream)), "vce_ngram_hash")
+
+
+def vce_ngram_embed_fwd(p, ids, W, T2, M2, T3, M3, E, seq_len=0, dev_status=None, stream=None) -> None:
+    _check(lib().vce_ngram_embed_fwd(ctypes.byref(p), _ptr(ids), _ptr(W), _ptr(T2), int(M2), _ptr(T3), int(M3),
+                                     int(seq_len), _ptr(E), _ptr(dev_status), _stream(stream)),
+           "vce_ngram_embed_fwd")
+
+
+def vce_ngram_workspace_size(p: VceProblem) -> int:
+    return int(lib().vce_ngram_workspace_size(ctypes.byref(p)))
+
+
+def vce_ngram_embed_bwd(p, ids, dE, dW, dT2, M2, dT3, M3, ws, ws_bytes=None, seq_len=0, dev_status=None,
+                        stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().vce_ngram_embed_bwd(ctypes.byref(p), _ptr(ids), _ptr(dE), _ptr(dW), _ptr(dT2), int(M2), _ptr(dT3),
+                                     int(M3), int(seq_len), _ptr(ws), nb, _ptr(dev_status), _stream(stream)),
+           "vce_ngram_embed_bwd")
+
+
 def vce_embed_bwd_chunk() -> int:
     return int(lib().vce_embed_bwd_chunk())
 
@@ -218,7 +251,8 @@ def vce_wait_selftest(limit_ns: int, dev_status, stream=None) -> None:
 
 KERNEL_KINDS = ["embed_gather", "embed_sort", "embed_reduce", "tc_fwd", "tc_grad", "tc_dh", "tc_dw",
                 "merge", "loss_mean", "count_valid", "simt_fwd", "simt_grad", "sgemm", "wait_selftest",
-                "dh_reduce", "sampled_cand", "sampled_scatter", "tc_argmax", "argmax_merge", "simt_argmax"]
+                "dh_reduce", "sampled_cand", "sampled_scatter", "tc_argmax", "argmax_merge", "simt_argmax",
+                "ngram_hash", "ngram_fwd"]
 
 
 def vce_launch_count() -> int:

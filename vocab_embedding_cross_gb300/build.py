@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libvocabce.so")
-SOURCES = ["vce_api.cu", "embed.cu", "merge.cu", "loss_simt.cu", "loss_tc.cu", "noalloc.cu", "sampled.cu"]
+SOURCES = ["vce_api.cu", "embed.cu", "merge.cu", "loss_simt.cu", "loss_tc.cu", "noalloc.cu", "sampled.cu", "ngram.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]

@@ -115,6 +115,13 @@ int tc_unit_width(const vce_problem& p);
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_t st);
 
+// Hashed n-gram embeddings.
+cudaError_t launch_ngram_hash(const int64_t* ids, int64_t T, int n, int64_t V, int64_t M, int64_t seq_len,
+                              int64_t* out, cudaStream_t st);
+cudaError_t launch_ngram_embed_fwd(const vce_problem& p, const int64_t* ids, const void* W, const void* T2,
+                                   int64_t M2, const void* T3, int64_t M3, int64_t seq_len, void* E,
+                                   cudaStream_t st);
+
 // Sampled-softmax candidate list.
 size_t sampled_ws_bytes(const vce_problem& p);
 cudaError_t launch_sampled_candidates(const vce_problem& p, const int64_t* targets, const int64_t* draws,

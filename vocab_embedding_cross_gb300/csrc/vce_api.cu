@@ -526,6 +526,84 @@ vce_status vce_greedy_argmax(const vce_problem* p, const void* h, const void* W,
   return cuda_status(launch_argmax_merge(pd, ug, part, argmax, max_logit, owner, st));
 }
 
+vce_status vce_ngram_hash(const int64_t* ids, int64_t T, int32_t n, int64_t V, int64_t M, int64_t seq_len,
+                          int64_t* out, void* stream) {
+  if (T < 0 || T >= (int64_t(1) << 31) || n < 1 || V < 1 || V >= (int64_t(1) << 31) || M < 1 ||
+      M >= (int64_t(1) << 31) || seq_len < 0)
+    return VCE_ERR_ARG;
+  if (T == 0) return VCE_OK;
+  if (!ids || !out) return VCE_ERR_ARG;
+  if (!aligned(ids, 8) || !aligned(out, 8)) return VCE_ERR_UNSUPPORTED;
+  return cuda_status(launch_ngram_hash(ids, T, n, V, M, seq_len, out, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+bool ngram_tables_ok(int64_t M2, const void* T2, int64_t M3, const void* T3) {
+  const int64_t lim = int64_t(1) << 31;
+  return M2 >= 0 && M2 < lim && M3 >= 0 && M3 < lim && (M2 == 0 || T2) && (M3 == 0 || T3);
+}
+// The embedding backward of one n-gram table: a problem whose "vocabulary" is the table's rows.
+vce_problem ngram_table_problem(const vce_problem& p, int64_t M) {
+  vce_problem q = p;
+  q.Vp = M;
+  q.V_real = M;
+  q.S = 1;
+  q.tied_weights = 0;
+  return q;
+}
+}  // namespace
+
+vce_status vce_ngram_embed_fwd(const vce_problem* p, const int64_t* ids, const void* W, const void* T2,
+                               int64_t M2, const void* T3, int64_t M3, int64_t seq_len, void* E,
+                               int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (!ngram_tables_ok(M2, T2, M3, T3) || seq_len < 0) return VCE_ERR_ARG;
+  if (p->T == 0) return VCE_OK;
+  if (!ids || !W || !E) return VCE_ERR_ARG;
+  if (!aligned(ids, 8) || !aligned(W, 16) || !aligned(T2, 16) || !aligned(T3, 16) || !aligned(E, 16))
+    return VCE_ERR_UNSUPPORTED;
+  return cuda_status(launch_ngram_embed_fwd(*p, ids, W, M2 ? T2 : nullptr, M2, M3 ? T3 : nullptr, M3, seq_len, E,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+size_t vce_ngram_workspace_size(const vce_problem* p) {
+  if (check_problem(p) != VCE_OK) return SIZE_MAX;
+  return 2 * align_up(sizeof(int64_t) * static_cast<size_t>(p->T), kWsAlign) + embed_bwd_ws_bytes(*p);
+}
+
+vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const void* dE, float* dW, float* dT2,
+                               int64_t M2, float* dT3, int64_t M3, int64_t seq_len, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, void* stream) {
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (!ngram_tables_ok(M2, dT2, M3, dT3) || seq_len < 0) return VCE_ERR_ARG;
+  if (p->T == 0) return VCE_OK;
+  if (!ids || !dE || !dW) return VCE_ERR_ARG;
+  if (!aligned(ids, 8) || !aligned(dE, 16) || !aligned(dW, 16) || !aligned(dT2, 16) || !aligned(dT3, 16))
+    return VCE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < vce_ngram_workspace_size(p)) return VCE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* b = static_cast<char*>(ws);
+  const size_t ids_bytes = align_up(sizeof(int64_t) * static_cast<size_t>(p->T), kWsAlign);
+  int64_t* idx2 = reinterpret_cast<int64_t*>(b);
+  int64_t* idx3 = reinterpret_cast<int64_t*>(b + ids_bytes);
+  void* ews = b + 2 * ids_bytes;
+  if (cudaError_t e = launch_embed_bwd(*p, ids, dE, dW, ews, dev_status, st)) return cuda_status(e);
+  if (M2 > 0) {
+    if (cudaError_t e = launch_ngram_hash(ids, p->T, 2, p->V_real, M2, seq_len, idx2, st)) return cuda_status(e);
+    if (cudaError_t e = launch_embed_bwd(ngram_table_problem(*p, M2), idx2, dE, dT2, ews, dev_status, st))
+      return cuda_status(e);
+  }
+  if (M3 > 0) {
+    if (cudaError_t e = launch_ngram_hash(ids, p->T, 3, p->V_real, M3, seq_len, idx3, st)) return cuda_status(e);
+    if (cudaError_t e = launch_embed_bwd(ngram_table_problem(*p, M3), idx3, dE, dT3, ews, dev_status, st))
+      return cuda_status(e);
+  }
+  return VCE_OK;
+}
+
 vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* stream) {
   if (!dev_status) return VCE_ERR_ARG;
   return cuda_status(launch_wait_selftest(limit_ns, dev_status, static_cast<cudaStream_t>(stream)));

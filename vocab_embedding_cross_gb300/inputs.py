@@ -26,7 +26,7 @@ IGNORE_INDEX = -100
 
 # Stream tags: one independent PCG64 stream per tensor.
 _TAG = {"W": 1, "h": 2, "targets": 3, "ids": 4, "dE": 5, "tokens": 6,
-        "corrupt": 7, "forced": 8, "cand": 9}
+        "corrupt": 7, "forced": 8, "cand": 9, "T2": 10, "T3": 11}
 
 
 @dataclass(frozen=True)
@@ -85,6 +85,25 @@ WORKLOADS: Dict[str, Workload] = {
 }
 
 SAMPLED_P = 8192   # candidates of the sampled-softmax workload
+
+
+# Hashed n-gram tables of the n-gram embedding case: 2^18 rows each (the
+# pages' OT-H tables hold billions of parameters; their ten-times-smaller
+# variant is of this order per table at H=2048), over sequences of 2048 tokens
+# (the Qwen3-like batch is 4 x 2048).
+NGRAM_ROWS = 1 << 18
+NGRAM_SEQ_LEN = 2048
+
+
+def make_ngram_table(wl: Workload, n: int, rows: int, chunk_rows: int = 1 << 15) -> np.ndarray:
+    """Table of the hashed n-grams (n = 2 or 3): [rows, H] ~ N(0, w_std^2), in the workload's dtype."""
+    rng = _rng(wl, "T2" if n == 2 else "T3")
+    out = np.empty((rows, wl.H), dtype=np.uint16 if wl.dtype == "bf16" else np.float32)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        x = rng.standard_normal((r1 - r0, wl.H), dtype=np.float32) * np.float32(wl.w_std)
+        out[r0:r1] = _store(x, wl.dtype)
+    return out
 
 
 def make_negative_draws(wl: Workload, n: int) -> np.ndarray:
