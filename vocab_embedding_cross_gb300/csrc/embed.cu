@@ -76,14 +76,16 @@ constexpr int kSortItems = 8;
 constexpr int kSortTile = kSortThreads * kSortItems;
 constexpr int kRadix = 256;
 constexpr int kSmemSortMax = 16384;                       // keys the shared-memory variant holds
-constexpr int kSmemItems = kSmemSortMax / kSortThreads;   // 16 keys per thread
+constexpr int kSmemItems = kSmemSortMax / kSortThreads;   // at most 16 rounds of 32 keys per warp
+constexpr int kSortDigitBits = 9;                         // radix of the shared-memory passes
+constexpr int kSortDigits = 1 << kSortDigitBits;
 // Shared-memory arrays are padded by one word per 32 (index i at i + i/32), so
 // that each thread's 16 consecutive entries fall in distinct banks across a warp.
 __host__ __device__ constexpr int pad32(int i) { return i + (i >> 5); }
 constexpr size_t kSmemSortBytes = 2 * pad32(kSmemSortMax) * sizeof(uint32_t) +
-                                  pad32(16 * kSortThreads) * sizeof(int) + 64 * sizeof(int);
+                                  kSortWarps * kSortDigits * sizeof(int) + 64 * sizeof(int);
 
-struct RunDesc {
+struct __align__(16) RunDesc {
   int32_t start, end;   // sorted positions [start, end)
   int32_t id;
   int32_t slot;         // partial slot (multi-run ids) or -1
@@ -132,7 +134,7 @@ int bit_width(int64_t x) {   // bits needed for values in [0, x)
   return b;
 }
 
-// Block-wide exclusive scan of one int per thread (1024 threads).
+// Block-wide exclusive scan of one int per thread (up to 1024 threads).
 __device__ __forceinline__ int block_excl_scan(int v, int* sh_warp, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -144,7 +146,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sh_warp, int* total) 
   if (lane == 31) sh_warp[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = sh_warp[lane];
+    int w = lane < static_cast<int>(blockDim.x >> 5) ? sh_warp[lane] : 0;
     int s = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -216,6 +218,7 @@ __device__ __forceinline__ void build_runs(SegAt seg, int nseg, int n, int per_t
     hdr[1] = t_runs;
     hdr[3] = t_multi;
     hdr[4] = t_slots;
+    hdr[5] = 0;
   }
 }
 
@@ -226,20 +229,26 @@ __global__ void __launch_bounds__(kSortThreads, 1)
   extern __shared__ __align__(16) uint32_t smem_keys[];
   uint32_t* ka = smem_keys;
   uint32_t* kb = smem_keys + pad32(kSmemSortMax);
-  int* ctab = reinterpret_cast<int*>(smem_keys + 2 * pad32(kSmemSortMax));   // [16 digits][1024 threads]
-  int* sh_warp = ctab + pad32(16 * kSortThreads);
+  int* ctab = reinterpret_cast<int*>(smem_keys + 2 * pad32(kSmemSortMax));   // [32 warps][512 digits]
+  int* sh_warp = ctab + kSortWarps * kSortDigits;                              // 64 ints
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
 
   // Phase 0: stable compaction of the valid ids. Warp w reads its contiguous
-  // block of tokens 32 at a time (coalesced); ballots give the order.
+  // block of tokens 32 at a time (coalesced, all loads issued before use);
+  // ballots give the order.
   const int tpw = ((T + kSortWarps - 1) / kSortWarps + 31) / 32 * 32;   // tokens per warp, <= 512
-  int wcount = 0;
-  for (int j = 0; j < tpw / 32; ++j) {
+  constexpr uint32_t kNoKey = 0xFFFFFFFFu;
+  uint32_t tkey[kSmemItems];
+#pragma unroll
+  for (int j = 0; j < kSmemItems; ++j) {
     const int t = warp * tpw + j * 32 + lane;
-    const int64_t id = t < T ? ids[t] : -1;
-    wcount += __popc(__ballot_sync(0xffffffffu, id >= 0 && id < V_real));
+    const int64_t id = (j < tpw / 32 && t < T) ? ids[t] : -1;
+    tkey[j] = (id >= 0 && id < V_real) ? (static_cast<uint32_t>(id) << tbits) | static_cast<uint32_t>(t) : kNoKey;
   }
+  int wcount = 0;
+#pragma unroll
+  for (int j = 0; j < kSmemItems; ++j) wcount += __popc(__ballot_sync(0xffffffffu, tkey[j] != kNoKey));
   if (lane == 0) sh_warp[warp] = wcount;
   __syncthreads();
   int wbase = 0, n = 0;
@@ -249,151 +258,405 @@ __global__ void __launch_bounds__(kSortThreads, 1)
     n += c;
   }
   __syncthreads();
-  for (int j = 0; j < tpw / 32; ++j) {
-    const int t = warp * tpw + j * 32 + lane;
-    const int64_t id = t < T ? ids[t] : -1;
-    const bool ok = id >= 0 && id < V_real;
+#pragma unroll
+  for (int j = 0; j < kSmemItems; ++j) {
+    const bool ok = tkey[j] != kNoKey;
     const unsigned bal = __ballot_sync(0xffffffffu, ok);
-    if (ok) ka[pad32(wbase + __popc(bal & lt_mask))] = (static_cast<uint32_t>(id) << tbits) | static_cast<uint32_t>(t);
+    if (ok) ka[pad32(wbase + __popc(bal & lt_mask))] = tkey[j];
     wbase += __popc(bal);
   }
   __syncthreads();
 
-  // Phase 1: stable LSD radix passes over the id bits, 4 bits per pass. Thread
-  // tid owns kpt consecutive keys and ranks them with its own shared-memory
-  // counter per digit; the table of counters (digit-major, thread-minor) is
-  // scanned once per pass, which gives every key its stable destination.
-  const int kpt = (n + kSortThreads - 1) / kSortThreads;   // keys per thread, <= 16
-  const int k0 = tid * kpt;
+  // Phase 1: stable LSD radix passes over the id bits, 9 bits per pass. Warp
+  // w owns the kpw consecutive keys [w*kpw, (w+1)*kpw) and takes them 32 at a
+  // time; lanes holding the same digit find each other with one ballot per
+  // digit bit, which gives each key its rank among the warp's keys of that
+  // digit (in key order). The per-warp digit counts are then scanned digit-major, warp-minor,
+  // so every key lands at a stable position.
+  const int kpw = ((n + kSortWarps - 1) / kSortWarps + 31) & ~31;   // keys per warp, <= 512
+  const int rounds = kpw >> 5;                                      // <= 16
+  int* whist = ctab + warp * kSortDigits;                            // this warp's digit counts
   uint32_t* src = ka;
   uint32_t* dst = kb;
-  for (int shift = tbits; shift < tbits + idbits; shift += 4) {
+  for (int shift = tbits; shift < tbits + idbits; shift += kSortDigitBits) {
+    for (int i = tid; i < kSortWarps * kSortDigits; i += kSortThreads) ctab[i] = 0;
+    __syncthreads();
     uint32_t key[kSmemItems];
-    uint32_t lrw[kSmemItems / 4] = {};   // byte j%4 of word j/4: rank among this thread's keys of that digit
-#pragma unroll
-    for (int b = 0; b < 16; ++b) ctab[pad32(b * kSortThreads + tid)] = 0;
+    uint32_t rk[kSmemItems / 2] = {};   // 16-bit ranks, two per word
 #pragma unroll
     for (int j = 0; j < kSmemItems; ++j) {
-      const bool ok = j < kpt && k0 + j < n;
-      key[j] = ok ? src[pad32(k0 + j)] : 0u;
-      if (ok) {
-        int* c = &ctab[pad32(static_cast<int>((key[j] >> shift) & 15u) * kSortThreads + tid)];
-        const int v = *c;
-        *c = v + 1;
-        lrw[j >> 2] |= static_cast<uint32_t>(v) << ((j & 3) * 8);
+      if (j < rounds) {
+        const int q = warp * kpw + j * 32 + lane;
+        const bool ok = q < n;
+        key[j] = ok ? src[pad32(q)] : 0u;
+        const uint32_t d = ok ? (key[j] >> shift) & (kSortDigits - 1) : kSortDigits;
+        uint32_t peers = __ballot_sync(0xffffffffu, ok);
+#pragma unroll
+        for (int b = 0; b < kSortDigitBits; ++b) {
+          const uint32_t bb = __ballot_sync(0xffffffffu, (d >> b) & 1u);
+          peers &= ((d >> b) & 1u) ? bb : ~bb;
+        }
+        int base = 0;
+        if (ok) base = whist[d];
+        __syncwarp();
+        if (ok) {
+          rk[j >> 1] |= static_cast<uint32_t>(base + __popc(peers & lt_mask)) << ((j & 1) * 16);
+          if (lane == __ffs(peers) - 1) whist[d] = base + __popc(peers);
+        }
+        __syncwarp();
       }
     }
     __syncthreads();
     {
+      // Thread tid scans digit tid/2 over warps [16*(tid&1), +16).
+      const int d = tid >> 1, w0 = (tid & 1) * 16;
       int v[16];
       int sum = 0;
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        v[k] = ctab[pad32(tid * 16 + k)];
+        v[k] = ctab[(w0 + k) * kSortDigits + d];
         sum += v[k];
       }
       int all;
       int run = block_excl_scan(sum, sh_warp, &all);
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        ctab[pad32(tid * 16 + k)] = run;
+        ctab[(w0 + k) * kSortDigits + d] = run;
         run += v[k];
       }
     }
     __syncthreads();
 #pragma unroll
-    for (int j = 0; j < kSmemItems; ++j)
-      if (j < kpt && k0 + j < n)
-        dst[pad32(ctab[pad32(static_cast<int>((key[j] >> shift) & 15u) * kSortThreads + tid)] +
-                  static_cast<int>((lrw[j >> 2] >> ((j & 3) * 8)) & 0xFFu))] = key[j];
+    for (int j = 0; j < kSmemItems; ++j) {
+      const int q = warp * kpw + j * 32 + lane;
+      if (j < rounds && q < n) {
+        const int d = static_cast<int>((key[j] >> shift) & (kSortDigits - 1));
+        dst[pad32(whist[d] + static_cast<int>((rk[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu))] = key[j];
+      }
+    }
     __syncthreads();
     uint32_t* tmp = src;
     src = dst;
     dst = tmp;
   }
 
-  // Phase 2: sorted token indices to global memory; segment starts into the
-  // free key buffer (seg), one entry per distinct id, at most n <= 16384.
+  // Phase 2: sorted token indices to global memory (coalesced within each
+  // warp's chunk) and the segment heads (first position of every distinct id)
+  // into the free key buffer.
   const uint32_t tmask = (1u << tbits) - 1u;
   int* seg = reinterpret_cast<int*>(dst);
-  int heads = 0;
-  for (int j = 0; j < kpt; ++j) {
-    const int q = k0 + j;
-    if (q < n) {
-      tsorted[q] = static_cast<int32_t>(src[pad32(q)] & tmask);
-      if (q == 0 || (src[pad32(q)] >> tbits) != (src[pad32(q - 1)] >> tbits)) ++heads;
-    }
+  auto is_head = [&](int q) { return q == 0 || (src[pad32(q)] >> tbits) != (src[pad32(q - 1)] >> tbits); };
+  int wheads = 0;
+  for (int j = 0; j < rounds; ++j) {
+    const int q = warp * kpw + j * 32 + lane;
+    const bool ok = q < n;
+    if (ok) tsorted[q] = static_cast<int32_t>(src[pad32(q)] & tmask);
+    wheads += __popc(__ballot_sync(0xffffffffu, ok && is_head(q)));
   }
-  int nseg;
-  int sidx = block_excl_scan(heads, sh_warp, &nseg);
-  for (int j = 0; j < kpt; ++j) {
-    const int q = k0 + j;
-    if (q < n && (q == 0 || (src[pad32(q)] >> tbits) != (src[pad32(q - 1)] >> tbits))) seg[pad32(sidx++)] = q;
+  if (lane == 0) sh_warp[32 + warp] = wheads;
+  __syncthreads();
+  int hbase = 0, nseg = 0;
+  for (int w = 0; w < kSortWarps; ++w) {
+    const int c = sh_warp[32 + w];
+    hbase += w < warp ? c : 0;
+    nseg += c;
+  }
+  for (int j = 0; j < rounds; ++j) {
+    const int q = warp * kpw + j * 32 + lane;
+    const bool h = q < n && is_head(q);
+    const uint32_t bal = __ballot_sync(0xffffffffu, h);
+    if (h) seg[pad32(hbase + __popc(bal & lt_mask))] = q;
+    hbase += __popc(bal);
   }
   __syncthreads();
 
-  // Phase 3: runs of kEmbedBwdChunk tokens. Per segment s: nr runs; packed
-  // prefix rb[s] = (runs before s) << 16 | (multi-run segments before s) in
-  // ctab. Then each run is written by one thread, which finds its segment by
-  // binary search.
+  // Phase 3: runs of kEmbedBwdChunk tokens. Warp w takes segments
+  // [w*spw, (w+1)*spw), one per lane per round; a block scan of the warps'
+  // (runs, multi-run segments) totals gives each segment its first run and
+  // first partial slot, and the lane holding a segment writes its runs.
   auto seg_end = [&](int sg) { return sg + 1 < nseg ? seg[pad32(sg + 1)] : n; };
-  const int spt = (nseg + kSortThreads - 1) / kSortThreads;   // segments per thread, <= 16
-  const int s0 = tid * spt;
-  int packed = 0;
-  for (int j = 0; j < spt; ++j) {
-    const int sg = s0 + j;
+  const int spw = ((nseg + kSortWarps - 1) / kSortWarps + 31) & ~31;
+  int wpacked = 0;   // (runs << 16) | multi-run segments, over this warp's segments
+  for (int j = 0; j < spw; j += 32) {
+    const int sg = warp * spw + j + lane;
+    int pk = 0;
     if (sg < nseg) {
       const int nr = (seg_end(sg) - seg[pad32(sg)] + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
-      packed += (nr << 16) | (nr > 1 ? 1 : 0);
+      pk = (nr << 16) | (nr > 1 ? 1 : 0);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pk += __shfl_xor_sync(0xffffffffu, pk, o);
+    wpacked += pk;
   }
   int tot_packed;
-  int pre = block_excl_scan(packed, sh_warp, &tot_packed);
-  for (int j = 0; j < spt; ++j) {
-    const int sg = s0 + j;
-    if (sg < nseg) {
-      ctab[pad32(sg)] = pre;
-      const int nr = (seg_end(sg) - seg[pad32(sg)] + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
-      pre += (nr << 16) | (nr > 1 ? 1 : 0);
-    }
-  }
-  __syncthreads();
+  int pre = block_excl_scan(lane == 0 ? wpacked : 0, sh_warp, &tot_packed);
+  pre = __shfl_sync(0xffffffffu, pre, 0);
   const int n_runs = tot_packed >> 16, n_multi = tot_packed & 0xFFFF;
-  for (int r = tid; r < n_runs; r += kSortThreads) {
-    int lo = 0, hi = nseg - 1;   // largest sg with runs-before(sg) <= r
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if ((ctab[pad32(mid)] >> 16) <= r)
-        lo = mid;
-      else
-        hi = mid - 1;
+  for (int j = 0; j < spw; j += 32) {
+    const int sg = warp * spw + j + lane;
+    int nr = 0, st = 0, en = 0;
+    if (sg < nseg) {
+      st = seg[pad32(sg)];
+      en = seg_end(sg);
+      nr = (en - st + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
     }
-    const int sg = lo;
-    const int rb = ctab[pad32(sg)] >> 16, mb = ctab[pad32(sg)] & 0xFFFF;
-    const int st = seg[pad32(sg)], en = seg_end(sg);
-    const int nr = (en - st + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
-    const int k = r - rb;
-    const bool multi = nr > 1;
-    const int q0 = rb - (sg - mb);   // slots used by the multi-run segments before sg
-    RunDesc rd;
-    rd.start = st + k * kEmbedBwdChunk;
-    rd.end = min(en, rd.start + kEmbedBwdChunk);
-    rd.id = static_cast<int32_t>(src[pad32(st)] >> tbits);
-    rd.slot = multi ? q0 + k : -1;
-    rd.mseg = multi ? mb : -1;
-    rd.nruns = nr;
-    rd.first_slot = multi ? q0 : -1;
-    rd.pad = 0;
-    runs[r] = rd;
-    if (multi && k == 0)
-      for (int hh = 0; hh < nh; ++hh) counters[mb * nh + hh] = 0;
+    const int pk = sg < nseg ? (nr << 16) | (nr > 1 ? 1 : 0) : 0;
+    int incl = pk;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int mine = pre + incl - pk;   // packed prefix before this segment
+    pre += __shfl_sync(0xffffffffu, incl, 31);
+    if (sg < nseg) {
+      const int rb = mine >> 16, mb = mine & 0xFFFF;
+      const bool multi = nr > 1;
+      const int q0 = rb - (sg - mb);   // slots used by the multi-run segments before sg
+      const int32_t id = static_cast<int32_t>(src[pad32(st)] >> tbits);
+      for (int k = 0; k < nr; ++k) {
+        RunDesc rd;
+        rd.start = st + k * kEmbedBwdChunk;
+        rd.end = min(en, rd.start + kEmbedBwdChunk);
+        rd.id = id;
+        rd.slot = multi ? q0 + k : -1;
+        rd.mseg = multi ? mb : -1;
+        rd.nruns = nr;
+        rd.first_slot = multi ? q0 : -1;
+        rd.pad = 0;
+        runs[rb + k] = rd;
+      }
+      if (multi)
+        for (int hh = 0; hh < nh; ++hh) counters[mb * nh + hh] = 0;
+    }
   }
   if (tid == 0) {
     hdr[0] = n;
     hdr[1] = n_runs;
     hdr[2] = nseg;
     hdr[3] = n_multi;
-    hdr[4] = (tot_packed >> 16) - (nseg - n_multi);
+    hdr[4] = n_runs - (nseg - n_multi);
+    hdr[5] = 0;
+  }
+}
+
+// Bucketed variant: the sort spread over gridDim.x CTAs (one per SM). CTA b
+// takes the valid ids with id % NB == b, in token order, and sorts them by
+// id / NB (stable LSD radix, 6-bit digits, warp-level ranking by ballots) in
+// shared memory. It then cuts its ids into runs exactly as the single-CTA
+// variants do and claims space for its sorted tokens, runs and partial slots
+// with atomic additions on the header, which the host zeroes first. The
+// order of the buckets in the arrays depends on which CTA claims first; every
+// id's runs and their order do not, so the reduce gives the same bits.
+constexpr int kBktThreads = 1024;
+constexpr int kBktWarps = kBktThreads / 32;
+constexpr int kBktDigitBits = 6;
+constexpr int kBktDigits = 1 << kBktDigitBits;
+
+size_t bucket_sort_smem(int64_t T) {   // two key buffers, 16-bit ranks (whole words), digit counts, scratch
+  return static_cast<size_t>(T) * 2 * sizeof(uint32_t) + static_cast<size_t>((T + 1) / 2) * sizeof(uint32_t) +
+         kBktWarps * kBktDigits * sizeof(int) + 96 * sizeof(int);
+}
+
+__global__ void __launch_bounds__(kBktThreads, 1)
+    embed_sort_bucket_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int qbits, int nh,
+                             int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
+  extern __shared__ __align__(16) uint32_t bsm[];
+  uint32_t* ka = bsm;
+  uint32_t* kb = bsm + T;
+  uint16_t* rank16 = reinterpret_cast<uint16_t*>(bsm + 2 * T);
+  int* hist = reinterpret_cast<int*>(bsm + 2 * T + (T + 1) / 2);   // [warps][64 digits]
+  // 96 ints of scratch: [0, 32) per-warp counts, [32, 65) the block scan, [80, 84) broadcasts
+  int* sh = hist + kBktWarps * kBktDigits;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const uint32_t NB = gridDim.x, b = blockIdx.x;
+
+  // Phase A: this bucket's ids in token order. Warp w scans tokens
+  // [w*tpw, (w+1)*tpw) 32 at a time; ballots give the order.
+  const int tpw = ((T + kBktWarps - 1) / kBktWarps + 31) & ~31;
+  auto key_of = [&](int t) -> uint32_t {
+    const int64_t id = t < T ? ids[t] : -1;
+    if (id < 0 || id >= V_real) return 0xFFFFFFFFu;
+    const uint32_t u = static_cast<uint32_t>(id);
+    const uint32_t q = u / NB;
+    if (u - q * NB != b) return 0xFFFFFFFFu;
+    return (q << tbits) | static_cast<uint32_t>(t);
+  };
+  constexpr int kMaxRounds = kSmemSortMax / kBktWarps / 32;   // 32 rounds of 32 tokens per warp at most
+  uint32_t tkey[kMaxRounds];
+#pragma unroll
+  for (int j = 0; j < kMaxRounds; ++j) tkey[j] = j * 32 < tpw ? key_of(warp * tpw + j * 32 + lane) : 0xFFFFFFFFu;
+  int wcount = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxRounds; ++j) wcount += __popc(__ballot_sync(0xffffffffu, tkey[j] != 0xFFFFFFFFu));
+  if (lane == 0) sh[warp] = wcount;
+  __syncthreads();
+  int wbase = 0, m = 0;
+  for (int w = 0; w < kBktWarps; ++w) {
+    const int c = sh[w];
+    wbase += w < warp ? c : 0;
+    m += c;
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxRounds; ++j) {
+    const bool ok = tkey[j] != 0xFFFFFFFFu;
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    if (ok) ka[wbase + __popc(bal & lt_mask)] = tkey[j];
+    wbase += __popc(bal);
+  }
+  if (tid == 0) sh[80] = m > 0 ? atomicAdd(&hdr[0], m) : 0;   // this bucket's place in tsorted
+  __syncthreads();
+  const int tbase = sh[80];
+
+  // Phase B: stable LSD radix passes over the id / NB bits.
+  const int kpw = ((m + kBktWarps - 1) / kBktWarps + 31) & ~31;
+  int* whist = hist + warp * kBktDigits;
+  uint32_t* src = ka;
+  uint32_t* dst = kb;
+  for (int shift = tbits; shift < tbits + qbits; shift += kBktDigitBits) {
+    for (int i = tid; i < kBktWarps * kBktDigits; i += kBktThreads) hist[i] = 0;
+    __syncthreads();
+    for (int j = 0; j < kpw; j += 32) {
+      const int q = warp * kpw + j + lane;
+      const bool ok = q < m;
+      const uint32_t d = ok ? (src[q] >> shift) & (kBktDigits - 1) : kBktDigits;
+      uint32_t peers = __ballot_sync(0xffffffffu, ok);
+#pragma unroll
+      for (int bit = 0; bit < kBktDigitBits; ++bit) {
+        const uint32_t bb = __ballot_sync(0xffffffffu, (d >> bit) & 1u);
+        peers &= ((d >> bit) & 1u) ? bb : ~bb;
+      }
+      int base = 0;
+      if (ok) base = whist[d];
+      __syncwarp();
+      if (ok) {
+        rank16[q] = static_cast<uint16_t>(base + __popc(peers & lt_mask));
+        if (lane == __ffs(peers) - 1) whist[d] = base + __popc(peers);
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+    {
+      // digits x warps, digit-major, two entries per thread: thread tid takes
+      // digit tid / (warps/2) and warps 2 * (tid % (warps/2)), +1.
+      static_assert(kBktWarps * kBktDigits == 2 * kBktThreads, "two scan entries per thread");
+      const int d = tid / (kBktWarps / 2), w0 = (tid % (kBktWarps / 2)) * 2;
+      const int v0 = hist[w0 * kBktDigits + d], v1 = hist[(w0 + 1) * kBktDigits + d];
+      int all;
+      const int run = block_excl_scan(v0 + v1, sh + 32, &all);
+      hist[w0 * kBktDigits + d] = run;
+      hist[(w0 + 1) * kBktDigits + d] = run + v0;
+    }
+    __syncthreads();
+    for (int j = 0; j < kpw; j += 32) {
+      const int q = warp * kpw + j + lane;
+      if (q < m) {
+        const uint32_t k = src[q];
+        dst[whist[(k >> shift) & (kBktDigits - 1)] + rank16[q]] = k;
+      }
+    }
+    __syncthreads();
+    uint32_t* tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+
+  // Phase C: sorted tokens, segment heads, runs.
+  const uint32_t tmask = (1u << tbits) - 1u;
+  int* seg = reinterpret_cast<int*>(dst);
+  auto is_head = [&](int q) { return q == 0 || (src[q] >> tbits) != (src[q - 1] >> tbits); };
+  int wheads = 0;
+  for (int j = 0; j < kpw; j += 32) {
+    const int q = warp * kpw + j + lane;
+    const bool ok = q < m;
+    if (ok) tsorted[tbase + q] = static_cast<int32_t>(src[q] & tmask);
+    wheads += __popc(__ballot_sync(0xffffffffu, ok && is_head(q)));
+  }
+  if (lane == 0) sh[warp] = wheads;
+  __syncthreads();
+  int hbase = 0, nseg = 0;
+  for (int w = 0; w < kBktWarps; ++w) {
+    const int c = sh[w];
+    hbase += w < warp ? c : 0;
+    nseg += c;
+  }
+  for (int j = 0; j < kpw; j += 32) {
+    const int q = warp * kpw + j + lane;
+    const bool h = q < m && is_head(q);
+    const uint32_t bal = __ballot_sync(0xffffffffu, h);
+    if (h) seg[hbase + __popc(bal & lt_mask)] = q;
+    hbase += __popc(bal);
+  }
+  __syncthreads();
+  auto seg_end = [&](int sg) { return sg + 1 < nseg ? seg[sg + 1] : m; };
+  const int spw = ((nseg + kBktWarps - 1) / kBktWarps + 31) & ~31;
+  int wpacked = 0;   // (runs << 16) | multi-run segments, over this warp's segments
+  for (int j = 0; j < spw; j += 32) {
+    const int sg = warp * spw + j + lane;
+    int pk = 0;
+    if (sg < nseg) {
+      const int nr = (seg_end(sg) - seg[sg] + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+      pk = (nr << 16) | (nr > 1 ? 1 : 0);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pk += __shfl_xor_sync(0xffffffffu, pk, o);
+    wpacked += pk;
+  }
+  int tot_packed;
+  int pre = block_excl_scan(lane == 0 ? wpacked : 0, sh + 32, &tot_packed);
+  pre = __shfl_sync(0xffffffffu, pre, 0);
+  const int n_runs = tot_packed >> 16, n_multi = tot_packed & 0xFFFF;
+  const int n_single = nseg - n_multi;
+  const int n_slots = n_runs - n_single;
+  // Runs of multi-run ids are placed from the front of the run list (a run's
+  // partial slot has the same index), single runs from the back: the reduce
+  // then starts with the ids whose runs must be combined.
+  if (tid == 0) {
+    sh[81] = n_slots > 0 ? atomicAdd(&hdr[1], n_slots) : 0;
+    sh[82] = n_multi > 0 ? atomicAdd(&hdr[3], n_multi) : 0;
+    sh[83] = n_single > 0 ? atomicAdd(&hdr[5], n_single) : 0;
+    if (nseg > 0) atomicAdd(&hdr[2], nseg);
+  }
+  __syncthreads();
+  const int sbase = sh[81], mbase = sh[82], bbase = sh[83];
+  for (int j = 0; j < spw; j += 32) {
+    const int sg = warp * spw + j + lane;
+    int nr = 0, st = 0, en = 0;
+    if (sg < nseg) {
+      st = seg[sg];
+      en = seg_end(sg);
+      nr = (en - st + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+    }
+    const int pk = sg < nseg ? (nr << 16) | (nr > 1 ? 1 : 0) : 0;
+    int incl = pk;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int mine = pre + incl - pk;
+    pre += __shfl_sync(0xffffffffu, incl, 31);
+    if (sg < nseg) {
+      const int rb = mine >> 16, mb = mine & 0xFFFF;
+      const bool multi = nr > 1;
+      const int q0 = rb - (sg - mb);
+      const int32_t id = static_cast<int32_t>((src[st] >> tbits) * NB + b);
+      for (int k = 0; k < nr; ++k) {
+        RunDesc rd;
+        rd.start = tbase + st + k * kEmbedBwdChunk;
+        rd.end = tbase + min(en, st + (k + 1) * kEmbedBwdChunk);
+        rd.id = id;
+        rd.slot = multi ? sbase + q0 + k : -1;
+        rd.mseg = multi ? mbase + mb : -1;
+        rd.nruns = nr;
+        rd.first_slot = multi ? sbase + q0 : -1;
+        rd.pad = 0;
+        runs[multi ? sbase + q0 + k : T - 1 - (bbase + (sg - mb))] = rd;
+      }
+      if (multi)
+        for (int hh = 0; hh < nh; ++hh) counters[(mbase + mb) * nh + hh] = 0;
+    }
   }
 }
 
@@ -562,16 +825,19 @@ template <typename TE>
 __global__ void __launch_bounds__(128)
     embed_reduce_kernel(const int32_t* __restrict__ hdr, const int32_t* __restrict__ tsorted,
                         const RunDesc* __restrict__ runs, const TE* __restrict__ dE, float* __restrict__ dW,
-                        float* partials, int32_t* counters, int H, int nh) {
+                        float* partials, int32_t* counters, int H, int nh, int cap) {
   constexpr int VEC = 16 / sizeof(TE);
   constexpr int NQ = VEC / 4;
   constexpr int U = 8;   // rows loaded ahead of the sequential adds
   __shared__ int s_last;
   const int lane = threadIdx.x & 31;
-  const int n_items = hdr[1] * nh;
+  // Runs [0, n_front) sit at the front of the list, the other n_back at its
+  // end (indices cap-1, cap-2, ...).
+  const int n_front = hdr[1], n_back = hdr[5];
+  const int n_items = (n_front + n_back) * nh;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int r = item / nh, hs = item - r * nh;
-    const RunDesc rd = runs[r];
+    const RunDesc rd = runs[r < n_front ? r : cap - 1 - (r - n_front)];
     const int len = rd.end - rd.start;   // <= 32
     const int col = hs * 128 * VEC + static_cast<int>(threadIdx.x) * VEC;
     const bool active = col < H;
@@ -699,7 +965,21 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   float* partials = reinterpret_cast<float*>(b + L.partials);
   const int tbits = bit_width(p.T);
   const int idbits = bit_width(p.V_real);
-  if (p.T <= kSmemSortMax && tbits + idbits <= 32) {
+  const DevInfo di = current_device_info();
+  const int nb = di.num_sms > 0 ? di.num_sms : 1;
+  const int qbits = bit_width(ceil_div(p.V_real, nb));
+  if (p.T <= kSmemSortMax && tbits + qbits <= 32 && nb > 1) {
+    static bool configured = false;
+    if (!configured) {
+      cudaError_t e = cudaFuncSetAttribute(embed_sort_bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(bucket_sort_smem(kSmemSortMax)));
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    if (cudaError_t e = cudaMemsetAsync(hdr, 0, 8 * sizeof(int32_t), st)) return e;
+    embed_sort_bucket_kernel<<<nb, kBktThreads, bucket_sort_smem(p.T), st>>>(
+        ids, static_cast<int>(p.T), p.V_real, tbits, qbits, L.nh, hdr, tsorted, runs, counters);
+  } else if (p.T <= kSmemSortMax && tbits + idbits <= 32) {
     static bool configured = false;
     if (!configured) {
       cudaError_t e = cudaFuncSetAttribute(embed_sort_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -716,14 +996,15 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   note_launch(VCE_K_EMBED_SORT, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const DevInfo di = current_device_info();
   const int grid = di.num_sms * 8;
   if (p.dtype == VCE_BF16)
     embed_reduce_kernel<uint16_t><<<grid, 128, 0, st>>>(hdr, tsorted, runs, static_cast<const uint16_t*>(dE), dW,
-                                                        partials, counters, static_cast<int>(p.H), L.nh);
+                                                        partials, counters, static_cast<int>(p.H), L.nh,
+                                                        static_cast<int>(p.T));
   else
     embed_reduce_kernel<float><<<grid, 128, 0, st>>>(hdr, tsorted, runs, static_cast<const float*>(dE), dW,
-                                                     partials, counters, static_cast<int>(p.H), L.nh);
+                                                     partials, counters, static_cast<int>(p.H), L.nh,
+                                                     static_cast<int>(p.T));
   note_launch(VCE_K_EMBED_REDUCE, st);
   return cudaGetLastError();
 }
