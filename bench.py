@@ -28,6 +28,12 @@ sys.path.insert(0, ROOT)
 METRIC = "fused vocab-CE fwd+bwd tokens/s & % BF16 TC peak; embed gather/bwd GB/s vs HBM"
 WORKLOAD = "qwen3_tied"
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# roofline kernel on this workload, from one ncu capture of that kernel (its
+# summary is kept under profiles/). A change to the kernel makes the figure
+# stale: it must then be removed (the line reports null) or taken again.
+MEASURED_TRAFFIC = {("qwen3_tied", "tc_grad"): 1656291200}
+
 
 def load_peaks():
     try:
@@ -43,6 +49,25 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def max_over_ranks(ms: float, world: int, device="cuda") -> float:
+    """The slowest replica's time per step: every rank gets the maximum over
+    ranks (all-reduce MAX, then a barrier). One rank returns its own time."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Replicas: every rank processes its own batch, so the job's throughput is
+    all ranks' tokens over the slowest rank's step time (weak scaling)."""
+    return world * tokens_per_rank / (ms / 1e3)
 
 
 class Clocks:
@@ -175,13 +200,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     launches = vce.vce_launch_count() - n0
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.barrier()
-        ms = float(t.item())
-    value = world * T / (ms / 1e3)
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    value = whole_job_tokens_per_s(T, world, ms)
 
     # ---- per-launch timing (separate pass, events after every launch) ----
     # A spin kernel first holds the stream so that every launch below is queued
@@ -215,8 +235,10 @@ def run_ours(args):
         t_ms, n = per_kind[dom]
         achieved = flops[dom] / (t_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
+        traffic = MEASURED_TRAFFIC.get((args.workload, dom)) if not (args.bwd_cols or args.no_dh_split) else None
         roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                     "launches_per_step": n, "ms_per_step": round(t_ms, 4),
                     "peak_kind": f"bf16_tflops_sustained ({peak_src})"}
     credited = 6.0 * T * H * V
