@@ -265,6 +265,9 @@ def run_ours(args):
     # ---- end to end through the C ABI with host buffers ----
     e2e = run_e2e(args, vce, D, d, p, W, E, loss, lse, dH, dW, st, ws_f, ws_b, ws_e, stream, wl)
 
+    # ---- the embedding on the GPT-OSS-shaped table ----
+    emb_gptoss = run_embedding(args, vce, D, I, stream, peaks, "gptoss_embed")
+
     # ---- greedy argmax over the same head (decoding), device resident ----
     greedy = run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks)
 
@@ -298,6 +301,7 @@ def run_ours(args):
                              "executed_flops": 8.0 * T * H * V, "vc": int(vc)},
             "embedding": emb,
             "sampled_softmax": sampled,
+            "embedding_gptoss": emb_gptoss,
             "greedy_argmax": greedy,
             "ngram_embedding": ngram,
             "per_kernel_ms": {k: round(v[0], 4) for k, v in sorted(per_kind.items())},
@@ -337,6 +341,60 @@ def run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks):
     tf = 2.0 * T * H * V / (ms / 1e3) / 1e12
     return {"tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_call": round(ms, 4), "calls": n,
             "TFLOPs": round(tf, 1), "frac_of_burst": round(tf / peaks["bf16_tflops"], 4)}
+
+
+def run_embedding(args, vce, D, I, stream, peaks, name):
+    """Masked lookup and deterministic backward on a workload of their own (the
+    GPT-OSS-shaped table [201088, 3072], T=16384 Zipf ids with 2% padding and
+    1% out-of-range ids): microseconds per call and GB/s of the algorithmic
+    bytes (ids, the distinct valid rows read, E written; dE read, touched dW
+    rows read-modify-written in fp32). L2 is flushed before every call."""
+    import torch
+    wl = I.WORKLOADS[name]
+    d = I.make_all(wl, ("W", "ids", "dE"))
+    T, H = wl.T, wl.H
+    p = vce.problem(T, H, wl.Vp, wl.V_real, wl.S, vce.VCE_BF16)
+    W, dE = D.to_device(d["W"]), D.to_device(d["dE"])
+    ids = torch.from_numpy(d["ids"]).cuda()
+    E = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    dW = torch.zeros((wl.Vp, H), device="cuda")
+    ws = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_EMBED_BWD))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = stream.cuda_stream
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    valid = (d["ids"] >= 0) & (d["ids"] < wl.V_real)
+    import numpy as np
+    U = int(np.unique(d["ids"][valid]).size)
+    gather_bytes = 8 * T + U * H * 2 + T * H * 2
+    bwd_bytes = 8 * T + T * H * 2 + U * H * 8
+
+    def timed(fn, n):
+        tot = 0.0
+        for i in range(n + 3):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                tot += e0.elapsed_time(e1)
+        return tot / n
+
+    n = max(10, args.steps // 2)
+    g_ms = timed(lambda: vce.vce_embed_fwd(p, ids, W, E, dev_status=st, stream=sp), n)
+    b_ms = timed(lambda: vce.vce_embed_bwd(p, ids, dE, dW, ws, dev_status=st, stream=sp), n)
+    assert int(st.item()) == 0, vce.status_str(int(st.item()))
+    del W, dE, E, dW, ws, flush
+    torch.cuda.empty_cache()
+    return {"workload": f"{name}: W[{wl.Vp},{H}] bf16, T={T} Zipf(1.1) ids, 2% padding id, 1% out of range, "
+                        f"{U} distinct valid rows", "l2": "flushed (256 MB write) before every call",
+            "gather_us": round(g_ms * 1e3, 2), "gather_GBps": round(gather_bytes / (g_ms / 1e3) / 1e9, 1),
+            "gather_frac": round(gather_bytes / (g_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "bwd_us": round(b_ms * 1e3, 2), "bwd_GBps": round(bwd_bytes / (b_ms / 1e3) / 1e9, 1),
+            "bwd_frac": round(bwd_bytes / (b_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "gather_bytes": gather_bytes, "bwd_bytes": bwd_bytes}
 
 
 def run_ngram(args, vce, D, I, wl, d, p, W, dE, stream, peaks):
