@@ -969,23 +969,23 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   const int nb = di.num_sms > 0 ? di.num_sms : 1;
   const int qbits = bit_width(ceil_div(p.V_real, nb));
   if (p.T <= kSmemSortMax && tbits + qbits <= 32 && nb > 1) {
-    static bool configured = false;
-    if (!configured) {
+    static std::atomic<uint64_t> configured{0};
+    if (device_pending(configured)) {
       cudaError_t e = cudaFuncSetAttribute(embed_sort_bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(bucket_sort_smem(kSmemSortMax)));
       if (e != cudaSuccess) return e;
-      configured = true;
+      mark_device_done(configured);
     }
     if (cudaError_t e = cudaMemsetAsync(hdr, 0, 8 * sizeof(int32_t), st)) return e;
     embed_sort_bucket_kernel<<<nb, kBktThreads, bucket_sort_smem(p.T), st>>>(
         ids, static_cast<int>(p.T), p.V_real, tbits, qbits, L.nh, hdr, tsorted, runs, counters);
   } else if (p.T <= kSmemSortMax && tbits + idbits <= 32) {
-    static bool configured = false;
-    if (!configured) {
+    static std::atomic<uint64_t> configured{0};
+    if (device_pending(configured)) {
       cudaError_t e = cudaFuncSetAttribute(embed_sort_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemSortBytes));
       if (e != cudaSuccess) return e;
-      configured = true;
+      mark_device_done(configured);
     }
     embed_sort_smem_kernel<<<1, kSortThreads, kSmemSortBytes, st>>>(ids, static_cast<int>(p.T), p.V_real, tbits,
                                                                     idbits, L.nh, hdr, tsorted, runs, counters);

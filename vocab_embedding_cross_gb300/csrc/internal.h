@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libvocabce.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -52,6 +53,20 @@ struct DevInfo {
   int num_sms = 0;
 };
 DevInfo current_device_info();
+
+// Per-device one-time setup (a kernel's shared-memory limit is a property of
+// the device): true until mark_device_done has run for the current device.
+// Two threads may both see "not done" and both do the (idempotent) setup.
+inline bool device_pending(const std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev < 0 || dev >= 64 || (done.load(std::memory_order_acquire) & (uint64_t(1) << dev)) == 0;
+}
+inline void mark_device_done(std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64) done.fetch_or(uint64_t(1) << dev, std::memory_order_release);
+}
 uint64_t wait_limit_ns();
 // Called after every kernel launch: counts it and, when a table is installed,
 // records the next timing event on `st` (see vce_set_launch_events).

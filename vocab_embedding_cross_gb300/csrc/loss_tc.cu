@@ -724,37 +724,39 @@ __global__ void wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
   __syncthreads();
 }
 
+// Clusters of this mode that fit on the device at once (asked once per device,
+// after the kernel's shared-memory limit has been set there).
 template <int MODE>
-int max_clusters(int num_sms) {
-  static int cached = -1;
-  if (cached < 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<MODE>();
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_loss_kernel<MODE>, &cfg) != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      n = num_sms / 2;
-    }
-    cached = n;
+int max_clusters(const DevInfo& di) {
+  static std::atomic<int> cached[64];
+  if (di.device < 0 || di.device >= 64) return di.num_sms / 2;
+  int n = cached[di.device].load(std::memory_order_acquire);
+  if (n > 0) return n;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(di.num_sms & ~1), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes<MODE>();
+  if (cudaOccupancyMaxActiveClusters(&n, tc_loss_kernel<MODE>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return di.num_sms / 2;   // not cached: the query may succeed once the kernel is configured
   }
-  return cached;
+  cached[di.device].store(n, std::memory_order_release);
+  return n;
 }
 
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mO, const TcArgs& a,
                         cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<uint64_t> configured{0};
+  if (device_pending(configured)) {
     cudaError_t e = cudaFuncSetAttribute(tc_loss_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes<MODE>()));
     if (e != cudaSuccess) return e;
-    configured = true;
+    mark_device_done(configured);
   }
   if (a.n_items <= 0) return cudaSuccess;
   const DevInfo di = current_device_info();
-  const int mc = max_clusters<MODE>(di.num_sms);
+  const int mc = max_clusters<MODE>(di);
   const int clusters = a.n_items < mc ? a.n_items : mc;
   tc_loss_kernel<MODE><<<2 * clusters, kThreads, smem_bytes<MODE>(), st>>>(mA, mB, mO, a);
   note_launch(MODE == MODE_ARGMAX ? VCE_K_TC_ARGMAX : VCE_K_TC_FWD + MODE, st);
@@ -833,7 +835,7 @@ int tc_unit_width(const vce_problem& p) {
 
 int tc_dh_parts(const vce_problem& p, int vc_act) {
   const DevInfo di = current_device_info();
-  const int clusters = max_clusters<MODE_DH>(di.num_sms);
+  const int clusters = max_clusters<MODE_DH>(di);
   const int tiles = static_cast<int>(ceil_div(p.T, BMP) * ceil_div(p.H, BN));
   const int kb = static_cast<int>(ceil_div(vc_act, BK));
   // Fewest parts whose tile count fills the clusters' waves to >= 95%, each

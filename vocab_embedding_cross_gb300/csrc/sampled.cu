@@ -226,10 +226,12 @@ cudaError_t launch_sampled_candidates(const vce_problem& p, const int64_t* targe
   const size_t table = cand_table_bytes(p.V_real);
   const bool use_smem = table <= kCandSmemBudget;
   const size_t smem = use_smem ? table : 0;
-  if (use_smem) {
+  static std::atomic<uint64_t> configured{0};
+  if (use_smem && device_pending(configured)) {
     cudaError_t e = cudaFuncSetAttribute(sampled_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kCandSmemBudget));
     if (e != cudaSuccess) return e;
+    mark_device_done(configured);
   }
   uint32_t* g_bits = static_cast<uint32_t*>(ws);
   int32_t* g_wpre = reinterpret_cast<int32_t*>(g_bits + (p.V_real + 31) / 32);
