@@ -51,6 +51,16 @@ def dist_env():
     return rank, world, local
 
 
+def arm_config(workload: str, world: int) -> dict:
+    """The `config` object of the JSON line; both arms print the same one."""
+    from vocab_embedding_cross_gb300 import inputs as I
+    wl = I.WORKLOADS[workload]
+    return {"workload": f"{workload}: T={wl.T} H={wl.H} V_real={wl.V_real} Vp={wl.Vp} S={wl.S} tied={wl.tied}",
+            "step": "embed_fwd + loss_fwd + loss_bwd + embed_bwd (+ tied dW zeroing)",
+            "l2": "inputs larger than L2 (W 622 MB, G chunks of 1.25 GB); no extra flush",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def max_over_ranks(ms: float, world: int, device="cuda") -> float:
     """The slowest replica's time per step: every rank gets the maximum over
     ranks (all-reduce MAX, then a barrier). One rank returns its own time."""
@@ -288,10 +298,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; Zipf(1.1) token ids, RMS-normalised h, W ~ N(0, 0.02^2))",
-            "config": {"workload": f"{args.workload}: T={T} H={H} V_real={V} Vp={Vp} S={wl.S} tied={wl.tied}",
-                       "step": "embed_fwd + loss_fwd + loss_bwd + embed_bwd (+ tied dW zeroing)",
-                       "l2": "inputs larger than L2 (W 622 MB, G chunk per pass 256 MB); no extra flush",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "config": arm_config(args.workload, world),
             "roofline": roofline,
             "loss_fwd_bwd": {"ms": round(loss_ms, 4), "credited_flops": credited,
                              "credited_TFLOPs": round(loss_tflops, 1) if loss_tflops else None,
@@ -561,14 +568,15 @@ def run_e2e(args, vce, D, d, p, W, E, loss, lse, dH, dW, st, ws_f, ws_b, ws_e, s
 # CPU oracle (bench's cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(args, sample_tokens):
-    """Runs the oracle in a child process with an explicit BLAS thread count."""
+def cpu_baseline(args, sample_tokens, steps=1, warmup=0):
+    """Runs the oracle in a child process with an explicit BLAS thread count:
+    `warmup` untimed steps, then `steps` timed ones, each on the same sample."""
     cores = len(os.sched_getaffinity(0))
     env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores),
                MKL_NUM_THREADS=str(cores))
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", args.workload,
-           "--cpu-sample", str(sample_tokens), "--steps", "1"]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+           "--cpu-sample", str(sample_tokens), "--steps", str(steps), "--warmup", str(warmup)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
     try:
         out = json.loads(r.stdout.strip().splitlines()[-1])
     except Exception:
@@ -588,20 +596,24 @@ def oracle_child(args):
     n = min(args.cpu_sample, wl.T)
     # a bounded sample of the workload: the first n tokens, full vocabulary and hidden size
     h, y, ids, dE = d["h"][:n], d["targets"][:n], d["ids"][:n], d["dE"][:n]
-    times = []
-    for _ in range(max(1, args.steps)):
-        t0 = time.perf_counter()
+    def one_step():
         O.embed_forward(ids, d["W"], wl.V_real)
         O.cross_entropy_forward(h, d["W"], y, wl.V_real)
         dH, dWh = O.cross_entropy_backward(h, d["W"], y, wl.V_real, wl.Vp)
         dWe = O.embed_backward(ids, dE, wl.V_real, wl.Vp)
-        _ = dWh + dWe
-        times.append(time.perf_counter() - t0)
-    t = statistics.median(times)
+        return dWh + dWe
+
+    for _ in range(max(0, args.warmup)):
+        one_step()
+    steps = max(1, args.steps)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    t = (time.perf_counter() - t0) / steps
     print(json.dumps({"value": round(n / t, 3), "unit": "tokens/s", "kind": "oracle",
                       "sample": f"first {n} of {wl.T} tokens of {args.workload}, full V={wl.V_real} and "
                                 f"H={wl.H}; embed fwd + loss fwd + loss bwd + embed bwd in fp64 numpy",
-                      "seconds": round(t, 3)}))
+                      "seconds": round(t, 3), "steps": steps}))
 
 
 def run_reference(args):
@@ -609,11 +621,14 @@ def run_reference(args):
     if rank != 0:
         return
     cores = len(os.sched_getaffinity(0))
-    res = cpu_baseline(argparse.Namespace(workload=args.workload), sample_tokens=args.cpu_sample)
+    res = cpu_baseline(argparse.Namespace(workload=args.workload), sample_tokens=args.cpu_sample,
+                       steps=args.steps, warmup=args.warmup)
+    secs = res.get("seconds")
     line = {"impl": "reference", "metric": METRIC, "value": res.get("value"), "unit": "tokens/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs * 1e3, 1) if secs else None, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
+            "config": arm_config(args.workload, world),
             "cpu_baseline": {"value": res.get("value"), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": res.get("sample")},
             "e2e": {"value": res.get("value"), "unit": "tokens/s", "h2d_bytes_per_step": 0,
