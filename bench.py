@@ -87,9 +87,12 @@ class Clocks:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the raw samples are kept for inspection: VCE_CLOCK_LOG_DIR, else the temp dir
+        log_dir = os.environ.get("VCE_CLOCK_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(log_dir, f"clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
