@@ -377,7 +377,7 @@ typedef enum vce_kernel_kind {
   VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13,
   VCE_K_DH_REDUCE = 14, VCE_K_SAMPLED_CAND = 15, VCE_K_SAMPLED_SCATTER = 16,
   VCE_K_TC_ARGMAX = 17, VCE_K_ARGMAX_MERGE = 18, VCE_K_SIMT_ARGMAX = 19,
-  VCE_K_NGRAM_HASH = 20, VCE_K_NGRAM_FWD = 21
+  VCE_K_NGRAM_HASH = 20, VCE_K_NGRAM_FWD = 21, VCE_K_EMBED_HDR = 22
 } vce_kernel_kind;
 uint64_t vce_launch_count(void);
 vce_status vce_profile_begin(int32_t capacity, void* stream);

@@ -23,6 +23,14 @@
 namespace vce {
 namespace {
 
+// Programmatic dependent launch (sm_90 and later). A kernel launched with the
+// programmatic-serialisation attribute may start once every CTA of the
+// previous kernel in the stream has called grid_dep_launch() or exited;
+// grid_dep_wait() then blocks until that kernel has completed and its writes
+// are visible. Both are no-ops in a kernel launched the ordinary way.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Forward gather: one warp per token row.
 // ---------------------------------------------------------------------------
@@ -219,6 +227,7 @@ __device__ __forceinline__ void build_runs(SegAt seg, int nseg, int n, int per_t
     hdr[3] = t_multi;
     hdr[4] = t_slots;
     hdr[5] = 0;
+    hdr[6] = 0;   // the reduce's item counter
   }
 }
 
@@ -437,7 +446,35 @@ __global__ void __launch_bounds__(kSortThreads, 1)
     hdr[3] = n_multi;
     hdr[4] = n_runs - (nseg - n_multi);
     hdr[5] = 0;
+    hdr[6] = 0;   // the reduce's item counter
   }
+}
+
+// Zeroes the workspace header that the bucketed sort's CTAs claim space from.
+// It lets its dependent (the sort) start at once: the sort loads and filters
+// its ids, then waits for this kernel before its first claim.
+__global__ void embed_hdr_zero_kernel(int32_t* hdr) {
+  grid_dep_launch();
+  if (threadIdx.x < 8) hdr[threadIdx.x] = 0;
+}
+
+// Launches `kern` with programmatic stream serialisation: it may start while
+// the previous kernel in the stream is still running, and must call
+// grid_dep_wait() before it touches anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 // Bucketed variant: the sort spread over gridDim.x CTAs (one per SM). CTA b
@@ -445,7 +482,7 @@ __global__ void __launch_bounds__(kSortThreads, 1)
 // id / NB (stable LSD radix, 6-bit digits, warp-level ranking by ballots) in
 // shared memory. It then cuts its ids into runs exactly as the single-CTA
 // variants do and claims space for its sorted tokens, runs and partial slots
-// with atomic additions on the header, which the host zeroes first. The
+// with atomic additions on the header, which a kernel zeroes first. The
 // order of the buckets in the arrays depends on which CTA claims first; every
 // id's runs and their order do not, so the reduce gives the same bits.
 constexpr int kBktThreads = 1024;
@@ -460,7 +497,8 @@ size_t bucket_sort_smem(int64_t T) {   // two key buffers, 16-bit ranks (whole w
 
 __global__ void __launch_bounds__(kBktThreads, 1)
     embed_sort_bucket_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int qbits, int nh,
-                             int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
+                             uint32_t nb_magic, int32_t* hdr, int32_t* tsorted, RunDesc* runs,
+                             int32_t* counters) {
   extern __shared__ __align__(16) uint32_t bsm[];
   uint32_t* ka = bsm;
   uint32_t* kb = bsm + T;
@@ -472,21 +510,31 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   const uint32_t lt_mask = (1u << lane) - 1u;
   const uint32_t NB = gridDim.x, b = blockIdx.x;
 
+  grid_dep_launch();   // the reduce may be scheduled from here on; it waits for this grid to end
+
   // Phase A: this bucket's ids in token order. Warp w scans tokens
-  // [w*tpw, (w+1)*tpw) 32 at a time; ballots give the order.
+  // [w*tpw, (w+1)*tpw) 32 at a time; ballots give the order. Every id a
+  // thread needs is loaded before any is used, so the loads are in flight
+  // together.
   const int tpw = ((T + kBktWarps - 1) / kBktWarps + 31) & ~31;
-  auto key_of = [&](int t) -> uint32_t {
-    const int64_t id = t < T ? ids[t] : -1;
-    if (id < 0 || id >= V_real) return 0xFFFFFFFFu;
-    const uint32_t u = static_cast<uint32_t>(id);
-    const uint32_t q = u / NB;
-    if (u - q * NB != b) return 0xFFFFFFFFu;
-    return (q << tbits) | static_cast<uint32_t>(t);
-  };
-  constexpr int kMaxRounds = kSmemSortMax / kBktWarps / 32;   // 32 rounds of 32 tokens per warp at most
+  constexpr int kMaxRounds = kSmemSortMax / kBktWarps / 32;   // 16 rounds of 32 tokens per warp at most
+  int64_t idv[kMaxRounds];
+#pragma unroll
+  for (int j = 0; j < kMaxRounds; ++j) {
+    const int t = warp * tpw + j * 32 + lane;
+    idv[j] = (j * 32 < tpw && t < T) ? __ldg(ids + t) : -1;
+  }
   uint32_t tkey[kMaxRounds];
 #pragma unroll
-  for (int j = 0; j < kMaxRounds; ++j) tkey[j] = j * 32 < tpw ? key_of(warp * tpw + j * 32 + lane) : 0xFFFFFFFFu;
+  for (int j = 0; j < kMaxRounds; ++j) {
+    uint32_t k = 0xFFFFFFFFu;
+    if (idv[j] >= 0 && idv[j] < V_real) {
+      const uint32_t u = static_cast<uint32_t>(idv[j]);
+      const uint32_t q = __umulhi(u, nb_magic);   // u / NB, exact for u < 2^32 / NB
+      if (u - q * NB == b) k = (q << tbits) | static_cast<uint32_t>(warp * tpw + j * 32 + lane);
+    }
+    tkey[j] = k;
+  }
   int wcount = 0;
 #pragma unroll
   for (int j = 0; j < kMaxRounds; ++j) wcount += __popc(__ballot_sync(0xffffffffu, tkey[j] != 0xFFFFFFFFu));
@@ -505,9 +553,12 @@ __global__ void __launch_bounds__(kBktThreads, 1)
     if (ok) ka[wbase + __popc(bal & lt_mask)] = tkey[j];
     wbase += __popc(bal);
   }
-  if (tid == 0) sh[80] = m > 0 ? atomicAdd(&hdr[0], m) : 0;   // this bucket's place in tsorted
-  __syncthreads();
-  const int tbase = sh[80];
+  // This bucket's place in tsorted. The header is zeroed by the kernel before
+  // this one; the claim's result is first needed after phase B, so its round
+  // trip overlaps the passes.
+  grid_dep_wait();
+  int tb = 0;
+  if (tid == 0 && m > 0) tb = atomicAdd(&hdr[0], m);
 
   // Phase B: stable LSD radix passes over the id / NB bits.
   const int kpw = ((m + kBktWarps - 1) / kBktWarps + 31) & ~31;
@@ -561,6 +612,10 @@ __global__ void __launch_bounds__(kBktThreads, 1)
     src = dst;
     dst = tmp;
   }
+
+  if (tid == 0) sh[80] = tb;
+  __syncthreads();
+  const int tbase = sh[80];
 
   // Phase C: sorted tokens, segment heads, runs.
   const uint32_t tmask = (1u << tbits) - 1u;
@@ -823,19 +878,29 @@ __device__ __forceinline__ void widen<float>(const uint4& v, float (&o)[4]) {
 
 template <typename TE>
 __global__ void __launch_bounds__(128)
-    embed_reduce_kernel(const int32_t* __restrict__ hdr, const int32_t* __restrict__ tsorted,
+    embed_reduce_kernel(int32_t* hdr, const int32_t* __restrict__ tsorted,
                         const RunDesc* __restrict__ runs, const TE* __restrict__ dE, float* __restrict__ dW,
                         float* partials, int32_t* counters, int H, int nh, int cap) {
   constexpr int VEC = 16 / sizeof(TE);
   constexpr int NQ = VEC / 4;
-  constexpr int U = 8;   // rows loaded ahead of the sequential adds
+  constexpr int U = 8;               // rows loaded ahead of the sequential adds
+  constexpr int kCombineAhead = 4;   // run sums loaded ahead in a combine
   __shared__ int s_last;
+  __shared__ int s_next[2];
   const int lane = threadIdx.x & 31;
+  grid_dep_wait();   // the sort's header, runs and tokens
   // Runs [0, n_front) sit at the front of the list, the other n_back at its
   // end (indices cap-1, cap-2, ...).
   const int n_front = hdr[1], n_back = hdr[5];
   const int n_items = (n_front + n_back) * nh;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+  // Items are handed out in list order: the first one per CTA by its index,
+  // the rest from a counter in the header (zeroed before this kernel), claimed one
+  // item ahead so that the claim's round trip overlaps the current item.
+  int32_t* item_ctr = hdr + 6;
+  int it = 0;
+  for (int item = blockIdx.x; item < n_items; ++it) {
+    int next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(item_ctr, 1) + static_cast<int>(gridDim.x);
     const int r = item / nh, hs = item - r * nh;
     const RunDesc rd = runs[r < n_front ? r : cap - 1 - (r - n_front)];
     const int len = rd.end - rd.start;   // <= 32
@@ -905,16 +970,29 @@ __global__ void __launch_bounds__(128)
           float4 a = __ldcg(s0 + q);
           tot[4 * q] = a.x; tot[4 * q + 1] = a.y; tot[4 * q + 2] = a.z; tot[4 * q + 3] = a.w;
         }
-        for (int j = 1; j < rd.nruns; ++j) {
-          const float4* sj =
-              reinterpret_cast<const float4*>(partials + static_cast<int64_t>(rd.first_slot + j) * H + col);
+        // Run sums are loaded kCombineAhead at a time, so a hot id's combine
+        // waits for about nruns / kCombineAhead round trips, not nruns.
+        for (int j0 = 1; j0 < rd.nruns; j0 += kCombineAhead) {
+          float4 a[kCombineAhead][NQ];
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) {
-            float4 a = __ldcg(sj + q);
-            tot[4 * q] = tot[4 * q] + a.x;
-            tot[4 * q + 1] = tot[4 * q + 1] + a.y;
-            tot[4 * q + 2] = tot[4 * q + 2] + a.z;
-            tot[4 * q + 3] = tot[4 * q + 3] + a.w;
+          for (int k = 0; k < kCombineAhead; ++k) {
+            const int j = min(j0 + k, rd.nruns - 1);   // past the end: a valid slot, not added
+            const float4* sj =
+                reinterpret_cast<const float4*>(partials + static_cast<int64_t>(rd.first_slot + j) * H + col);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) a[k][q] = __ldcg(sj + q);
+          }
+#pragma unroll
+          for (int k = 0; k < kCombineAhead; ++k) {
+            if (j0 + k < rd.nruns) {   // left to right
+#pragma unroll
+              for (int q = 0; q < NQ; ++q) {
+                tot[4 * q] = tot[4 * q] + a[k][q].x;
+                tot[4 * q + 1] = tot[4 * q + 1] + a[k][q].y;
+                tot[4 * q + 2] = tot[4 * q + 2] + a[k][q].z;
+                tot[4 * q + 3] = tot[4 * q + 3] + a[k][q].w;
+              }
+            }
           }
         }
 #pragma unroll
@@ -929,6 +1007,9 @@ __global__ void __launch_bounds__(128)
       }
       __syncthreads();
     }
+    if (threadIdx.x == 0) s_next[it & 1] = next;
+    __syncthreads();
+    item = s_next[it & 1];
   }
 }
 
@@ -968,7 +1049,10 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   const DevInfo di = current_device_info();
   const int nb = di.num_sms > 0 ? di.num_sms : 1;
   const int qbits = bit_width(ceil_div(p.V_real, nb));
-  if (p.T <= kSmemSortMax && tbits + qbits <= 32 && nb > 1) {
+  // The bucketed sort divides ids by NB with a multiply-high, exact for ids
+  // below 2^32 / NB.
+  const bool magic_ok = static_cast<uint64_t>(p.V_real) * static_cast<uint64_t>(nb) <= (uint64_t(1) << 32);
+  if (p.T <= kSmemSortMax && tbits + qbits <= 32 && nb > 1 && magic_ok) {
     static std::atomic<uint64_t> configured{0};
     if (device_pending(configured)) {
       cudaError_t e = cudaFuncSetAttribute(embed_sort_bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -976,9 +1060,14 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
       if (e != cudaSuccess) return e;
       mark_device_done(configured);
     }
-    if (cudaError_t e = cudaMemsetAsync(hdr, 0, 8 * sizeof(int32_t), st)) return e;
-    embed_sort_bucket_kernel<<<nb, kBktThreads, bucket_sort_smem(p.T), st>>>(
-        ids, static_cast<int>(p.T), p.V_real, tbits, qbits, L.nh, hdr, tsorted, runs, counters);
+    embed_hdr_zero_kernel<<<1, 32, 0, st>>>(hdr);
+    note_launch(VCE_K_EMBED_HDR, st);
+    if (cudaError_t e = cudaGetLastError()) return e;
+    const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb) + 1u;   // floor((2^32 - 1) / NB) + 1
+    if (cudaError_t e = launch_dependent(embed_sort_bucket_kernel, dim3(nb), dim3(kBktThreads), bucket_sort_smem(p.T),
+                                         st, ids, static_cast<int>(p.T), p.V_real, tbits, qbits, L.nh, nb_magic, hdr,
+                                         tsorted, runs, counters))
+      return e;
   } else if (p.T <= kSmemSortMax && tbits + idbits <= 32) {
     static std::atomic<uint64_t> configured{0};
     if (device_pending(configured)) {
@@ -998,15 +1087,15 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   if (e != cudaSuccess) return e;
   const int grid = di.num_sms * 8;
   if (p.dtype == VCE_BF16)
-    embed_reduce_kernel<uint16_t><<<grid, 128, 0, st>>>(hdr, tsorted, runs, static_cast<const uint16_t*>(dE), dW,
-                                                        partials, counters, static_cast<int>(p.H), L.nh,
-                                                        static_cast<int>(p.T));
+    e = launch_dependent(embed_reduce_kernel<uint16_t>, dim3(grid), dim3(128), 0, st, hdr, tsorted, runs,
+                         static_cast<const uint16_t*>(dE), dW, partials, counters, static_cast<int>(p.H), L.nh,
+                         static_cast<int>(p.T));
   else
-    embed_reduce_kernel<float><<<grid, 128, 0, st>>>(hdr, tsorted, runs, static_cast<const float*>(dE), dW,
-                                                     partials, counters, static_cast<int>(p.H), L.nh,
-                                                     static_cast<int>(p.T));
+    e = launch_dependent(embed_reduce_kernel<float>, dim3(grid), dim3(128), 0, st, hdr, tsorted, runs,
+                         static_cast<const float*>(dE), dW, partials, counters, static_cast<int>(p.H), L.nh,
+                         static_cast<int>(p.T));
   note_launch(VCE_K_EMBED_REDUCE, st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace vce
