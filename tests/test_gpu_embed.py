@@ -151,9 +151,12 @@ def test_embed_bwd_gptoss_full_deterministic():
         assert torch.equal(dW_d.view(torch.int32), first.view(torch.int32))
 
 
-@pytest.mark.parametrize("T,V_real,Vp", [(20000, 1000, 1024),      # more tokens than the shared-memory sort holds
-                                         (5000, 1048000, 1048064)])  # id and t need more than 32 bits together
+@pytest.mark.parametrize("T,V_real,Vp", [(20000, 1000, 1024),      # more tokens than the shared-memory sorts hold
+                                         (5000, 1048000, 1048064)])  # too many id / NB values for the counting sort
 def test_embed_bwd_workspace_sort_path(T, V_real, Vp):
+    """The sorts other than the bucketed counting sort: the 64-bit workspace
+    sort (T above 16384) and the bucketed radix sort (about 6900 values of
+    id / NB, more per-warp counters than the counting sort's shared memory)."""
     wl = I.custom(T=T, H=64, V_real=V_real, Vp=Vp, S=8, dtype="bf16", seed=16, pad_id_frac=0.05, oor_id_frac=0.05)
     d = I.make_all(wl, ("ids", "dE"))
     ids = d["ids"].copy()

@@ -9,11 +9,12 @@
 // zero rows.
 //
 // Backward (same page, paragraph 2: repeated tokens accumulate into the same
-// owned row): the valid (id, t) pairs are sorted (stable LSD radix sort on the
-// id, one CTA), the tokens of each id are cut into runs of kEmbedBwdChunk,
-// each run is summed in fp32 in ascending t, run sums are combined left to
-// right, and the total is added once into the fp32 row. The order is fixed,
-// so results are bit-identical from run to run.
+// owned row): the valid (id, t) pairs are sorted stably by id (for T <= 16384
+// one CTA per SM sorts the ids with id mod NB equal to its index; otherwise one
+// CTA sorts 64-bit keys), the tokens of each id are cut into runs of
+// kEmbedBwdChunk, each run is summed in fp32 in ascending t, run sums are
+// combined left to right, and the total is added once into the fp32 row. The
+// order is fixed, so results are bit-identical from run to run.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -166,6 +167,35 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sh_warp, int* total) 
   }
   __syncthreads();
   const int res = sh_warp[warp] + x - v;
+  *total = sh_warp[32];
+  __syncthreads();
+  return res;
+}
+
+// The same scan over 64-bit values (four 16-bit counters packed in one word).
+__device__ __forceinline__ uint64_t block_excl_scan64(uint64_t v, uint64_t* sh_warp, uint64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const uint64_t w = lane < static_cast<int>(blockDim.x >> 5) ? sh_warp[lane] : 0;
+    uint64_t s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    sh_warp[lane] = s - w;
+    if (lane == 31) sh_warp[32] = s;
+  }
+  __syncthreads();
+  const uint64_t res = sh_warp[warp] + x - v;
   *total = sh_warp[32];
   __syncthreads();
   return res;
@@ -876,6 +906,212 @@ __device__ __forceinline__ void widen<float>(const uint4& v, float (&o)[4]) {
   o[3] = __uint_as_float(v.w);
 }
 
+// Bucketed counting sort: the bucketed variant's CTAs, each sorting its ids by
+// q = id / NB with one counting pass instead of radix passes. With nq values
+// of q, kCntWarps warps each own a contiguous share of the bucket's keys (in
+// token order) and a row of nq counters:
+//   1. each warp counts its keys per q (warp-aggregated by __match_any_sync);
+//   2. per q, the rows become exclusive prefixes across the warps, and a block
+//      scan over q gives each q's first sorted position, the runs before it,
+//      the ids (non-empty q) before it and the multi-run ids before it;
+//   3. each warp places its keys' tokens straight into tsorted, in token order
+//      within each q, so the sort is stable;
+//   4. the bucket's runs are written in parallel, one thread per run, each
+//      finding its q by binary search over the runs-before counts.
+// The tokens, runs and run order produced are exactly those of the radix
+// variant.
+constexpr int kCntWarps = 8;
+constexpr size_t kCountSmemBudget = 200 * 1024;
+
+size_t count_sort_smem(int64_t T, int64_t nq) {   // keys, kCntWarps rows, three per-q arrays
+  return static_cast<size_t>(T) * sizeof(uint32_t) + static_cast<size_t>(kCntWarps + 3) * nq * sizeof(int);
+}
+
+__global__ void __launch_bounds__(kBktThreads, 1)
+    embed_sort_count_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int nq, int nh,
+                            uint32_t nb_magic, int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
+  extern __shared__ __align__(16) uint32_t csm[];
+  uint32_t* ka = csm;                                  // [T] this bucket's keys, token order
+  int* rows = reinterpret_cast<int*>(csm + T);         // [kCntWarps][nq]
+  int* bstart = rows + kCntWarps * nq;                 // [nq] first sorted position of q (its count, in step 2)
+  int* brun = bstart + nq;                             // [nq] runs before q
+  int* bseg = brun + nq;                               // [nq] ids before q | multi-run ids before q << 16
+  __shared__ int sh[96];
+  __shared__ uint64_t sh64[33];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const uint32_t NB = gridDim.x, b = blockIdx.x;
+
+  grid_dep_launch();   // the reduce may be scheduled from here on; it waits for this grid to end
+
+  // Phase A, as in the radix variant: every id loaded before any is used.
+  const int tpw = ((T + kBktWarps - 1) / kBktWarps + 31) & ~31;
+  constexpr int kMaxRounds = kSmemSortMax / kBktWarps / 32;
+  int64_t idv[kMaxRounds];
+#pragma unroll
+  for (int j = 0; j < kMaxRounds; ++j) {
+    const int t = warp * tpw + j * 32 + lane;
+    idv[j] = (j * 32 < tpw && t < T) ? __ldg(ids + t) : -1;
+  }
+  for (int i = tid; i < kCntWarps * nq; i += kBktThreads) rows[i] = 0;   // while the loads are in flight
+  uint32_t tkey[kMaxRounds];
+#pragma unroll
+  for (int j = 0; j < kMaxRounds; ++j) {
+    uint32_t k = 0xFFFFFFFFu;
+    if (idv[j] >= 0 && idv[j] < V_real) {
+      const uint32_t u = static_cast<uint32_t>(idv[j]);
+      const uint32_t q = __umulhi(u, nb_magic);   // u / NB, exact for u < 2^32 / NB
+      if (u - q * NB == b) k = (q << tbits) | static_cast<uint32_t>(warp * tpw + j * 32 + lane);
+    }
+    tkey[j] = k;
+  }
+  int wcount = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxRounds; ++j) wcount += __popc(__ballot_sync(0xffffffffu, tkey[j] != 0xFFFFFFFFu));
+  if (lane == 0) sh[warp] = wcount;
+  __syncthreads();
+  int wbase = 0, m = 0;
+  for (int w = 0; w < kBktWarps; ++w) {
+    const int c = sh[w];
+    wbase += w < warp ? c : 0;
+    m += c;
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxRounds; ++j) {
+    const bool ok = tkey[j] != 0xFFFFFFFFu;
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    if (ok) ka[wbase + __popc(bal & lt_mask)] = tkey[j];
+    wbase += __popc(bal);
+  }
+  // This bucket's place in tsorted; the header is zeroed by the kernel before
+  // this one. The claim's result is first needed in step 3.
+  grid_dep_wait();
+  int tb = 0;
+  if (tid == 0 && m > 0) tb = atomicAdd(&hdr[0], m);
+  __syncthreads();
+
+  // Step 1: per-warp counts of each q.
+  const int cpw = ((m + kCntWarps - 1) / kCntWarps + 31) & ~31;   // keys per counting warp, whole rounds
+  if (warp < kCntWarps) {
+    int* row = rows + warp * nq;
+    for (int j = 0; j < cpw; j += 32) {
+      const int i = warp * cpw + j + lane;
+      const bool ok = i < m;
+      const uint32_t q = ok ? ka[i] >> tbits : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, q);
+      if (ok && lane == __ffs(peers) - 1) row[q] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  // Step 2: thread tid owns the q in [q0, q1). Rows become exclusive prefixes
+  // across the warps; the four per-q counts are scanned packed 16 bits each
+  // (every total is at most T <= 16384).
+  const int bpt = (nq + kBktThreads - 1) / kBktThreads;
+  const int q0 = min(tid * bpt, nq), q1 = min(q0 + bpt, nq);
+  uint64_t mine = 0;
+  for (int q = q0; q < q1; ++q) {
+    int run = 0;
+    for (int w = 0; w < kCntWarps; ++w) {
+      const int c = rows[w * nq + q];
+      rows[w * nq + q] = run;
+      run += c;
+    }
+    bstart[q] = run;
+    const int nr = (run + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+    mine += static_cast<uint64_t>(run) | (static_cast<uint64_t>(nr) << 16) |
+            (static_cast<uint64_t>(run > 0) << 32) | (static_cast<uint64_t>(nr > 1) << 48);
+  }
+  uint64_t tot;
+  uint64_t pre = block_excl_scan64(mine, sh64, &tot);
+  for (int q = q0; q < q1; ++q) {
+    const int cnt = bstart[q];
+    const int p_cnt = static_cast<int>(pre & 0xFFFF), p_run = static_cast<int>((pre >> 16) & 0xFFFF);
+    const int p_seg = static_cast<int>((pre >> 32) & 0xFFFF), p_multi = static_cast<int>(pre >> 48);
+    bstart[q] = p_cnt;
+    brun[q] = p_run;
+    bseg[q] = p_seg | (p_multi << 16);
+    for (int w = 0; w < kCntWarps; ++w) rows[w * nq + q] += p_cnt;
+    const int nr = (cnt + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+    pre += static_cast<uint64_t>(cnt) | (static_cast<uint64_t>(nr) << 16) | (static_cast<uint64_t>(cnt > 0) << 32) |
+           (static_cast<uint64_t>(nr > 1) << 48);
+  }
+  const int n_runs = static_cast<int>((tot >> 16) & 0xFFFF);
+  const int nseg = static_cast<int>((tot >> 32) & 0xFFFF), n_multi = static_cast<int>(tot >> 48);
+  const int n_single = nseg - n_multi, n_slots = n_runs - n_single;
+  // Runs of multi-run ids go to the front of the run list (a run's partial
+  // slot has the same index), single runs to its back, as in the radix variant.
+  int c_slot = 0, c_multi = 0, c_single = 0;
+  if (tid == 0) {
+    sh[80] = tb;
+    c_slot = n_slots > 0 ? atomicAdd(&hdr[1], n_slots) : 0;
+    c_multi = n_multi > 0 ? atomicAdd(&hdr[3], n_multi) : 0;
+    c_single = n_single > 0 ? atomicAdd(&hdr[5], n_single) : 0;
+    if (nseg > 0) atomicAdd(&hdr[2], nseg);
+  }
+  __syncthreads();
+  const int tbase = sh[80];
+  const uint32_t tmask = (1u << tbits) - 1u;
+
+  // Step 3: tokens into place.
+  if (warp < kCntWarps) {
+    int* row = rows + warp * nq;
+    for (int j = 0; j < cpw; j += 32) {
+      const int i = warp * cpw + j + lane;
+      const bool ok = i < m;
+      const uint32_t key = ok ? ka[i] : 0u;
+      const uint32_t q = ok ? key >> tbits : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, q);
+      int base = 0;
+      if (ok) base = row[q];
+      __syncwarp();
+      if (ok) {
+        tsorted[tbase + base + __popc(peers & lt_mask)] = static_cast<int32_t>(key & tmask);
+        if (lane == __ffs(peers) - 1) row[q] = base + __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  if (tid == 0) {
+    sh[81] = c_slot;
+    sh[82] = c_multi;
+    sh[83] = c_single;
+  }
+  __syncthreads();
+  const int sbase = sh[81], mbase = sh[82], bbase = sh[83];
+
+  // Step 4: the runs, one thread each.
+  for (int r = tid; r < n_runs; r += kBktThreads) {
+    int lo = 0, hi = nq - 1;   // the largest q with brun[q] <= r is the run's (non-empty) q
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (brun[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    const int q = lo;
+    const int st = bstart[q];
+    const int cnt = (q + 1 < nq ? bstart[q + 1] : m) - st;
+    const int nr = (cnt + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
+    const int k = r - brun[q];
+    const int p_seg = bseg[q] & 0xFFFF, p_multi = bseg[q] >> 16;
+    const bool multi = nr > 1;
+    const int first = brun[q] - (p_seg - p_multi);   // slots of the multi-run ids before q
+    RunDesc rd;
+    rd.start = tbase + st + k * kEmbedBwdChunk;
+    rd.end = tbase + st + min(cnt, (k + 1) * kEmbedBwdChunk);
+    rd.id = static_cast<int32_t>(static_cast<uint32_t>(q) * NB + b);
+    rd.slot = multi ? sbase + first + k : -1;
+    rd.mseg = multi ? mbase + p_multi : -1;
+    rd.nruns = nr;
+    rd.first_slot = multi ? sbase + first : -1;
+    rd.pad = 0;
+    runs[multi ? sbase + first + k : T - 1 - (bbase + (p_seg - p_multi))] = rd;
+    if (multi && k == 0)
+      for (int hh = 0; hh < nh; ++hh) counters[(mbase + p_multi) * nh + hh] = 0;
+  }
+}
+
 template <typename TE>
 __global__ void __launch_bounds__(128)
     embed_reduce_kernel(int32_t* hdr, const int32_t* __restrict__ tsorted,
@@ -1052,7 +1288,26 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   // The bucketed sort divides ids by NB with a multiply-high, exact for ids
   // below 2^32 / NB.
   const bool magic_ok = static_cast<uint64_t>(p.V_real) * static_cast<uint64_t>(nb) <= (uint64_t(1) << 32);
-  if (p.T <= kSmemSortMax && tbits + qbits <= 32 && nb > 1 && magic_ok) {
+  // Keys (q << tbits) | t stay below the all-ones word that marks "not mine".
+  const bool bucketed = p.T <= kSmemSortMax && tbits + qbits <= 31 && nb > 1 && magic_ok;
+  const int64_t nq = ceil_div(p.V_real, nb);
+  if (bucketed && count_sort_smem(p.T, nq) <= kCountSmemBudget) {
+    static std::atomic<uint64_t> configured{0};
+    if (device_pending(configured)) {
+      cudaError_t e = cudaFuncSetAttribute(embed_sort_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kCountSmemBudget));
+      if (e != cudaSuccess) return e;
+      mark_device_done(configured);
+    }
+    embed_hdr_zero_kernel<<<1, 32, 0, st>>>(hdr);
+    note_launch(VCE_K_EMBED_HDR, st);
+    if (cudaError_t e = cudaGetLastError()) return e;
+    const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb) + 1u;   // floor((2^32 - 1) / NB) + 1
+    if (cudaError_t e = launch_dependent(embed_sort_count_kernel, dim3(nb), dim3(kBktThreads),
+                                         count_sort_smem(p.T, nq), st, ids, static_cast<int>(p.T), p.V_real, tbits,
+                                         static_cast<int>(nq), L.nh, nb_magic, hdr, tsorted, runs, counters))
+      return e;
+  } else if (bucketed) {
     static std::atomic<uint64_t> configured{0};
     if (device_pending(configured)) {
       cudaError_t e = cudaFuncSetAttribute(embed_sort_bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
