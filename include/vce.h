@@ -64,7 +64,8 @@ typedef enum vce_op {
  * One problem. Shapes:
  *   h[T,H], W[Vp,H], E[T,H], dE[T,H]   row-major, element type `dtype`;
  *   ids[T], targets[T]                 int64;
- *   dW[Vp,H], dH[T,H]                  fp32, row-major;
+ *   dW[Vp,H], dH[T,H]                  fp32, row-major (dH bf16 with
+ *                                      VCE_FLAG_DH_BF16);
  *   lse[T], token_loss[T]              fp32;  owner maps int32.
  * Rows of every 2-D tensor are contiguous with stride H elements; H*size(dtype)
  * must be a multiple of 16 bytes and every 2-D tensor 16-byte aligned.
@@ -97,7 +98,12 @@ typedef enum vce_flag {
    * Over-Tokenized Transformer", Setup: a second head on h[:-1] predicting
    * tokens[2:] at weight 0.1) accumulate its gradient into the first one's dH:
    * pass dH itself with T-1 rows and g = 0.1. */
-  VCE_FLAG_ACCUMULATE_DH = 1
+  VCE_FLAG_ACCUMULATE_DH = 1,
+  /* vce_loss_bwd, vce_sampled_loss: dH is bf16 [T,H] instead of fp32. The sum
+   * over the vocabulary is kept in fp32 in the workspace and rounded to bf16
+   * (nearest, ties to even) once; with VCE_FLAG_ACCUMULATE_DH the bf16 value
+   * already in dH is added in fp32 before that rounding. */
+  VCE_FLAG_DH_BF16 = 2
 } vce_flag;
 
 /* Bytes of workspace the call `op` needs for problem `p` (0 if none, SIZE_MAX
@@ -169,7 +175,8 @@ vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W,
  * times the loss scale; SPN p.3: averaged once over the valid tokens].
  *   G[t,v] = (exp(z[t,v] - lse[t]) - [v == y_t]) * g / N_valid
  * for valid t and real v, 0 elsewhere; z is recomputed tile by tile.
- *   dH  = G W        (fp32, overwritten; added into with VCE_FLAG_ACCUMULATE_DH)
+ *   dH  = G W        (fp32, or bf16 with VCE_FLAG_DH_BF16; overwritten, or
+ *                     added into with VCE_FLAG_ACCUMULATE_DH)
  *   dW  = G^T h      rows [V_real,Vp) are 0:
  *         tied_weights == 0: dW is overwritten;
  *         tied_weights == 1: dW is accumulated into (+=), so that the embedding
@@ -178,11 +185,12 @@ vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W,
  * gradient of the scalar loss (1 for a plain mean).
  * bf16: G is formed in bf16 for the two tensor-core GEMMs; fp32: all fp32.
  * Workspace: at least vce_workspace_size_min(p, VCE_OP_LOSS_BWD) bytes; the
- * vocabulary is processed in column chunks that fit the workspace.
+ * vocabulary is processed in column chunks that fit the workspace. With
+ * VCE_FLAG_DH_BF16 both sizes include T*H*4 bytes for the fp32 sum of dH.
  */
 vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W,
                         const int64_t* targets, const float* lse, float g,
-                        float* dH, float* dW, void* ws, size_t ws_bytes,
+                        void* dH, float* dW, void* ws, size_t ws_bytes,
                         int32_t* dev_status, void* stream);
 
 /*
@@ -221,7 +229,8 @@ vce_status vce_sampled_candidates(const vce_problem* p, const int64_t* targets, 
  *      (vce_loss_fwd with Vp = P rounded up to 64, V_real = P, S = 1,
  *      targets = pos) -> *loss (mean over valid tokens), lse[T]
  *   4. its backward (vce_loss_bwd, untied) -> dH[T,H] overwritten (added
- *      into when p->flags has VCE_FLAG_ACCUMULATE_DH), and the
+ *      into when p->flags has VCE_FLAG_ACCUMULATE_DH; bf16 with
+ *      VCE_FLAG_DH_BF16), and the
  *      candidate rows' gradient dWc[P,H] in the workspace
  *   5. dW[cand[i], :] += dWc[i, :], one fp32 addition per element (the
  *      candidates are distinct); rows of dW that are not candidates, and
@@ -237,7 +246,7 @@ vce_status vce_sampled_candidates(const vce_problem* p, const int64_t* targets, 
 size_t vce_sampled_workspace_size(const vce_problem* p, int64_t P);
 vce_status vce_sampled_loss(const vce_problem* p, const void* h, const void* W, const int64_t* targets,
                             const int64_t* draws, int64_t n_draws, int64_t P, float g, float* loss,
-                            float* lse, float* dH, float* dW, int64_t* cand, int64_t* pos,
+                            float* lse, void* dH, float* dW, int64_t* cand, int64_t* pos,
                             int32_t* n_unique, void* ws, size_t ws_bytes, int32_t* dev_status,
                             void* stream);
 
@@ -377,7 +386,7 @@ typedef enum vce_kernel_kind {
   VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13,
   VCE_K_DH_REDUCE = 14, VCE_K_SAMPLED_CAND = 15, VCE_K_SAMPLED_SCATTER = 16,
   VCE_K_TC_ARGMAX = 17, VCE_K_ARGMAX_MERGE = 18, VCE_K_SIMT_ARGMAX = 19,
-  VCE_K_NGRAM_HASH = 20, VCE_K_NGRAM_FWD = 21, VCE_K_EMBED_HDR = 22
+  VCE_K_NGRAM_HASH = 20, VCE_K_NGRAM_FWD = 21, VCE_K_EMBED_HDR = 22, VCE_K_DH_BF16 = 23
 } vce_kernel_kind;
 uint64_t vce_launch_count(void);
 vce_status vce_profile_begin(int32_t capacity, void* stream);

@@ -59,6 +59,8 @@ def P(**kw):
     (dict(H=4), vce.VCE_ERR_UNSUPPORTED),         # 8 bytes per bf16 row
     (dict(dtype=7), vce.VCE_ERR_UNSUPPORTED),
     (dict(T=1 << 31), vce.VCE_ERR_UNSUPPORTED),
+    (dict(flags=4), vce.VCE_ERR_ARG),            # no such flag
+    (dict(flags=1 << 20), vce.VCE_ERR_ARG),
 ])
 def test_bad_problem_rejected_on_host(L, kw, code):
     p = P(**kw)
@@ -100,6 +102,29 @@ def test_workspace_sizes(L):
     # the embedding backward workspace holds keys, runs and run partial slots
     p4 = P(T=16384, H=3072, Vp=201088, V_real=201088, S=8)
     assert vce.vce_workspace_size(p4, vce.VCE_OP_EMBED_BWD) < 64 << 20
+
+
+def test_bf16_dh_workspace(L):
+    """A bf16 dH adds its fp32 sum (T*H*4 bytes) to both backward sizes, and a
+    workspace without room for it is refused before anything is launched."""
+    import ctypes
+    for T, H in ((8192, 2048), (100, 72)):
+        p = P(T=T, H=H, Vp=151936, V_real=151936, S=8)
+        q = P(T=T, H=H, Vp=151936, V_real=151936, S=8, flags=vce.VCE_FLAG_DH_BF16)
+        acc = -(-(T * H * 4) // 256) * 256
+        for fn in (vce.vce_workspace_size, vce.vce_workspace_size_min):
+            assert fn(q, vce.VCE_OP_LOSS_BWD) == fn(p, vce.VCE_OP_LOSS_BWD) + acc
+        both = P(T=T, H=H, Vp=151936, V_real=151936, S=8,
+                 flags=vce.VCE_FLAG_DH_BF16 | vce.VCE_FLAG_ACCUMULATE_DH)
+        assert vce.vce_workspace_size(both, vce.VCE_OP_LOSS_BWD) == vce.vce_workspace_size(q, vce.VCE_OP_LOSS_BWD)
+        mn = vce.vce_workspace_size_min(q, vce.VCE_OP_LOSS_BWD)
+        args = (0x1000, 0x2000, 0x3000, 0x4000, 1.0, 0x5000, 0x6000, 0x10000)
+        assert L.vce_loss_bwd(ctypes.byref(q), *args, mn - 256, None, None) == vce.VCE_ERR_WORKSPACE
+        assert L.vce_loss_bwd(ctypes.byref(q), *args, acc - 256, None, None) == vce.VCE_ERR_WORKSPACE
+    # the sampled loss's workspace holds the sum too
+    q = P(T=4096, H=1024, Vp=50048, V_real=50000, S=8, flags=vce.VCE_FLAG_DH_BF16)
+    p = P(T=4096, H=1024, Vp=50048, V_real=50000, S=8)
+    assert vce.vce_sampled_workspace_size(q, 8192) >= vce.vce_sampled_workspace_size(p, 8192) + 4096 * 1024 * 4
 
 
 def test_workspace_too_small_rejected_on_host(L):

@@ -19,6 +19,7 @@ VCE_OK, VCE_ERR_ARG, VCE_ERR_UNSUPPORTED, VCE_ERR_CUDA = 0, 1, 2, 3
 VCE_ERR_BAD_INDEX, VCE_ERR_TIMEOUT, VCE_ERR_WORKSPACE = 4, 5, 6
 VCE_F32, VCE_BF16 = 0, 1
 VCE_FLAG_ACCUMULATE_DH = 1
+VCE_FLAG_DH_BF16 = 2
 VCE_OP_EMBED_FWD, VCE_OP_EMBED_BWD, VCE_OP_LOSS_FWD, VCE_OP_LOSS_BWD = 0, 1, 2, 3
 VCE_OP_SAMPLED_CANDIDATES = 4
 VCE_OP_GREEDY_ARGMAX = 5
@@ -252,7 +253,7 @@ def vce_wait_selftest(limit_ns: int, dev_status, stream=None) -> None:
 KERNEL_KINDS = ["embed_gather", "embed_sort", "embed_reduce", "tc_fwd", "tc_grad", "tc_dh", "tc_dw",
                 "merge", "loss_mean", "count_valid", "simt_fwd", "simt_grad", "sgemm", "wait_selftest",
                 "dh_reduce", "sampled_cand", "sampled_scatter", "tc_argmax", "argmax_merge", "simt_argmax",
-                "ngram_hash", "ngram_fwd", "embed_hdr"]
+                "ngram_hash", "ngram_fwd", "embed_hdr", "dh_bf16"]
 
 
 def vce_launch_count() -> int:

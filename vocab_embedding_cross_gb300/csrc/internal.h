@@ -94,6 +94,9 @@ cudaError_t launch_merge(const ProbDev& pd, const UnitGrid& ug, const int64_t* t
 int merge_blocks(int64_t T);
 cudaError_t launch_count_valid(const ProbDev& pd, const int64_t* targets, int32_t* n_valid, int32_t* status,
                                cudaStream_t st);
+// dH[T,H] in bf16 from its fp32 sum (n = T*H, a multiple of 4): rounded once,
+// after adding the bf16 values already there when accumulating.
+cudaError_t launch_dh_to_bf16(const float* acc, void* out, int64_t n, bool accumulate, cudaStream_t st);
 // Greedy argmax: merge of the units' (max, column) partials (column stored as the float's bits).
 cudaError_t launch_argmax_merge(const ProbDev& pd, const UnitGrid& ug, const float2* part, int64_t* argmax,
                                 float* max_logit, int32_t* owner, cudaStream_t st);

@@ -11,6 +11,7 @@
 // (paragraph 4: fused implementations may use other reduction schedules).
 // The loss is then averaged once over the valid tokens ("Sequence-parallel
 // normalization", paragraph 3) with a fixed-order, deterministic reduction.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -199,9 +200,41 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   }
 }
 
+// dH in bf16: out[i] = bf16(acc[i]) or, accumulating, bf16(float(out[i]) + acc[i]),
+// rounded to nearest even once. Four elements per step (8-byte stores).
+__global__ void __launch_bounds__(256) dh_to_bf16_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
+                                                         int64_t n4, int accumulate) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = __ldcs(acc + i);
+    if (accumulate) {
+      const uint2 o = out[i];
+      a.x = a.x + __uint_as_float(o.x << 16);
+      a.y = a.y + __uint_as_float(o.x & 0xFFFF0000u);
+      a.z = a.z + __uint_as_float(o.y << 16);
+      a.w = a.w + __uint_as_float(o.y & 0xFFFF0000u);
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    out[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  }
+}
+
 }  // namespace
 
 int merge_blocks(int64_t T) { return static_cast<int>(ceil_div(T, kMergeWarps)); }
+
+cudaError_t launch_dh_to_bf16(const float* acc, void* out, int64_t n, bool accumulate, cudaStream_t st) {
+  const int64_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  const DevInfo di = current_device_info();
+  int64_t blocks = ceil_div(n4, 256 * 4);
+  const int64_t cap = static_cast<int64_t>(di.num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  dh_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const float4*>(acc),
+                                                                   static_cast<uint2*>(out), n4, accumulate ? 1 : 0);
+  note_launch(VCE_K_DH_BF16, st);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_argmax_merge(const ProbDev& pd, const UnitGrid& ug, const float2* part, int64_t* argmax,
                                 float* max_logit, int32_t* owner, cudaStream_t st) {

@@ -99,7 +99,7 @@ int esize_of(const vce_problem& p) { return p.dtype == VCE_BF16 ? 2 : 4; }
 
 vce_status check_problem(const vce_problem* p) {
   if (!p) return VCE_ERR_ARG;
-  if ((p->flags & ~VCE_FLAG_ACCUMULATE_DH) != 0) return VCE_ERR_ARG;
+  if ((p->flags & ~(VCE_FLAG_ACCUMULATE_DH | VCE_FLAG_DH_BF16)) != 0) return VCE_ERR_ARG;
   if (p->dtype != VCE_F32 && p->dtype != VCE_BF16) return VCE_ERR_UNSUPPORTED;
   if (p->T < 0 || p->H < 1 || p->V_real < 1 || p->S < 1) return VCE_ERR_ARG;
   if (p->Vp < 64 || p->Vp % 64 != 0) return VCE_ERR_ARG;   // the padded vocabulary must be 64-aligned
@@ -185,6 +185,13 @@ size_t dh_part_bytes(const vce_problem& p) {
                   kWsAlign);
 }
 
+// fp32 sum of dH when dH itself is bf16 (VCE_FLAG_DH_BF16), at the front of
+// the backward's workspace.
+size_t dh_acc_bytes(const vce_problem& p) {
+  if ((p.flags & VCE_FLAG_DH_BF16) == 0 || p.T == 0) return 0;
+  return align_up(static_cast<size_t>(p.T) * static_cast<size_t>(p.H) * sizeof(float), kWsAlign);
+}
+
 // ----- sampled softmax: the sub-problems and the workspace layout -----
 // Candidate table: P rows, padded to a multiple of 64 for the loss kernels.
 int64_t cand_rows(int64_t P) { return ceil_div(P, 64) * 64; }
@@ -221,8 +228,8 @@ SampledLayout sampled_layout(const vce_problem& p, int64_t P) {
   L.scratch = L.loss + kWsAlign;
   size_t common = sampled_ws_bytes(p);
   common = common > fwd_layout(pl).total ? common : fwd_layout(pl).total;
-  const size_t bwd_min = bwd_bytes_for(pl, pl.T == 0 ? 0 : 256);
-  const size_t bwd_rec = bwd_bytes_for(pl, bwd_recommended_cols(pl)) + dh_part_bytes(pl);
+  const size_t bwd_min = dh_acc_bytes(pl) + bwd_bytes_for(pl, pl.T == 0 ? 0 : 256);
+  const size_t bwd_rec = dh_acc_bytes(pl) + bwd_bytes_for(pl, bwd_recommended_cols(pl)) + dh_part_bytes(pl);
   L.scratch_min = common > bwd_min ? common : bwd_min;
   const size_t rec = common > bwd_rec ? common : bwd_rec;
   L.total = L.scratch + rec;
@@ -300,7 +307,8 @@ size_t vce_workspace_size(const vce_problem* p, int32_t op) {
     case VCE_OP_EMBED_FWD: return 0;
     case VCE_OP_EMBED_BWD: return embed_bwd_ws_bytes(*p);
     case VCE_OP_LOSS_FWD: return fwd_layout(*p).total;
-    case VCE_OP_LOSS_BWD: return bwd_bytes_for(*p, bwd_recommended_cols(*p)) + dh_part_bytes(*p);
+    case VCE_OP_LOSS_BWD:
+      return dh_acc_bytes(*p) + bwd_bytes_for(*p, bwd_recommended_cols(*p)) + dh_part_bytes(*p);
     case VCE_OP_SAMPLED_CANDIDATES: return sampled_ws_bytes(*p);
     case VCE_OP_GREEDY_ARGMAX: return argmax_ws_bytes(*p);
   }
@@ -309,7 +317,7 @@ size_t vce_workspace_size(const vce_problem* p, int32_t op) {
 
 size_t vce_workspace_size_min(const vce_problem* p, int32_t op) {
   if (check_problem(p) != VCE_OK) return SIZE_MAX;
-  if (op == VCE_OP_LOSS_BWD) return bwd_bytes_for(*p, p->T == 0 ? 0 : 256);
+  if (op == VCE_OP_LOSS_BWD) return dh_acc_bytes(*p) + bwd_bytes_for(*p, p->T == 0 ? 0 : 256);
   return vce_workspace_size(p, op);
 }
 
@@ -372,7 +380,7 @@ vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W, cons
 }
 
 vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, const int64_t* targets,
-                        const float* lse, float g, float* dH, float* dW, void* ws, size_t ws_bytes,
+                        const float* lse, float g, void* dH_out, float* dW, void* ws, size_t ws_bytes,
                         int32_t* dev_status, void* stream) {
   vce_status s = check_problem(p);
   if (s != VCE_OK) return s;
@@ -383,11 +391,18 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
     if (!p->tied_weights) return cuda_status(cudaMemsetAsync(dW, 0, row_bytes * p->Vp, st));
     return VCE_OK;
   }
-  if (!h || !W || !targets || !lse || !dH) return VCE_ERR_ARG;
-  if (!aligned(h, 16) || !aligned(W, 16) || !aligned(targets, 8) || !aligned(lse, 4) || !aligned(dH, 16) ||
+  if (!h || !W || !targets || !lse || !dH_out) return VCE_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(W, 16) || !aligned(targets, 8) || !aligned(lse, 4) || !aligned(dH_out, 16) ||
       !aligned(dW, 16))
     return VCE_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, kWsAlign)) return VCE_ERR_WORKSPACE;
+  // A bf16 dH is summed in fp32 at the front of the workspace and rounded once
+  // at the end; the rest of the layout follows it.
+  const size_t acc_bytes = dh_acc_bytes(*p);
+  if (ws_bytes < acc_bytes) return VCE_ERR_WORKSPACE;
+  float* dH = acc_bytes ? static_cast<float*>(ws) : static_cast<float*>(dH_out);
+  ws = static_cast<char*>(ws) + acc_bytes;
+  ws_bytes -= acc_bytes;
   // Layout: header | dH K-part partials (when the workspace has room) | G chunk.
   const size_t part_bytes = dh_part_bytes(*p);
   const bool use_parts = part_bytes > 0 && ws_bytes >= bwd_bytes_for(*p, 256) + part_bytes;
@@ -409,7 +424,8 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
         cudaSuccess)
       return VCE_ERR_CUDA;
   }
-  const bool acc_dh = (p->flags & VCE_FLAG_ACCUMULATE_DH) != 0;
+  const bool acc_out = (p->flags & VCE_FLAG_ACCUMULATE_DH) != 0;
+  const bool acc_dh = acc_out && acc_bytes == 0;   // a bf16 dH is added in the rounding step
   for (int64_t c0 = 0; c0 < p->V_real; c0 += vc) {
     const int vc_act = static_cast<int>((p->V_real - c0) < vc ? (p->V_real - c0) : vc);
     cudaError_t e;
@@ -432,6 +448,8 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
     }
     if (e != cudaSuccess) return cuda_status(e);
   }
+  if (acc_bytes)
+    return cuda_status(launch_dh_to_bf16(dH, dH_out, p->T * p->H, acc_out, st));
   return VCE_OK;
 }
 
@@ -456,7 +474,7 @@ size_t vce_sampled_workspace_size(const vce_problem* p, int64_t P) {
 
 vce_status vce_sampled_loss(const vce_problem* p, const void* h, const void* W, const int64_t* targets,
                             const int64_t* draws, int64_t n_draws, int64_t P, float g, float* loss, float* lse,
-                            float* dH, float* dW, int64_t* cand, int64_t* pos, int32_t* n_unique, void* ws,
+                            void* dH, float* dW, int64_t* cand, int64_t* pos, int32_t* n_unique, void* ws,
                             size_t ws_bytes, int32_t* dev_status, void* stream) {
   vce_status s = check_problem(p);
   if (s != VCE_OK) return s;
