@@ -286,6 +286,10 @@ def run_ours(args):
     # ---- greedy argmax over the same head (decoding), device resident ----
     greedy = run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks)
 
+    # ---- the loss alone on the GPT-2-like head and on the GPT-OSS shapes ----
+    loss_configs = {name: run_loss_config(args, vce, D, I, stream, peaks, name)
+                    for name in ("gpt2_head", "gptoss_embed")}
+
     # ---- hashed n-gram input embeddings on the same ids ----
     ngram = run_ngram(args, vce, D, I, wl, d, p, W, dE, stream, peaks)
 
@@ -296,6 +300,10 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args, sample_tokens=args.cpu_sample)
+        # one-thread figures on the small configurations: the whole fp32 case, and
+        # a 64-token sample of the GPT-2-like head
+        cpu["one_thread"] = {w: cpu_baseline(args, sample_tokens=n, threads=1, workload=w)
+                             for w, n in (("tiny_f32", 64), ("gpt2_head", 64))}
 
     if rank == 0:
         line = {
@@ -315,6 +323,7 @@ def run_ours(args):
             "sampled_softmax": sampled,
             "embedding_gptoss": emb_gptoss,
             "greedy_argmax": greedy,
+            "loss_configs": loss_configs,
             "ngram_embedding": ngram,
             "per_kernel_ms": {k: round(v[0], 4) for k, v in sorted(per_kind.items())},
             "per_kernel_launches": {k: v[1] for k, v in sorted(per_kind.items())},
@@ -355,6 +364,52 @@ def run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks):
             "TFLOPs": round(tf, 1), "frac_of_burst": round(tf / peaks["bf16_tflops"], 4)}
 
 
+def run_loss_config(args, vce, D, I, stream, peaks, name):
+    """Loss forward + backward alone on another configuration's shapes (inputs
+    resident in HBM, larger than L2): tokens/s and 6*T*H*V_real credited FLOP
+    over the measured time, against the bf16 peaks."""
+    import torch
+    wl = I.WORKLOADS[name]
+    d = I.make_all(wl, ("W", "h", "targets"))
+    T, H, V = wl.T, wl.H, wl.V_real
+    p = vce.problem(T, H, wl.Vp, V, wl.S, vce.VCE_BF16)
+    W, h = D.to_device(d["W"]), D.to_device(d["h"])
+    y = torch.from_numpy(d["targets"]).cuda()
+    loss = torch.empty(1, device="cuda")
+    lse = torch.empty(T, device="cuda")
+    dH = torch.empty((T, H), device="cuda")
+    dW = torch.empty((wl.Vp, H), device="cuda")
+    ws_f = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD))
+    ws_b = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_LOSS_BWD))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = stream.cuda_stream
+
+    def step():
+        vce.vce_loss_fwd(p, h, W, y, loss, lse, ws=ws_f, dev_status=st, stream=sp)
+        vce.vce_loss_bwd(p, h, W, y, lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(5, args.steps // 4)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, vce.status_str(int(st.item()))
+    ms = e0.elapsed_time(e1) / n
+    tf = 6.0 * T * H * V / (ms / 1e3) / 1e12
+    del W, h, dH, dW, ws_f, ws_b
+    torch.cuda.empty_cache()
+    return {"workload": f"{name}: T={T} H={H} V_real={V} Vp={wl.Vp} S={wl.S} bf16 untied",
+            "tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_step": round(ms, 4), "steps": n,
+            "credited_TFLOPs": round(tf, 1), "frac_of_burst": round(tf / peaks["bf16_tflops"], 4),
+            "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
+
+
 def run_embedding(args, vce, D, I, stream, peaks, name):
     """Masked lookup and deterministic backward on a workload of their own (the
     GPT-OSS-shaped table [201088, 3072], T=16384 Zipf ids with 2% padding and
@@ -385,6 +440,7 @@ def run_embedding(args, vce, D, I, stream, peaks, name):
     U = int(np.unique(d["ids"][valid]).size)
     gather_bytes = 8 * T + U * H * 2 + T * H * 2
     bwd_bytes = 8 * T + T * H * 2 + U * H * 8
+    logical_bytes = 8 * T + int(valid.sum()) * H * 2 + T * H * 2
 
     def timed(fn, n, clean_l2=True):
         tot = 0.0
@@ -421,7 +477,11 @@ def run_embedding(args, vce, D, I, stream, peaks, name):
             "bwd_frac": frac(bwd_bytes, b_ms),
             "gather_us_dirty_l2": round(g_dirty * 1e3, 2), "gather_frac_dirty_l2": frac(gather_bytes, g_dirty),
             "bwd_us_dirty_l2": round(b_dirty * 1e3, 2), "bwd_frac_dirty_l2": frac(bwd_bytes, b_dirty),
-            "gather_bytes": gather_bytes, "bwd_bytes": bwd_bytes}
+            "gather_bytes": gather_bytes, "bwd_bytes": bwd_bytes,
+            # every valid row counted as read (repeats hit L2), and the nominal 8 TB/s HBM3e
+            "gather_logical_bytes": logical_bytes,
+            "gather_frac_of_8TBps": round(gather_bytes / (g_ms / 1e3) / 8e12, 4),
+            "bwd_frac_of_8TBps": round(bwd_bytes / (b_ms / 1e3) / 8e12, 4)}
 
 
 def run_ngram(args, vce, D, I, wl, d, p, W, dE, stream, peaks):
@@ -613,13 +673,14 @@ def run_e2e(args, vce, D, d, p, p_head, W, E, loss, lse, dH, dW, st, ws_f, ws_b,
 # CPU oracle (bench's cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(args, sample_tokens, steps=1, warmup=0):
-    """Runs the oracle in a child process with an explicit BLAS thread count:
-    `warmup` untimed steps, then `steps` timed ones, each on the same sample."""
-    cores = len(os.sched_getaffinity(0))
+def cpu_baseline(args, sample_tokens, steps=1, warmup=0, threads=None, workload=None):
+    """Runs the oracle in a child process with an explicit BLAS thread count
+    (every core the process may use, unless `threads` is given): `warmup`
+    untimed steps, then `steps` timed ones, each on the same sample."""
+    cores = threads or len(os.sched_getaffinity(0))
     env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores),
                MKL_NUM_THREADS=str(cores))
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", args.workload,
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", "--workload", workload or args.workload,
            "--cpu-sample", str(sample_tokens), "--steps", str(steps), "--warmup", str(warmup)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
     try:
