@@ -95,9 +95,28 @@ struct TcArgs {
   int ksplit;    // DH: the K range (vocabulary columns) is cut into ksplit parts
   int kb_per;    // DH: K blocks per part
   int t_pad;     // DH with ksplit > 1: rows per partial buffer
+  int gm;        // FWD, ARGMAX, GRAD: token blocks per item group (see item_mc)
+  int n_cols;    // FWD, ARGMAX: units; GRAD: column blocks
   int32_t* status;
   uint64_t limit_ns;
 };
+
+// Items of the forward-like modes and of GRAD are (token block m, column
+// unit or block c) pairs, taken in groups of gm token blocks: group g covers
+// m in [g*gm, g*gm + gsz) and every c, c-major within the group. The clusters
+// working at the same time then share one or two column blocks and at most gm
+// blocks of h, a working set chosen to stay in L2 (with gm = n_mblk this is
+// plain c-major order).
+struct MC {
+  int m, c;
+};
+__host__ __device__ __forceinline__ MC item_mc(int item, int gm, int n_mblk, int n_cols) {
+  const int per_group = gm * n_cols;
+  const int g = item / per_group, r = item - g * per_group;
+  const int m0 = g * gm;
+  const int gsz = n_mblk - m0 < gm ? n_mblk - m0 : gm;
+  return MC{m0 + r % gsz, r / gsz};
+}
 
 // Columns [vb, vlim) of forward work unit u, and its number of 256-wide tiles.
 struct UnitSpan {
@@ -119,7 +138,7 @@ __device__ __forceinline__ UnitSpan unit_span(const TcArgs& a, int u) {
 template <int MODE>
 __device__ __forceinline__ int item_tiles(const TcArgs& a, int item) {
   if constexpr (kFwdLike<MODE>) {
-    return unit_span(a, item / a.n_mblk).ntiles;
+    return unit_span(a, item_mc(item, a.gm, a.n_mblk, a.n_cols).c).ntiles;
   } else {
     return 1;
   }
@@ -135,31 +154,33 @@ template <int MODE>
 __device__ __forceinline__ TileCoord tile_coord(const TcArgs& a, int item, int tt, int rank) {
   TileCoord c;
   if constexpr (kFwdLike<MODE>) {
-    const int m_blk = item % a.n_mblk;
-    const UnitSpan us = unit_span(a, item / a.n_mblk);
-    c.am = m_blk * BMP + rank * BM;
+    const MC mc = item_mc(item, a.gm, a.n_mblk, a.n_cols);
+    const UnitSpan us = unit_span(a, mc.c);
+    c.am = mc.m * BMP + rank * BM;
     c.bn = static_cast<int32_t>(us.vb + static_cast<int64_t>(tt) * BN) + rank * BNH;
   } else if constexpr (MODE == MODE_GRAD) {
-    const int m_blk = item % a.n_mblk, n_blk = item / a.n_mblk;
-    c.am = m_blk * BMP + rank * BM;
-    c.bn = a.v0 + n_blk * BN + rank * BNH;
+    const MC mc = item_mc(item, a.gm, a.n_mblk, a.n_cols);
+    c.am = mc.m * BMP + rank * BM;
+    c.bn = a.v0 + mc.c * BN + rank * BNH;
   } else {
-    const int n_blk = item % a.n_nblk, m_blk = (item / a.n_nblk) / a.ksplit;
+    const int n_blk = item % a.n_nblk, m_blk = (item / a.n_nblk) % a.n_mblk;
     c.am = m_blk * BMP + rank * BM;
     c.bn = n_blk * BN + rank * BNH;
   }
   return c;
 }
 
-// K blocks [kb0, kb1) of an item: all of K, except for DH cut into parts
-// (item = (m_blk * ksplit + part) * n_nblk + n_blk).
+// K blocks [kb0, kb1) of an item: all of K, except for DH cut into parts.
+// DH and DW items are (part * n_mblk + m_blk) * n_nblk + n_blk: the parts run
+// one after the other, so the clusters working at the same time read one K
+// range of W.
 struct KRange {
   int kb0, kb1;
 };
 template <int MODE>
 __device__ __forceinline__ KRange item_krange(const TcArgs& a, int item) {
   if constexpr (MODE == MODE_DH) {
-    const int part = (item / a.n_nblk) % a.ksplit;
+    const int part = (item / a.n_nblk) / a.n_mblk;
     const int kb0 = part * a.kb_per;
     const int kb1 = kb0 + a.kb_per < a.num_kb ? kb0 + a.kb_per : a.num_kb;
     return KRange{kb0, kb1};
@@ -427,7 +448,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
     for (int item = first_item; ok && item < a.n_items; item += item_step) {
       if constexpr (MODE == MODE_ARGMAX) {
-        const int m_blk = item % a.n_mblk, u = item / a.n_mblk;
+        const MC mc = item_mc(item, a.gm, a.n_mblk, a.n_cols);
+        const int m_blk = mc.m, u = mc.c;
         const UnitSpan us = unit_span(a, u);
         const int t = m_blk * BMP + static_cast<int>(rank) * BM + r;
         float m_run = -INFINITY;
@@ -507,7 +529,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ++items_done;
       } else if constexpr (MODE == MODE_FWD) {
-        const int m_blk = item % a.n_mblk, u = item / a.n_mblk;
+        const MC mc = item_mc(item, a.gm, a.n_mblk, a.n_cols);
+        const int m_blk = mc.m, u = mc.c;
         const UnitSpan us = unit_span(a, u);
         const int t = m_blk * BMP + static_cast<int>(rank) * BM + r;
         const bool row_ok = t < a.pd.T;
@@ -613,14 +636,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       } else {
         int m_blk, n_blk, row0, col0;
         if constexpr (MODE == MODE_GRAD) {
-          m_blk = item % a.n_mblk;
-          n_blk = item / a.n_mblk;
+          const MC mc = item_mc(item, a.gm, a.n_mblk, a.n_cols);
+          m_blk = mc.m;
+          n_blk = mc.c;
           row0 = m_blk * BMP + static_cast<int>(rank) * BM;
           col0 = n_blk * BN + half * 128;   // chunk-local column of this warp's half
         } else {
           n_blk = item % a.n_nblk;
-          m_blk = (item / a.n_nblk) / a.ksplit;
-          const int part = (item / a.n_nblk) % a.ksplit;   // DH: partial buffer of this K part
+          m_blk = (item / a.n_nblk) % a.n_mblk;
+          const int part = (item / a.n_nblk) / a.n_mblk;   // DH: partial buffer of this K part
           row0 = (MODE == MODE_DW ? a.out_row0 : part * a.t_pad) + m_blk * BMP + static_cast<int>(rank) * BM;
           col0 = n_blk * BN + half * 128;
         }
@@ -770,7 +794,22 @@ TcArgs base_args(const vce_problem& p, const int64_t* targets, int32_t* status) 
   a.status = status;
   a.limit_ns = wait_limit_ns();
   a.ksplit = 1;
+  a.gm = 1;
+  a.n_cols = 1;
   return a;
+}
+
+// Token blocks per item group (see item_mc): the most whose rows of h fit in
+// kGroupBytes, spread evenly over the groups. The Qwen3-like step (32 blocks
+// of 1 MB) keeps a single group.
+constexpr int64_t kGroupBytes = int64_t(40) << 20;
+int tc_group_mblk(const vce_problem& p) {
+  const int64_t n_mblk = ceil_div(p.T, BMP);
+  if (n_mblk <= 1) return 1;
+  int64_t gmax = kGroupBytes / (static_cast<int64_t>(BMP) * p.H * 2);
+  if (gmax < 1) gmax = 1;
+  const int64_t groups = ceil_div(n_mblk, gmax);
+  return static_cast<int>(ceil_div(n_mblk, groups));
 }
 
 // dH = (accumulate ? dH : 0) + P[0] + P[1] + ... in this order (deterministic).
@@ -801,26 +840,33 @@ int tc_unit_width(const vce_problem& p) {
   const int64_t n_mblk = ceil_div(p.T, BMP);
   if (n_mblk == 0) return kTcUnitWidth;
   struct Memo {
-    int64_t T, Vp, V_real, clusters;
+    int64_t T, Vp, V_real, H, clusters;
     int32_t S, uw;
   };
-  thread_local Memo memo{-1, -1, -1, -1, -1, 0};
-  if (memo.T == p.T && memo.Vp == p.Vp && memo.V_real == p.V_real && memo.S == p.S && memo.clusters == clusters)
+  thread_local Memo memo{-1, -1, -1, -1, -1, -1, 0};
+  if (memo.T == p.T && memo.Vp == p.Vp && memo.V_real == p.V_real && memo.H == p.H && memo.S == p.S &&
+      memo.clusters == clusters)
     return memo.uw;
+  const int gm = tc_group_mblk(p);
   int best_uw = kTcUnitWidth;
   int64_t best_load = -1;
-  std::vector<int64_t> load;
+  std::vector<int64_t> load, unit_tiles;
   for (int uw = kTcUnitWidth; uw >= 512; uw -= BN) {
     const UnitGrid ug = unit_grid(p, uw);
-    load.assign(static_cast<size_t>(clusters), 0);
+    unit_tiles.assign(static_cast<size_t>(ug.n_units), 0);
     for (int64_t u = 0; u < ug.n_units; ++u) {
       const int64_t k = u / ug.ups, j = u - k * ug.ups;
       const int64_t lo = shard_lo(k, p.Vp, p.S), hi = shard_lo(k + 1, p.Vp, p.S);
       const int64_t vb = lo + j * uw;
       int64_t ve = vb + uw < hi ? vb + uw : hi;
       if (ve > p.V_real) ve = p.V_real;
-      const int64_t tiles = ve > vb ? ceil_div(ve - vb, BN) : 0;
-      for (int64_t m = 0; m < n_mblk; ++m) load[static_cast<size_t>((u * n_mblk + m) % clusters)] += tiles;
+      unit_tiles[static_cast<size_t>(u)] = ve > vb ? ceil_div(ve - vb, BN) : 0;
+    }
+    load.assign(static_cast<size_t>(clusters), 0);
+    const int64_t n_items = n_mblk * ug.n_units;
+    for (int64_t item = 0; item < n_items; ++item) {   // cluster c takes items c, c + clusters, ...
+      const MC mc = item_mc(static_cast<int>(item), gm, static_cast<int>(n_mblk), static_cast<int>(ug.n_units));
+      load[static_cast<size_t>(item % clusters)] += unit_tiles[static_cast<size_t>(mc.c)];
     }
     int64_t mx = 0;
     for (int64_t v : load) mx = v > mx ? v : mx;
@@ -829,7 +875,7 @@ int tc_unit_width(const vce_problem& p) {
       best_load = mx;
     }
   }
-  memo = Memo{p.T, p.Vp, p.V_real, clusters, p.S, best_uw};
+  memo = Memo{p.T, p.Vp, p.V_real, p.H, clusters, p.S, best_uw};
   return best_uw;
 }
 
@@ -865,6 +911,8 @@ cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* 
   TcArgs a = base_args(p, targets, status);
   a.n_mblk = static_cast<int>(ceil_div(p.T, BMP));
   a.n_items = a.n_mblk * ug.n_units;
+  a.gm = tc_group_mblk(p);
+  a.n_cols = ug.n_units;
   a.num_kb = static_cast<int>(ceil_div(p.H, BK));
   a.ug = ug;
   a.part = part;
@@ -881,6 +929,8 @@ cudaError_t launch_tc_argmax(const vce_problem& p, const UnitGrid& ug, const voi
   TcArgs a = base_args(p, nullptr, status);
   a.n_mblk = static_cast<int>(ceil_div(p.T, BMP));
   a.n_items = a.n_mblk * ug.n_units;
+  a.gm = tc_group_mblk(p);
+  a.n_cols = ug.n_units;
   a.num_kb = static_cast<int>(ceil_div(p.H, BK));
   a.ug = ug;
   a.part = part;
@@ -905,6 +955,8 @@ cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void*
     a.n_mblk = static_cast<int>(ceil_div(p.T, BMP));
     a.n_nblk = static_cast<int>(ceil_div(vc_act, BN));
     a.n_items = a.n_mblk * a.n_nblk;
+    a.gm = tc_group_mblk(p);
+    a.n_cols = a.n_nblk;
     a.num_kb = static_cast<int>(ceil_div(p.H, BK));
     a.lse = lse;
     a.n_valid = n_valid;

@@ -1,13 +1,14 @@
 """Small, self-contained invocations of the library for a profiler.
 
-    python -m vocab_embedding_cross_gb300.profile_case loss    [--tokens T] [--iters N]
+    python -m vocab_embedding_cross_gb300.profile_case loss    [--workload NAME] [--tokens T] [--iters N]
     python -m vocab_embedding_cross_gb300.profile_case embed   [--workload NAME] [--iters N]
     python -m vocab_embedding_cross_gb300.profile_case sampled [--tokens T] [--iters N]
 
-`loss` runs the loss forward and backward (tied dW) on the Qwen3-like shapes
-(H=2048, V=151936, S=8) with T tokens; `embed` runs the embedding lookup and
-its backward on a named workload; `sampled` runs vce_sampled_loss (P=8192) with
-T tokens. Inputs are the seeded synthetic ones of `inputs.py`. Each case checks
+`loss` runs the loss forward and backward on a named workload's shapes
+(default the Qwen3-like H=2048, V=151936, S=8, tied dW), with T tokens or the
+workload's own; `embed` runs the embedding lookup and its backward on a named
+workload; `sampled` runs vce_sampled_loss (P=8192) with T tokens (default
+2048). Inputs are the seeded synthetic ones of `inputs.py`. Each case checks
 the device status word and exits non-zero on any error, so that a profiler is
 only pointed at a command that has already run cleanly.
 """
@@ -24,9 +25,11 @@ from . import inputs as I
 
 
 def _loss(args):
-    wl = I.with_T(I.WORKLOADS["qwen3_tied"], args.tokens)
+    wl = I.WORKLOADS[args.workload]
+    if args.tokens:
+        wl = I.with_T(wl, args.tokens)
     d = I.make_all(wl, ("W", "h", "targets"))
-    p = vce.problem(wl.T, wl.H, wl.Vp, wl.V_real, wl.S, vce.VCE_BF16, tied=True)
+    p = vce.problem(wl.T, wl.H, wl.Vp, wl.V_real, wl.S, vce.VCE_BF16, tied=wl.tied)
     W, h = D.to_device(d["W"]), D.to_device(d["h"])
     y = torch.from_numpy(d["targets"]).cuda()
     loss = torch.empty(1, device="cuda")
@@ -63,7 +66,7 @@ def _embed(args):
 
 
 def _sampled(args):
-    wl = I.with_T(I.WORKLOADS["sampled"], args.tokens)
+    wl = I.with_T(I.WORKLOADS["sampled"], args.tokens or 2048)
     P = I.SAMPLED_P
     d = I.make_all(wl, ("W", "h", "targets"))
     p = vce.problem(wl.T, wl.H, wl.Vp, wl.V_real, wl.S, vce.VCE_BF16)
@@ -87,7 +90,7 @@ def _sampled(args):
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("case", choices=["loss", "embed", "sampled"])
-    ap.add_argument("--tokens", type=int, default=2048)
+    ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--workload", default="qwen3_tied")
     ap.add_argument("--iters", type=int, default=2)
     args = ap.parse_args(argv)
