@@ -4,7 +4,8 @@
   is 0, an untied dW is zeroed, a tied or accumulated dW is left alone;
 - hidden sizes that are not multiples of the 64-wide K block of the
   tensor-core tiles (H = 72, 200), a wide one (H = 8192, 16 KB rows), and an
-  fp32 width that is not a multiple of 64 (H = 100).
+  fp32 width that is not a multiple of 64 (H = 100);
+- token-block item groups of unequal size with a ragged last block.
 """
 import numpy as np
 import pytest
@@ -61,6 +62,39 @@ def test_empty_batch_every_entry(tied):
     torch.cuda.synchronize()
     assert torch.equal(dW2, init) and not d2.any().item()
     assert int(st.item()) == 0
+
+
+def test_uneven_token_block_groups():
+    """H = 8192 puts 4 MB of h in each 256-token block, so the tensor-core items
+    come in groups of at most 10 token blocks. T = 5500 gives 22 blocks, the
+    last one ragged, in groups of 8, 8 and 6; the backward runs in several
+    column chunks (minimal workspace)."""
+    wl = I.custom("groups", T=5500, H=8192, V_real=3000, Vp=3008, S=3, dtype="bf16", seed=85,
+                  ignore_frac=0.05, pad_fill=8.0)
+    d = I.make_all(wl, ("W", "h", "targets"))
+    h_d, W_d = D.to_device(d["h"]), D.to_device(d["W"])
+    out = R.loss_fwd(wl, h_d, W_d, d["targets"], maps=False)
+    ref = O.cross_entropy_forward(d["h"], d["W"], d["targets"], wl.V_real)
+    assert out["status"] == 0
+    assert R.rel(out["loss"], ref["loss"]) <= 1e-3
+    assert np.all(np.abs(out["lse"] - ref["lse"]) <= 1e-3 * np.maximum(np.abs(ref["lse"]), 1.0))
+    ws_min = R.vce.vce_workspace_size_min(R.prob(wl), R.vce.VCE_OP_LOSS_BWD)
+    dH, dW, st = R.loss_bwd(wl, h_d, W_d, out["targets_d"], out["lse_d"], ws_bytes=ws_min)
+    assert st == 0
+    rdH, rdW = O.cross_entropy_backward(d["h"], d["W"], d["targets"], wl.V_real, wl.Vp)
+    assert R.max_abs_rel(dH.cpu().numpy(), rdH) <= 2e-2
+    assert R.max_abs_rel(dW.cpu().numpy(), rdW) <= 2e-2
+    # greedy argmax walks the same item groups
+    p = R.prob(wl)
+    arg = torch.empty(wl.T, dtype=torch.int64, device="cuda")
+    ws = D.workspace(R.vce.vce_workspace_size(p, R.vce.VCE_OP_GREEDY_ARGMAX))
+    R.vce.vce_greedy_argmax(p, h_d, W_d, arg, ws=ws)
+    torch.cuda.synchronize()
+    z = O.logits(d["h"], d["W"], wl.V_real)
+    got = arg.cpu().numpy()
+    zmax = z.max(axis=1)
+    assert np.all((got >= 0) & (got < wl.V_real))
+    assert np.all(z[np.arange(wl.T), got] >= zmax - 1e-3 * np.maximum(np.abs(zmax), 1.0))
 
 
 @pytest.mark.parametrize("dtype,H", [("bf16", 72), ("bf16", 200), ("bf16", 8192), ("f32", 100)])
