@@ -76,7 +76,9 @@ typedef enum vce_op {
  * Shards [TP, VS p.1]: S logical shards on one GPU; shard k owns the contiguous
  * rows [floor(k*Vp/S), floor((k+1)*Vp/S)). Any 1 <= S <= Vp is allowed.
  *
- * Limits: 0 <= T < 2^31, 1 <= H <= 65536, 64 <= Vp < 2^31, 1 <= V_real <= Vp.
+ * Limits: 0 <= T < 2^31, 1 <= H <= 65536, 64 <= Vp < 2^31, 1 <= V_real <= Vp,
+ * and (T/256 + 1) * (Vp/256 + S) < 2^31 (the tensor-core kernels number their
+ * work items in 32 bits); larger problems return VCE_ERR_UNSUPPORTED.
  * `flags` is 0 or a combination of the vce_flag bits below (other bits are
  * rejected with VCE_ERR_ARG).
  */

@@ -59,6 +59,7 @@ def P(**kw):
     (dict(H=4), vce.VCE_ERR_UNSUPPORTED),         # 8 bytes per bf16 row
     (dict(dtype=7), vce.VCE_ERR_UNSUPPORTED),
     (dict(T=1 << 31), vce.VCE_ERR_UNSUPPORTED),
+    (dict(T=(1 << 31) - 1, Vp=1 << 30, V_real=1 << 30), vce.VCE_ERR_UNSUPPORTED),   # 2^41 work items
     (dict(flags=4), vce.VCE_ERR_ARG),            # no such flag
     (dict(flags=1 << 20), vce.VCE_ERR_ARG),
 ])

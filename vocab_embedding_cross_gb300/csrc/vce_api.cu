@@ -107,6 +107,9 @@ vce_status check_problem(const vce_problem* p) {
   if (p->tied_weights != 0 && p->tied_weights != 1) return VCE_ERR_ARG;
   if (p->T >= (int64_t(1) << 31) || p->Vp >= (int64_t(1) << 31) || p->H > 65536) return VCE_ERR_UNSUPPORTED;
   if ((p->H * esize_of(*p)) % 16 != 0) return VCE_ERR_UNSUPPORTED;
+  // Work items of the tensor-core kernels ((token block, unit or column block)
+  // pairs) are numbered in 32 bits.
+  if ((p->T / 256 + 1) * (p->Vp / 256 + p->S) >= (int64_t(1) << 31)) return VCE_ERR_UNSUPPORTED;
   return VCE_OK;
 }
 
