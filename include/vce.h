@@ -78,7 +78,8 @@ typedef enum vce_op {
  *
  * Limits: 0 <= T < 2^31, 1 <= H <= 65536, 64 <= Vp < 2^31, 1 <= V_real <= Vp,
  * and (T/256 + 1) * (Vp/256 + S) < 2^31 (the tensor-core kernels number their
- * work items in 32 bits); larger problems return VCE_ERR_UNSUPPORTED.
+ * work items in 32 bits); larger problems return VCE_ERR_UNSUPPORTED. The
+ * embedding backward also needs T * ceil(H / (128 * 16 / sizeof(dtype))) < 2^31.
  * `flags` is 0 or a combination of the vce_flag bits below (other bits are
  * rejected with VCE_ERR_ARG).
  */

@@ -906,6 +906,30 @@ __device__ __forceinline__ void widen<float>(const uint4& v, float (&o)[4]) {
   o[3] = __uint_as_float(v.w);
 }
 
+// acc += dE rows t_p, t_{p+1}, ..., t_{p+N-1} (this thread's 16-byte column
+// chunk), the N loads issued before the first add, the adds in token order.
+// Token t_j is lane j's my_t. Straight-line code for each N, so a short run
+// issues only its own loads and adds.
+template <int N, typename TE>
+__device__ __forceinline__ void add_rows(const TE* __restrict__ dE, int64_t H, int col, int my_t, int p, bool active,
+                                         float (&acc)[16 / sizeof(TE)]) {
+  constexpr int VEC = 16 / sizeof(TE);
+  uint4 v[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int t = __shfl_sync(0xffffffffu, my_t, (p + k) & 31);
+    v[k] = make_uint4(0, 0, 0, 0);
+    if (active) v[k] = __ldg(reinterpret_cast<const uint4*>(dE + static_cast<int64_t>(t) * H + col));
+  }
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    float f[VEC];
+    widen<TE>(v[k], f);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = acc[e] + f[e];
+  }
+}
+
 // Bucketed counting sort: the bucketed variant's CTAs, each sorting its ids by
 // q = id / NB with one counting pass instead of radix passes. With nq values
 // of q, kCntWarps warps each own a contiguous share of the bucket's keys (in
@@ -1116,7 +1140,7 @@ template <typename TE>
 __global__ void __launch_bounds__(128)
     embed_reduce_kernel(int32_t* hdr, const int32_t* __restrict__ tsorted,
                         const RunDesc* __restrict__ runs, const TE* __restrict__ dE, float* __restrict__ dW,
-                        float* partials, int32_t* counters, int H, int nh, int cap) {
+                        float* partials, int32_t* counters, int H, int nh, uint32_t nh_magic, int cap) {
   constexpr int VEC = 16 / sizeof(TE);
   constexpr int NQ = VEC / 4;
   constexpr int U = 8;               // rows loaded ahead of the sequential adds
@@ -1137,7 +1161,9 @@ __global__ void __launch_bounds__(128)
   for (int item = blockIdx.x; item < n_items; ++it) {
     int next = 0;
     if (threadIdx.x == 0) next = atomicAdd(item_ctr, 1) + static_cast<int>(gridDim.x);
-    const int r = item / nh, hs = item - r * nh;
+    // item / nh by a multiply-high when the host found it exact for every item
+    const int r = nh_magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(item), nh_magic)) : item / nh;
+    const int hs = item - r * nh;
     const RunDesc rd = runs[r < n_front ? r : cap - 1 - (r - n_front)];
     const int len = rd.end - rd.start;   // <= 32
     const int col = hs * 128 * VEC + static_cast<int>(threadIdx.x) * VEC;
@@ -1153,22 +1179,16 @@ __global__ void __launch_bounds__(128)
     float acc[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
-    for (int p = 0; p < len; p += U) {
-      uint4 v[U];
-#pragma unroll
-      for (int k = 0; k < U; ++k) {
-        const int t = __shfl_sync(0xffffffffu, my_t, (p + k) & 31);
-        v[k] = make_uint4(0, 0, 0, 0);
-        if (active && p + k < len) v[k] = __ldg(reinterpret_cast<const uint4*>(dE + static_cast<int64_t>(t) * H + col));
-      }
-#pragma unroll
-      for (int k = 0; k < U; ++k) {
-        if (p + k < len) {          // tokens in ascending t, one add each
-          float f[VEC];
-          widen<TE>(v[k], f);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) acc[e] = acc[e] + f[e];
-        }
+    for (int p = 0; p < len; p += U) {   // tokens in ascending t, one add each
+      switch (len - p < U ? len - p : U) {
+        case 1: add_rows<1>(dE, H, col, my_t, p, active, acc); break;
+        case 2: add_rows<2>(dE, H, col, my_t, p, active, acc); break;
+        case 3: add_rows<3>(dE, H, col, my_t, p, active, acc); break;
+        case 4: add_rows<4>(dE, H, col, my_t, p, active, acc); break;
+        case 5: add_rows<5>(dE, H, col, my_t, p, active, acc); break;
+        case 6: add_rows<6>(dE, H, col, my_t, p, active, acc); break;
+        case 7: add_rows<7>(dE, H, col, my_t, p, active, acc); break;
+        default: add_rows<U>(dE, H, col, my_t, p, active, acc); break;
       }
     }
     if (rd.slot < 0) {
@@ -1266,6 +1286,10 @@ cudaError_t launch_embed_fwd(const vce_problem& p, const int64_t* ids, const voi
 
 size_t embed_bwd_ws_bytes(const vce_problem& p) { return bwd_layout(p).total; }
 
+bool embed_bwd_supported(const vce_problem& p) {   // the reduce numbers its items (<= T * nh) in 32 bits
+  return static_cast<int64_t>(p.T) * bwd_layout(p).nh < (int64_t(1) << 31);
+}
+
 cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const void* dE, float* dW, void* ws,
                              int32_t* status, cudaStream_t st) {
   (void)status;
@@ -1341,14 +1365,20 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int grid = di.num_sms * 8;
+  // Items number at most T * nh (a run per token at most); the multiply-high
+  // gives item / nh exactly for items below 2^32 / nh.
+  const uint64_t max_items = static_cast<uint64_t>(p.T) * static_cast<uint64_t>(L.nh);
+  const uint32_t nh_magic = (L.nh > 1 && max_items * static_cast<uint64_t>(L.nh) < (uint64_t(1) << 32))
+                                ? 0xFFFFFFFFu / static_cast<uint32_t>(L.nh) + 1u
+                                : 0u;
   if (p.dtype == VCE_BF16)
     e = launch_dependent(embed_reduce_kernel<uint16_t>, dim3(grid), dim3(128), 0, st, hdr, tsorted, runs,
                          static_cast<const uint16_t*>(dE), dW, partials, counters, static_cast<int>(p.H), L.nh,
-                         static_cast<int>(p.T));
+                         nh_magic, static_cast<int>(p.T));
   else
     e = launch_dependent(embed_reduce_kernel<float>, dim3(grid), dim3(128), 0, st, hdr, tsorted, runs,
                          static_cast<const float*>(dE), dW, partials, counters, static_cast<int>(p.H), L.nh,
-                         static_cast<int>(p.T));
+                         nh_magic, static_cast<int>(p.T));
   note_launch(VCE_K_EMBED_REDUCE, st);
   return e;
 }

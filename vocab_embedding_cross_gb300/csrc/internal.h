@@ -84,6 +84,8 @@ cudaError_t launch_embed_fwd(const vce_problem& p, const int64_t* ids, const voi
                              int32_t* local, cudaStream_t st);
 
 size_t embed_bwd_ws_bytes(const vce_problem& p);
+// False when the embedding backward's work items would not fit in 32 bits.
+bool embed_bwd_supported(const vce_problem& p);
 cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const void* dE, float* dW, void* ws,
                              int32_t* status, cudaStream_t st);
 

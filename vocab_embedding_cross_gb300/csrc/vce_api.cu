@@ -343,6 +343,7 @@ vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* d
   if (p->T == 0) return VCE_OK;
   if (!ids || !dE || !dW) return VCE_ERR_ARG;
   if (!aligned(ids, 8) || !aligned(dE, 16) || !aligned(dW, 16)) return VCE_ERR_UNSUPPORTED;
+  if (!embed_bwd_supported(*p)) return VCE_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, kWsAlign) || ws_bytes < embed_bwd_ws_bytes(*p)) return VCE_ERR_WORKSPACE;
   return cuda_status(launch_embed_bwd(*p, ids, dE, dW, ws, dev_status, static_cast<cudaStream_t>(stream)));
 }
@@ -604,6 +605,7 @@ vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const v
   if (!ids || !dE || !dW) return VCE_ERR_ARG;
   if (!aligned(ids, 8) || !aligned(dE, 16) || !aligned(dW, 16) || !aligned(dT2, 16) || !aligned(dT3, 16))
     return VCE_ERR_UNSUPPORTED;
+  if (!embed_bwd_supported(*p)) return VCE_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, kWsAlign) || ws_bytes < vce_ngram_workspace_size(p)) return VCE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* b = static_cast<char*>(ws);
