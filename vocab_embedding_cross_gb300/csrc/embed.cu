@@ -951,6 +951,9 @@ size_t count_sort_smem(int64_t T, int64_t nq) {   // keys, kCntWarps rows, three
   return static_cast<size_t>(T) * sizeof(uint32_t) + static_cast<size_t>(kCntWarps + 3) * nq * sizeof(int);
 }
 
+// ROUNDS: rounds of 32 tokens per warp in phase A (T <= 32 * 32 * ROUNDS), so
+// that a smaller batch does not issue the larger one's predicated rounds.
+template <int ROUNDS>
 __global__ void __launch_bounds__(kBktThreads, 1)
     embed_sort_count_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int nq, int nh,
                             uint32_t nb_magic, int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
@@ -970,7 +973,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
 
   // Phase A, as in the radix variant: every id loaded before any is used.
   const int tpw = ((T + kBktWarps - 1) / kBktWarps + 31) & ~31;
-  constexpr int kMaxRounds = kSmemSortMax / kBktWarps / 32;
+  constexpr int kMaxRounds = ROUNDS;
   int64_t idv[kMaxRounds];
 #pragma unroll
   for (int j = 0; j < kMaxRounds; ++j) {
@@ -1316,20 +1319,30 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   const bool bucketed = p.T <= kSmemSortMax && tbits + qbits <= 31 && nb > 1 && magic_ok;
   const int64_t nq = ceil_div(p.V_real, nb);
   if (bucketed && count_sort_smem(p.T, nq) <= kCountSmemBudget) {
+    // Phase A's rounds of 32 tokens per warp: 2, 4, 8 or 16.
+    const int rounds = p.T <= 2048 ? 2 : p.T <= 4096 ? 4 : p.T <= 8192 ? 8 : 16;
+    void (*kern)(const int64_t*, int, int64_t, int, int, int, uint32_t, int32_t*, int32_t*, RunDesc*, int32_t*) =
+        rounds == 2 ? embed_sort_count_kernel<2>
+        : rounds == 4 ? embed_sort_count_kernel<4>
+        : rounds == 8 ? embed_sort_count_kernel<8>
+                      : embed_sort_count_kernel<16>;
     static std::atomic<uint64_t> configured{0};
     if (device_pending(configured)) {
-      cudaError_t e = cudaFuncSetAttribute(embed_sort_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kCountSmemBudget));
-      if (e != cudaSuccess) return e;
+      for (auto k : {embed_sort_count_kernel<2>, embed_sort_count_kernel<4>, embed_sort_count_kernel<8>,
+                     embed_sort_count_kernel<16>}) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kCountSmemBudget));
+        if (e != cudaSuccess) return e;
+      }
       mark_device_done(configured);
     }
     embed_hdr_zero_kernel<<<1, 32, 0, st>>>(hdr);
     note_launch(VCE_K_EMBED_HDR, st);
     if (cudaError_t e = cudaGetLastError()) return e;
     const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb) + 1u;   // floor((2^32 - 1) / NB) + 1
-    if (cudaError_t e = launch_dependent(embed_sort_count_kernel, dim3(nb), dim3(kBktThreads),
-                                         count_sort_smem(p.T, nq), st, ids, static_cast<int>(p.T), p.V_real, tbits,
-                                         static_cast<int>(nq), L.nh, nb_magic, hdr, tsorted, runs, counters))
+    if (cudaError_t e = launch_dependent(kern, dim3(nb), dim3(kBktThreads), count_sort_smem(p.T, nq), st, ids,
+                                         static_cast<int>(p.T), p.V_real, tbits, static_cast<int>(nq), L.nh,
+                                         nb_magic, hdr, tsorted, runs, counters))
       return e;
   } else if (bucketed) {
     static std::atomic<uint64_t> configured{0};
