@@ -480,12 +480,15 @@ __global__ void __launch_bounds__(kSortThreads, 1)
   }
 }
 
-// Zeroes the workspace header that the bucketed sort's CTAs claim space from.
-// It lets its dependent (the sort) start at once: the sort loads and filters
-// its ids, then waits for this kernel before its first claim.
-__global__ void embed_hdr_zero_kernel(int32_t* hdr) {
+// Zeroes the workspace headers (up to three; null ones are skipped) that the
+// bucketed sorts' CTAs claim space from. It lets its dependent (the first sort)
+// start at once: a sort loads and filters its ids, then waits for the kernel
+// before it before its first claim.
+__global__ void embed_hdr_zero_kernel(int32_t* h0, int32_t* h1, int32_t* h2) {
   grid_dep_launch();
-  if (threadIdx.x < 8) hdr[threadIdx.x] = 0;
+  const int i = threadIdx.x & 7, k = threadIdx.x >> 3;
+  int32_t* h = k == 0 ? h0 : (k == 1 ? h1 : h2);
+  if (k < 3 && h) h[i] = 0;
 }
 
 // Launches `kern` with programmatic stream serialisation: it may start while
@@ -1139,11 +1142,27 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   }
 }
 
+// One sorted problem for the reduce: its workspace arrays and its dW. The
+// n-gram backward reduces three (the token table and two n-gram tables) in one
+// launch, their items numbered one problem after the other.
+struct EmbSlot {
+  int32_t* hdr;
+  const int32_t* tsorted;
+  const RunDesc* runs;
+  float* dW;
+  float* partials;
+  int32_t* counters;
+};
+constexpr int kMaxSlots = 3;
+struct EmbSlots {
+  EmbSlot s[kMaxSlots];
+  int n;
+};
+
 template <typename TE>
 __global__ void __launch_bounds__(128)
-    embed_reduce_kernel(int32_t* hdr, const int32_t* __restrict__ tsorted,
-                        const RunDesc* __restrict__ runs, const TE* __restrict__ dE, float* __restrict__ dW,
-                        float* partials, int32_t* counters, int H, int nh, uint32_t nh_magic, int cap) {
+    embed_reduce_kernel(const __grid_constant__ EmbSlots sl, const TE* __restrict__ dE, int H, int nh,
+                        uint32_t nh_magic, int cap) {
   constexpr int VEC = 16 / sizeof(TE);
   constexpr int NQ = VEC / 4;
   constexpr int U = 8;               // rows loaded ahead of the sequential adds
@@ -1151,22 +1170,37 @@ __global__ void __launch_bounds__(128)
   __shared__ int s_last;
   __shared__ int s_next[2];
   const int lane = threadIdx.x & 31;
-  grid_dep_wait();   // the sort's header, runs and tokens
-  // Runs [0, n_front) sit at the front of the list, the other n_back at its
-  // end (indices cap-1, cap-2, ...).
-  const int n_front = hdr[1], n_back = hdr[5];
-  const int n_items = (n_front + n_back) * nh;
-  // Items are handed out in list order: the first one per CTA by its index,
-  // the rest from a counter in the header (zeroed before this kernel), claimed one
-  // item ahead so that the claim's round trip overlaps the current item.
-  int32_t* item_ctr = hdr + 6;
+  grid_dep_wait();   // the sorts' headers, runs and tokens
+  // In each problem, runs [0, n_front) sit at the front of the list, the other
+  // n_back at its end (indices cap-1, cap-2, ...). Problem k's items are
+  // [base_k, base_k+1).
+  const int nf0 = sl.s[0].hdr[1];
+  const int nf1 = sl.n > 1 ? sl.s[1].hdr[1] : 0;
+  const int nf2 = sl.n > 2 ? sl.s[2].hdr[1] : 0;
+  const int base1 = (nf0 + sl.s[0].hdr[5]) * nh;
+  const int base2 = base1 + (sl.n > 1 ? (nf1 + sl.s[1].hdr[5]) * nh : 0);
+  const int n_items = base2 + (sl.n > 2 ? (nf2 + sl.s[2].hdr[5]) * nh : 0);
+  // Items are handed out in order: the first one per CTA by its index, the
+  // rest from a counter in the first problem's header (zeroed before this
+  // kernel), claimed one item ahead so that the claim's round trip overlaps
+  // the current item.
+  int32_t* item_ctr = sl.s[0].hdr + 6;
   int it = 0;
   for (int item = blockIdx.x; item < n_items; ++it) {
     int next = 0;
     if (threadIdx.x == 0) next = atomicAdd(item_ctr, 1) + static_cast<int>(gridDim.x);
-    // item / nh by a multiply-high when the host found it exact for every item
-    const int r = nh_magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(item), nh_magic)) : item / nh;
-    const int hs = item - r * nh;
+    // this item's problem (a uniform choice among at most three)
+    const int k = item >= base2 ? 2 : (item >= base1 ? 1 : 0);
+    const int li = item - (k == 2 ? base2 : (k == 1 ? base1 : 0));
+    const int n_front = k == 2 ? nf2 : (k == 1 ? nf1 : nf0);
+    const RunDesc* __restrict__ runs = k == 2 ? sl.s[2].runs : (k == 1 ? sl.s[1].runs : sl.s[0].runs);
+    const int32_t* __restrict__ tsorted = k == 2 ? sl.s[2].tsorted : (k == 1 ? sl.s[1].tsorted : sl.s[0].tsorted);
+    float* __restrict__ dW = k == 2 ? sl.s[2].dW : (k == 1 ? sl.s[1].dW : sl.s[0].dW);
+    float* partials = k == 2 ? sl.s[2].partials : (k == 1 ? sl.s[1].partials : sl.s[0].partials);
+    int32_t* counters = k == 2 ? sl.s[2].counters : (k == 1 ? sl.s[1].counters : sl.s[0].counters);
+    // li / nh by a multiply-high when the host found it exact for every item
+    const int r = nh_magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(li), nh_magic)) : li / nh;
+    const int hs = li - r * nh;
     const RunDesc rd = runs[r < n_front ? r : cap - 1 - (r - n_front)];
     const int len = rd.end - rd.start;   // <= 32
     const int col = hs * 128 * VEC + static_cast<int>(threadIdx.x) * VEC;
@@ -1293,10 +1327,40 @@ bool embed_bwd_supported(const vce_problem& p) {   // the reduce numbers its ite
   return static_cast<int64_t>(p.T) * bwd_layout(p).nh < (int64_t(1) << 31);
 }
 
-cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const void* dE, float* dW, void* ws,
-                             int32_t* status, cudaStream_t st) {
-  (void)status;
-  if (p.T == 0) return cudaSuccess;
+namespace {
+
+EmbSlot emb_slot(const vce_problem& p, void* ws, float* dW) {
+  const BwdLayout L = bwd_layout(p);
+  char* b = static_cast<char*>(ws);
+  EmbSlot sl;
+  sl.hdr = reinterpret_cast<int32_t*>(b + L.hdr);
+  sl.tsorted = reinterpret_cast<const int32_t*>(b + L.tsorted);
+  sl.runs = reinterpret_cast<const RunDesc*>(b + L.runs);
+  sl.dW = dW;
+  sl.partials = reinterpret_cast<float*>(b + L.partials);
+  sl.counters = reinterpret_cast<int32_t*>(b + L.counters);
+  return sl;
+}
+
+enum class SortPath { kCount, kBucket, kSmem, kGlobal };
+
+SortPath sort_path(const vce_problem& p, int nb) {
+  const int tbits = bit_width(p.T);
+  const int qbits = bit_width(ceil_div(p.V_real, nb));
+  // The bucketed sorts divide ids by NB with a multiply-high, exact for ids
+  // below 2^32 / NB; keys (q << tbits) | t stay below the all-ones word that
+  // marks "not mine".
+  const bool magic_ok = static_cast<uint64_t>(p.V_real) * static_cast<uint64_t>(nb) <= (uint64_t(1) << 32);
+  const bool bucketed = p.T <= kSmemSortMax && tbits + qbits <= 31 && nb > 1 && magic_ok;
+  if (bucketed) return count_sort_smem(p.T, ceil_div(p.V_real, nb)) <= kCountSmemBudget ? SortPath::kCount
+                                                                                       : SortPath::kBucket;
+  if (p.T <= kSmemSortMax && tbits + bit_width(p.V_real) <= 32) return SortPath::kSmem;
+  return SortPath::kGlobal;
+}
+
+// Sorts one problem's valid (id, t) pairs into its workspace and builds its
+// runs. A bucketed sort needs its header zeroed by the kernel before it.
+cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, SortPath path, int nb, cudaStream_t st) {
   const BwdLayout L = bwd_layout(p);
   char* b = static_cast<char*>(ws);
   int32_t* hdr = reinterpret_cast<int32_t*>(b + L.hdr);
@@ -1306,19 +1370,11 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
   int32_t* tsorted = reinterpret_cast<int32_t*>(b + L.tsorted);
   RunDesc* runs = reinterpret_cast<RunDesc*>(b + L.runs);
   int32_t* counters = reinterpret_cast<int32_t*>(b + L.counters);
-  float* partials = reinterpret_cast<float*>(b + L.partials);
   const int tbits = bit_width(p.T);
-  const int idbits = bit_width(p.V_real);
-  const DevInfo di = current_device_info();
-  const int nb = di.num_sms > 0 ? di.num_sms : 1;
   const int qbits = bit_width(ceil_div(p.V_real, nb));
-  // The bucketed sort divides ids by NB with a multiply-high, exact for ids
-  // below 2^32 / NB.
-  const bool magic_ok = static_cast<uint64_t>(p.V_real) * static_cast<uint64_t>(nb) <= (uint64_t(1) << 32);
-  // Keys (q << tbits) | t stay below the all-ones word that marks "not mine".
-  const bool bucketed = p.T <= kSmemSortMax && tbits + qbits <= 31 && nb > 1 && magic_ok;
   const int64_t nq = ceil_div(p.V_real, nb);
-  if (bucketed && count_sort_smem(p.T, nq) <= kCountSmemBudget) {
+  const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb > 1 ? nb : 2) + 1u;   // floor((2^32 - 1) / NB) + 1
+  if (path == SortPath::kCount) {
     // Phase A's rounds of 32 tokens per warp: 2, 4, 8 or 16.
     const int rounds = p.T <= 2048 ? 2 : p.T <= 4096 ? 4 : p.T <= 8192 ? 8 : 16;
     void (*kern)(const int64_t*, int, int64_t, int, int, int, uint32_t, int32_t*, int32_t*, RunDesc*, int32_t*) =
@@ -1336,15 +1392,11 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
       }
       mark_device_done(configured);
     }
-    embed_hdr_zero_kernel<<<1, 32, 0, st>>>(hdr);
-    note_launch(VCE_K_EMBED_HDR, st);
-    if (cudaError_t e = cudaGetLastError()) return e;
-    const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb) + 1u;   // floor((2^32 - 1) / NB) + 1
     if (cudaError_t e = launch_dependent(kern, dim3(nb), dim3(kBktThreads), count_sort_smem(p.T, nq), st, ids,
                                          static_cast<int>(p.T), p.V_real, tbits, static_cast<int>(nq), L.nh,
                                          nb_magic, hdr, tsorted, runs, counters))
       return e;
-  } else if (bucketed) {
+  } else if (path == SortPath::kBucket) {
     static std::atomic<uint64_t> configured{0};
     if (device_pending(configured)) {
       cudaError_t e = cudaFuncSetAttribute(embed_sort_bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1352,15 +1404,11 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
       if (e != cudaSuccess) return e;
       mark_device_done(configured);
     }
-    embed_hdr_zero_kernel<<<1, 32, 0, st>>>(hdr);
-    note_launch(VCE_K_EMBED_HDR, st);
-    if (cudaError_t e = cudaGetLastError()) return e;
-    const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb) + 1u;   // floor((2^32 - 1) / NB) + 1
     if (cudaError_t e = launch_dependent(embed_sort_bucket_kernel, dim3(nb), dim3(kBktThreads), bucket_sort_smem(p.T),
                                          st, ids, static_cast<int>(p.T), p.V_real, tbits, qbits, L.nh, nb_magic, hdr,
                                          tsorted, runs, counters))
       return e;
-  } else if (p.T <= kSmemSortMax && tbits + idbits <= 32) {
+  } else if (path == SortPath::kSmem) {
     static std::atomic<uint64_t> configured{0};
     if (device_pending(configured)) {
       cudaError_t e = cudaFuncSetAttribute(embed_sort_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1369,31 +1417,74 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
       mark_device_done(configured);
     }
     embed_sort_smem_kernel<<<1, kSortThreads, kSmemSortBytes, st>>>(ids, static_cast<int>(p.T), p.V_real, tbits,
-                                                                    idbits, L.nh, hdr, tsorted, runs, counters);
+                                                                    bit_width(p.V_real), L.nh, hdr, tsorted, runs,
+                                                                    counters);
   } else {
     embed_sort_kernel<<<1, kSortThreads, 0, st>>>(ids, p.T, p.V_real, L.nh, hdr, ka, kb, seg, tsorted, runs,
                                                   counters);
   }
   note_launch(VCE_K_EMBED_SORT, st);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// One reduce over the sorted problems in `sl` (all with p's T, H and dtype).
+cudaError_t launch_reduce(const vce_problem& p, const EmbSlots& sl, const void* dE, cudaStream_t st) {
+  const BwdLayout L = bwd_layout(p);
+  const DevInfo di = current_device_info();
   const int grid = di.num_sms * 8;
-  // Items number at most T * nh (a run per token at most); the multiply-high
-  // gives item / nh exactly for items below 2^32 / nh.
+  // Items of one problem number at most T * nh (a run per token at most); the
+  // multiply-high gives item / nh exactly for items below 2^32 / nh.
   const uint64_t max_items = static_cast<uint64_t>(p.T) * static_cast<uint64_t>(L.nh);
   const uint32_t nh_magic = (L.nh > 1 && max_items * static_cast<uint64_t>(L.nh) < (uint64_t(1) << 32))
                                 ? 0xFFFFFFFFu / static_cast<uint32_t>(L.nh) + 1u
                                 : 0u;
+  cudaError_t e;
   if (p.dtype == VCE_BF16)
-    e = launch_dependent(embed_reduce_kernel<uint16_t>, dim3(grid), dim3(128), 0, st, hdr, tsorted, runs,
-                         static_cast<const uint16_t*>(dE), dW, partials, counters, static_cast<int>(p.H), L.nh,
-                         nh_magic, static_cast<int>(p.T));
+    e = launch_dependent(embed_reduce_kernel<uint16_t>, dim3(grid), dim3(128), 0, st, sl,
+                         static_cast<const uint16_t*>(dE), static_cast<int>(p.H), L.nh, nh_magic,
+                         static_cast<int>(p.T));
   else
-    e = launch_dependent(embed_reduce_kernel<float>, dim3(grid), dim3(128), 0, st, hdr, tsorted, runs,
-                         static_cast<const float*>(dE), dW, partials, counters, static_cast<int>(p.H), L.nh,
-                         nh_magic, static_cast<int>(p.T));
+    e = launch_dependent(embed_reduce_kernel<float>, dim3(grid), dim3(128), 0, st, sl,
+                         static_cast<const float*>(dE), static_cast<int>(p.H), L.nh, nh_magic,
+                         static_cast<int>(p.T));
   note_launch(VCE_K_EMBED_REDUCE, st);
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* ids, float* const* dW,
+                                   void* const* ws, int n, const void* dE, cudaStream_t st) {
+  if (n < 1 || n > kMaxSlots || ps[0].T == 0) return n < 1 || n > kMaxSlots ? cudaErrorInvalidValue : cudaSuccess;
+  const DevInfo di = current_device_info();
+  const int nb = di.num_sms > 0 ? di.num_sms : 1;
+  SortPath path[kMaxSlots];
+  int32_t* zero[kMaxSlots] = {nullptr, nullptr, nullptr};
+  bool any_bucketed = false;
+  EmbSlots sl{};
+  sl.n = n;
+  for (int k = 0; k < n; ++k) {
+    path[k] = sort_path(ps[k], nb);
+    sl.s[k] = emb_slot(ps[k], ws[k], dW[k]);
+    if (path[k] == SortPath::kCount || path[k] == SortPath::kBucket) {
+      zero[k] = sl.s[k].hdr;
+      any_bucketed = true;
+    }
+  }
+  if (any_bucketed) {
+    embed_hdr_zero_kernel<<<1, 32, 0, st>>>(zero[0], zero[1], zero[2]);
+    note_launch(VCE_K_EMBED_HDR, st);
+    if (cudaError_t e = cudaGetLastError()) return e;
+  }
+  for (int k = 0; k < n; ++k)
+    if (cudaError_t e = launch_sort(ps[k], ids[k], ws[k], path[k], nb, st)) return e;
+  return launch_reduce(ps[0], sl, dE, st);
+}
+
+cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const void* dE, float* dW, void* ws,
+                             int32_t* status, cudaStream_t st) {
+  (void)status;
+  return launch_embed_bwd_multi(&p, &ids, &dW, &ws, 1, dE, st);
 }
 
 }  // namespace vce

@@ -88,6 +88,11 @@ size_t embed_bwd_ws_bytes(const vce_problem& p);
 bool embed_bwd_supported(const vce_problem& p);
 cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const void* dE, float* dW, void* ws,
                              int32_t* status, cudaStream_t st);
+// n (1 to 3) backward problems with the same T, H and dtype and the same dE,
+// each with its own ids, dW and workspace (embed_bwd_ws_bytes of it): one
+// header-zeroing launch, one sort per problem, one reduce over all of them.
+cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* ids, float* const* dW,
+                                   void* const* ws, int n, const void* dE, cudaStream_t st);
 
 // Merge of the forward partials into lse, per-token loss and the mean.
 cudaError_t launch_merge(const ProbDev& pd, const UnitGrid& ug, const int64_t* targets, const float2* part,

@@ -592,7 +592,8 @@ vce_status vce_ngram_embed_fwd(const vce_problem* p, const int64_t* ids, const v
 
 size_t vce_ngram_workspace_size(const vce_problem* p) {
   if (check_problem(p) != VCE_OK) return SIZE_MAX;
-  return 2 * align_up(sizeof(int64_t) * static_cast<size_t>(p->T), kWsAlign) + embed_bwd_ws_bytes(*p);
+  // the two n-gram row-index arrays, then one embedding-backward workspace per table
+  return 2 * align_up(sizeof(int64_t) * static_cast<size_t>(p->T), kWsAlign) + 3 * embed_bwd_ws_bytes(*p);
 }
 
 vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const void* dE, float* dW, float* dT2,
@@ -612,19 +613,27 @@ vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const v
   const size_t ids_bytes = align_up(sizeof(int64_t) * static_cast<size_t>(p->T), kWsAlign);
   int64_t* idx2 = reinterpret_cast<int64_t*>(b);
   int64_t* idx3 = reinterpret_cast<int64_t*>(b + ids_bytes);
-  void* ews = b + 2 * ids_bytes;
-  if (cudaError_t e = launch_embed_bwd(*p, ids, dE, dW, ews, dev_status, st)) return cuda_status(e);
+  const size_t ews_bytes = embed_bwd_ws_bytes(*p);
+  // The row indices first; then the three tables' backward problems are
+  // sorted one after the other and reduced in one launch.
+  vce_problem ps[3] = {*p, ngram_table_problem(*p, M2 > 0 ? M2 : 1), ngram_table_problem(*p, M3 > 0 ? M3 : 1)};
+  const int64_t* pid[3] = {ids, idx2, idx3};
+  float* pdw[3] = {dW, dT2, dT3};
+  void* pws[3] = {b + 2 * ids_bytes, b + 2 * ids_bytes + ews_bytes, b + 2 * ids_bytes + 2 * ews_bytes};
+  int n = 1;
   if (M2 > 0) {
     if (cudaError_t e = launch_ngram_hash(ids, p->T, 2, p->V_real, M2, seq_len, idx2, st)) return cuda_status(e);
-    if (cudaError_t e = launch_embed_bwd(ngram_table_problem(*p, M2), idx2, dE, dT2, ews, dev_status, st))
-      return cuda_status(e);
+    ++n;
   }
   if (M3 > 0) {
     if (cudaError_t e = launch_ngram_hash(ids, p->T, 3, p->V_real, M3, seq_len, idx3, st)) return cuda_status(e);
-    if (cudaError_t e = launch_embed_bwd(ngram_table_problem(*p, M3), idx3, dE, dT3, ews, dev_status, st))
-      return cuda_status(e);
+    ps[n] = ps[2];
+    pid[n] = idx3;
+    pdw[n] = dT3;
+    pws[n] = pws[2];
+    ++n;
   }
-  return VCE_OK;
+  return cuda_status(launch_embed_bwd_multi(ps, pid, pdw, pws, n, dE, st));
 }
 
 vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* stream) {
