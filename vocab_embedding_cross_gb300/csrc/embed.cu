@@ -1455,7 +1455,8 @@ cudaError_t launch_reduce(const vce_problem& p, const EmbSlots& sl, const void* 
 
 cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* ids, float* const* dW,
                                    void* const* ws, int n, const void* dE, cudaStream_t st) {
-  if (n < 1 || n > kMaxSlots || ps[0].T == 0) return n < 1 || n > kMaxSlots ? cudaErrorInvalidValue : cudaSuccess;
+  if (n < 1 || n > kMaxSlots) return cudaErrorInvalidValue;
+  if (ps[0].T == 0) return cudaSuccess;
   const DevInfo di = current_device_info();
   const int nb = di.num_sms > 0 ? di.num_sms : 1;
   SortPath path[kMaxSlots];
