@@ -24,13 +24,6 @@
 namespace vce {
 namespace {
 
-// Programmatic dependent launch (sm_90 and later). A kernel launched with the
-// programmatic-serialisation attribute may start once every CTA of the
-// previous kernel in the stream has called grid_dep_launch() or exited;
-// grid_dep_wait() then blocks until that kernel has completed and its writes
-// are visible. Both are no-ops in a kernel launched the ordinary way.
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // Forward gather: one warp per token row.
@@ -491,24 +484,6 @@ __global__ void embed_hdr_zero_kernel(int32_t* h0, int32_t* h1, int32_t* h2) {
   if (k < 3 && h) h[i] = 0;
 }
 
-// Launches `kern` with programmatic stream serialisation: it may start while
-// the previous kernel in the stream is still running, and must call
-// grid_dep_wait() before it touches anything that kernel writes.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                             Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
-}
 
 // Bucketed variant: the sort spread over gridDim.x CTAs (one per SM). CTA b
 // takes the valid ids with id % NB == b, in token order, and sorts them by

@@ -265,6 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const bool leader = rank == 0;
   const int first_item = static_cast<int>(cluster_id_x());
   const int item_step = static_cast<int>(cluster_count_x());
+  grid_dep_launch();   // the next kernel may set itself up once every CTA is here
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);     // the even CTA's expect_tx; bytes from both CTAs
@@ -292,6 +293,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const WaitCtx wc{s_abort, a.status, a.limit_ns};
+  // Launched as a dependent launch: barriers and TMEM are set up while the
+  // previous kernel drains; nothing in global memory is touched before it ends.
+  grid_dep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -782,9 +786,10 @@ cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const CUte
   const DevInfo di = current_device_info();
   const int mc = max_clusters<MODE>(di);
   const int clusters = a.n_items < mc ? a.n_items : mc;
-  tc_loss_kernel<MODE><<<2 * clusters, kThreads, smem_bytes<MODE>(), st>>>(mA, mB, mO, a);
+  const cudaError_t e = launch_dependent(tc_loss_kernel<MODE>, dim3(2 * clusters), dim3(kThreads), smem_bytes<MODE>(),
+                                         st, mA, mB, mO, a);
   note_launch(MODE == MODE_ARGMAX ? VCE_K_TC_ARGMAX : VCE_K_TC_FWD + MODE, st);
-  return cudaGetLastError();
+  return e;
 }
 
 TcArgs base_args(const vce_problem& p, const int64_t* targets, int32_t* status) {
@@ -815,6 +820,8 @@ int tc_group_mblk(const vce_problem& p) {
 // dH = (accumulate ? dH : 0) + P[0] + P[1] + ... in this order (deterministic).
 __global__ void __launch_bounds__(256) dh_reduce_kernel(const float4* __restrict__ P, int nparts, int64_t part_stride4,
                                                         float4* __restrict__ dH, int64_t n4, int accumulate) {
+  grid_dep_launch();
+  grid_dep_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float4 s = accumulate ? dH[i] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -994,10 +1001,11 @@ cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void*
       const int64_t n4 = p.T * p.H / 4;
       const int64_t stride4 = static_cast<int64_t>(t_pad) * p.H / 4;
       const DevInfo di = current_device_info();
-      dh_reduce_kernel<<<di.num_sms * 8, 256, 0, st>>>(reinterpret_cast<const float4*>(dh_part), parts, stride4,
-                                                       reinterpret_cast<float4*>(dH), n4, dH_accumulate ? 1 : 0);
+      e = launch_dependent(dh_reduce_kernel, dim3(di.num_sms * 8), dim3(256), 0, st,
+                           reinterpret_cast<const float4*>(dh_part), parts, stride4, reinterpret_cast<float4*>(dH), n4,
+                           dH_accumulate ? 1 : 0);
       note_launch(VCE_K_DH_REDUCE, st);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if (e != cudaSuccess) return e;
     }
   }
   // DW: dW[v0:v0+vc_act, :] (+)= G[:, 0:vc_act]^T h

@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
                  int32_t* status) {
   __shared__ float sh_loss[kMergeWarps];
   __shared__ int sh_cnt[kMergeWarps];
+  grid_dep_launch();   // launched as a dependent launch: wait for the kernel before
+  grid_dep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
   float my_loss = 0.0f;
@@ -116,6 +118,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 // One block: sum of the block partials in block order, then the mean.
 __global__ void __launch_bounds__(1024) loss_mean_kernel(const float* __restrict__ block_sums, int nblocks,
                                                          float* __restrict__ loss) {
+  grid_dep_launch();   // launched as a dependent launch: wait for the kernel before
+  grid_dep_wait();
   __shared__ double sh_a[1024];
   __shared__ long long sh_c[1024];
   double a = 0.0;
@@ -142,6 +146,8 @@ __global__ void __launch_bounds__(1024) loss_mean_kernel(const float* __restrict
 
 __global__ void __launch_bounds__(1024) count_valid_kernel(ProbDev pd, const int64_t* __restrict__ targets,
                                                            int32_t* n_valid, int32_t* status) {
+  grid_dep_launch();   // launched as a dependent launch: wait for the kernel before
+  grid_dep_wait();
   __shared__ int sh[32];
   int c = 0;
   bool bad = false;
@@ -170,6 +176,8 @@ __global__ void __launch_bounds__(1024) count_valid_kernel(ProbDev pd, const int
 __global__ void __launch_bounds__(kMergeWarps * 32)
     argmax_merge_kernel(ProbDev pd, UnitGrid ug, const float2* __restrict__ part, int64_t* __restrict__ argmax,
                         float* __restrict__ max_logit, int32_t* __restrict__ owner) {
+  grid_dep_launch();   // launched as a dependent launch: wait for the kernel before
+  grid_dep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
   if (t >= pd.T) return;
@@ -204,6 +212,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 // rounded to nearest even once. Four elements per step (8-byte stores).
 __global__ void __launch_bounds__(256) dh_to_bf16_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
                                                          int64_t n4, int accumulate) {
+  grid_dep_launch();   // launched as a dependent launch: wait for the kernel before
+  grid_dep_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float4 a = __ldcs(acc + i);
@@ -230,38 +240,39 @@ cudaError_t launch_dh_to_bf16(const float* acc, void* out, int64_t n, bool accum
   int64_t blocks = ceil_div(n4, 256 * 4);
   const int64_t cap = static_cast<int64_t>(di.num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  dh_to_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(reinterpret_cast<const float4*>(acc),
-                                                                   static_cast<uint2*>(out), n4, accumulate ? 1 : 0);
+  const cudaError_t e = launch_dependent(dh_to_bf16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                                         reinterpret_cast<const float4*>(acc), static_cast<uint2*>(out), n4,
+                                         accumulate ? 1 : 0);
   note_launch(VCE_K_DH_BF16, st);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_argmax_merge(const ProbDev& pd, const UnitGrid& ug, const float2* part, int64_t* argmax,
                                 float* max_logit, int32_t* owner, cudaStream_t st) {
-  argmax_merge_kernel<<<merge_blocks(pd.T), kMergeWarps * 32, 0, st>>>(pd, ug, part, argmax, max_logit, owner);
+  const cudaError_t e = launch_dependent(argmax_merge_kernel, dim3(merge_blocks(pd.T)), dim3(kMergeWarps * 32), 0, st,
+                                         pd, ug, part, argmax, max_logit, owner);
   note_launch(VCE_K_ARGMAX_MERGE, st);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_merge(const ProbDev& pd, const UnitGrid& ug, const int64_t* targets, const float2* part,
                          const float* ztgt, float* lse, float* token_loss, int32_t* target_owner,
                          int32_t* max_owner, float* block_sums, float* loss, int32_t* status, cudaStream_t st) {
   const int nb = merge_blocks(pd.T);
-  merge_kernel<<<nb, kMergeWarps * 32, 0, st>>>(pd, ug, targets, part, ztgt, lse, token_loss, target_owner,
-                                                 max_owner, block_sums, status);
+  cudaError_t e = launch_dependent(merge_kernel, dim3(nb), dim3(kMergeWarps * 32), 0, st, pd, ug, targets, part, ztgt,
+                                   lse, token_loss, target_owner, max_owner, block_sums, status);
   note_launch(VCE_K_MERGE, st);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  loss_mean_kernel<<<1, 1024, 0, st>>>(block_sums, nb, loss);
+  e = launch_dependent(loss_mean_kernel, dim3(1), dim3(1024), 0, st, static_cast<const float*>(block_sums), nb, loss);
   note_launch(VCE_K_LOSS_MEAN, st);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_count_valid(const ProbDev& pd, const int64_t* targets, int32_t* n_valid, int32_t* status,
                                cudaStream_t st) {
-  count_valid_kernel<<<1, 1024, 0, st>>>(pd, targets, n_valid, status);
+  const cudaError_t e = launch_dependent(count_valid_kernel, dim3(1), dim3(1024), 0, st, pd, targets, n_valid, status);
   note_launch(VCE_K_COUNT_VALID, st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace vce
