@@ -85,6 +85,8 @@ def _replays(wl, ids, dE, M2, M3, seq_len, inits):
     ("bf16", 300, 128, 1000, 1024, 613, 1024, 50),
     ("bf16", 520, 256, 5000, 5056, 4096, 0, 0),        # 3-gram table left out
     ("bf16", 129, 64, 1000, 1024, 0, 97, 16),           # 2-gram table left out
+    ("bf16", 700, 8, 1000, 1024, 613, 1 << 21, 0),     # the 3-gram table sorted by radix buckets, the others counted
+    ("bf16", 20000, 8, 1000, 1024, 613, 1024, 0),      # T above the shared-memory sorts: every table in the workspace
 ])
 def test_ngram_fwd_bwd_exact(dtype, T, H, V_real, Vp, M2, M3, seq_len):
     wl, d, T2, T3 = _case(dtype, T, H, V_real, Vp, M2, M3, seed=71 + T)
