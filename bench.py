@@ -290,6 +290,9 @@ def run_ours(args):
     # ---- greedy argmax over the same head (decoding), device resident ----
     greedy = run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks)
 
+    # ---- the OT-H auxiliary head on the same workload ----
+    oth = run_oth(args, vce, D, p, h, W, y, stream, T, H, Vp, V, wl.S, peaks)
+
     # ---- the loss alone on the GPT-2-like head and on the GPT-OSS shapes ----
     loss_configs = {name: run_loss_config(args, vce, D, I, stream, peaks, name)
                     for name in ("gpt2_head", "gptoss_embed")}
@@ -328,6 +331,7 @@ def run_ours(args):
             "embedding_gptoss": emb_gptoss,
             "greedy_argmax": greedy,
             "loss_configs": loss_configs,
+            "oth_head": oth,
             "ngram_embedding": ngram,
             "per_kernel_ms": {k: round(v[0], 4) for k, v in sorted(per_kind.items())},
             "per_kernel_launches": {k: v[1] for k, v in sorted(per_kind.items())},
@@ -366,6 +370,63 @@ def run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks):
     tf = 2.0 * T * H * V / (ms / 1e3) / 1e12
     return {"tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_call": round(ms, 4), "calls": n,
             "TFLOPs": round(tf, 1), "frac_of_burst": round(tf / peaks["bf16_tflops"], 4)}
+
+
+def run_oth(args, vce, D, p, h, W, y, stream, T, H, Vp, V, S, peaks):
+    """The OT-H auxiliary head on the main workload: head one scores h on the
+    next tokens, head two (its own weights W2, here a copy of W) scores h[:-1]
+    on the tokens two ahead at weight 0.1 and adds its dH into head one's
+    (VCE_FLAG_ACCUMULATE_DH). One step is both heads' forward and backward;
+    the plain head's forward and backward is timed beside it."""
+    import torch
+    W2 = W.clone()
+    y2 = y[1:]
+    p1 = vce.problem(T, H, Vp, V, S, vce.VCE_BF16)
+    p2 = vce.problem(T - 1, H, Vp, V, S, vce.VCE_BF16)
+    p2_acc = vce.problem(T - 1, H, Vp, V, S, vce.VCE_BF16, flags=vce.VCE_FLAG_ACCUMULATE_DH)
+    loss1 = torch.empty(1, device="cuda")
+    loss2 = torch.empty(1, device="cuda")
+    lse1 = torch.empty(T, device="cuda")
+    lse2 = torch.empty(T - 1, device="cuda")
+    dH = torch.empty((T, H), device="cuda")
+    dW1 = torch.empty((Vp, H), device="cuda")
+    dW2 = torch.empty((Vp, H), device="cuda")
+    ws_f = D.workspace(vce.vce_workspace_size(p1, vce.VCE_OP_LOSS_FWD))
+    ws_b = D.workspace(vce.vce_workspace_size(p1, vce.VCE_OP_LOSS_BWD))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = stream.cuda_stream
+
+    def one_head():
+        vce.vce_loss_fwd(p1, h, W, y, loss1, lse1, ws=ws_f, dev_status=st, stream=sp)
+        vce.vce_loss_bwd(p1, h, W, y, lse1, 1.0, dH, dW1, ws_b, dev_status=st, stream=sp)
+
+    def two_heads():
+        one_head()
+        vce.vce_loss_fwd(p2, h, W2, y2, loss2, lse2, ws=ws_f, dev_status=st, stream=sp)
+        vce.vce_loss_bwd(p2_acc, h, W2, y2, lse2, 0.1, dH, dW2, ws_b, dev_status=st, stream=sp)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    n = max(3, args.steps // 4)
+    ms1 = timed(one_head, n)
+    ms2 = timed(two_heads, n)
+    assert int(st.item()) == 0, vce.status_str(int(st.item()))
+    del W2, dW1, dW2, ws_f, ws_b
+    torch.cuda.empty_cache()
+    return {"step": "head one fwd+bwd, head two (T-1 rows, weight 0.1) fwd+bwd adding into dH",
+            "ms_per_step": round(ms2, 4), "tokens_per_s": round(T / (ms2 / 1e3), 1),
+            "one_head_ms": round(ms1, 4), "ratio_to_one_head": round(ms2 / ms1, 4), "steps": n}
 
 
 def run_loss_config(args, vce, D, I, stream, peaks, name):
