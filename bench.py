@@ -268,10 +268,11 @@ def run_ours(args):
         emb["gather_GBps"] = round(gather_bytes / (g_ms / 1e3) / 1e9, 1)
         emb["gather_us"] = round(g_ms * 1e3, 2)
     if "embed_reduce" in per_kind:
-        b_ms = sum(per_kind.get(k, (0.0, 0))[0] for k in ("embed_hdr", "embed_sort", "embed_reduce"))
+        sorts = ("embed_sort", "embed_sort_cluster")
+        b_ms = sum(per_kind.get(k, (0.0, 0))[0] for k in ("embed_hdr", "embed_reduce") + sorts)
         emb["bwd_GBps"] = round(bwd_bytes / (b_ms / 1e3) / 1e9, 1)
         emb["bwd_us"] = round(b_ms * 1e3, 2)
-        emb["bwd_sort_us"] = round(per_kind.get("embed_sort", (0.0, 0))[0] * 1e3, 2)
+        emb["bwd_sort_us"] = round(sum(per_kind.get(k, (0.0, 0))[0] for k in sorts) * 1e3, 2)
     emb["hbm_peak_GBps"] = peaks["hbm_gbs"]
     for k in ("gather", "bwd"):
         if f"{k}_GBps" in emb:

@@ -144,6 +144,13 @@ vce_status vce_embed_fwd(const vce_problem* p, const int64_t* ids, const void* W
  * is summed in fp32 from 0.0 in ascending t; the run sums are added left to
  * right; the total is added to dW[v] with one fp32 rounding. Results are
  * bit-identical run to run.
+ * How the pairs are sorted does not change the result. Up to 16384 tokens the
+ * ids are bucketed over the SMs. Above 8192 tokens, clusters of 8 CTAs share
+ * the id loads through distributed shared memory (kernel kind
+ * VCE_K_EMBED_SORT_CLUSTER); otherwise every CTA loads all ids itself
+ * (VCE_K_EMBED_SORT). The environment variable VCE_EMBED_SORT_CLUSTER, read
+ * at each call, overrides the choice: 1 for the clusters whenever the bucketed
+ * counting sort runs, 0 for never.
  * Workspace: vce_workspace_size(p, VCE_OP_EMBED_BWD) bytes.
  */
 vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* dE,
@@ -389,7 +396,8 @@ typedef enum vce_kernel_kind {
   VCE_K_SIMT_FWD = 10, VCE_K_SIMT_GRAD = 11, VCE_K_SGEMM = 12, VCE_K_WAIT_SELFTEST = 13,
   VCE_K_DH_REDUCE = 14, VCE_K_SAMPLED_CAND = 15, VCE_K_SAMPLED_SCATTER = 16,
   VCE_K_TC_ARGMAX = 17, VCE_K_ARGMAX_MERGE = 18, VCE_K_SIMT_ARGMAX = 19,
-  VCE_K_NGRAM_HASH = 20, VCE_K_NGRAM_FWD = 21, VCE_K_EMBED_HDR = 22, VCE_K_DH_BF16 = 23
+  VCE_K_NGRAM_HASH = 20, VCE_K_NGRAM_FWD = 21, VCE_K_EMBED_HDR = 22, VCE_K_DH_BF16 = 23,
+  VCE_K_EMBED_SORT_CLUSTER = 24
 } vce_kernel_kind;
 uint64_t vce_launch_count(void);
 vce_status vce_profile_begin(int32_t capacity, void* stream);

@@ -165,3 +165,40 @@ def test_embed_bwd_workspace_sort_path(T, V_real, Vp):
     ids = rng.permutation(ids)
     dW0 = np.zeros((wl.Vp, wl.H), np.float32)
     _check_bwd(wl, ids, d["dE"], dW0)
+
+
+def _sort_kinds(wl, ids, dE, dW0):
+    R.vce.vce_profile_begin(16)
+    got = _check_bwd(wl, ids, dE, dW0)
+    kinds = [k for k, _ in R.vce.vce_profile_end(16)]
+    return got, kinds
+
+
+@pytest.mark.parametrize("T,V_real", [(1, 1000), (33, 1000), (2049, 151936), (8192, 151936), (8193, 5000),
+                                      (16384, 201088)])
+def test_embed_bwd_clustered_and_per_cta_id_loads(T, V_real, monkeypatch):
+    """The counting sort's two id loads: clusters of eight CTAs sharing the
+    loads through distributed shared memory (VCE_EMBED_SORT_CLUSTER=1), and
+    every CTA loading all ids (=0). T spans one and two load rounds per warp,
+    and a batch so small that most ranks load nothing. Both are bit-exact
+    against the replay, with one heavy id over many runs; without the variable
+    the clusters run above 8192 tokens only."""
+    wl = I.custom(T=T, H=136, V_real=V_real, Vp=-(-V_real // 64) * 64, S=8, dtype="bf16", seed=17,
+                  pad_id_frac=0.03, oor_id_frac=0.02)
+    d = I.make_all(wl, ("ids", "dE"))
+    ids = d["ids"].copy()
+    ids[: T // 5] = 7
+    ids = np.random.default_rng(9).permutation(ids)
+    dW0 = np.random.default_rng(10).standard_normal((wl.Vp, wl.H)).astype(np.float32)
+    res = {}
+    for env, kind in (("1", "embed_sort_cluster"), ("0", "embed_sort"), (None, None)):
+        if env is None:
+            monkeypatch.delenv("VCE_EMBED_SORT_CLUSTER", raising=False)
+            kind = "embed_sort_cluster" if T > 8192 else "embed_sort"
+        else:
+            monkeypatch.setenv("VCE_EMBED_SORT_CLUSTER", env)
+        got, kinds = _sort_kinds(wl, ids, d["dE"], dW0)
+        other = "embed_sort" if kind == "embed_sort_cluster" else "embed_sort_cluster"
+        assert kind in kinds and other not in kinds
+        res[env] = got
+    assert np.array_equal(res["1"].view(np.uint32), res["0"].view(np.uint32))

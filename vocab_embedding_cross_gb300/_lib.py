@@ -253,7 +253,7 @@ def vce_wait_selftest(limit_ns: int, dev_status, stream=None) -> None:
 KERNEL_KINDS = ["embed_gather", "embed_sort", "embed_reduce", "tc_fwd", "tc_grad", "tc_dh", "tc_dw",
                 "merge", "loss_mean", "count_valid", "simt_fwd", "simt_grad", "sgemm", "wait_selftest",
                 "dh_reduce", "sampled_cand", "sampled_scatter", "tc_argmax", "argmax_merge", "simt_argmax",
-                "ngram_hash", "ngram_fwd", "embed_hdr", "dh_bf16"]
+                "ngram_hash", "ngram_fwd", "embed_hdr", "dh_bf16", "embed_sort_cluster"]
 
 
 def vce_launch_count() -> int:

@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "internal.h"
 
@@ -925,68 +926,174 @@ __device__ __forceinline__ void add_rows(const TE* __restrict__ dE, int64_t H, i
 constexpr int kCntWarps = 8;
 constexpr size_t kCountSmemBudget = 200 * 1024;
 
-size_t count_sort_smem(int64_t T, int64_t nq) {   // keys, kCntWarps rows, three per-q arrays
-  return static_cast<size_t>(T) * sizeof(uint32_t) + static_cast<size_t>(kCntWarps + 3) * nq * sizeof(int);
+// Keys per segment: with CL > 1, CTA rank r of a cluster loads tokens
+// [r * Tc, (r + 1) * Tc) and every CTA keeps one segment of Tc keys per rank.
+__host__ __device__ constexpr int count_seg_cap(int T, int CL) {
+  return CL == 1 ? T : (((T + CL - 1) / CL + 31) & ~31);
 }
 
-// ROUNDS: rounds of 32 tokens per warp in phase A (T <= 32 * 32 * ROUNDS), so
-// that a smaller batch does not issue the larger one's predicated rounds.
-template <int ROUNDS>
+size_t count_sort_smem(int64_t T, int64_t nq, int CL) {   // key segments, kCntWarps rows, three per-q arrays
+  return static_cast<size_t>(CL) * count_seg_cap(static_cast<int>(T), CL) * sizeof(uint32_t) +
+         static_cast<size_t>(kCntWarps + 3) * nq * sizeof(int);
+}
+
+// Thread-block-cluster helpers for the clustered id load.
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_map(const void* p, uint32_t rank) {   // the same smem word in CTA `rank`
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cl_store(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cl_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// ROUNDS: rounds of 32 tokens per warp in phase A, so that a smaller batch
+// does not issue the larger one's predicated rounds.
+//
+// CL: CTAs per thread-block cluster. With CL == 1 every CTA loads all T ids and
+// keeps its own bucket's keys. With CL > 1 the cluster's CTAs own CL
+// consecutive buckets and share the loading: rank r loads tokens
+// [r * Tc, (r + 1) * Tc) and stores each key of the cluster's buckets into the
+// owning CTA's segment r, through distributed shared memory, so the ids cross
+// L2 once per cluster instead of once per CTA. Segment r then holds bucket
+// keys in token order, and segments follow token order too. The counting
+// warps take the segments in order (kCntWarps / CL warps each), which keeps
+// the sort stable exactly as with one contiguous key array.
+template <int ROUNDS, int CL>
 __global__ void __launch_bounds__(kBktThreads, 1)
     embed_sort_count_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int nq, int nh,
                             uint32_t nb_magic, int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
+  static_assert(CL >= 1 && CL <= 8 && kCntWarps % CL == 0, "counting warps split evenly over the segments");
   extern __shared__ __align__(16) uint32_t csm[];
-  uint32_t* ka = csm;                                  // [T] this bucket's keys, token order
-  int* rows = reinterpret_cast<int*>(csm + T);         // [kCntWarps][nq]
+  const int Tc = count_seg_cap(T, CL);
+  uint32_t* ka = csm;                                  // [CL][Tc] this bucket's keys, token order
+  int* rows = reinterpret_cast<int*>(csm + CL * Tc);   // [kCntWarps][nq]
   int* bstart = rows + kCntWarps * nq;                 // [nq] first sorted position of q (its count, in step 2)
   int* brun = bstart + nq;                             // [nq] runs before q
   int* bseg = brun + nq;                               // [nq] ids before q | multi-run ids before q << 16
   __shared__ int sh[96];
   __shared__ uint64_t sh64[33];
+  __shared__ int segn[CL];                             // keys in each segment
+  __shared__ int wdc[CL > 1 ? kBktWarps * CL : 1];     // per warp and destination rank: keys sent
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
   const uint32_t NB = gridDim.x, b = blockIdx.x;
 
   grid_dep_launch();   // the reduce may be scheduled from here on; it waits for this grid to end
 
-  // Phase A, as in the radix variant: every id loaded before any is used.
-  const int tpw = ((T + kBktWarps - 1) / kBktWarps + 31) & ~31;
-  constexpr int kMaxRounds = ROUNDS;
-  int64_t idv[kMaxRounds];
+  int m = 0;
+  if constexpr (CL == 1) {
+    // Phase A, as in the radix variant: every id loaded before any is used.
+    const int tpw = ((T + kBktWarps - 1) / kBktWarps + 31) & ~31;
+    int64_t idv[ROUNDS];
 #pragma unroll
-  for (int j = 0; j < kMaxRounds; ++j) {
-    const int t = warp * tpw + j * 32 + lane;
-    idv[j] = (j * 32 < tpw && t < T) ? __ldg(ids + t) : -1;
-  }
-  for (int i = tid; i < kCntWarps * nq; i += kBktThreads) rows[i] = 0;   // while the loads are in flight
-  uint32_t tkey[kMaxRounds];
-#pragma unroll
-  for (int j = 0; j < kMaxRounds; ++j) {
-    uint32_t k = 0xFFFFFFFFu;
-    if (idv[j] >= 0 && idv[j] < V_real) {
-      const uint32_t u = static_cast<uint32_t>(idv[j]);
-      const uint32_t q = __umulhi(u, nb_magic);   // u / NB, exact for u < 2^32 / NB
-      if (u - q * NB == b) k = (q << tbits) | static_cast<uint32_t>(warp * tpw + j * 32 + lane);
+    for (int j = 0; j < ROUNDS; ++j) {
+      const int t = warp * tpw + j * 32 + lane;
+      idv[j] = (j * 32 < tpw && t < T) ? __ldg(ids + t) : -1;
     }
-    tkey[j] = k;
-  }
-  int wcount = 0;
+    for (int i = tid; i < kCntWarps * nq; i += kBktThreads) rows[i] = 0;   // while the loads are in flight
+    uint32_t tkey[ROUNDS];
 #pragma unroll
-  for (int j = 0; j < kMaxRounds; ++j) wcount += __popc(__ballot_sync(0xffffffffu, tkey[j] != 0xFFFFFFFFu));
-  if (lane == 0) sh[warp] = wcount;
-  __syncthreads();
-  int wbase = 0, m = 0;
-  for (int w = 0; w < kBktWarps; ++w) {
-    const int c = sh[w];
-    wbase += w < warp ? c : 0;
-    m += c;
-  }
+    for (int j = 0; j < ROUNDS; ++j) {
+      uint32_t k = 0xFFFFFFFFu;
+      if (idv[j] >= 0 && idv[j] < V_real) {
+        const uint32_t u = static_cast<uint32_t>(idv[j]);
+        const uint32_t q = __umulhi(u, nb_magic);   // u / NB, exact for u < 2^32 / NB
+        if (u - q * NB == b) k = (q << tbits) | static_cast<uint32_t>(warp * tpw + j * 32 + lane);
+      }
+      tkey[j] = k;
+    }
+    int wcount = 0;
 #pragma unroll
-  for (int j = 0; j < kMaxRounds; ++j) {
-    const bool ok = tkey[j] != 0xFFFFFFFFu;
-    const unsigned bal = __ballot_sync(0xffffffffu, ok);
-    if (ok) ka[wbase + __popc(bal & lt_mask)] = tkey[j];
-    wbase += __popc(bal);
+    for (int j = 0; j < ROUNDS; ++j) wcount += __popc(__ballot_sync(0xffffffffu, tkey[j] != 0xFFFFFFFFu));
+    if (lane == 0) sh[warp] = wcount;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < kBktWarps; ++w) {
+      const int c = sh[w];
+      wbase += w < warp ? c : 0;
+      m += c;
+    }
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+      const bool ok = tkey[j] != 0xFFFFFFFFu;
+      const unsigned bal = __ballot_sync(0xffffffffu, ok);
+      if (ok) ka[wbase + __popc(bal & lt_mask)] = tkey[j];
+      wbase += __popc(bal);
+    }
+    if (tid == 0) segn[0] = m;
+  } else {
+    // Phase A, clustered. The arrive marks this CTA as started; the wait
+    // before the first remote store makes sure every CTA of the cluster is.
+    cl_arrive_relaxed();
+    const uint32_t rank = cl_rank(), cbase = b - rank;
+    const int t_lo = static_cast<int>(rank) * Tc, t_hi = min(T, t_lo + Tc);
+    const int tpw = ((Tc + kBktWarps - 1) / kBktWarps + 31) & ~31;
+    int64_t idv[ROUNDS];
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+      const int t = t_lo + warp * tpw + j * 32 + lane;
+      idv[j] = (j * 32 < tpw && t < t_hi) ? __ldg(ids + t) : -1;
+    }
+    for (int i = tid; i < kCntWarps * nq; i += kBktThreads) rows[i] = 0;   // while the loads are in flight
+    uint32_t tkey[ROUNDS];
+    int dst[ROUNDS], lpos[ROUNDS];
+    int sent = 0;   // lane d < CL: this warp's keys for rank d so far
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+      uint32_t k = 0;
+      int d = CL;   // CL: not a bucket of this cluster
+      if (idv[j] >= 0 && idv[j] < V_real) {
+        const uint32_t u = static_cast<uint32_t>(idv[j]);
+        const uint32_t q = __umulhi(u, nb_magic);   // u / NB, exact for u < 2^32 / NB
+        const uint32_t r = u - q * NB - cbase;      // wraps above CL for buckets before this cluster's
+        if (r < static_cast<uint32_t>(CL)) {
+          d = static_cast<int>(r);
+          k = (q << tbits) | static_cast<uint32_t>(t_lo + warp * tpw + j * 32 + lane);
+        }
+      }
+      int lp = 0, add = 0;
+#pragma unroll
+      for (int dd = 0; dd < CL; ++dd) {
+        const unsigned bal = __ballot_sync(0xffffffffu, d == dd);
+        if (d == dd) lp = __popc(bal & lt_mask);
+        if (lane == dd) add = __popc(bal);
+      }
+      lpos[j] = __shfl_sync(0xffffffffu, sent, d < CL ? d : 0) + lp;
+      sent += add;
+      tkey[j] = k;
+      dst[j] = d;
+    }
+    if (lane < CL) wdc[warp * CL + lane] = sent;
+    __syncthreads();
+    int wpre = 0, tot = 0;   // lane d < CL: keys for rank d from the warps before this one, and from all
+    if (lane < CL)
+      for (int w = 0; w < kBktWarps; ++w) {
+        const int c = wdc[w * CL + lane];
+        wpre += w < warp ? c : 0;
+        tot += c;
+      }
+    cl_wait();   // every CTA of the cluster has started
+    if (warp == 0 && lane < CL) cl_store(cl_map(&segn[rank], lane), static_cast<uint32_t>(tot));
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+      const int base = __shfl_sync(0xffffffffu, wpre, dst[j] < CL ? dst[j] : 0);
+      if (dst[j] < CL) cl_store(cl_map(&ka[static_cast<int>(rank) * Tc + base + lpos[j]], dst[j]), tkey[j]);
+    }
+    cl_arrive();   // the stores above are visible cluster-wide after the wait
+    cl_wait();
+#pragma unroll
+    for (int r = 0; r < CL; ++r) m += segn[r];
   }
   // This bucket's place in tsorted; the header is zeroed by the kernel before
   // this one. The claim's result is first needed in step 3.
@@ -995,14 +1102,25 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   if (tid == 0 && m > 0) tb = atomicAdd(&hdr[0], m);
   __syncthreads();
 
+  // Counting warp w takes part w % (kCntWarps / CL) of segment w / (kCntWarps / CL).
+  constexpr int kSpw = kCntWarps / CL;
+  int k_lo = 0, k_hi = 0;
+  const uint32_t* kseg = ka;
+  if (warp < kCntWarps) {
+    const int sgi = warp / kSpw, scnt = segn[sgi];
+    const int share = ((scnt + kSpw - 1) / kSpw + 31) & ~31;   // whole rounds
+    k_lo = min((warp % kSpw) * share, scnt);
+    k_hi = min(k_lo + share, scnt);
+    kseg = ka + sgi * Tc;
+  }
+
   // Step 1: per-warp counts of each q.
-  const int cpw = ((m + kCntWarps - 1) / kCntWarps + 31) & ~31;   // keys per counting warp, whole rounds
   if (warp < kCntWarps) {
     int* row = rows + warp * nq;
-    for (int j = 0; j < cpw; j += 32) {
-      const int i = warp * cpw + j + lane;
-      const bool ok = i < m;
-      const uint32_t q = ok ? ka[i] >> tbits : 0xFFFFFFFFu;
+    for (int j = k_lo; j < k_hi; j += 32) {
+      const int i = j + lane;
+      const bool ok = i < k_hi;
+      const uint32_t q = ok ? kseg[i] >> tbits : 0xFFFFFFFFu;
       const uint32_t peers = __match_any_sync(0xffffffffu, q);
       if (ok && lane == __ffs(peers) - 1) row[q] += __popc(peers);
       __syncwarp();
@@ -1062,10 +1180,10 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   // Step 3: tokens into place.
   if (warp < kCntWarps) {
     int* row = rows + warp * nq;
-    for (int j = 0; j < cpw; j += 32) {
-      const int i = warp * cpw + j + lane;
-      const bool ok = i < m;
-      const uint32_t key = ok ? ka[i] : 0u;
+    for (int j = k_lo; j < k_hi; j += 32) {
+      const int i = j + lane;
+      const bool ok = i < k_hi;
+      const uint32_t key = ok ? kseg[i] : 0u;
       const uint32_t q = ok ? key >> tbits : 0xFFFFFFFFu;
       const uint32_t peers = __match_any_sync(0xffffffffu, q);
       int base = 0;
@@ -1319,7 +1437,7 @@ EmbSlot emb_slot(const vce_problem& p, void* ws, float* dW) {
 
 enum class SortPath { kCount, kBucket, kSmem, kGlobal };
 
-SortPath sort_path(const vce_problem& p, int nb) {
+SortPath sort_path(const vce_problem& p, int nb, int cl) {
   const int tbits = bit_width(p.T);
   const int qbits = bit_width(ceil_div(p.V_real, nb));
   // The bucketed sorts divide ids by NB with a multiply-high, exact for ids
@@ -1327,15 +1445,83 @@ SortPath sort_path(const vce_problem& p, int nb) {
   // marks "not mine".
   const bool magic_ok = static_cast<uint64_t>(p.V_real) * static_cast<uint64_t>(nb) <= (uint64_t(1) << 32);
   const bool bucketed = p.T <= kSmemSortMax && tbits + qbits <= 31 && nb > 1 && magic_ok;
-  if (bucketed) return count_sort_smem(p.T, ceil_div(p.V_real, nb)) <= kCountSmemBudget ? SortPath::kCount
-                                                                                       : SortPath::kBucket;
+  if (bucketed) return count_sort_smem(p.T, ceil_div(p.V_real, nb), cl) <= kCountSmemBudget ? SortPath::kCount
+                                                                                           : SortPath::kBucket;
   if (p.T <= kSmemSortMax && tbits + bit_width(p.V_real) <= 32) return SortPath::kSmem;
   return SortPath::kGlobal;
 }
 
+// The counting sort's choice for one problem: its path, its bucket count NB
+// (the grid) and its cluster size.
+struct SortPlan {
+  SortPath path;
+  int nb, cl;
+};
+
+constexpr int kSortCluster = 8;
+
+void set_count_smem_limit(void (*k)(const int64_t*, int, int64_t, int, int, int, uint32_t, int32_t*, int32_t*,
+                                    RunDesc*, int32_t*),
+                          cudaError_t* err) {
+  const cudaError_t e =
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kCountSmemBudget));
+  if (e != cudaSuccess && *err == cudaSuccess) *err = e;
+}
+
+// Buckets of the clustered counting sort on the current device: kSortCluster
+// times the clusters of one-CTA-per-SM sort blocks that can be resident at
+// once (0 if none can), so that the grid runs in one wave.
+int cluster_sort_buckets(cudaError_t* err) {
+  static std::atomic<uint64_t> configured{0};
+  static std::atomic<int> buckets{0};
+  if (device_pending(configured)) {
+    for (auto k : {embed_sort_count_kernel<2, 1>, embed_sort_count_kernel<4, 1>, embed_sort_count_kernel<8, 1>,
+                   embed_sort_count_kernel<16, 1>, embed_sort_count_kernel<1, kSortCluster>,
+                   embed_sort_count_kernel<2, kSortCluster>})
+      set_count_smem_limit(k, err);
+    if (*err != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kSortCluster * 64);
+    cfg.blockDim = dim3(kBktThreads);
+    cfg.dynamicSmemBytes = kCountSmemBudget;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSortCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, embed_sort_count_kernel<2, kSortCluster>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();   // no clusters of this size: the one-CTA load stays
+      n = 0;
+    }
+    buckets.store(n * kSortCluster);
+    mark_device_done(configured);
+  }
+  return buckets.load();
+}
+
+// The clustered load pays off once every CTA would load more than 8192 ids
+// (16 rounds per warp): measured on GB300, about 3 us less for 16384 tokens
+// and about 1 us more for 8192. VCE_EMBED_SORT_CLUSTER=1 in the environment
+// takes it whenever the counting sort runs, =0 never.
+SortPlan plan_sort(const vce_problem& p, int num_sms, cudaError_t* err) {
+  const char* env = std::getenv("VCE_EMBED_SORT_CLUSTER");
+  const bool set = env && (env[0] == '0' || env[0] == '1') && env[1] == 0;
+  const bool allow = set ? env[0] == '1' : p.T > 8192;
+  const int nbc = cluster_sort_buckets(err);
+  if (allow && nbc >= 2 * kSortCluster && sort_path(p, nbc, kSortCluster) == SortPath::kCount)
+    return {SortPath::kCount, nbc, kSortCluster};
+  const int nb = num_sms > 0 ? num_sms : 1;
+  return {sort_path(p, nb, 1), nb, 1};
+}
+
 // Sorts one problem's valid (id, t) pairs into its workspace and builds its
 // runs. A bucketed sort needs its header zeroed by the kernel before it.
-cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, SortPath path, int nb, cudaStream_t st) {
+cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, const SortPlan& plan, cudaStream_t st) {
+  const SortPath path = plan.path;
+  const int nb = plan.nb;
   const BwdLayout L = bwd_layout(p);
   char* b = static_cast<char*>(ws);
   int32_t* hdr = reinterpret_cast<int32_t*>(b + L.hdr);
@@ -1350,26 +1536,40 @@ cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, Sort
   const int64_t nq = ceil_div(p.V_real, nb);
   const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb > 1 ? nb : 2) + 1u;   // floor((2^32 - 1) / NB) + 1
   if (path == SortPath::kCount) {
-    // Phase A's rounds of 32 tokens per warp: 2, 4, 8 or 16.
-    const int rounds = p.T <= 2048 ? 2 : p.T <= 4096 ? 4 : p.T <= 8192 ? 8 : 16;
-    void (*kern)(const int64_t*, int, int64_t, int, int, int, uint32_t, int32_t*, int32_t*, RunDesc*, int32_t*) =
-        rounds == 2 ? embed_sort_count_kernel<2>
-        : rounds == 4 ? embed_sort_count_kernel<4>
-        : rounds == 8 ? embed_sort_count_kernel<8>
-                      : embed_sort_count_kernel<16>;
-    static std::atomic<uint64_t> configured{0};
-    if (device_pending(configured)) {
-      for (auto k : {embed_sort_count_kernel<2>, embed_sort_count_kernel<4>, embed_sort_count_kernel<8>,
-                     embed_sort_count_kernel<16>}) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kCountSmemBudget));
-        if (e != cudaSuccess) return e;
-      }
-      mark_device_done(configured);
+    using CountKern = void (*)(const int64_t*, int, int64_t, int, int, int, uint32_t, int32_t*, int32_t*, RunDesc*,
+                               int32_t*);
+    CountKern kern;
+    if (plan.cl == 1) {
+      // Phase A's rounds of 32 tokens per warp: 2, 4, 8 or 16.
+      const int rounds = p.T <= 2048 ? 2 : p.T <= 4096 ? 4 : p.T <= 8192 ? 8 : 16;
+      kern = rounds == 2   ? embed_sort_count_kernel<2, 1>
+             : rounds == 4 ? embed_sort_count_kernel<4, 1>
+             : rounds == 8 ? embed_sort_count_kernel<8, 1>
+                           : embed_sort_count_kernel<16, 1>;
+    } else {
+      // Each rank loads a segment of Tc <= 2048 tokens: one or two rounds per warp.
+      const int tc = count_seg_cap(static_cast<int>(p.T), kSortCluster);
+      const int tpw = ((tc + kBktWarps - 1) / kBktWarps + 31) & ~31;
+      if (tpw > 64) return cudaErrorInvalidValue;
+      kern = tpw <= 32 ? embed_sort_count_kernel<1, kSortCluster> : embed_sort_count_kernel<2, kSortCluster>;
     }
-    if (cudaError_t e = launch_dependent(kern, dim3(nb), dim3(kBktThreads), count_sort_smem(p.T, nq), st, ids,
-                                         static_cast<int>(p.T), p.V_real, tbits, static_cast<int>(nq), L.nh,
-                                         nb_magic, hdr, tsorted, runs, counters))
+    const size_t smem = count_sort_smem(p.T, nq, plan.cl);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nb);
+    cfg.blockDim = dim3(kBktThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = plan.cl;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = plan.cl > 1 ? 2 : 1;
+    if (cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ids, static_cast<int>(p.T), p.V_real, tbits,
+                                           static_cast<int>(nq), L.nh, nb_magic, hdr, tsorted, runs, counters))
       return e;
   } else if (path == SortPath::kBucket) {
     static std::atomic<uint64_t> configured{0};
@@ -1398,7 +1598,7 @@ cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, Sort
     embed_sort_kernel<<<1, kSortThreads, 0, st>>>(ids, p.T, p.V_real, L.nh, hdr, ka, kb, seg, tsorted, runs,
                                                   counters);
   }
-  note_launch(VCE_K_EMBED_SORT, st);
+  note_launch(path == SortPath::kCount && plan.cl > 1 ? VCE_K_EMBED_SORT_CLUSTER : VCE_K_EMBED_SORT, st);
   return cudaGetLastError();
 }
 
@@ -1433,16 +1633,17 @@ cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* 
   if (n < 1 || n > kMaxSlots) return cudaErrorInvalidValue;
   if (ps[0].T == 0) return cudaSuccess;
   const DevInfo di = current_device_info();
-  const int nb = di.num_sms > 0 ? di.num_sms : 1;
-  SortPath path[kMaxSlots];
+  SortPlan plan[kMaxSlots];
   int32_t* zero[kMaxSlots] = {nullptr, nullptr, nullptr};
   bool any_bucketed = false;
   EmbSlots sl{};
   sl.n = n;
   for (int k = 0; k < n; ++k) {
-    path[k] = sort_path(ps[k], nb);
+    cudaError_t err = cudaSuccess;
+    plan[k] = plan_sort(ps[k], di.num_sms, &err);
+    if (err != cudaSuccess) return err;
     sl.s[k] = emb_slot(ps[k], ws[k], dW[k]);
-    if (path[k] == SortPath::kCount || path[k] == SortPath::kBucket) {
+    if (plan[k].path == SortPath::kCount || plan[k].path == SortPath::kBucket) {
       zero[k] = sl.s[k].hdr;
       any_bucketed = true;
     }
@@ -1453,7 +1654,7 @@ cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* 
     if (cudaError_t e = cudaGetLastError()) return e;
   }
   for (int k = 0; k < n; ++k)
-    if (cudaError_t e = launch_sort(ps[k], ids[k], ws[k], path[k], nb, st)) return e;
+    if (cudaError_t e = launch_sort(ps[k], ids[k], ws[k], plan[k], st)) return e;
   return launch_reduce(ps[0], sl, dE, st);
 }
 
