@@ -280,29 +280,39 @@ def run_ours(args):
 
     # ---- end to end through the C ABI with host buffers ----
     e2e = run_e2e(args, vce, D, d, p, p_head, W, E, loss, lse, dH, dW, st, ws_f, ws_b, ws_e, stream, wl)
+    # the library's launches made by each leg, in order (they split a profiler's launch list)
+    leg_marks = [("step", vce.vce_launch_count())]
 
     # ---- the embedding on the GPT-OSS-shaped table ----
     emb_gptoss = run_embedding(args, vce, D, I, stream, peaks, "gptoss_embed")
+    leg_marks.append(("embedding_gptoss", vce.vce_launch_count()))
     # the main workload's lookup and backward, each call timed alone the same way
     # (the figures above come from the step's per-launch events)
     emb["isolated"] = {k: v for k, v in run_embedding(args, vce, D, I, stream, peaks, args.workload).items()
                        if k != "workload"}
+    leg_marks.append(("embedding_isolated", vce.vce_launch_count()))
 
     # ---- greedy argmax over the same head (decoding), device resident ----
     greedy = run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks)
+    leg_marks.append(("greedy_argmax", vce.vce_launch_count()))
 
     # ---- the OT-H auxiliary head on the same workload ----
     oth = run_oth(args, vce, D, p, h, W, y, stream, T, H, Vp, V, wl.S, peaks)
+    leg_marks.append(("oth_head", vce.vce_launch_count()))
 
     # ---- the loss alone on the GPT-2-like head and on the GPT-OSS shapes ----
     loss_configs = {name: run_loss_config(args, vce, D, I, stream, peaks, name)
                     for name in ("gpt2_head", "gptoss_embed")}
+    leg_marks.append(("loss_configs", vce.vce_launch_count()))
 
     # ---- hashed n-gram input embeddings on the same ids ----
     ngram = run_ngram(args, vce, D, I, wl, d, p, W, dE, stream, peaks)
+    leg_marks.append(("ngram_embedding", vce.vce_launch_count()))
 
     # ---- sampled-softmax variant, against the full-vocabulary loss ----
     sampled = run_sampled(args, vce, D, I, stream, peaks, full_loss_tok_s=T / (loss_ms / 1e3) if loss_ms else None)
+    leg_marks.append(("sampled_softmax", vce.vce_launch_count()))
+    leg_launches = {name: n - (leg_marks[i - 1][1] if i else 0) for i, (name, n) in enumerate(leg_marks)}
 
     # ---- CPU baseline (rank 0, N = 1 only) ----
     cpu = None
@@ -337,6 +347,7 @@ def run_ours(args):
             "per_kernel_ms": {k: round(v[0], 4) for k, v in sorted(per_kind.items())},
             "per_kernel_launches": {k: v[1] for k, v in sorted(per_kind.items())},
             "gpu_launches": int(launches),
+            "leg_launches": leg_launches,
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -1459,6 +1459,7 @@ struct SortPlan {
 };
 
 constexpr int kSortCluster = 8;
+constexpr int kClusterRounds = (kSmemSortMax / kSortCluster + 1023) / 1024;   // rounds per warp at most
 
 void set_count_smem_limit(void (*k)(const int64_t*, int, int64_t, int, int, int, uint32_t, int32_t*, int32_t*,
                                     RunDesc*, int32_t*),
@@ -1477,7 +1478,7 @@ int cluster_sort_buckets(cudaError_t* err) {
   if (device_pending(configured)) {
     for (auto k : {embed_sort_count_kernel<2, 1>, embed_sort_count_kernel<4, 1>, embed_sort_count_kernel<8, 1>,
                    embed_sort_count_kernel<16, 1>, embed_sort_count_kernel<1, kSortCluster>,
-                   embed_sort_count_kernel<2, kSortCluster>})
+                   embed_sort_count_kernel<2, kSortCluster>, embed_sort_count_kernel<kClusterRounds, kSortCluster>})
       set_count_smem_limit(k, err);
     if (*err != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
@@ -1547,11 +1548,13 @@ cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, cons
              : rounds == 8 ? embed_sort_count_kernel<8, 1>
                            : embed_sort_count_kernel<16, 1>;
     } else {
-      // Each rank loads a segment of Tc <= 2048 tokens: one or two rounds per warp.
+      // Each rank loads a segment of Tc <= 16384 / kSortCluster tokens: up to 512 / kSortCluster rounds per warp.
       const int tc = count_seg_cap(static_cast<int>(p.T), kSortCluster);
       const int tpw = ((tc + kBktWarps - 1) / kBktWarps + 31) & ~31;
-      if (tpw > 64) return cudaErrorInvalidValue;
-      kern = tpw <= 32 ? embed_sort_count_kernel<1, kSortCluster> : embed_sort_count_kernel<2, kSortCluster>;
+      if (tpw > 32 * kClusterRounds) return cudaErrorInvalidValue;
+      kern = tpw <= 32 ? embed_sort_count_kernel<1, kSortCluster>
+             : tpw <= 64 ? embed_sort_count_kernel<2, kSortCluster>
+                         : embed_sort_count_kernel<kClusterRounds, kSortCluster>;
     }
     const size_t smem = count_sort_smem(p.T, nq, plan.cl);
     cudaLaunchConfig_t cfg = {};
