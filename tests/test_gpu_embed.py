@@ -202,3 +202,22 @@ def test_embed_bwd_clustered_and_per_cta_id_loads(T, V_real, monkeypatch):
         assert kind in kinds and other not in kinds
         res[env] = got
     assert np.array_equal(res["1"].view(np.uint32), res["0"].view(np.uint32))
+
+
+def _draw_large(i):
+    g = np.random.default_rng(300 + i)
+    V = int(g.integers(2, 300000))
+    return dict(T=int(g.integers(8193, 16385)), H=8 * int(g.integers(1, 40)), V_real=V,
+                Vp=-(-V // 64) * 64 + 64 * int(g.integers(0, 2)), S=int(g.integers(1, 9)))
+
+
+@pytest.mark.parametrize("case", [_draw_large(i) for i in range(6)],
+                         ids=lambda c: "T{T}_H{H}_V{V_real}".format(**c))
+def test_embed_bwd_random_large_batches(case):
+    """Seeded batches between 8192 and 16384 tokens (the clustered counting
+    sort, or the radix buckets where the vocabulary is too large for its
+    counters), random H and V: bit-exact against the replay."""
+    wl = I.custom(dtype="bf16", pad_id_frac=0.02, oor_id_frac=0.02, seed=19, **case)
+    d = I.make_all(wl, ("ids", "dE"))
+    dW0 = np.random.default_rng(11).standard_normal((wl.Vp, wl.H)).astype(np.float32)
+    _check_bwd(wl, d["ids"], d["dE"], dW0)

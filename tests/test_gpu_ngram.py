@@ -87,6 +87,7 @@ def _replays(wl, ids, dE, M2, M3, seq_len, inits):
     ("bf16", 129, 64, 1000, 1024, 0, 97, 16),           # 2-gram table left out
     ("bf16", 700, 8, 1000, 1024, 613, 1 << 21, 0),     # the 3-gram table sorted by radix buckets, the others counted
     ("bf16", 20000, 8, 1000, 1024, 613, 1024, 0),      # T above the shared-memory sorts: every table in the workspace
+    ("bf16", 12000, 16, 5000, 5056, 613, 1 << 18, 3000),  # 8192 < T <= 16384: three clustered counting sorts
 ])
 def test_ngram_fwd_bwd_exact(dtype, T, H, V_real, Vp, M2, M3, seq_len):
     wl, d, T2, T3 = _case(dtype, T, H, V_real, Vp, M2, M3, seed=71 + T)
