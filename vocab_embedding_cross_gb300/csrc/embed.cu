@@ -932,9 +932,16 @@ __host__ __device__ constexpr int count_seg_cap(int T, int CL) {
   return CL == 1 ? T : (((T + CL - 1) / CL + 31) & ~31);
 }
 
-size_t count_sort_smem(int64_t T, int64_t nq, int CL) {   // key segments, kCntWarps rows, three per-q arrays
+// The per-warp counters of q live two warps to a 32-bit word (every count and
+// position is below T <= 16384 < 2^16), in rows padded by one word per 32 q so
+// that a thread's consecutive q fall in distinct banks across a warp.
+__host__ __device__ constexpr int qpad(int q) { return q + (q >> 5); }
+__host__ __device__ constexpr int64_t count_row_words(int64_t nq) { return nq + (nq >> 5) + 1; }
+
+size_t count_sort_smem(int64_t T, int64_t nq, int CL) {   // key segments, packed counter rows, three per-q arrays
   return static_cast<size_t>(CL) * count_seg_cap(static_cast<int>(T), CL) * sizeof(uint32_t) +
-         static_cast<size_t>(kCntWarps + 3) * nq * sizeof(int);
+         static_cast<size_t>(kCntWarps / 2) * count_row_words(nq) * sizeof(uint32_t) +
+         static_cast<size_t>(3) * nq * sizeof(int);
 }
 
 // Thread-block-cluster helpers for the clustered id load.
@@ -977,8 +984,9 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   extern __shared__ __align__(16) uint32_t csm[];
   const int Tc = count_seg_cap(T, CL);
   uint32_t* ka = csm;                                  // [CL][Tc] this bucket's keys, token order
-  int* rows = reinterpret_cast<int*>(csm + CL * Tc);   // [kCntWarps][nq]
-  int* bstart = rows + kCntWarps * nq;                 // [nq] first sorted position of q (its count, in step 2)
+  const int nqp = static_cast<int>(count_row_words(nq));
+  uint32_t* rows = csm + CL * Tc;                      // [kCntWarps / 2][nqp] warps 2k, 2k+1 in halves of word k
+  int* bstart = reinterpret_cast<int*>(rows + (kCntWarps / 2) * nqp);   // [nq] first sorted position of q (its count, in step 2)
   int* brun = bstart + nq;                             // [nq] runs before q
   int* bseg = brun + nq;                               // [nq] ids before q | multi-run ids before q << 16
   __shared__ int sh[96];
@@ -1001,7 +1009,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
       const int t = warp * tpw + j * 32 + lane;
       idv[j] = (j * 32 < tpw && t < T) ? __ldg(ids + t) : -1;
     }
-    for (int i = tid; i < kCntWarps * nq; i += kBktThreads) rows[i] = 0;   // while the loads are in flight
+    for (int i = tid; i < (kCntWarps / 2) * nqp; i += kBktThreads) rows[i] = 0;   // while the loads are in flight
     uint32_t tkey[ROUNDS];
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) {
@@ -1045,7 +1053,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
       const int t = t_lo + warp * tpw + j * 32 + lane;
       idv[j] = (j * 32 < tpw && t < t_hi) ? __ldg(ids + t) : -1;
     }
-    for (int i = tid; i < kCntWarps * nq; i += kBktThreads) rows[i] = 0;   // while the loads are in flight
+    for (int i = tid; i < (kCntWarps / 2) * nqp; i += kBktThreads) rows[i] = 0;   // while the loads are in flight
     uint32_t tkey[ROUNDS];
     int dst[ROUNDS], lpos[ROUNDS];
     int sent = 0;   // lane d < CL: this warp's keys for rank d so far
@@ -1114,18 +1122,12 @@ __global__ void __launch_bounds__(kBktThreads, 1)
     kseg = ka + sgi * Tc;
   }
 
-  // Step 1: per-warp counts of each q.
-  if (warp < kCntWarps) {
-    int* row = rows + warp * nq;
-    for (int j = k_lo; j < k_hi; j += 32) {
-      const int i = j + lane;
-      const bool ok = i < k_hi;
-      const uint32_t q = ok ? kseg[i] >> tbits : 0xFFFFFFFFu;
-      const uint32_t peers = __match_any_sync(0xffffffffu, q);
-      if (ok && lane == __ffs(peers) - 1) row[q] += __popc(peers);
-      __syncwarp();
-    }
-  }
+  // Step 1: per-warp counts of each q, by shared-memory atomics (the counts do
+  // not depend on the order of the additions).
+  uint32_t* const row = rows + ((warp % kCntWarps) >> 1) * nqp;   // used by the counting warps only
+  const uint32_t half = 16u * static_cast<uint32_t>(warp & 1);
+  if (warp < kCntWarps)
+    for (int i = k_lo + lane; i < k_hi; i += 32) atomicAdd(&row[qpad(static_cast<int>(kseg[i] >> tbits))], 1u << half);
   __syncthreads();
 
   // Step 2: thread tid owns the q in [q0, q1). Rows become exclusive prefixes
@@ -1135,11 +1137,14 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   const int q0 = min(tid * bpt, nq), q1 = min(q0 + bpt, nq);
   uint64_t mine = 0;
   for (int q = q0; q < q1; ++q) {
+    const int qi = qpad(q);
     int run = 0;
-    for (int w = 0; w < kCntWarps; ++w) {
-      const int c = rows[w * nq + q];
-      rows[w * nq + q] = run;
-      run += c;
+#pragma unroll
+    for (int k = 0; k < kCntWarps / 2; ++k) {
+      const uint32_t v = rows[k * nqp + qi];
+      const int c0 = static_cast<int>(v & 0xFFFFu), c1 = static_cast<int>(v >> 16);
+      rows[k * nqp + qi] = static_cast<uint32_t>(run) | (static_cast<uint32_t>(run + c0) << 16);
+      run += c0 + c1;
     }
     bstart[q] = run;
     const int nr = (run + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
@@ -1155,7 +1160,9 @@ __global__ void __launch_bounds__(kBktThreads, 1)
     bstart[q] = p_cnt;
     brun[q] = p_run;
     bseg[q] = p_seg | (p_multi << 16);
-    for (int w = 0; w < kCntWarps; ++w) rows[w * nq + q] += p_cnt;
+    const int qi = qpad(q);
+#pragma unroll
+    for (int k = 0; k < kCntWarps / 2; ++k) rows[k * nqp + qi] += static_cast<uint32_t>(p_cnt) * 0x10001u;
     const int nr = (cnt + kEmbedBwdChunk - 1) / kEmbedBwdChunk;
     pre += static_cast<uint64_t>(cnt) | (static_cast<uint64_t>(nr) << 16) | (static_cast<uint64_t>(cnt > 0) << 32) |
            (static_cast<uint64_t>(nr > 1) << 48);
@@ -1179,7 +1186,6 @@ __global__ void __launch_bounds__(kBktThreads, 1)
 
   // Step 3: tokens into place.
   if (warp < kCntWarps) {
-    int* row = rows + warp * nq;
     for (int j = k_lo; j < k_hi; j += 32) {
       const int i = j + lane;
       const bool ok = i < k_hi;
@@ -1187,11 +1193,12 @@ __global__ void __launch_bounds__(kBktThreads, 1)
       const uint32_t q = ok ? key >> tbits : 0xFFFFFFFFu;
       const uint32_t peers = __match_any_sync(0xffffffffu, q);
       int base = 0;
-      if (ok) base = row[q];
+      if (ok) base = static_cast<int>((row[qpad(static_cast<int>(q))] >> half) & 0xFFFFu);
       __syncwarp();
       if (ok) {
         tsorted[tbase + base + __popc(peers & lt_mask)] = static_cast<int32_t>(key & tmask);
-        if (lane == __ffs(peers) - 1) row[q] = base + __popc(peers);
+        if (lane == __ffs(peers) - 1)   // the other half belongs to warp w ^ 1
+          atomicAdd(&row[qpad(static_cast<int>(q))], static_cast<uint32_t>(__popc(peers)) << half);
       }
       __syncwarp();
     }
@@ -1474,7 +1481,10 @@ void set_count_smem_limit(void (*k)(const int64_t*, int, int64_t, int, int, int,
 // once (0 if none can), so that the grid runs in one wave.
 int cluster_sort_buckets(cudaError_t* err) {
   static std::atomic<uint64_t> configured{0};
-  static std::atomic<int> buckets{0};
+  static std::atomic<int> buckets[64];   // per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 0;
   if (device_pending(configured)) {
     for (auto k : {embed_sort_count_kernel<2, 1>, embed_sort_count_kernel<4, 1>, embed_sort_count_kernel<8, 1>,
                    embed_sort_count_kernel<16, 1>, embed_sort_count_kernel<1, kSortCluster>,
@@ -1497,10 +1507,10 @@ int cluster_sort_buckets(cudaError_t* err) {
       (void)cudaGetLastError();   // no clusters of this size: the one-CTA load stays
       n = 0;
     }
-    buckets.store(n * kSortCluster);
+    buckets[dev].store(n * kSortCluster);
     mark_device_done(configured);
   }
-  return buckets.load();
+  return buckets[dev].load();
 }
 
 // The clustered load pays off once every CTA would load more than 8192 ids
