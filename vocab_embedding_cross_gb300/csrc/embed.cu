@@ -10,7 +10,8 @@
 //
 // Backward (same page, paragraph 2: repeated tokens accumulate into the same
 // owned row): the valid (id, t) pairs are sorted stably by id (for T <= 16384
-// one CTA per SM sorts the ids with id mod NB equal to its index; otherwise one
+// one CTA per SM sorts the ids with id mod NB equal to its index, its CTAs
+// grouped in clusters that share the id loads above 8192 tokens; otherwise one
 // CTA sorts 64-bit keys), the tokens of each id are cut into runs of
 // kEmbedBwdChunk, each run is summed in fp32 in ascending t, run sums are
 // combined left to right, and the total is added once into the fp32 row. The
@@ -913,7 +914,8 @@ __device__ __forceinline__ void add_rows(const TE* __restrict__ dE, int64_t H, i
 // q = id / NB with one counting pass instead of radix passes. With nq values
 // of q, kCntWarps warps each own a contiguous share of the bucket's keys (in
 // token order) and a row of nq counters:
-//   1. each warp counts its keys per q (warp-aggregated by __match_any_sync);
+//   1. each warp counts its keys per q (shared-memory atomics; the rows of
+//      warps 2k and 2k+1 share 32-bit words, one 16-bit half each);
 //   2. per q, the rows become exclusive prefixes across the warps, and a block
 //      scan over q gives each q's first sorted position, the runs before it,
 //      the ids (non-empty q) before it and the multi-run ids before it;
