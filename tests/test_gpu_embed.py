@@ -152,7 +152,8 @@ def test_embed_bwd_gptoss_full_deterministic():
 
 
 @pytest.mark.parametrize("T,V_real,Vp", [(20000, 1000, 1024),      # more tokens than the shared-memory sorts hold
-                                         (5000, 1048000, 1048064)])  # too many id / NB values for the counting sort
+                                         (5000, 1048000, 1048064),   # too many id / NB values for the counting sort
+                                         (12000, 1048000, 1048064)])  # the same above 8192 tokens: no clustered sort
 def test_embed_bwd_workspace_sort_path(T, V_real, Vp):
     """The sorts other than the bucketed counting sort: the 64-bit workspace
     sort (T above 16384) and the bucketed radix sort (about 6900 values of
