@@ -899,7 +899,8 @@ __device__ __forceinline__ void add_rows(const TE* __restrict__ dE, int64_t H, i
   for (int k = 0; k < N; ++k) {
     const int t = __shfl_sync(0xffffffffu, my_t, (p + k) & 31);
     v[k] = make_uint4(0, 0, 0, 0);
-    if (active) v[k] = __ldg(reinterpret_cast<const uint4*>(dE + static_cast<int64_t>(t) * H + col));
+    // dE is read once: streaming loads (evict first) keep the L2 for the dW rows
+    if (active) v[k] = __ldcs(reinterpret_cast<const uint4*>(dE + static_cast<int64_t>(t) * H + col));
   }
 #pragma unroll
   for (int k = 0; k < N; ++k) {
@@ -1313,7 +1314,7 @@ __global__ void __launch_bounds__(128)
     float4 w[NQ];
     if (rd.slot < 0 && active) {   // single-run id: fetch the row now, add once the sum is ready
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) w[q] = row[q];
+      for (int q = 0; q < NQ; ++q) w[q] = __ldcg(row + q);   // at L2: the row is not read again here
     }
     float acc[VEC];
 #pragma unroll
