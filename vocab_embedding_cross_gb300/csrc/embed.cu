@@ -890,7 +890,7 @@ __device__ __forceinline__ void widen<float>(const uint4& v, float (&o)[4]) {
 // chunk), the N loads issued before the first add, the adds in token order.
 // Token t_j is lane j's my_t. Straight-line code for each N, so a short run
 // issues only its own loads and adds.
-template <int N, typename TE>
+template <int N, typename TE, bool STREAM>
 __device__ __forceinline__ void add_rows(const TE* __restrict__ dE, int64_t H, int col, int my_t, int p, bool active,
                                          float (&acc)[16 / sizeof(TE)]) {
   constexpr int VEC = 16 / sizeof(TE);
@@ -899,8 +899,10 @@ __device__ __forceinline__ void add_rows(const TE* __restrict__ dE, int64_t H, i
   for (int k = 0; k < N; ++k) {
     const int t = __shfl_sync(0xffffffffu, my_t, (p + k) & 31);
     v[k] = make_uint4(0, 0, 0, 0);
-    // dE is read once: streaming loads (evict first) keep the L2 for the dW rows
-    if (active) v[k] = __ldcs(reinterpret_cast<const uint4*>(dE + static_cast<int64_t>(t) * H + col));
+    // With one problem dE is read once: streaming loads (evict first) keep the
+    // L2 for the dW rows. The n-gram tables read dE once each, from L2.
+    const uint4* src = reinterpret_cast<const uint4*>(dE + static_cast<int64_t>(t) * H + col);
+    if (active) v[k] = STREAM ? __ldcs(src) : __ldg(src);
   }
 #pragma unroll
   for (int k = 0; k < N; ++k) {
@@ -1262,7 +1264,8 @@ struct EmbSlots {
   int n;
 };
 
-template <typename TE>
+// STREAM: dE is read once (one problem), with evict-first loads.
+template <typename TE, bool STREAM>
 __global__ void __launch_bounds__(128)
     embed_reduce_kernel(const __grid_constant__ EmbSlots sl, const TE* __restrict__ dE, int H, int nh,
                         uint32_t nh_magic, int cap) {
@@ -1321,14 +1324,14 @@ __global__ void __launch_bounds__(128)
     for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
     for (int p = 0; p < len; p += U) {   // tokens in ascending t, one add each
       switch (len - p < U ? len - p : U) {
-        case 1: add_rows<1>(dE, H, col, my_t, p, active, acc); break;
-        case 2: add_rows<2>(dE, H, col, my_t, p, active, acc); break;
-        case 3: add_rows<3>(dE, H, col, my_t, p, active, acc); break;
-        case 4: add_rows<4>(dE, H, col, my_t, p, active, acc); break;
-        case 5: add_rows<5>(dE, H, col, my_t, p, active, acc); break;
-        case 6: add_rows<6>(dE, H, col, my_t, p, active, acc); break;
-        case 7: add_rows<7>(dE, H, col, my_t, p, active, acc); break;
-        default: add_rows<U>(dE, H, col, my_t, p, active, acc); break;
+        case 1: add_rows<1, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+        case 2: add_rows<2, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+        case 3: add_rows<3, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+        case 4: add_rows<4, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+        case 5: add_rows<5, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+        case 6: add_rows<6, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+        case 7: add_rows<7, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+        default: add_rows<U, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
       }
     }
     if (rd.slot < 0) {
@@ -1629,14 +1632,16 @@ cudaError_t launch_reduce(const vce_problem& p, const EmbSlots& sl, const void* 
   const uint32_t nh_magic = (L.nh > 1 && max_items * static_cast<uint64_t>(L.nh) < (uint64_t(1) << 32))
                                 ? 0xFFFFFFFFu / static_cast<uint32_t>(L.nh) + 1u
                                 : 0u;
+  // One problem reads dE once; the n-gram tables read it once each.
+  const bool stream = sl.n == 1;
   cudaError_t e;
   if (p.dtype == VCE_BF16)
-    e = launch_dependent(embed_reduce_kernel<uint16_t>, dim3(grid), dim3(128), 0, st, sl,
-                         static_cast<const uint16_t*>(dE), static_cast<int>(p.H), L.nh, nh_magic,
-                         static_cast<int>(p.T));
+    e = launch_dependent(stream ? embed_reduce_kernel<uint16_t, true> : embed_reduce_kernel<uint16_t, false>,
+                         dim3(grid), dim3(128), 0, st, sl, static_cast<const uint16_t*>(dE), static_cast<int>(p.H),
+                         L.nh, nh_magic, static_cast<int>(p.T));
   else
-    e = launch_dependent(embed_reduce_kernel<float>, dim3(grid), dim3(128), 0, st, sl,
-                         static_cast<const float*>(dE), static_cast<int>(p.H), L.nh, nh_magic,
+    e = launch_dependent(stream ? embed_reduce_kernel<float, true> : embed_reduce_kernel<float, false>, dim3(grid),
+                         dim3(128), 0, st, sl, static_cast<const float*>(dE), static_cast<int>(p.H), L.nh, nh_magic,
                          static_cast<int>(p.T));
   note_launch(VCE_K_EMBED_REDUCE, st);
   return e;
