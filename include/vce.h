@@ -82,6 +82,10 @@ typedef enum vce_op {
  * embedding backward also needs T * ceil(H / (128 * 16 / sizeof(dtype))) < 2^31.
  * `flags` is 0 or a combination of the vce_flag bits below (other bits are
  * rejected with VCE_ERR_ARG).
+ * ignore_index must lie outside [0, V_real): a value that names a real class
+ * could not be told from a target of that class, so it is rejected with
+ * VCE_ERR_ARG. The loss ignores targets equal to it, and an id equal to it is
+ * the embedding's padding id (a zero row, no gradient).
  */
 typedef struct vce_problem {
   int64_t T;
@@ -331,12 +335,16 @@ vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const v
  * exits; a problem whose forward workspace (vce_workspace_size(p,
  * VCE_OP_LOSS_FWD)) is larger returns VCE_ERR_WORKSPACE before anything is
  * enqueued. No device memory is allocated by the call.
+ * It takes the same problems, flags and pointers as vce_loss_fwd and checks
+ * them by the same rules; on a refusal for size, vce_last_error() names the
+ * scratch the problem needs and the array's size.
  * The first call on a device looks up the array's device address for that
- * device (the device must be current); make that first call before any stream
- * capture. All calls share the one array: calls that may overlap on the GPU
- * (different streams without ordering, or different host threads) race on it
- * and must not be used. When dev_status is NULL the status word inside the
- * array is cleared at the start of each call.
+ * device (the device must be current) and keeps it; make that first call
+ * before any stream capture. A device reset after it is not supported (the
+ * kept address would be stale). All calls share the one array: calls that may
+ * overlap on the GPU (different streams without ordering, or different host
+ * threads) race on it and must not be used. When dev_status is NULL the status
+ * word inside the array is cleared at the start of each call.
  */
 vce_status vce_loss_fwd_noalloc(const vce_problem* p, const void* h, const void* W,
                                 const int64_t* targets, float* loss, float* lse,
@@ -348,7 +356,9 @@ size_t vce_loss_fwd_noalloc_max_scratch(void);
 const char* vce_status_str(vce_status s);
 
 /* Name and text of the CUDA error behind the calling thread's last
- * VCE_ERR_CUDA ("" if none); static storage, valid until the next call. */
+ * VCE_ERR_CUDA, or the reason for vce_loss_fwd_noalloc's last refusal for
+ * size ("" if none); thread-local storage, valid until the thread's next
+ * call. */
 const char* vce_last_error(void);
 
 /* The run length of the embedding backward's fixed summation order (tokens). */

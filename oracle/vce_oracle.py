@@ -32,7 +32,8 @@ Readings where the pages leave a step open (each is listed in the design notes):
   R1 shard k covers [floor(k*Vp/S), floor((k+1)*Vp/S)); uneven S is allowed.
   R2 a class is valid iff 0 <= v < V_real; padded rows may hold anything.
   R3 a target outside [0, V_real) that is not ignore_index is a data error; the
-     token is then treated as ignored (flagged in ``bad``).
+     token is then treated as ignored (flagged in ``bad``). The ignore value
+     itself lies outside [0, V_real): one naming a real class is refused.
   R4 loss = g * sum of per-token losses / N_valid; with N_valid == 0 the loss
      and every gradient are 0 (the pages are silent; torch would give NaN).
   R5 the upstream scale g multiplies the loss and the gradient.
@@ -171,6 +172,8 @@ def ownership(ids: np.ndarray, V_real: int, Vp: int, S: int):
 
 def target_status(targets: np.ndarray, V_real: int, ignore_index: int = IGNORE_INDEX):
     """(valid, bad) masks of the loss targets (P4 and readings R3)."""
+    if 0 <= ignore_index < V_real:
+        raise ValueError("ignore_index names a real class")
     y = np.asarray(targets, dtype=np.int64)
     valid = (y >= 0) & (y < V_real)
     bad = ~valid & (y != ignore_index)

@@ -325,6 +325,17 @@ def pin_ignored_and_bad(O):
     assert O.cross_entropy_forward(h, W, yn, 90)["loss"] == 0.0
     dHn, dWn = O.cross_entropy_backward(h, W, yn, 90, 128)
     assert not dHn.any() and not dWn.any()
+    # an ignore value naming a real class is refused; one past the real classes is not
+    for ig in (0, 89):
+        try:
+            O.cross_entropy_forward(h, W, y, 90, ignore_index=ig)
+        except ValueError:
+            pass
+        else:
+            raise AssertionError(f"ignore_index {ig} accepted")
+    y3 = y2.copy(); y3[5] = 90                      # 90 is the ignore value now; -100 is bad
+    r90 = O.cross_entropy_forward(h, W, y3, 90, ignore_index=90)
+    assert r90["n_valid"] == 9 and list(np.nonzero(r90["bad"])[0]) == [0, 7]
 
 
 # --------------------------------------------------------------------------
@@ -504,6 +515,42 @@ def pin_greedy_argmax(O):
         assert np.array_equal(a_s, arg)
 
 
+def pin_max_owner(O):
+    """max_owner against a head whose logits are known in closed form: with
+    orthonormal rows Q_v and h = sum_v a_v Q_v, the logit of class v is a_v, so
+    the owner of the largest one and the gap to the second largest are fixed
+    by the chosen a. Ties (two identical rows) go to the lowest column, hence
+    the lowest shard, with a gap of exactly 0; padded rows never count."""
+    rng = np.random.default_rng(95)
+    V, H, Vp, S = 48, 64, 64, 4                      # shards of 16 rows: [0,16), [16,32), [32,48), [48,64)
+    Q, _ = np.linalg.qr(rng.standard_normal((H, H)))
+    W = np.zeros((Vp, H))
+    W[:V] = Q[:V]
+    W[V:] = 8.0 * Q[V:]                              # padding rows: orthonormal directions with large logits
+    # (largest class, its logit, second class, its logit) per token
+    cases = [(3, 5.0, 40, 4.25), (20, 2.5, 21, 2.0), (47, 1.0, 0, -0.5), (33, 7.0, 17, 6.875)]
+    a = np.full((len(cases), Vp), -3.0)
+    a[:, V:] = 9.0                                   # padded classes hold the largest coefficients
+    for t, (c1, v1, c2, v2) in enumerate(cases):
+        a[t, c1], a[t, c2] = v1, v2
+    h = a @ Q                                        # z_tv = a_tv for every v
+    own, gap = O.max_owner(h, W, V, Vp, S)
+    assert list(own) == [0, 1, 2, 2]
+    want = [v1 - v2 for (_, v1, _, v2) in cases]
+    assert np.allclose(gap, want, rtol=0, atol=1e-12), (gap, want)
+    # identical rows 5 and 37 (shards 0 and 2): the lowest column's shard, gap 0
+    W2 = W.copy()
+    W2[37] = W2[5]
+    h2 = 6.0 * W2[5][None, :]
+    own2, gap2 = O.max_owner(h2, W2, V, Vp, S)
+    assert list(own2) == [0] and gap2[0] == 0.0
+    # the same rows moved so that the tie spans shards 1 and 3's real part
+    W3 = W.copy()
+    W3[45] = W3[18]
+    own3, gap3 = O.max_owner(4.0 * W3[18][None, :], W3, V, Vp, S)
+    assert list(own3) == [1] and gap3[0] == 0.0
+
+
 def pin_ngram_hash(O):
     """The n-gram row index: hand-worked in base 10, sequence starts, invalid
     ids, and base-V digits recovered exactly when M = V^n."""
@@ -575,6 +622,6 @@ ALL_PINS = [
     pin_equal_logits, pin_normalisation, pin_padded_head_demo, pin_bruteforce_decimal,
     pin_torch_cross_entropy, pin_shard_invariance, pin_ignored_and_bad,
     pin_finite_differences, pin_gradient_invariants, pin_sampled_candidates,
-    pin_sampled_full_set_is_full_softmax, pin_oth_head, pin_greedy_argmax, pin_ngram_hash,
+    pin_sampled_full_set_is_full_softmax, pin_oth_head, pin_greedy_argmax, pin_max_owner, pin_ngram_hash,
     pin_ngram_embedding,
 ]

@@ -60,6 +60,8 @@ def P(**kw):
     (dict(dtype=7), vce.VCE_ERR_UNSUPPORTED),
     (dict(T=1 << 31), vce.VCE_ERR_UNSUPPORTED),
     (dict(T=(1 << 31) - 1, Vp=1 << 30, V_real=1 << 30), vce.VCE_ERR_UNSUPPORTED),   # 2^41 work items
+    (dict(ignore_index=0), vce.VCE_ERR_ARG),     # the ignore value names a real class
+    (dict(ignore_index=999), vce.VCE_ERR_ARG),
     (dict(flags=4), vce.VCE_ERR_ARG),            # no such flag
     (dict(flags=1 << 20), vce.VCE_ERR_ARG),
 ])
@@ -154,3 +156,33 @@ def test_sampled_candidates_rejected_on_host(L):
                 None) == vce.VCE_ERR_WORKSPACE
     assert call(ctypes.byref(p), fake, fake, 10, 100, fake, fake, fake, None, ws_need, None,
                 None) == vce.VCE_ERR_WORKSPACE
+
+
+def test_ignore_value_outside_the_real_classes_accepted(L):
+    """-100, V_real and any value past the padded vocabulary are all usable
+    ignore values: only one naming a real class is refused."""
+    for ig in (-100, -1, 1000, 1023, 5000):
+        assert vce.vce_workspace_size(P(ignore_index=ig), vce.VCE_OP_LOSS_FWD) != vce.SIZE_MAX
+
+
+def test_noalloc_checks_like_the_workspace_forward(L):
+    """The allocation-free forward applies vce_loss_fwd's argument rules: the
+    same problems are refused with the same codes, and the bf16-dH flag that a
+    caller may share between forward and backward is accepted by both."""
+    import ctypes
+    fake = 1 << 20   # never dereferenced: every case below fails validation first
+    for kw, code in ((dict(Vp=1000), vce.VCE_ERR_ARG), (dict(flags=4), vce.VCE_ERR_ARG),
+                     (dict(ignore_index=0), vce.VCE_ERR_ARG), (dict(H=4), vce.VCE_ERR_UNSUPPORTED),
+                     (dict(T=(1 << 31) - 1, Vp=1 << 30, V_real=1 << 30), vce.VCE_ERR_UNSUPPORTED)):
+        p = P(**kw)
+        a = L.vce_loss_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, None, None, None, fake, 1 << 30, None,
+                           None)
+        b = L.vce_loss_fwd_noalloc(ctypes.byref(p), fake, fake, fake, fake, fake, None, None, None, None, None)
+        assert a == b == code, (kw, a, b)
+    # the flags vce_loss_fwd accepts pass the noalloc check too: the call gets as
+    # far as the alignment check of h (8-byte aligned here, 16 needed)
+    for flags in (vce.VCE_FLAG_DH_BF16, vce.VCE_FLAG_ACCUMULATE_DH | vce.VCE_FLAG_DH_BF16):
+        p = P(flags=flags)
+        assert L.vce_loss_fwd_noalloc(ctypes.byref(p), fake + 8, fake, fake, fake, fake, None, None, None, None,
+                                      None) == vce.VCE_ERR_UNSUPPORTED
+        assert vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD) != vce.SIZE_MAX

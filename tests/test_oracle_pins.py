@@ -97,6 +97,18 @@ MUTATIONS = {
     # target positions off by one in the candidate list
     "sampled_pos_shift": ("    pos[valid] = np.searchsorted(uniq, y[valid])",
                           "    pos[valid] = np.searchsorted(uniq, y[valid], side='right')"),
+    # max_owner: the gap taken the wrong way round
+    "max_owner_gap_sign": ("    return owner, top2[:, 1] - top2[:, 0]", "    return owner, top2[:, 0] - top2[:, 1]"),
+    # max_owner: the gap to the third largest logit instead of the second
+    "max_owner_gap_third": ("np.sort(z, axis=1)[:, -2:]", "np.sort(z, axis=1)[:, -3:-1]"),
+    # max_owner: ties go to the highest column
+    "max_owner_ties_high": ("    arg = z.argmax(axis=1)\n    top2",
+                            "    arg = z.shape[1] - 1 - z[:, ::-1].argmax(axis=1)\n    top2"),
+    # max_owner over the padded classes too
+    "max_owner_padded": ("    z = logits(h, W, V_real)\n    arg = z.argmax(axis=1)\n",
+                         "    z = logits(h, W, W.shape[0])\n    arg = z.argmax(axis=1)\n"),
+    # an ignore value inside the real classes accepted
+    "ignore_index_unchecked": ("    if 0 <= ignore_index < V_real:\n        raise", "    if False:\n        raise"),
     # target logit taken from the wrong shard offset
     "target_local_off": ("z_tgt[t] = blocks[owner[t]][t, local[t]]",
                          "z_tgt[t] = blocks[owner[t]][t, max(local[t] - 1, 0)]"),

@@ -76,5 +76,26 @@ def test_noalloc_rejects_problems_larger_than_its_scratch():
     with pytest.raises(R.vce.VceError) as e:
         R.vce.vce_loss_fwd_noalloc(p, h, W, y, out["loss"], out["lse"])
     assert e.value.status == R.vce.VCE_ERR_WORKSPACE
+    # the refusal says why: the scratch this problem needs and the array's size
+    why = R.vce.lib().vce_last_error().decode()
+    need = R.vce.vce_workspace_size(p, R.vce.VCE_OP_LOSS_FWD)
+    assert "vce_loss_fwd_noalloc" in why and str(need) in why and str(cap) in why, why
     torch.cuda.synchronize()
     assert torch.isnan(out["loss"]).all().item()     # nothing was enqueued
+
+
+def test_noalloc_accepts_the_bf16_dh_flag():
+    """A problem that carries VCE_FLAG_DH_BF16 for its backward runs through
+    both forwards unchanged (the flag concerns the backward only)."""
+    wl = I.custom(T=200, H=128, V_real=900, Vp=960, S=4, dtype="bf16", seed=44)
+    d = I.make_all(wl, ("W", "h", "targets"))
+    p = R.prob(wl, flags=R.vce.VCE_FLAG_DH_BF16)
+    h, W = D.to_device(d["h"]), D.to_device(d["W"])
+    y = torch.from_numpy(d["targets"]).cuda()
+    a, b = _outputs(wl.T), _outputs(wl.T)
+    ws = D.workspace(R.vce.vce_workspace_size(p, R.vce.VCE_OP_LOSS_FWD))
+    R.vce.vce_loss_fwd(p, h, W, y, a["loss"], a["lse"], ws=ws, dev_status=a["st"])
+    R.vce.vce_loss_fwd_noalloc(p, h, W, y, b["loss"], b["lse"], dev_status=b["st"])
+    torch.cuda.synchronize()
+    assert int(a["st"].item()) == int(b["st"].item()) == 0
+    assert torch.equal(a["loss"], b["loss"]) and torch.equal(a["lse"], b["lse"])

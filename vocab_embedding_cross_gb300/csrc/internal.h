@@ -75,6 +75,23 @@ inline ProbDev prob_dev(const vce_problem& p) {
                  static_cast<int32_t>(p.V_real), p.S, p.ignore_index};
 }
 
+// Host-side argument rules shared by every entry point that takes a problem
+// (shapes, flags, dtype, the ignore value, 32-bit work-item numbering).
+vce_status check_problem(const vce_problem* p);
+// VCE_OK, or VCE_ERR_CUDA with the error's name and text kept for
+// vce_last_error (the sticky error is cleared).
+vce_status cuda_status(cudaError_t e);
+// Returns `s` and keeps `why` as the calling thread's vce_last_error text.
+vce_status refuse(vce_status s, const char* why);
+
+// Workspace of the loss forward: status word, per-(token, unit) partials,
+// target logits and the mean's block sums, each 256-byte aligned.
+struct FwdLayout {
+  size_t status, part, ztgt, block_sums, total;
+  UnitGrid ug;
+};
+FwdLayout fwd_layout(const vce_problem& p);
+
 struct DevInfo {
   int device = -1;
   int num_sms = 0;

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <mutex>
 
 #include "internal.h"
@@ -28,8 +29,9 @@ std::mutex g_mu;
 void* g_scratch_ptr[64] = {};
 
 // Device address of the scratch array for the current device. In host code the
-// array's name only stands for the symbol; its device address must be asked
-// for, once per device, with that device current.
+// array's name only stands for the symbol; its device address is asked for
+// once per device, with that device current, and kept. A device reset after
+// that first call would leave the kept address stale; that is not supported.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -46,27 +48,6 @@ cudaError_t scratch_address(void** out) {
   return cudaSuccess;
 }
 
-struct Layout {
-  size_t status, part, ztgt, block_sums, total;
-  UnitGrid ug;
-};
-Layout layout(const vce_problem& p) {
-  Layout L{};
-  L.ug = unit_grid(p, p.dtype == VCE_BF16 ? tc_unit_width(p) : kSimtUnitWidth);
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    size_t o = off;
-    off = align_up(off + bytes, kWsAlign);
-    return o;
-  };
-  L.status = take(16);
-  L.part = take(sizeof(float2) * static_cast<size_t>(p.T) * L.ug.n_units);
-  L.ztgt = take(sizeof(float) * static_cast<size_t>(p.T));
-  L.block_sums = take(sizeof(float) * 2 * static_cast<size_t>(merge_blocks(p.T)));
-  L.total = off;
-  return L;
-}
-
 bool aligned_to(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 }  // namespace
@@ -81,35 +62,32 @@ size_t vce_loss_fwd_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
 vce_status vce_loss_fwd_noalloc(const vce_problem* p, const void* h, const void* W, const int64_t* targets,
                                 float* loss, float* lse, float* token_loss, int32_t* target_owner,
                                 int32_t* max_owner, int32_t* dev_status, void* stream) {
-  // Same argument rules as vce_loss_fwd.
-  if (!p || (p->flags & ~VCE_FLAG_ACCUMULATE_DH) != 0) return VCE_ERR_ARG;
-  if (p->dtype != VCE_F32 && p->dtype != VCE_BF16) return VCE_ERR_UNSUPPORTED;
-  if (p->T < 0 || p->H < 1 || p->V_real < 1 || p->S < 1 || p->Vp < 64 || p->Vp % 64 != 0 ||
-      p->V_real > p->Vp || p->S > p->Vp || (p->tied_weights != 0 && p->tied_weights != 1))
-    return VCE_ERR_ARG;
-  if (p->T >= (int64_t(1) << 31) || p->Vp >= (int64_t(1) << 31) || p->H > 65536 ||
-      (p->H * (p->dtype == VCE_BF16 ? 2 : 4)) % 16 != 0)
-    return VCE_ERR_UNSUPPORTED;
+  // The argument rules and the scratch layout are vce_loss_fwd's own.
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
   if (!loss) return VCE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (p->T > 0) {
-    if (!h || !W || !targets || !lse) return VCE_ERR_ARG;
-    if (!aligned_to(h, 16) || !aligned_to(W, 16) || !aligned_to(targets, 8) || !aligned_to(loss, 4) ||
-        !aligned_to(lse, 4) || !aligned_to(token_loss, 4) || !aligned_to(target_owner, 4) ||
-        !aligned_to(max_owner, 4))
-      return VCE_ERR_UNSUPPORTED;
-    const Layout L = layout(*p);
-    if (L.total > kNoAllocScratchBytes) return VCE_ERR_WORKSPACE;   // problem too large for the fixed scratch
+  if (p->T == 0) return cuda_status(cudaMemsetAsync(loss, 0, sizeof(float), st));
+  if (!h || !W || !targets || !lse) return VCE_ERR_ARG;
+  if (!aligned_to(h, 16) || !aligned_to(W, 16) || !aligned_to(targets, 8) || !aligned_to(loss, 4) ||
+      !aligned_to(lse, 4) || !aligned_to(token_loss, 4) || !aligned_to(target_owner, 4) ||
+      !aligned_to(max_owner, 4))
+    return VCE_ERR_UNSUPPORTED;
+  const FwdLayout L = fwd_layout(*p);
+  if (L.total > kNoAllocScratchBytes) {   // problem too large for the fixed scratch: nothing is enqueued
+    char why[160];
+    snprintf(why, sizeof(why),
+             "vce_loss_fwd_noalloc: the forward needs %zu bytes of scratch, more than the fixed %zu-byte array",
+             L.total, kNoAllocScratchBytes);
+    return refuse(VCE_ERR_WORKSPACE, why);
   }
   void* base = nullptr;
-  if (scratch_address(&base) != cudaSuccess) return VCE_ERR_CUDA;
-  if (p->T == 0) return cudaMemsetAsync(loss, 0, sizeof(float), st) == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
-  const Layout L = layout(*p);
+  if (cudaError_t e = scratch_address(&base)) return cuda_status(e);
   char* b = static_cast<char*>(base);
   int32_t* status = dev_status;
   if (!status) {   // the shared status word must start at zero on every call
     status = reinterpret_cast<int32_t*>(b + L.status);
-    if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return VCE_ERR_CUDA;
+    if (cudaError_t me = cudaMemsetAsync(status, 0, sizeof(int32_t), st)) return cuda_status(me);
   }
   float2* part = reinterpret_cast<float2*>(b + L.part);
   float* ztgt = reinterpret_cast<float*>(b + L.ztgt);
@@ -121,10 +99,9 @@ vce_status vce_loss_fwd_noalloc(const vce_problem* p, const void* h, const void*
   else
     e = launch_simt_fwd(pd, L.ug, static_cast<const float*>(h), static_cast<const float*>(W), targets, part, ztgt,
                         st);
-  if (e != cudaSuccess) return VCE_ERR_CUDA;
-  e = launch_merge(pd, L.ug, targets, part, ztgt, lse, token_loss, target_owner, max_owner, bsum, loss, status,
-                   st);
-  return e == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(
+      launch_merge(pd, L.ug, targets, part, ztgt, lse, token_loss, target_owner, max_owner, bsum, loss, status, st));
 }
 
 }  // extern "C"

@@ -94,8 +94,10 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int 
 }
 
 namespace {
-
 int esize_of(const vce_problem& p) { return p.dtype == VCE_BF16 ? 2 : 4; }
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+thread_local char g_last_err[256] = "";
+}  // namespace
 
 vce_status check_problem(const vce_problem* p) {
   if (!p) return VCE_ERR_ARG;
@@ -105,6 +107,9 @@ vce_status check_problem(const vce_problem* p) {
   if (p->Vp < 64 || p->Vp % 64 != 0) return VCE_ERR_ARG;   // the padded vocabulary must be 64-aligned
   if (p->V_real > p->Vp || p->S > p->Vp) return VCE_ERR_ARG;
   if (p->tied_weights != 0 && p->tied_weights != 1) return VCE_ERR_ARG;
+  // The ignore value must not name a real class: a target equal to it could
+  // then not be told from a target of that class.
+  if (p->ignore_index >= 0 && p->ignore_index < p->V_real) return VCE_ERR_ARG;
   if (p->T >= (int64_t(1) << 31) || p->Vp >= (int64_t(1) << 31) || p->H > 65536) return VCE_ERR_UNSUPPORTED;
   if ((p->H * esize_of(*p)) % 16 != 0) return VCE_ERR_UNSUPPORTED;
   // Work items of the tensor-core kernels ((token block, unit or column block)
@@ -113,9 +118,6 @@ vce_status check_problem(const vce_problem* p) {
   return VCE_OK;
 }
 
-bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
-
-thread_local char g_last_err[256] = "";
 vce_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return VCE_OK;
   snprintf(g_last_err, sizeof(g_last_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
@@ -123,11 +125,11 @@ vce_status cuda_status(cudaError_t e) {
   return VCE_ERR_CUDA;
 }
 
-// ----- workspace layouts -----
-struct FwdLayout {
-  size_t status, part, ztgt, block_sums, total;
-  UnitGrid ug;
-};
+vce_status refuse(vce_status s, const char* why) {
+  snprintf(g_last_err, sizeof(g_last_err), "%s", why);
+  return s;
+}
+
 FwdLayout fwd_layout(const vce_problem& p) {
   FwdLayout L{};
   L.ug = unit_grid(p, p.dtype == VCE_BF16 ? tc_unit_width(p) : kSimtUnitWidth);
@@ -144,6 +146,8 @@ FwdLayout fwd_layout(const vce_problem& p) {
   L.total = off;
   return L;
 }
+
+namespace {
 
 // Greedy argmax: one (max, column) pair per (token, unit).
 size_t argmax_ws_bytes(const vce_problem& p) {
