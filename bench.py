@@ -28,11 +28,31 @@ sys.path.insert(0, ROOT)
 METRIC = "fused vocab-CE fwd+bwd tokens/s & % BF16 TC peak; embed gather/bwd GB/s vs HBM"
 WORKLOAD = "qwen3_tied"
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# roofline kernel on this workload, from one ncu capture of that kernel (its
-# summary is kept under profiles/). A change to the kernel makes the figure
-# stale: it must then be removed (the line reports null) or taken again.
-MEASURED_TRAFFIC = {("qwen3_tied", "tc_grad"): 1684623744}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the loss path's
+# tensor-core launches in one step of a workload, from one ncu capture whose
+# summary is kept under profiles/. `source` is the sha256 prefix of the
+# tensor-core kernel's source file that the capture ran: once that file has
+# changed the figure is stale, and the line reports null until it is retaken.
+MEASURED_TRAFFIC = {
+    "qwen3_tied": {"bytes_per_step": 16378760960,
+                   "per_kernel": {"tc_fwd": 814285056, "tc_grad": 3369247488, "tc_dh": 5398940672,
+                                  "tc_dw": 6796287744},
+                   "source": "aa524c94a4261308",
+                   "profile": "profiles/tc_loss_kernel_qwen3_T8192_dram.md"},
+}
+TC_SOURCE = os.path.join(ROOT, "vocab_embedding_cross_gb300", "csrc", "loss_tc.cu")
+
+
+def measured_traffic(workload: str):
+    """The captured loss-path traffic of `workload` if it belongs to the
+    tensor-core kernel as it is now, else None."""
+    import hashlib
+    rec = MEASURED_TRAFFIC.get(workload)
+    if rec is None:
+        return None
+    with open(TC_SOURCE, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec if sha == rec["source"] else None
 
 
 def load_peaks():
@@ -236,27 +256,46 @@ def run_ours(args):
         per_kind[k] = (tot + dt, n + 1)
     per_kind = {k: (tot / reps, n // reps) for k, (tot, n) in per_kind.items()}
 
-    # ---- roofline ----
+    # ---- roofline: the loss path, credited 6*T*H*V_real FLOP ----
+    # The headline fraction is the credited work of the loss forward and
+    # backward (2*T*H*V_real each for the logits, dH and dW; the backward's
+    # recompute of the logits is not credited) over the summed per-launch
+    # times of the loss path's kernels, against the measured burst bf16 rate.
+    # Each tensor-core mode's executed rate (2*T*H*V_real per step) is kept
+    # beside it.
     peaks, peak_src = load_peaks()
     dh_part = 0 if args.no_dh_split else 8 * (-(-T // 256) * 256) * H * 4
     vc = min((ws_b_bytes - 256 - dh_part) // (T * 2), -(-V // 256) * 256)
-    flops = {"tc_fwd": 2.0 * T * H * V, "tc_grad": 2.0 * T * H * V, "tc_dh": 2.0 * T * H * V,
-             "tc_dw": 2.0 * T * H * V}
-    loss_kinds = ["tc_fwd", "tc_grad", "tc_dh", "tc_dw", "dh_reduce", "merge", "loss_mean", "count_valid"]
+    tc_kinds = ["tc_fwd", "tc_grad", "tc_dh", "tc_dw"]
+    loss_kinds = tc_kinds + ["dh_reduce", "merge", "loss_mean", "count_valid"]
     loss_ms = sum(per_kind.get(k, (0.0, 0))[0] for k in loss_kinds)
-    dom = max((k for k in flops if k in per_kind), key=lambda k: per_kind[k][0], default=None)
+    credited_flops = 6.0 * T * H * V
     roofline = None
-    if dom is not None:
-        t_ms, n = per_kind[dom]
-        achieved = flops[dom] / (t_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        traffic = MEASURED_TRAFFIC.get((args.workload, dom)) if not (args.bwd_cols or args.no_dh_split) else None
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                    "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-                    "launches_per_step": n, "ms_per_step": round(t_ms, 4),
-                    "peak_kind": f"bf16_tflops_sustained ({peak_src})"}
-    credited = 6.0 * T * H * V
+    if loss_ms > 0:
+        achieved = credited_flops / (loss_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        tr = measured_traffic(args.workload) if not (args.bwd_cols or args.no_dh_split) else None
+        per_tc = {}
+        for k in tc_kinds:
+            if k in per_kind:
+                tf = 2.0 * T * H * V / (per_kind[k][0] / 1e3) / 1e12
+                per_tc[k] = {"ms_per_step": round(per_kind[k][0], 4), "launches_per_step": per_kind[k][1],
+                             "executed_TFLOPs": round(tf, 1), "frac_of_burst": round(tf / peak, 4),
+                             "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
+        roofline = {"bound": "tensor", "kernel": "loss path: tc_loss_kernel FWD, GRAD, DH, DW and the merge, "
+                                                "mean, valid-count and dH-part kernels",
+                    "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4),
+                    "traffic": tr["bytes_per_step"] if tr else None,
+                    "traffic_unit": "bytes per step of the loss path's tensor-core launches "
+                                    "(ncu dram__bytes_read.sum + dram__bytes_write.sum)",
+                    "traffic_source": (f"{tr['profile']} (tensor-core source sha256 {tr['source']})" if tr
+                                       else "stale or not captured for this configuration"),
+                    "credited_flops_per_step": credited_flops, "ms_per_step": round(loss_ms, 4),
+                    "peak_kind": f"bf16_tflops burst ({peak_src})",
+                    "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                    "per_kernel_executed": per_tc}
+    credited = credited_flops
     loss_tflops = credited / (loss_ms / 1e3) / 1e12 if loss_ms else None
     valid = (d["ids"] >= 0) & (d["ids"] < V)
     U = int(np.unique(d["ids"][valid]).size)
@@ -277,6 +316,9 @@ def run_ours(args):
     for k in ("gather", "bwd"):
         if f"{k}_GBps" in emb:
             emb[f"{k}_frac"] = round(emb[f"{k}_GBps"] / peaks["hbm_gbs"], 4)
+
+    # ---- the head backward in its tied (+=) form at this size ----
+    tied_flag = run_tied_flag(args, vce, p, p_head, h, W, y, lse, dH, dW, ws_b, stream)
 
     # ---- end to end through the C ABI with host buffers ----
     e2e = run_e2e(args, vce, D, d, p, p_head, W, E, loss, lse, dH, dW, st, ws_f, ws_b, ws_e, stream, wl)
@@ -322,6 +364,9 @@ def run_ours(args):
         # a 64-token sample of the GPT-2-like head
         cpu["one_thread"] = {w: cpu_baseline(args, sample_tokens=n, threads=1, workload=w)
                              for w, n in (("tiny_f32", 64), ("gpt2_head", 64))}
+        # every core, per operation, on the other loss configurations
+        cpu["configs"] = {w: cpu_baseline(args, sample_tokens=n, workload=w)
+                          for w, n in (("tiny_f32", 64), ("gpt2_head", 128), ("gptoss_embed", 128))}
 
     if rank == 0:
         line = {
@@ -337,6 +382,7 @@ def run_ours(args):
                              "frac_of_sustained": round(loss_tflops / peaks["bf16_tflops_sustained"], 4)
                              if loss_tflops else None,
                              "executed_flops": 8.0 * T * H * V, "vc": int(vc)},
+            "head_bwd_tied_flag": tied_flag,
             "embedding": emb,
             "sampled_softmax": sampled,
             "embedding_gptoss": emb_gptoss,
@@ -356,6 +402,37 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_tied_flag(args, vce, p, p_head, h, W, y, lse, dH, dW, ws_b, stream):
+    """vce_loss_bwd with tied_weights = 1 (dW += G^T h, a TMA reduce-add into
+    the fp32 gradient) against the overwrite form the step uses (the head's
+    dW written, then the embedding's rows added), on the main workload. A
+    caller of the tied form zeroes dW once per step; that fill is timed too."""
+    import torch
+    sp = stream.cuda_stream
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def timed(fn, n):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    n = max(3, args.steps // 4)
+    ow = timed(lambda: vce.vce_loss_bwd(p_head, h, W, y, lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp), n)
+    acc = timed(lambda: vce.vce_loss_bwd(p, h, W, y, lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp), n)
+    zero = timed(lambda: dW.zero_(), n)
+    assert int(st.item()) == 0, vce.status_str(int(st.item()))
+    return {"overwrite_ms": round(ow, 4), "accumulate_ms": round(acc, 4), "dW_zero_ms": round(zero, 4),
+            "calls": n}
 
 
 def run_greedy(args, vce, D, p, h, W, stream, T, H, V, peaks):
@@ -779,24 +856,31 @@ def oracle_child(args):
     n = min(args.cpu_sample, wl.T)
     # a bounded sample of the workload: the first n tokens, full vocabulary and hidden size
     h, y, ids, dE = d["h"][:n], d["targets"][:n], d["ids"][:n], d["dE"][:n]
-    def one_step():
-        O.embed_forward(ids, d["W"], wl.V_real)
-        O.cross_entropy_forward(h, d["W"], y, wl.V_real)
-        dH, dWh = O.cross_entropy_backward(h, d["W"], y, wl.V_real, wl.Vp)
-        dWe = O.embed_backward(ids, dE, wl.V_real, wl.Vp)
-        return dWh + dWe
+    ops = {
+        "embed_fwd": lambda: O.embed_forward(ids, d["W"], wl.V_real),
+        "loss_fwd": lambda: O.cross_entropy_forward(h, d["W"], y, wl.V_real),
+        "loss_bwd": lambda: O.cross_entropy_backward(h, d["W"], y, wl.V_real, wl.Vp),
+        "embed_bwd": lambda: O.embed_backward(ids, dE, wl.V_real, wl.Vp),
+    }
 
     for _ in range(max(0, args.warmup)):
-        one_step()
+        for fn in ops.values():
+            fn()
     steps = max(1, args.steps)
-    t0 = time.perf_counter()
+    per_op = {k: 0.0 for k in ops}
     for _ in range(steps):
-        one_step()
-    t = (time.perf_counter() - t0) / steps
+        for k, fn in ops.items():   # one step: the four calls in the path's order, each timed
+            t0 = time.perf_counter()
+            fn()
+            per_op[k] += time.perf_counter() - t0
+    per_op = {k: v / steps for k, v in per_op.items()}
+    t = sum(per_op.values())
     print(json.dumps({"value": round(n / t, 3), "unit": "tokens/s", "kind": "oracle",
                       "sample": f"first {n} of {wl.T} tokens of {args.workload}, full V={wl.V_real} and "
                                 f"H={wl.H}; embed fwd + loss fwd + loss bwd + embed bwd in fp64 numpy",
-                      "seconds": round(t, 3), "steps": steps}))
+                      "seconds": round(t, 3), "steps": steps,
+                      "per_op": {k: {"seconds": round(v, 4), "tokens_per_s": round(n / v, 3) if v > 0 else None}
+                                 for k, v in per_op.items()}}))
 
 
 def run_reference(args):

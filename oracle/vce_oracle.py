@@ -559,4 +559,4 @@ def _as_f64(x: np.ndarray) -> np.ndarray:
     x = np.asarray(x)
     if x.dtype == np.uint16:
         return (x.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
-    return x.astype(np.float64)
+    return x.astype(np.float64, copy=False)

@@ -1,8 +1,8 @@
 """Small, self-contained invocations of the library for a profiler.
 
-    python -m vocab_embedding_cross_gb300.profile_case loss    [--workload NAME] [--tokens T] [--iters N]
-    python -m vocab_embedding_cross_gb300.profile_case embed   [--workload NAME] [--iters N]
-    python -m vocab_embedding_cross_gb300.profile_case sampled [--tokens T] [--iters N]
+    python profile_case.py loss    [--workload NAME] [--tokens T] [--iters N]
+    python profile_case.py embed   [--workload NAME] [--iters N]
+    python profile_case.py sampled [--tokens T] [--iters N]
 
 `loss` runs the loss forward and backward on a named workload's shapes
 (default the Qwen3-like H=2048, V=151936, S=8, tied dW), with T tokens or the
@@ -15,13 +15,16 @@ only pointed at a command that has already run cleanly.
 from __future__ import annotations
 
 import argparse
+import os
 import sys
 
 import torch
 
-from . import _lib as vce
-from . import device as D
-from . import inputs as I
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+from vocab_embedding_cross_gb300 import _lib as vce  # noqa: E402
+from vocab_embedding_cross_gb300 import device as D  # noqa: E402
+from vocab_embedding_cross_gb300 import inputs as I  # noqa: E402
 
 
 def _loss(args):

@@ -167,60 +167,120 @@ def test_loss_gpt2_head_full():
 
 
 def _oracle_rows_all(h, W, y, V_real, rows=1024):
-    """The oracle's per-token quantities for every token, a block of rows at a time."""
+    """The oracle's per-token quantities for every token, a block of rows at a
+    time (h and W widened to fp64 once)."""
+    hf, Wf = O._as_f64(h), O._as_f64(W)
     lse = np.empty(h.shape[0])
     tl = np.empty(h.shape[0])
     for i in range(0, h.shape[0], rows):
-        r = O.cross_entropy_rows(h[i:i + rows], W, y[i:i + rows], V_real)
+        r = O.cross_entropy_rows(hf[i:i + rows], Wf, y[i:i + rows], V_real)
         lse[i:i + rows] = r["lse"]
         tl[i:i + rows] = r["token_loss"]
     return lse, tl
 
 
-def _full_size_check(wl, with_dw_rows):
-    d = I.make_all(wl, ("W", "h", "targets"))
+def _check_sampled_rows(wl, d, out, dH, tol, rng):
+    """lse, token losses and dH on a sample of tokens (first and last included)."""
     h, W, y = d["h"], d["W"], d["targets"]
-    h_d, W_d = D.to_device(h), D.to_device(W)
-    out = R.loss_fwd(wl, h_d, W_d, y)
-    assert out["status"] == 0
-    tol = TOL["bf16"]
-    rng = np.random.default_rng(0)
     sample = np.unique(np.concatenate([rng.choice(wl.T, 48, replace=False), [0, wl.T - 1]]))
     r = O.cross_entropy_rows(h[sample], W, y[sample], wl.V_real)
     assert np.all(np.abs(out["lse"][sample] - r["lse"]) <= tol["lse"] * np.abs(r["lse"]))
     assert R.max_abs_rel(out["token_loss"][sample], r["token_loss"]) <= tol["loss"]
     nv = O.n_valid(y, wl.V_real)
-    dW = torch.zeros((wl.Vp, wl.H), dtype=torch.float32, device="cuda")
-    dH, dW, st = R.loss_bwd(wl, h_d, W_d, out["targets_d"], out["lse_d"], dW=dW)
-    assert st == 0
     ref_dH = O.hidden_gradient_rows(h[sample], W, y[sample], wl.V_real, 1.0 / nv)
     assert R.max_abs_rel(dH.cpu().numpy()[sample], ref_dH) <= tol["grad"]
-    if with_dw_rows:
-        t0 = time.time()
-        lse_all, tl_all = _oracle_rows_all(h, W, y, wl.V_real)
-        assert R.rel(out["loss"], tl_all.sum() / nv) <= tol["loss"]
-        assert np.all(np.abs(out["lse"] - lse_all) <= tol["lse"] * np.abs(lse_all))
-        # sampled rows of dW_head: most frequent targets, random classes, the last class
-        valid = (y >= 0) & (y < wl.V_real)
-        counts = np.bincount(y[valid], minlength=wl.V_real)
-        vs = np.unique(np.concatenate([np.argsort(-counts)[:8], rng.choice(wl.V_real, 8, replace=False),
-                                       [wl.V_real - 1]]))
-        ref_rows = O.head_gradient_rows(h, W, y, wl.V_real, lse_all, 1.0 / nv, vs)
-        got_rows = dW.index_select(0, torch.from_numpy(vs).cuda()).cpu().numpy()
-        assert R.max_abs_rel(got_rows, ref_rows) <= tol["grad"]
-        print(f"oracle over the full batch: {time.time() - t0:.1f}s")
-    # properties at any size: finite, padded rows zero
-    assert torch.isfinite(dW).all().item() and torch.isfinite(dH).all().item()
-    assert int((dW[wl.V_real:] != 0).sum().item()) == 0
 
 
-def test_loss_qwen3_full():
-    """T=8192, H=2048, V_real=151936, S=8, Zipf next-token targets: sampled lse,
-    token losses and dH rows; the exact loss, every lse and sampled dW rows
-    from the oracle's full-batch lse."""
-    _full_size_check(I.WORKLOADS["qwen3_tied"], with_dw_rows=True)
+def _head_rows(wl, y, rng, n_top=16, n_rand=8):
+    """Rows of dW to compare: the most frequent target classes (the Zipf head),
+    random classes and the last real class."""
+    valid = (y >= 0) & (y < wl.V_real)
+    counts = np.bincount(y[valid], minlength=wl.V_real)
+    return np.unique(np.concatenate([np.argsort(-counts, kind="stable")[:n_top],
+                                     rng.choice(wl.V_real, n_rand, replace=False), [wl.V_real - 1]]))
+
+
+def _check_full_batch(wl, d, out, dW_head_rows, vs, tol):
+    """The exact loss scalar, every lse, and the head's dW rows vs from the
+    oracle's full-batch lse. Returns the oracle's head rows."""
+    h, W, y = d["h"], d["W"], d["targets"]
+    t0 = time.time()
+    lse_all, tl_all = _oracle_rows_all(h, W, y, wl.V_real)
+    nv = O.n_valid(y, wl.V_real)
+    assert R.rel(out["loss"], tl_all.sum() / nv) <= tol["loss"]
+    assert np.all(np.abs(out["lse"] - lse_all) <= tol["lse"] * np.abs(lse_all))
+    assert R.max_abs_rel(out["token_loss"], tl_all) <= tol["loss"]
+    ref_rows = O.head_gradient_rows(O._as_f64(h), O._as_f64(W), y, wl.V_real, lse_all, 1.0 / nv, vs)
+    assert R.max_abs_rel(dW_head_rows, ref_rows) <= tol["grad"]
+    print(f"oracle over the full batch: {time.time() - t0:.1f}s")
+    return ref_rows
 
 
 def test_loss_gptoss_full():
-    """T=16384, H=3072, V_real=201088, S=8: sampled lse, token losses, dH rows."""
-    _full_size_check(I.WORKLOADS["gptoss_embed"], with_dw_rows=False)
+    """T=16384, H=3072, V_real=201088, S=8, Zipf next-token targets, untied:
+    sampled lse, token losses and dH rows; then the loss scalar, every lse and
+    every token loss, and dW rows of the most frequent, random and last
+    classes, all from the oracle's full-batch lse."""
+    wl = I.WORKLOADS["gptoss_embed"]
+    d = I.make_all(wl, ("W", "h", "targets"))
+    h_d, W_d = D.to_device(d["h"]), D.to_device(d["W"])
+    out = R.loss_fwd(wl, h_d, W_d, d["targets"])
+    assert out["status"] == 0
+    tol = TOL["bf16"]
+    rng = np.random.default_rng(0)
+    dW = torch.full((wl.Vp, wl.H), float("nan"), dtype=torch.float32, device="cuda")
+    dH, dW, st = R.loss_bwd(wl, h_d, W_d, out["targets_d"], out["lse_d"], dW=dW)
+    assert st == 0
+    _check_sampled_rows(wl, d, out, dH, tol, rng)
+    vs = _head_rows(wl, d["targets"], rng)
+    got = dW.index_select(0, torch.from_numpy(vs).cuda()).cpu().numpy()
+    _check_full_batch(wl, d, out, got, vs, tol)
+    # properties at any size: finite everywhere
+    assert torch.isfinite(dW).all().item() and torch.isfinite(dH).all().item()
+
+
+def test_qwen3_tied_pipeline_full():
+    """The Qwen3-like tied step at full size (T=8192, H=2048, V=151936, S=8),
+    run as one pipeline on one W and one fp32 dW, with the tied flag set:
+    embedding lookup of the input ids, loss forward, loss backward adding the
+    head's gradient into dW, embedding backward adding the input gradient into
+    the same dW ("Vocabulary shards", paragraph 2: one logical parameter, all
+    contributions combined). Checked against the oracle: the lookup bit for
+    bit; the loss scalar, every lse and every token loss; the head's dW rows of
+    the most frequent (Zipf head) ids, random ids and the last id; the
+    embedding's contribution to every touched row; and the combined rows."""
+    wl = I.WORKLOADS["qwen3_tied"]
+    assert wl.tied
+    d = I.make_all(wl)
+    h, W, y, ids, dE = d["h"], d["W"], d["targets"], d["ids"], d["dE"]
+    tol = TOL["bf16"]
+    rng = np.random.default_rng(1)
+    W_d, h_d, dE_d = D.to_device(W), D.to_device(h), D.to_device(dE)
+    # 1. lookup
+    E = R.embed_fwd(wl, W_d, ids, maps=False)["E"]
+    assert np.array_equal(E, O.embed_forward(ids, W, wl.V_real))
+    # 2. loss forward
+    out = R.loss_fwd(wl, h_d, W_d, y)
+    assert out["status"] == 0
+    # 3. loss backward with tied_weights = 1: dW += G^T h into a zeroed gradient
+    dW = torch.zeros((wl.Vp, wl.H), dtype=torch.float32, device="cuda")
+    dH, dW, st = R.loss_bwd(wl, h_d, W_d, out["targets_d"], out["lse_d"], dW=dW)
+    assert st == 0
+    vs = np.unique(np.concatenate([_head_rows(wl, y, rng), _head_rows(wl, ids, rng, n_rand=0)]))
+    vs_d = torch.from_numpy(vs).cuda()
+    head_rows = dW.index_select(0, vs_d).cpu().numpy()
+    touched = np.unique(ids[(ids >= 0) & (ids < wl.V_real)])
+    touched_d = torch.from_numpy(touched).cuda()
+    head_touched = dW.index_select(0, touched_d).double()
+    # 4. embedding backward into the same dW
+    assert R.embed_bwd(wl, ids, dE_d, dW) == 0
+    _check_sampled_rows(wl, d, out, dH, tol, rng)
+    ref_head = _check_full_batch(wl, d, out, head_rows, vs, tol)
+    ref_embed = O.embed_backward(ids, dE, wl.V_real, wl.Vp)
+    # the embedding's contribution on every touched row: fp32 run sums against fp64
+    got_embed = (dW.index_select(0, touched_d).double() - head_touched).cpu().numpy()
+    assert R.max_abs_rel(got_embed, ref_embed[touched]) <= 1e-5
+    # the combined tied gradient on the compared rows
+    final_rows = dW.index_select(0, vs_d).cpu().numpy()
+    assert R.max_abs_rel(final_rows, ref_head + ref_embed[vs]) <= tol["grad"]
+    assert torch.isfinite(dW).all().item() and torch.isfinite(dH).all().item()
