@@ -239,14 +239,16 @@ def run_ours(args):
     ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
     value = whole_job_tokens_per_s(T, world, ms)
 
-    # ---- per-launch timing (separate pass, events after every launch) ----
-    # A spin kernel first holds the stream so that every launch below is queued
-    # before the GPU reaches it: the intervals then contain no host gaps.
+    # ---- per-launch timing: K more steps, right after the timed ones ----
+    # Events after every launch. The pass follows the timed steps with no
+    # pause, so that the kernels run in the same power-capped state (a cooled
+    # GPU runs the first steps at a higher clock). A short spin kernel first
+    # holds the stream so that the first launches are queued before the GPU
+    # reaches them; later launches are queued far ahead of the GPU anyway.
     cap = 8192
     per_kind = {}
-    reps = max(3, min(args.steps, 10))
-    torch.cuda.synchronize()
-    torch.cuda._sleep(200_000_000)
+    reps = args.steps
+    torch.cuda._sleep(2_000_000)
     vce.vce_profile_begin(cap, stream=sp)
     for _ in range(reps):
         step_ops()
@@ -376,6 +378,8 @@ def run_ours(args):
             "data": "synthetic (seeded; Zipf(1.1) token ids, RMS-normalised h, W ~ N(0, 0.02^2))",
             "config": arm_config(args.workload, world),
             "roofline": roofline,
+            "per_launch_sum_ms": round(sum(v[0] for v in per_kind.values()), 4),
+            "step_credited_frac_of_burst": round(credited / (ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
             "loss_fwd_bwd": {"ms": round(loss_ms, 4), "credited_flops": credited,
                              "credited_TFLOPs": round(loss_tflops, 1) if loss_tflops else None,
                              "frac_of_burst": round(loss_tflops / peaks["bf16_tflops"], 4) if loss_tflops else None,

@@ -398,6 +398,9 @@ vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* strea
  * launches recorded (at most `capacity`, -1 on error). Launches on one stream
  * run back to back, so each interval is that launch's duration including its
  * launch gap. Process-wide; not for concurrent callers.
+ * VCE_K_LOSS_MEAN and VCE_K_DH_REDUCE keep their numbers but are no longer
+ * launched (the merge's last block takes the mean; the dH K parts are added
+ * inside the DH kernel); VCE_K_COUNT_VALID is launched by the fp32 path only.
  */
 typedef enum vce_kernel_kind {
   VCE_K_EMBED_GATHER = 0, VCE_K_EMBED_SORT = 1, VCE_K_EMBED_REDUCE = 2,

@@ -84,8 +84,9 @@ vce_status cuda_status(cudaError_t e);
 // Returns `s` and keeps `why` as the calling thread's vce_last_error text.
 vce_status refuse(vce_status s, const char* why);
 
-// Workspace of the loss forward: status word, per-(token, unit) partials,
-// target logits and the mean's block sums, each 256-byte aligned.
+// Workspace of the loss forward: status word (and, 4 bytes on, the merge's
+// last-block counter), per-(token, unit) partials, target logits and the
+// mean's block sums, each 256-byte aligned.
 struct FwdLayout {
   size_t status, part, ztgt, block_sums, total;
   UnitGrid ug;
@@ -138,10 +139,12 @@ cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const voi
 cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* ids, float* const* dW,
                                    void* const* ws, int n, const void* dE, cudaStream_t st);
 
-// Merge of the forward partials into lse, per-token loss and the mean.
+// Merge of the forward partials into lse, per-token loss and the mean. The
+// forward kernel before it zeroes `counter` (the merge's last-block counter).
 cudaError_t launch_merge(const ProbDev& pd, const UnitGrid& ug, const int64_t* targets, const float2* part,
                          const float* ztgt, float* lse, float* token_loss, int32_t* target_owner,
-                         int32_t* max_owner, float* block_sums, float* loss, int32_t* status, cudaStream_t st);
+                         int32_t* max_owner, float* block_sums, int32_t* counter, float* loss, int32_t* status,
+                         cudaStream_t st);
 int merge_blocks(int64_t T);
 cudaError_t launch_count_valid(const ProbDev& pd, const int64_t* targets, int32_t* n_valid, int32_t* status,
                                cudaStream_t st);
@@ -154,7 +157,7 @@ cudaError_t launch_argmax_merge(const ProbDev& pd, const UnitGrid& ug, const flo
 
 // fp32 SIMT path.
 cudaError_t launch_simt_fwd(const ProbDev& pd, const UnitGrid& ug, const float* h, const float* W,
-                            const int64_t* targets, float2* part, float* ztgt, cudaStream_t st);
+                            const int64_t* targets, float2* part, float* ztgt, int32_t* merge_ctr, cudaStream_t st);
 cudaError_t launch_simt_argmax(const ProbDev& pd, const UnitGrid& ug, const float* h, const float* W, float2* part,
                                cudaStream_t st);
 cudaError_t launch_simt_grad(const ProbDev& pd, const float* h, const float* W, const int64_t* targets,
@@ -167,13 +170,14 @@ cudaError_t launch_sgemm(int M, int N, int K, const float* A, int64_t sam, int64
 
 // bf16 tensor-core path.
 cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* h, const void* W,
-                          const int64_t* targets, float2* part, float* ztgt, int32_t* status, cudaStream_t st);
+                          const int64_t* targets, float2* part, float* ztgt, int32_t* merge_ctr, int32_t* status,
+                          cudaStream_t st);
 cudaError_t launch_tc_argmax(const vce_problem& p, const UnitGrid& ug, const void* h, const void* W, float2* part,
                              int32_t* status, cudaStream_t st);
 cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void* W, const int64_t* targets,
-                                const float* lse, const int32_t* n_valid, float g, int v0, int vc_act,
+                                const float* lse, float g, int v0, int vc_act,
                                 void* G, int g_ld, float* dH, bool dH_accumulate, float* dW, bool dW_accumulate,
-                                float* dh_part, int dh_parts, int32_t* status, cudaStream_t st);
+                                int32_t* dh_flags, int dh_parts, int32_t* status, cudaStream_t st);
 // Number of K parts for the dH GEMM of one column chunk (fills the waves of
 // the persistent grid); at most kMaxDhParts.
 constexpr int kMaxDhParts = 8;

@@ -70,8 +70,9 @@ __device__ __forceinline__ float hsum16(float v) {
 __global__ void __launch_bounds__(256) simt_fwd_kernel(ProbDev pd, UnitGrid ug, const float* __restrict__ h,
                                                        const float* __restrict__ W,
                                                        const int64_t* __restrict__ targets, float2* __restrict__ part,
-                                                       float* __restrict__ ztgt) {
+                                                       float* __restrict__ ztgt, int32_t* merge_ctr) {
   __shared__ float hs[TK][TM + 4];
+  if (merge_ctr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *merge_ctr = 0;   // for the merge after it
   __shared__ float ws[TK][TN + 4];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int m0 = blockIdx.x * TM;
@@ -292,9 +293,9 @@ __global__ void __launch_bounds__(256) sgemm_kernel(int M, int N, int K, const f
 }  // namespace
 
 cudaError_t launch_simt_fwd(const ProbDev& pd, const UnitGrid& ug, const float* h, const float* W,
-                            const int64_t* targets, float2* part, float* ztgt, cudaStream_t st) {
+                            const int64_t* targets, float2* part, float* ztgt, int32_t* merge_ctr, cudaStream_t st) {
   dim3 grid(static_cast<unsigned>(ceil_div(pd.T, TM)), static_cast<unsigned>(ug.n_units));
-  simt_fwd_kernel<<<grid, 256, 0, st>>>(pd, ug, h, W, targets, part, ztgt);
+  simt_fwd_kernel<<<grid, 256, 0, st>>>(pd, ug, h, W, targets, part, ztgt, merge_ctr);
   note_launch(VCE_K_SIMT_FWD, st);
   return cudaGetLastError();
 }

@@ -86,7 +86,6 @@ struct TcArgs {
   float2* part;
   float* ztgt;
   const float* lse;
-  const int32_t* n_valid;
   float g;
   int v0;
   int vc;
@@ -94,11 +93,14 @@ struct TcArgs {
   int accumulate;
   int ksplit;    // DH: the K range (vocabulary columns) is cut into ksplit parts
   int kb_per;    // DH: K blocks per part
-  int t_pad;     // DH with ksplit > 1: rows per partial buffer
+  int32_t* dh_flags;   // DH with ksplit > 1: per (tile, CTA, epilogue warp), parts added so far;
+                       // GRAD zeroes them for the DH launch that follows it
+  int n_dh_flags;
   int gm;        // FWD, ARGMAX, GRAD: token blocks per item group (see item_mc)
   int n_cols;    // FWD, ARGMAX: units; GRAD: column blocks
   int32_t* status;
   uint64_t limit_ns;
+  int32_t* merge_ctr;   // FWD: the merge's block counter, zeroed here for the merge that follows
 };
 
 // Items of the forward-like modes and of GRAD are (token block m, column
@@ -258,6 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* comb_empty = comb_full + 4;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(comb_empty + 4);
   int* s_abort = reinterpret_cast<int*>(s_tmem + 1);
+  int* s_cnt = reinterpret_cast<int*>(tail + 216);   // GRAD: the epilogue warps' valid-target counts
   float4* comb = reinterpret_cast<float4*>(tail + 256);   // [4 quarters][32 lanes], forward only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -296,6 +299,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // Launched as a dependent launch: barriers and TMEM are set up while the
   // previous kernel drains; nothing in global memory is touched before it ends.
   grid_dep_wait();
+  if constexpr (MODE == MODE_FWD) {
+    if (a.merge_ctr && blockIdx.x == 0 && threadIdx.x == 0) *a.merge_ctr = 0;
+  }
+  if constexpr (MODE == MODE_GRAD) {   // the next DH launch's part counters start at zero
+    for (int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); i < a.n_dh_flags;
+         i += static_cast<int>(gridDim.x * blockDim.x))
+      a.dh_flags[i] = 0;
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -427,7 +438,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     float scale = 0.0f;
     if constexpr (MODE == MODE_GRAD) {
-      const int nv = a.n_valid[0];
+      // N_valid, the mean's denominator: the epilogue warps of every CTA count
+      // the valid targets themselves (T int64 reads from L2) while the first
+      // tile's MMAs run, so no separate counting launch precedes the backward.
+      int cnt = 0;
+      bool bad = false;
+      constexpr int kStep = 32 * kEpiWarps;
+      // eight independent loads in flight per thread, then their tests
+      for (int t0 = static_cast<int>(threadIdx.x) - 64; t0 < a.pd.T; t0 += 8 * kStep) {
+        int64_t y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) y[j] = t0 + j * kStep < a.pd.T ? __ldg(a.targets + t0 + j * kStep) : a.pd.ignore_index;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const bool v = (y[j] >= 0) && (y[j] < a.pd.V_real);
+          cnt += v ? 1 : 0;
+          bad |= !v && y[j] != a.pd.ignore_index;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      bad = __any_sync(0xffffffffu, bad);
+      if (lane == 0) s_cnt[e] = cnt;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");   // the epilogue warps only
+      int nv = 0;
+#pragma unroll
+      for (int w = 0; w < kEpiWarps; ++w) nv += s_cnt[w];
+      if (bad && lane == 0 && blockIdx.x == 0) record_status(a.status, VCE_ERR_BAD_INDEX);
       scale = nv > 0 ? a.g / static_cast<float>(nv) : 0.0f;
     }
     auto release = [&](uint32_t acc) {
@@ -436,6 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
     };
     // One 32-row x 128-byte TMA store (or reduce-add) from this warp's staging box.
+    bool add_out = MODE != MODE_GRAD && a.accumulate;
     auto store_box = [&](const uint32_t (&w)[32], int col, int row) {
       if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
@@ -443,7 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        if (MODE != MODE_GRAD && a.accumulate)
+        if (add_out)
           tma_reduce_add_2d(&mapOut, my_staging, col, row);
         else
           tma_store_2d(&mapOut, my_staging, col, row);
@@ -638,7 +676,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ++items_done;
       } else {
-        int m_blk, n_blk, row0, col0;
+        int m_blk, n_blk, row0, col0, part = 0;
         if constexpr (MODE == MODE_GRAD) {
           const MC mc = item_mc(item, a.gm, a.n_mblk, a.n_cols);
           m_blk = mc.m;
@@ -648,8 +686,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else {
           n_blk = item % a.n_nblk;
           m_blk = (item / a.n_nblk) % a.n_mblk;
-          const int part = (item / a.n_nblk) / a.n_mblk;   // DH: partial buffer of this K part
-          row0 = (MODE == MODE_DW ? a.out_row0 : part * a.t_pad) + m_blk * BMP + static_cast<int>(rank) * BM;
+          part = (item / a.n_nblk) / a.n_mblk;   // DH: this item's K part
+          row0 = (MODE == MODE_DW ? a.out_row0 : 0) + m_blk * BMP + static_cast<int>(rank) * BM;
           col0 = n_blk * BN + half * 128;
         }
         const int orow = row0 + q * 32;
@@ -659,6 +697,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        int32_t* flag = nullptr;
+        if constexpr (MODE == MODE_DH) {
+          // K parts of one tile are added into dH one after the other, in part
+          // order, so the sum dH (+)= P0 + P1 + ... is the same at every run.
+          // Parts are numbered part-major, so part k - 1 of this tile ran a
+          // wave earlier and its count is normally there already.
+          if (a.ksplit > 1) {
+            flag = a.dh_flags + ((m_blk * a.n_nblk + n_blk) * 2 + static_cast<int>(rank)) * kEpiWarps + e;
+            if (part > 0 && !flag_wait_ge(flag, part, lane, wc)) {
+              ok = false;
+              break;
+            }
+          }
+          add_out = a.accumulate || part > 0;
+        }
         const uint32_t ta = lane_base + acc * BN;
         if constexpr (MODE == MODE_GRAD) {
           const int t = m_blk * BMP + static_cast<int>(rank) * BM + r;
@@ -716,6 +769,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           reg_fence(xb);
           release(acc);
           store_box(xb, col0 + 96, orow);
+          if (MODE == MODE_DH && flag && part + 1 < a.ksplit) {
+            // This part's additions are complete in global memory before the
+            // next part may add on top of them.
+            if (lane == 0) {
+              bulk_wait<0>();
+              fence_proxy_async_global();
+              flag_release(flag, part + 1);
+            }
+            __syncwarp();
+          }
         }
         ++tile_count;
       }
@@ -817,25 +880,6 @@ int tc_group_mblk(const vce_problem& p) {
   return static_cast<int>(ceil_div(n_mblk, groups));
 }
 
-// dH = (accumulate ? dH : 0) + P[0] + P[1] + ... in this order (deterministic).
-__global__ void __launch_bounds__(256) dh_reduce_kernel(const float4* __restrict__ P, int nparts, int64_t part_stride4,
-                                                        float4* __restrict__ dH, int64_t n4, int accumulate) {
-  grid_dep_launch();
-  grid_dep_wait();
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float4 s = accumulate ? dH[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < nparts; ++k) {
-      const float4 v = __ldcs(P + k * part_stride4 + i);
-      s.x = s.x + v.x;
-      s.y = s.y + v.y;
-      s.z = s.z + v.z;
-      s.w = s.w + v.w;
-    }
-    dH[i] = s;
-  }
-}
-
 }  // namespace
 
 int tc_unit_width(const vce_problem& p) {
@@ -910,7 +954,8 @@ int tc_dh_parts(const vce_problem& p, int vc_act) {
 }
 
 cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* h, const void* W,
-                          const int64_t* targets, float2* part, float* ztgt, int32_t* status, cudaStream_t st) {
+                          const int64_t* targets, float2* part, float* ztgt, int32_t* merge_ctr, int32_t* status,
+                          cudaStream_t st) {
   CUtensorMap mh, mw;
   if (!make_tmap_2d(&mh, h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, p.T, p.H, 64, BM, true) ||
       !make_tmap_2d(&mw, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, p.V_real, p.H, 64, BNH, true))
@@ -924,6 +969,7 @@ cudaError_t launch_tc_fwd(const vce_problem& p, const UnitGrid& ug, const void* 
   a.ug = ug;
   a.part = part;
   a.ztgt = ztgt;
+  a.merge_ctr = merge_ctr;
   return launch_mode<MODE_FWD>(mh, mw, mh, a, st);
 }
 
@@ -945,9 +991,11 @@ cudaError_t launch_tc_argmax(const vce_problem& p, const UnitGrid& ug, const voi
 }
 
 cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void* W, const int64_t* targets,
-                                const float* lse, const int32_t* n_valid, float g, int v0, int vc_act, void* G,
+                                const float* lse, float g, int v0, int vc_act, void* G,
                                 int g_ld, float* dH, bool dH_accumulate, float* dW, bool dW_accumulate,
-                                float* dh_part, int dh_parts, int32_t* status, cudaStream_t st) {
+                                int32_t* dh_flags, int dh_parts, int32_t* status, cudaStream_t st) {
+  const int parts = dh_flags ? dh_parts : 1;
+  const int n_flags = static_cast<int>(ceil_div(p.T, BMP) * ceil_div(p.H, BN)) * 2 * kEpiWarps;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   cudaError_t e;
@@ -966,25 +1014,21 @@ cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void*
     a.n_cols = a.n_nblk;
     a.num_kb = static_cast<int>(ceil_div(p.H, BK));
     a.lse = lse;
-    a.n_valid = n_valid;
     a.g = g;
     a.v0 = v0;
     a.vc = vc_act;
+    a.dh_flags = parts > 1 ? dh_flags : nullptr;
+    a.n_dh_flags = parts > 1 ? n_flags : 0;
     if ((e = launch_mode<MODE_GRAD>(mh, mw, mg, a, st)) != cudaSuccess) return e;
   }
   // DH: dH (+)= G[:, 0:vc_act] W[v0:v0+vc_act, :]. With dh_parts > 1 the K
-  // range is cut into parts that write fp32 partials (row blocks of t_pad rows
-  // in dh_part), added to dH in part order by dh_reduce_kernel.
+  // range is cut into parts; each part's tile is added into dH after the part
+  // before it (counters in dh_flags), so the order of the additions is fixed.
   {
-    const int parts = dh_part ? dh_parts : 1;
-    const int t_pad = static_cast<int>(ceil_div(p.T, BMP) * BMP);
     CUtensorMap mg, mw, mo;
-    const bool ok_out = parts > 1
-                            ? make_tmap_2d(&mo, dh_part, F32, 4, p.H, static_cast<uint64_t>(parts) * t_pad, p.H, 32,
-                                           32, true)
-                            : make_tmap_2d(&mo, dH, F32, 4, p.H, p.T, p.H, 32, 32, true);
     if (!make_tmap_2d(&mg, G, BF, 2, vc_act, p.T, g_ld, 64, BM, true) ||
-        !make_tmap_2d(&mw, W, BF, 2, p.H, p.V_real, p.H, 64, 64, true) || !ok_out)
+        !make_tmap_2d(&mw, W, BF, 2, p.H, p.V_real, p.H, 64, 64, true) ||
+        !make_tmap_2d(&mo, dH, F32, 4, p.H, p.T, p.H, 32, 32, true))
       return cudaErrorInvalidValue;
     TcArgs a = base_args(p, targets, status);
     a.n_mblk = static_cast<int>(ceil_div(p.T, BMP));
@@ -992,21 +1036,12 @@ cudaError_t launch_tc_bwd_chunk(const vce_problem& p, const void* h, const void*
     a.num_kb = static_cast<int>(ceil_div(vc_act, BK));
     a.ksplit = parts;
     a.kb_per = static_cast<int>(ceil_div(a.num_kb, parts));
-    a.t_pad = t_pad;
+    a.dh_flags = parts > 1 ? dh_flags : nullptr;
+    a.n_dh_flags = parts > 1 ? n_flags : 0;
     a.n_items = a.n_mblk * parts * a.n_nblk;
     a.v0 = v0;
-    a.accumulate = (parts == 1 && dH_accumulate) ? 1 : 0;
+    a.accumulate = dH_accumulate ? 1 : 0;
     if ((e = launch_mode<MODE_DH>(mg, mw, mo, a, st)) != cudaSuccess) return e;
-    if (parts > 1) {
-      const int64_t n4 = p.T * p.H / 4;
-      const int64_t stride4 = static_cast<int64_t>(t_pad) * p.H / 4;
-      const DevInfo di = current_device_info();
-      e = launch_dependent(dh_reduce_kernel, dim3(di.num_sms * 8), dim3(256), 0, st,
-                           reinterpret_cast<const float4*>(dh_part), parts, stride4, reinterpret_cast<float4*>(dH), n4,
-                           dH_accumulate ? 1 : 0);
-      note_launch(VCE_K_DH_REDUCE, st);
-      if (e != cudaSuccess) return e;
-    }
   }
   // DW: dW[v0:v0+vc_act, :] (+)= G[:, 0:vc_act]^T h
   {

@@ -10,7 +10,8 @@
 // which equals the page's "subtract the global maximum, sum, combine" schedule
 // (paragraph 4: fused implementations may use other reduction schedules).
 // The loss is then averaged once over the valid tokens ("Sequence-parallel
-// normalization", paragraph 3) with a fixed-order, deterministic reduction.
+// normalization", paragraph 3) with a fixed-order, deterministic reduction,
+// by the last merge block to finish.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -39,13 +40,20 @@ __device__ __forceinline__ void combine(float& m, float& s, float m2, float s2) 
   }
 }
 
+// The last block to finish (an atomic counter, zeroed by the forward kernel
+// before this one) also takes the mean: the block partials are added in block
+// order, each thread a contiguous range in double, then a fixed tree, so the
+// result does not depend on which block comes last.
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_kernel(ProbDev pd, UnitGrid ug, const int64_t* __restrict__ targets, const float2* __restrict__ part,
                  const float* __restrict__ ztgt, float* __restrict__ lse, float* __restrict__ token_loss,
-                 int32_t* __restrict__ target_owner, int32_t* __restrict__ max_owner, float* __restrict__ block_sums,
-                 int32_t* status) {
+                 int32_t* __restrict__ target_owner, int32_t* __restrict__ max_owner, float* block_sums,
+                 int32_t* counter, float* __restrict__ loss, int32_t* status) {
   __shared__ float sh_loss[kMergeWarps];
   __shared__ int sh_cnt[kMergeWarps];
+  __shared__ double sh_a[kMergeWarps * 32];
+  __shared__ long long sh_c[kMergeWarps * 32];
+  __shared__ int s_last;
   grid_dep_launch();   // launched as a dependent launch: wait for the kernel before
   grid_dep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -112,30 +120,27 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     }
     block_sums[2 * blockIdx.x] = a;
     block_sums[2 * blockIdx.x + 1] = __int_as_float(c);
+    __threadfence();
+    s_last = atomicAdd(counter, 1) == static_cast<int>(gridDim.x) - 1 ? 1 : 0;
   }
-}
-
-// One block: sum of the block partials in block order, then the mean.
-__global__ void __launch_bounds__(1024) loss_mean_kernel(const float* __restrict__ block_sums, int nblocks,
-                                                         float* __restrict__ loss) {
-  grid_dep_launch();   // launched as a dependent launch: wait for the kernel before
-  grid_dep_wait();
-  __shared__ double sh_a[1024];
-  __shared__ long long sh_c[1024];
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  constexpr int kT = kMergeWarps * 32;
+  const int nblocks = static_cast<int>(gridDim.x);
+  const int per = (nblocks + kT - 1) / kT;
+  const int b0 = static_cast<int>(threadIdx.x) * per;
   double a = 0.0;
   long long c = 0;
-  // contiguous block ranges per thread, then a fixed tree: deterministic
-  const int per = (nblocks + 1023) / 1024;
-  const int b0 = threadIdx.x * per;
   for (int b = b0; b < min(nblocks, b0 + per); ++b) {
-    a += static_cast<double>(block_sums[2 * b]);
-    c += __float_as_int(block_sums[2 * b + 1]);
+    a += static_cast<double>(__ldcg(block_sums + 2 * b));
+    c += __float_as_int(__ldcg(block_sums + 2 * b + 1));
   }
   sh_a[threadIdx.x] = a;
   sh_c[threadIdx.x] = c;
   __syncthreads();
-  for (int o = 512; o > 0; o >>= 1) {
-    if (threadIdx.x < o) {
+  for (int o = kT / 2; o > 0; o >>= 1) {
+    if (static_cast<int>(threadIdx.x) < o) {
       sh_a[threadIdx.x] += sh_a[threadIdx.x + o];
       sh_c[threadIdx.x] += sh_c[threadIdx.x + o];
     }
@@ -257,14 +262,13 @@ cudaError_t launch_argmax_merge(const ProbDev& pd, const UnitGrid& ug, const flo
 
 cudaError_t launch_merge(const ProbDev& pd, const UnitGrid& ug, const int64_t* targets, const float2* part,
                          const float* ztgt, float* lse, float* token_loss, int32_t* target_owner,
-                         int32_t* max_owner, float* block_sums, float* loss, int32_t* status, cudaStream_t st) {
+                         int32_t* max_owner, float* block_sums, int32_t* counter, float* loss, int32_t* status,
+                         cudaStream_t st) {
   const int nb = merge_blocks(pd.T);
-  cudaError_t e = launch_dependent(merge_kernel, dim3(nb), dim3(kMergeWarps * 32), 0, st, pd, ug, targets, part, ztgt,
-                                   lse, token_loss, target_owner, max_owner, block_sums, status);
+  const cudaError_t e = launch_dependent(merge_kernel, dim3(nb), dim3(kMergeWarps * 32), 0, st, pd, ug, targets, part,
+                                         ztgt, lse, token_loss, target_owner, max_owner, block_sums, counter, loss,
+                                         status);
   note_launch(VCE_K_MERGE, st);
-  if (e != cudaSuccess) return e;
-  e = launch_dependent(loss_mean_kernel, dim3(1), dim3(1024), 0, st, static_cast<const float*>(block_sums), nb, loss);
-  note_launch(VCE_K_LOSS_MEAN, st);
   return e;
 }
 

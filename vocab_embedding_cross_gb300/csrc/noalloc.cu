@@ -92,16 +92,17 @@ vce_status vce_loss_fwd_noalloc(const vce_problem* p, const void* h, const void*
   float2* part = reinterpret_cast<float2*>(b + L.part);
   float* ztgt = reinterpret_cast<float*>(b + L.ztgt);
   float* bsum = reinterpret_cast<float*>(b + L.block_sums);
+  int32_t* merge_ctr = reinterpret_cast<int32_t*>(b + L.status + 4);
   const ProbDev pd = prob_dev(*p);
   cudaError_t e;
   if (p->dtype == VCE_BF16)
-    e = launch_tc_fwd(*p, L.ug, h, W, targets, part, ztgt, status, st);
+    e = launch_tc_fwd(*p, L.ug, h, W, targets, part, ztgt, merge_ctr, status, st);
   else
     e = launch_simt_fwd(pd, L.ug, static_cast<const float*>(h), static_cast<const float*>(W), targets, part, ztgt,
-                        st);
+                        merge_ctr, st);
   if (e != cudaSuccess) return cuda_status(e);
-  return cuda_status(
-      launch_merge(pd, L.ug, targets, part, ztgt, lse, token_loss, target_owner, max_owner, bsum, loss, status, st));
+  return cuda_status(launch_merge(pd, L.ug, targets, part, ztgt, lse, token_loss, target_owner, max_owner, bsum,
+                                  merge_ctr, loss, status, st));
 }
 
 }  // extern "C"

@@ -62,7 +62,7 @@ __device__ __forceinline__ void record_status(int* status, int code) {
 // Wait for the phase with parity `parity` of `bar` to complete. Returns false
 // (and raises the CTA's abort flag, and records VCE_ERR_TIMEOUT = 5) when the
 // wait runs past limit_ns, or when another role of the CTA has aborted.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -76,6 +76,39 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Wai
       }
     }
   }
+}
+
+// Called by a whole warp: lane 0 waits until the counter at `p` (written by
+// another CTA of the same grid with flag_release) is at least `target`. Bounded
+// like mbar_wait: false (abort flag raised, VCE_ERR_TIMEOUT recorded) when the
+// wait runs past limit_ns or another role of the CTA has aborted.
+static __device__ __noinline__ bool flag_wait_ge(const int32_t* p, int target, int lane, const WaitCtx& w) {
+  int ok = 1;
+  if (lane == 0) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v < target) {
+      const uint64_t t0 = globaltimer_ns();
+      for (uint32_t it = 1;; ++it) {
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) break;
+        if ((it & 63u) == 0u) {
+          if (*w.abort) {
+            ok = 0;
+            break;
+          }
+          if (globaltimer_ns() - t0 > w.limit_ns) {
+            *w.abort = 1;
+            record_status(w.status, 5);
+            ok = 0;
+            break;
+          }
+        }
+      }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // the TMA operations that follow see it
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -117,6 +150,23 @@ __device__ __forceinline__ void bulk_wait() {
 // Generic-proxy writes to shared memory become visible to the async proxy (TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Orders global-memory accesses of the async proxy (TMA) and of the generic
+// proxy made by this thread.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Counters in global memory shared between CTAs of one grid
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void flag_release(int32_t* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -248,7 +298,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 // Bounded wait with cluster-scope acquire (arrivals may come from the peer CTA).
-__device__ __noinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+static __device__ __noinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {

@@ -183,12 +183,12 @@ int64_t bwd_recommended_cols(const vce_problem& p) {
   int64_t vc = ceil_div(ceil_div(cols, passes), 256) * 256;
   return vc > cols ? cols : vc;
 }
-// fp32 partials of the dH GEMM's K parts (bf16 path): kMaxDhParts buffers of
-// T rounded up to 256 rows.
-size_t dh_part_bytes(const vce_problem& p) {
+// Counters of the dH GEMM's K parts (bf16 path): one per (256 x 256 tile of
+// dH, CTA of the pair, epilogue warp).
+size_t dh_flag_bytes(const vce_problem& p) {
   if (p.dtype != VCE_BF16 || p.T == 0) return 0;
-  return align_up(static_cast<size_t>(kMaxDhParts) * static_cast<size_t>(ceil_div(p.T, 256) * 256) *
-                      static_cast<size_t>(p.H) * sizeof(float),
+  return align_up(static_cast<size_t>(ceil_div(p.T, 256)) * static_cast<size_t>(ceil_div(p.H, 256)) * 16 *
+                      sizeof(int32_t),
                   kWsAlign);
 }
 
@@ -236,7 +236,7 @@ SampledLayout sampled_layout(const vce_problem& p, int64_t P) {
   size_t common = sampled_ws_bytes(p);
   common = common > fwd_layout(pl).total ? common : fwd_layout(pl).total;
   const size_t bwd_min = dh_acc_bytes(pl) + bwd_bytes_for(pl, pl.T == 0 ? 0 : 256);
-  const size_t bwd_rec = dh_acc_bytes(pl) + bwd_bytes_for(pl, bwd_recommended_cols(pl)) + dh_part_bytes(pl);
+  const size_t bwd_rec = dh_acc_bytes(pl) + bwd_bytes_for(pl, bwd_recommended_cols(pl)) + dh_flag_bytes(pl);
   L.scratch_min = common > bwd_min ? common : bwd_min;
   const size_t rec = common > bwd_rec ? common : bwd_rec;
   L.total = L.scratch + rec;
@@ -315,7 +315,7 @@ size_t vce_workspace_size(const vce_problem* p, int32_t op) {
     case VCE_OP_EMBED_BWD: return embed_bwd_ws_bytes(*p);
     case VCE_OP_LOSS_FWD: return fwd_layout(*p).total;
     case VCE_OP_LOSS_BWD:
-      return dh_acc_bytes(*p) + bwd_bytes_for(*p, bwd_recommended_cols(*p)) + dh_part_bytes(*p);
+      return dh_acc_bytes(*p) + bwd_bytes_for(*p, bwd_recommended_cols(*p)) + dh_flag_bytes(*p);
     case VCE_OP_SAMPLED_CANDIDATES: return sampled_ws_bytes(*p);
     case VCE_OP_GREEDY_ARGMAX: return argmax_ws_bytes(*p);
   }
@@ -375,16 +375,17 @@ vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W, cons
   float2* part = reinterpret_cast<float2*>(b + L.part);
   float* ztgt = reinterpret_cast<float*>(b + L.ztgt);
   float* bsum = reinterpret_cast<float*>(b + L.block_sums);
+  int32_t* merge_ctr = reinterpret_cast<int32_t*>(b + L.status + 4);
   const ProbDev pd = prob_dev(*p);
   cudaError_t e;
   if (p->dtype == VCE_BF16)
-    e = launch_tc_fwd(*p, L.ug, h, W, targets, part, ztgt, status, st);
+    e = launch_tc_fwd(*p, L.ug, h, W, targets, part, ztgt, merge_ctr, status, st);
   else
     e = launch_simt_fwd(pd, L.ug, static_cast<const float*>(h), static_cast<const float*>(W), targets, part, ztgt,
-                        st);
+                        merge_ctr, st);
   if (e != cudaSuccess) return cuda_status(e);
-  return cuda_status(
-      launch_merge(pd, L.ug, targets, part, ztgt, lse, token_loss, target_owner, max_owner, bsum, loss, status, st));
+  return cuda_status(launch_merge(pd, L.ug, targets, part, ztgt, lse, token_loss, target_owner, max_owner, bsum,
+                                  merge_ctr, loss, status, st));
 }
 
 vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, const int64_t* targets,
@@ -411,8 +412,8 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
   float* dH = acc_bytes ? static_cast<float*>(ws) : static_cast<float*>(dH_out);
   ws = static_cast<char*>(ws) + acc_bytes;
   ws_bytes -= acc_bytes;
-  // Layout: header | dH K-part partials (when the workspace has room) | G chunk.
-  const size_t part_bytes = dh_part_bytes(*p);
+  // Layout: header | dH K-part counters (when the workspace has room) | G chunk.
+  const size_t part_bytes = dh_flag_bytes(*p);
   const bool use_parts = part_bytes > 0 && ws_bytes >= bwd_bytes_for(*p, 256) + part_bytes;
   const int64_t vc = bwd_chunk_cols(*p, use_parts ? ws_bytes - part_bytes : ws_bytes);
   if (vc < 256) return VCE_ERR_WORKSPACE;
@@ -423,10 +424,13 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
     status = reinterpret_cast<int32_t*>(b);
     if (cudaError_t me = cudaMemsetAsync(status, 0, sizeof(int32_t), st)) return cuda_status(me);
   }
-  float* dh_part = use_parts ? reinterpret_cast<float*>(b + kBwdHeader) : nullptr;
+  int32_t* dh_flags = use_parts ? reinterpret_cast<int32_t*>(b + kBwdHeader) : nullptr;
   void* G = b + kBwdHeader + (use_parts ? part_bytes : 0);
   const ProbDev pd = prob_dev(*p);
-  if (cudaError_t ce = launch_count_valid(pd, targets, n_valid, status, st)) return cuda_status(ce);
+  // The fp32 path counts the valid targets first; the tensor-core GRAD kernel
+  // counts them itself.
+  if (p->dtype != VCE_BF16)
+    if (cudaError_t ce = launch_count_valid(pd, targets, n_valid, status, st)) return cuda_status(ce);
   if (!p->tied_weights && p->Vp > p->V_real) {
     if (cudaMemsetAsync(dW + static_cast<size_t>(p->V_real) * p->H, 0, row_bytes * (p->Vp - p->V_real), st) !=
         cudaSuccess)
@@ -438,9 +442,9 @@ vce_status vce_loss_bwd(const vce_problem* p, const void* h, const void* W, cons
     const int vc_act = static_cast<int>((p->V_real - c0) < vc ? (p->V_real - c0) : vc);
     cudaError_t e;
     if (p->dtype == VCE_BF16) {
-      const int parts = dh_part ? tc_dh_parts(*p, vc_act) : 1;
-      e = launch_tc_bwd_chunk(*p, h, W, targets, lse, n_valid, g, static_cast<int>(c0), vc_act, G,
-                              static_cast<int>(vc), dH, c0 > 0 || acc_dh, dW, p->tied_weights != 0, dh_part, parts,
+      const int parts = dh_flags ? tc_dh_parts(*p, vc_act) : 1;
+      e = launch_tc_bwd_chunk(*p, h, W, targets, lse, g, static_cast<int>(c0), vc_act, G,
+                              static_cast<int>(vc), dH, c0 > 0 || acc_dh, dW, p->tied_weights != 0, dh_flags, parts,
                               status, st);
     } else {
       float* Gf = static_cast<float*>(G);
