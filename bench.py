@@ -34,11 +34,11 @@ WORKLOAD = "qwen3_tied"
 # tensor-core kernel's source file that the capture ran: once that file has
 # changed the figure is stale, and the line reports null until it is retaken.
 MEASURED_TRAFFIC = {
-    "qwen3_tied": {"bytes_per_step": 16378760960,
-                   "per_kernel": {"tc_fwd": 814285056, "tc_grad": 3369247488, "tc_dh": 5398940672,
-                                  "tc_dw": 6796287744},
-                   "source": "aa524c94a4261308",
-                   "profile": "profiles/tc_loss_kernel_qwen3_T8192_dram.md"},
+    "qwen3_tied": {"bytes_per_step": 16557217280,
+                   "per_kernel": {"tc_fwd": 795382272, "tc_grad": 3337183232, "tc_dh": 5540984320,
+                                  "tc_dw": 6883667456},
+                   "source": "12ebf909ff70ca64",
+                   "profile": "profiles/tc_loss_kernel_qwen3_T8192.md"},
 }
 TC_SOURCE = os.path.join(ROOT, "vocab_embedding_cross_gb300", "csrc", "loss_tc.cu")
 
