@@ -114,6 +114,13 @@ def test_loss_bad_target_flagged_and_ignored():
     out, ref = _fwd_check(wl, d, TOL["bf16"])
     assert out["status"] == R.vce.VCE_ERR_BAD_INDEX
     assert out["token_loss"][3] == 0 and out["target_owner"][40] == -1
+    # the backward on its own flags them too, and gives them no gradient
+    dH, dW, st = R.loss_bwd(wl, D.to_device(d["h"]), D.to_device(d["W"]), out["targets_d"], out["lse_d"])
+    assert st == R.vce.VCE_ERR_BAD_INDEX
+    assert not dH[3].any().item() and not dH[40].any().item()
+    rdH, rdW = O.cross_entropy_backward(d["h"], d["W"], d["targets"], wl.V_real, wl.Vp)
+    assert R.max_abs_rel(dH.cpu().numpy(), rdH) <= TOL["bf16"]["grad"]
+    assert R.max_abs_rel(dW.cpu().numpy(), rdW) <= TOL["bf16"]["grad"]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])

@@ -315,6 +315,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&mapB);
       int stage = 0;
       uint32_t phase = 0;
+      // the even CTA's full barriers, as cluster addresses (consecutive words)
+      const uint32_t full_leader0 = mapa_shared(smem_u32(&full[0]), 0);
       int last_parity[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
@@ -329,7 +331,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
+            const uint32_t full_leader = full_leader0 + static_cast<uint32_t>(stage) * 8u;
             if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
             const uint32_t sA = stage0 + stage * kStageBytes;
             issue_loads<MODE>(a, &mapA, &mapB, sA, sA + kABytes, full_leader, tc, kb);
@@ -385,19 +387,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t sA = stage0 + stage * kStageBytes;
             const uint32_t sB = sA + kABytes;
+            const uint64_t ad0 = Tr::a_mn ? smem_desc_sw128(sA, kAtomBytes, 1024u) : smem_desc_sw128(sA, 16u, 1024u);
+            const uint64_t bd0 = Tr::b_mn ? smem_desc_sw128(sB, kAtomBytes, 1024u) : smem_desc_sw128(sB, 16u, 1024u);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
-              uint64_t ad, bd;
-              if constexpr (Tr::a_mn) {
-                ad = smem_desc_sw128(sA + kk * 2048u, kAtomBytes, 1024u);
-              } else {
-                ad = smem_desc_sw128(sA + kk * 32u, 16u, 1024u);
-              }
-              if constexpr (Tr::b_mn) {
-                bd = smem_desc_sw128(sB + kk * 2048u, kAtomBytes, 1024u);
-              } else {
-                bd = smem_desc_sw128(sB + kk * 32u, 16u, 1024u);
-              }
+              const uint64_t ad = ad0 + static_cast<uint64_t>(Tr::a_mn ? kk * (2048u >> 4) : kk * (32u >> 4));
+              const uint64_t bd = bd0 + static_cast<uint64_t>(Tr::b_mn ? kk * (2048u >> 4) : kk * (32u >> 4));
               umma_f16_pair(d, ad, bd, Tr::idesc, (kb != kr.kb0 || kk != 0) ? 1u : 0u);
             }
             issued = true;

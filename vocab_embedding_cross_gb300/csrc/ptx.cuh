@@ -62,8 +62,11 @@ __device__ __forceinline__ void record_status(int* status, int code) {
 // Wait for the phase with parity `parity` of `bar` to complete. Returns false
 // (and raises the CTA's abort flag, and records VCE_ERR_TIMEOUT = 5) when the
 // wait runs past limit_ns, or when another role of the CTA has aborted.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
-  if (mbar_try_wait(bar, parity)) return true;
+// mbar_wait itself is inline and returns at once when the phase is already
+// complete (the common case in a fed pipeline); only a wait that has to spin
+// calls the out-of-line loop, so the issuing threads of the tensor-core
+// kernels pay no call per pipeline stage.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -109,6 +112,10 @@ static __device__ __noinline__ bool flag_wait_ge(const int32_t* p, int target, i
     asm volatile("fence.proxy.async.global;" ::: "memory");   // the TMA operations that follow see it
   }
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, w);
 }
 
 // ---------------------------------------------------------------------------
@@ -297,9 +304,9 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
       : "memory");
   return ok != 0;
 }
-// Bounded wait with cluster-scope acquire (arrivals may come from the peer CTA).
-static __device__ __noinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+// Bounded wait with cluster-scope acquire (arrivals may come from the peer
+// CTA); inline fast path as for mbar_wait.
+static __device__ __noinline__ bool mbar_wait_cl_slow(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
@@ -312,6 +319,9 @@ static __device__ __noinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity,
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  return mbar_try_wait_cluster(bar, parity) || mbar_wait_cl_slow(bar, parity, w);
 }
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier that may live in either CTA of the pair (cluster address).
