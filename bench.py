@@ -34,10 +34,10 @@ WORKLOAD = "qwen3_tied"
 # tensor-core kernel's source file that the capture ran: once that file has
 # changed the figure is stale, and the line reports null until it is retaken.
 MEASURED_TRAFFIC = {
-    "qwen3_tied": {"bytes_per_step": 16557217280,
-                   "per_kernel": {"tc_fwd": 795382272, "tc_grad": 3337183232, "tc_dh": 5540984320,
-                                  "tc_dw": 6883667456},
-                   "source": "12ebf909ff70ca64",
+    "qwen3_tied": {"bytes_per_step": 20405150464,
+                   "per_kernel": {"tc_fwd": 931232768, "tc_grad": 3473277184, "tc_dh": 8289566208,
+                                  "tc_dw": 7711074304},
+                   "source": "97a3f41eb0866d7d",
                    "profile": "profiles/tc_loss_kernel_qwen3_T8192.md"},
 }
 TC_SOURCE = os.path.join(ROOT, "vocab_embedding_cross_gb300", "csrc", "loss_tc.cu")
@@ -76,7 +76,8 @@ def arm_config(workload: str, world: int) -> dict:
     from vocab_embedding_cross_gb300 import inputs as I
     wl = I.WORKLOADS[workload]
     return {"workload": f"{workload}: T={wl.T} H={wl.H} V_real={wl.V_real} Vp={wl.Vp} S={wl.S} tied={wl.tied}",
-            "step": "embed_fwd + loss_fwd + loss_bwd (writes the tied dW) + embed_bwd (adds into it)",
+            "step": "embed_fwd + embed_bwd_plan (the ids' sort) + loss_fwd + loss_bwd (writes the tied dW) + "
+                    "embed_bwd_apply (adds into it)",
             "l2": "inputs larger than L2 (W 622 MB, G chunks of 1.25 GB); no extra flush",
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
@@ -205,11 +206,14 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
 
+    # The embedding backward's plan (the sort of the ids) is made at the lookup,
+    # where the ids are known; the backward then only applies it to dE.
     def step_ops():
         vce.vce_embed_fwd(p, ids, W, E, dev_status=st, stream=sp)
+        vce.vce_embed_bwd_plan(p, ids, ws_e, dev_status=st, stream=sp)
         vce.vce_loss_fwd(p, h, W, y, loss, lse, ws=ws_f, dev_status=st, stream=sp)
         vce.vce_loss_bwd(p_head, h, W, y, lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp)
-        vce.vce_embed_bwd(p, ids, dE, dW, ws_e, dev_status=st, stream=sp)
+        vce.vce_embed_bwd_apply(p, dE, dW, ws_e, dev_status=st, stream=sp)
 
     def step():
         step_ops()
@@ -314,8 +318,13 @@ def run_ours(args):
         emb["bwd_GBps"] = round(bwd_bytes / (b_ms / 1e3) / 1e9, 1)
         emb["bwd_us"] = round(b_ms * 1e3, 2)
         emb["bwd_sort_us"] = round(sum(per_kind.get(k, (0.0, 0))[0] for k in sorts) * 1e3, 2)
+        # the backward's own launch in the step: the plan's application (the plan
+        # is made after the lookup)
+        a_ms = per_kind["embed_reduce"][0]
+        emb["bwd_apply_GBps"] = round(bwd_bytes / (a_ms / 1e3) / 1e9, 1)
+        emb["bwd_apply_us"] = round(a_ms * 1e3, 2)
     emb["hbm_peak_GBps"] = peaks["hbm_gbs"]
-    for k in ("gather", "bwd"):
+    for k in ("gather", "bwd", "bwd_apply"):
         if f"{k}_GBps" in emb:
             emb[f"{k}_frac"] = round(emb[f"{k}_GBps"] / peaks["hbm_gbs"], 4)
 
@@ -578,7 +587,13 @@ def run_embedding(args, vce, D, I, stream, peaks, name):
     L2 is flushed before every call by writing a 256 MB buffer. The headline
     figures then read another 256 MB buffer, so that the L2 holds clean lines
     and the timed call is not charged for writing back the flush buffer's dirty
-    lines; the `*_dirty_l2` figures skip that read."""
+    lines; the `*_dirty_l2` figures skip that read.
+
+    `bwd_*` is the one-call backward (vce_embed_bwd: the sort of the ids, then
+    the addition of dE into dW); `bwd_plan_us` the sort alone
+    (vce_embed_bwd_plan); `bwd_apply_*` the addition by a plan made earlier
+    (vce_embed_bwd_apply), which is all the backward runs once the plan is
+    made at the lookup, and which moves all of the backward's bytes."""
     import torch
     wl = I.WORKLOADS[name]
     d = I.make_all(wl, ("W", "ids", "dE"))
@@ -619,8 +634,15 @@ def run_embedding(args, vce, D, I, stream, peaks, name):
     n = max(10, args.steps // 2)
     fwd = lambda: vce.vce_embed_fwd(p, ids, W, E, dev_status=st, stream=sp)
     bwd = lambda: vce.vce_embed_bwd(p, ids, dE, dW, ws, dev_status=st, stream=sp)
+    plan = lambda: vce.vce_embed_bwd_plan(p, ids, ws, dev_status=st, stream=sp)
+    apply = lambda: vce.vce_embed_bwd_apply(p, dE, dW, ws, dev_status=st, stream=sp)
     g_ms, b_ms = timed(fwd, n), timed(bwd, n)
     g_dirty, b_dirty = timed(fwd, n, clean_l2=False), timed(bwd, n, clean_l2=False)
+    # The backward split at its plan: the sort of the ids alone, then the
+    # application of the plan to dE (the workspace holds the plan of these ids,
+    # and every application leaves it in place).
+    plan_ms = timed(plan, n)
+    a_ms, a_dirty = timed(apply, n), timed(apply, n, clean_l2=False)
     assert int(st.item()) == 0, vce.status_str(int(st.item()))
     del W, dE, E, dW, ws, flush, clean
     torch.cuda.empty_cache()
@@ -635,6 +657,10 @@ def run_embedding(args, vce, D, I, stream, peaks, name):
             "bwd_frac": frac(bwd_bytes, b_ms),
             "gather_us_dirty_l2": round(g_dirty * 1e3, 2), "gather_frac_dirty_l2": frac(gather_bytes, g_dirty),
             "bwd_us_dirty_l2": round(b_dirty * 1e3, 2), "bwd_frac_dirty_l2": frac(bwd_bytes, b_dirty),
+            "bwd_plan_us": round(plan_ms * 1e3, 2),
+            "bwd_apply_us": round(a_ms * 1e3, 2), "bwd_apply_GBps": round(bwd_bytes / (a_ms / 1e3) / 1e9, 1),
+            "bwd_apply_frac": frac(bwd_bytes, a_ms),
+            "bwd_apply_us_dirty_l2": round(a_dirty * 1e3, 2), "bwd_apply_frac_dirty_l2": frac(bwd_bytes, a_dirty),
             "gather_bytes": gather_bytes, "bwd_bytes": bwd_bytes,
             # every valid row counted as read (repeats hit L2), and the nominal 8 TB/s HBM3e
             "gather_logical_bytes": logical_bytes,
@@ -792,9 +818,10 @@ def run_e2e(args, vce, D, d, p, p_head, W, E, loss, lse, dH, dW, st, ws_f, ws_b,
         stream.wait_event(ready[b])
         x = dev[b]
         vce.vce_embed_fwd(p, x["ids"], W, E, dev_status=st, stream=sp)
+        vce.vce_embed_bwd_plan(p, x["ids"], ws_e, dev_status=st, stream=sp)
         vce.vce_loss_fwd(p, x["h"], W, x["targets"], loss, lse, ws=ws_f, dev_status=st, stream=sp)
         vce.vce_loss_bwd(p_head, x["h"], W, x["targets"], lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp)
-        vce.vce_embed_bwd(p, x["ids"], x["dE"], dW, ws_e, dev_status=st, stream=sp)
+        vce.vce_embed_bwd_apply(p, x["dE"], dW, ws_e, dev_status=st, stream=sp)
         used[b].record(stream)
         loss_h.copy_(loss, non_blocking=True)
 

@@ -155,11 +155,41 @@ vce_status vce_embed_fwd(const vce_problem* p, const int64_t* ids, const void* W
  * (VCE_K_EMBED_SORT). The environment variable VCE_EMBED_SORT_CLUSTER, read
  * at each call, overrides the choice: 1 for the clusters whenever the bucketed
  * counting sort runs, 0 for never.
+ * The call is vce_embed_bwd_plan followed by vce_embed_bwd_apply on the same
+ * workspace, and it leaves the plan of `ids` there.
  * Workspace: vce_workspace_size(p, VCE_OP_EMBED_BWD) bytes.
  */
 vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* dE,
                          float* dW, void* ws, size_t ws_bytes,
                          int32_t* dev_status, void* stream);
+
+/*
+ * The embedding backward in two parts [VS p.2: the tokens of one id
+ * accumulate into its owned row]. The order of vce_embed_bwd depends on the
+ * ids alone, so it can be worked out as soon as the ids are known (at the
+ * lookup, for instance), before dE exists; only the application touches dE and
+ * dW, which carry all of the backward's memory traffic.
+ *
+ * vce_embed_bwd_plan sorts the valid (id, t) pairs, cuts each id's tokens into
+ * runs and writes this plan into `ws` (vce_workspace_size(p,
+ * VCE_OP_EMBED_BWD) bytes), replacing whatever the workspace held. It reads
+ * only `ids`. `dev_status` is unused and may be NULL.
+ *
+ * vce_embed_bwd_apply adds dE into dW by the plan held in `ws`, with exactly
+ * the results of vce_embed_bwd for the planned ids (same order, same bits),
+ * and leaves the plan unchanged: the same plan can be applied to another dE
+ * or again. `p` must have the T, H and dtype the plan was made with; ids are
+ * not passed again, and the caller must keep the plan's ids and workspace
+ * together. A workspace that holds no plan, or one made for another T or
+ * column count, adds nothing and reports VCE_ERR_ARG to dev_status. Two calls
+ * on the same workspace must not overlap on the GPU (they share the plan's
+ * counters).
+ */
+vce_status vce_embed_bwd_plan(const vce_problem* p, const int64_t* ids, void* ws,
+                              size_t ws_bytes, int32_t* dev_status, void* stream);
+vce_status vce_embed_bwd_apply(const vce_problem* p, const void* dE, float* dW,
+                               void* ws, size_t ws_bytes, int32_t* dev_status,
+                               void* stream);
 
 /*
  * Globally normalised cross-entropy, forward [VS p.3-5; PAD s.5; SPN p.3].

@@ -69,6 +69,8 @@ def test_bad_problem_rejected_on_host(L, kw, code):
     p = P(**kw)
     assert vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD) == vce.SIZE_MAX
     for fn, args in ((L.vce_embed_fwd, (None,) * 7), (L.vce_embed_bwd, (None, None, None, None, 0, None, None)),
+                     (L.vce_embed_bwd_plan, (None, None, 0, None, None)),
+                     (L.vce_embed_bwd_apply, (None, None, None, 0, None, None)),
                      (L.vce_loss_fwd, (None,) * 9 + (0, None, None)),
                      (L.vce_loss_bwd, (None, None, None, None, 1.0, None, None, None, 0, None, None))):
         import ctypes
@@ -82,6 +84,13 @@ def test_null_pointers_rejected(L):
     assert L.vce_loss_fwd(ctypes.byref(p), None, None, None, None, None, None, None, None, None, 0, None,
                           None) == vce.VCE_ERR_ARG
     assert L.vce_wait_selftest(1000, None, None) == vce.VCE_ERR_ARG
+    assert L.vce_embed_bwd_plan(ctypes.byref(p), None, 0x4000, 1 << 30, None, None) == vce.VCE_ERR_ARG
+    assert L.vce_embed_bwd_apply(ctypes.byref(p), None, 0x2000, 0x4000, 1 << 30, None, None) == vce.VCE_ERR_ARG
+    assert L.vce_embed_bwd_apply(ctypes.byref(p), 0x2000, None, 0x4000, 1 << 30, None, None) == vce.VCE_ERR_ARG
+    # an empty batch has nothing to plan or apply
+    p0 = P(T=0)
+    assert L.vce_embed_bwd_plan(ctypes.byref(p0), None, None, 0, None, None) == vce.VCE_OK
+    assert L.vce_embed_bwd_apply(ctypes.byref(p0), None, None, None, 0, None, None) == vce.VCE_OK
 
 
 def test_misaligned_pointers_rejected(L):
@@ -138,6 +147,15 @@ def test_workspace_too_small_rejected_on_host(L):
         vce.VCE_ERR_WORKSPACE
     assert L.vce_embed_bwd(ctypes.byref(p), 0x1000, 0x2000, 0x3000, 0x4010, need, None, None) == \
         vce.VCE_ERR_WORKSPACE                      # misaligned workspace
+    # the plan and its application use the same workspace size and alignment
+    assert L.vce_embed_bwd_plan(ctypes.byref(p), 0x1000, 0x4000, need - 1, None, None) == vce.VCE_ERR_WORKSPACE
+    assert L.vce_embed_bwd_plan(ctypes.byref(p), 0x1000, 0x4010, need, None, None) == vce.VCE_ERR_WORKSPACE
+    assert L.vce_embed_bwd_plan(ctypes.byref(p), 0x1000, None, need, None, None) == vce.VCE_ERR_WORKSPACE
+    assert L.vce_embed_bwd_apply(ctypes.byref(p), 0x2000, 0x3000, 0x4000, need - 1, None, None) == \
+        vce.VCE_ERR_WORKSPACE
+    assert L.vce_embed_bwd_apply(ctypes.byref(p), 0x2000, 0x3000, None, need, None, None) == vce.VCE_ERR_WORKSPACE
+    assert L.vce_embed_bwd_apply(ctypes.byref(p), 0x2008, 0x3000, 0x4000, need, None, None) == \
+        vce.VCE_ERR_UNSUPPORTED                    # dE not 16-byte aligned
 
 
 def test_sampled_candidates_rejected_on_host(L):

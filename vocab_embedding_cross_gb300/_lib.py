@@ -60,6 +60,10 @@ def lib():
         L.vce_embed_fwd.restype = c_int32
         L.vce_embed_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
         L.vce_embed_bwd.restype = c_int32
+        L.vce_embed_bwd_plan.argtypes = [P, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
+        L.vce_embed_bwd_plan.restype = c_int32
+        L.vce_embed_bwd_apply.argtypes = [P, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
+        L.vce_embed_bwd_apply.restype = c_int32
         L.vce_loss_fwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
         L.vce_loss_fwd.restype = c_int32
@@ -164,6 +168,18 @@ def vce_embed_bwd(p, ids, dE, dW, ws, ws_bytes=None, dev_status=None, stream=Non
     nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
     _check(lib().vce_embed_bwd(ctypes.byref(p), _ptr(ids), _ptr(dE), _ptr(dW), _ptr(ws), nb,
                                _ptr(dev_status), _stream(stream)), "vce_embed_bwd")
+
+
+def vce_embed_bwd_plan(p, ids, ws, ws_bytes=None, dev_status=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().vce_embed_bwd_plan(ctypes.byref(p), _ptr(ids), _ptr(ws), nb, _ptr(dev_status), _stream(stream)),
+           "vce_embed_bwd_plan")
+
+
+def vce_embed_bwd_apply(p, dE, dW, ws, ws_bytes=None, dev_status=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().vce_embed_bwd_apply(ctypes.byref(p), _ptr(dE), _ptr(dW), _ptr(ws), nb, _ptr(dev_status),
+                                     _stream(stream)), "vce_embed_bwd_apply")
 
 
 def vce_loss_fwd(p, h, W, targets, loss, lse, token_loss=None, target_owner=None, max_owner=None, ws=None,

@@ -16,6 +16,12 @@
 // kEmbedBwdChunk, each run is summed in fp32 in ascending t, run sums are
 // combined left to right, and the total is added once into the fp32 row. The
 // order is fixed, so results are bit-identical from run to run.
+//
+// The sort depends on the ids alone. It leaves a plan in the workspace (the
+// sorted tokens, the run descriptors, zeroed combine counters and a header
+// that names the problem's shape), and the reduce applies the plan to dE. The
+// reduce leaves the plan as it found it, so one plan can be applied again, and
+// a plan can be made as soon as the ids are known, before dE exists.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -98,6 +104,20 @@ struct __align__(16) RunDesc {
   int32_t first_slot;   // slot of the id's first run
   int32_t pad;
 };
+
+// The workspace header (16 words). The sorts claim space with atomic
+// additions on words 0-5; the reduce hands out items from word 6; words 8-10
+// describe the plan (its T, its column slices per row and a marker), so that
+// applying a plan made for another shape, or a workspace that holds none, is
+// refused on the device.
+constexpr int kHdrItem = 6, kHdrPlanT = 8, kHdrPlanNh = 9, kHdrPlanMark = 10;
+constexpr int32_t kPlanMark = 0x4E414C50;   // "PLAN"
+
+__device__ __forceinline__ void plan_seal(int32_t* hdr, int T, int nh) {
+  hdr[kHdrPlanT] = T;
+  hdr[kHdrPlanNh] = nh;
+  hdr[kHdrPlanMark] = kPlanMark;
+}
 
 struct BwdLayout {
   size_t hdr, keys_a, keys_b, seg_start, tsorted, runs, counters, partials, total;
@@ -252,7 +272,7 @@ __device__ __forceinline__ void build_runs(SegAt seg, int nseg, int n, int per_t
     hdr[3] = t_multi;
     hdr[4] = t_slots;
     hdr[5] = 0;
-    hdr[6] = 0;   // the reduce's item counter
+    hdr[kHdrItem] = 0;   // the reduce's item counter
   }
 }
 
@@ -471,7 +491,8 @@ __global__ void __launch_bounds__(kSortThreads, 1)
     hdr[3] = n_multi;
     hdr[4] = n_runs - (nseg - n_multi);
     hdr[5] = 0;
-    hdr[6] = 0;   // the reduce's item counter
+    hdr[kHdrItem] = 0;   // the reduce's item counter
+    plan_seal(hdr, T, nh);
   }
 }
 
@@ -481,7 +502,7 @@ __global__ void __launch_bounds__(kSortThreads, 1)
 // before it before its first claim.
 __global__ void embed_hdr_zero_kernel(int32_t* h0, int32_t* h1, int32_t* h2) {
   grid_dep_launch();
-  const int i = threadIdx.x & 7, k = threadIdx.x >> 3;
+  const int i = threadIdx.x & 15, k = threadIdx.x >> 4;
   int32_t* h = k == 0 ? h0 : (k == 1 ? h1 : h2);
   if (k < 3 && h) h[i] = 0;
 }
@@ -569,6 +590,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   grid_dep_wait();
   int tb = 0;
   if (tid == 0 && m > 0) tb = atomicAdd(&hdr[0], m);
+  if (tid == 0 && b == 0) plan_seal(hdr, T, nh);
 
   // Phase B: stable LSD radix passes over the id / NB bits.
   const int kpw = ((m + kBktWarps - 1) / kBktWarps + 31) & ~31;
@@ -860,6 +882,7 @@ __global__ void __launch_bounds__(kSortThreads, 1)
   if (tid == 0) {
     hdr[0] = n;
     hdr[2] = nseg;
+    plan_seal(hdr, static_cast<int>(T), nh);
   }
 }
 
@@ -1113,6 +1136,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   grid_dep_wait();
   int tb = 0;
   if (tid == 0 && m > 0) tb = atomicAdd(&hdr[0], m);
+  if (tid == 0 && b == 0) plan_seal(hdr, T, nh);
   __syncthreads();
 
   // Counting warp w takes part w % (kCntWarps / CL) of segment w / (kCntWarps / CL).
@@ -1268,7 +1292,7 @@ struct EmbSlots {
 template <typename TE, bool STREAM>
 __global__ void __launch_bounds__(128)
     embed_reduce_kernel(const __grid_constant__ EmbSlots sl, const TE* __restrict__ dE, int H, int nh,
-                        uint32_t nh_magic, int cap) {
+                        uint32_t nh_magic, int cap, int32_t* status) {
   constexpr int VEC = 16 / sizeof(TE);
   constexpr int NQ = VEC / 4;
   constexpr int U = 8;               // rows loaded ahead of the sequential adds
@@ -1277,6 +1301,16 @@ __global__ void __launch_bounds__(128)
   __shared__ int s_next[2];
   const int lane = threadIdx.x & 31;
   grid_dep_wait();   // the sorts' headers, runs and tokens
+  // Every problem must hold a plan made for this shape (T = cap); otherwise
+  // nothing is added and the call reports VCE_ERR_ARG.
+  bool planned = true;
+  for (int k = 0; k < sl.n; ++k)
+    planned = planned && sl.s[k].hdr[kHdrPlanMark] == kPlanMark && sl.s[k].hdr[kHdrPlanT] == cap &&
+              sl.s[k].hdr[kHdrPlanNh] == nh;
+  if (!planned) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && status) atomicCAS(status, 0, static_cast<int>(VCE_ERR_ARG));
+    return;
+  }
   // In each problem, runs [0, n_front) sit at the front of the list, the other
   // n_back at its end (indices cap-1, cap-2, ...). Problem k's items are
   // [base_k, base_k+1).
@@ -1290,11 +1324,17 @@ __global__ void __launch_bounds__(128)
   // rest from a counter in the first problem's header (zeroed before this
   // kernel), claimed one item ahead so that the claim's round trip overlaps
   // the current item.
-  int32_t* item_ctr = sl.s[0].hdr + 6;
+  int32_t* item_ctr = sl.s[0].hdr + kHdrItem;
   int it = 0;
   for (int item = blockIdx.x; item < n_items; ++it) {
     int next = 0;
-    if (threadIdx.x == 0) next = atomicAdd(item_ctr, 1) + static_cast<int>(gridDim.x);
+    if (threadIdx.x == 0) {
+      // One claim per item in all: the claim that draws n_items - 1 is the
+      // last one, and puts the counter back to zero for the plan's next use.
+      const int prev = atomicAdd(item_ctr, 1);
+      if (prev == n_items - 1) atomicExch(item_ctr, 0);
+      next = prev + static_cast<int>(gridDim.x);
+    }
     // this item's problem (a uniform choice among at most three)
     const int k = item >= base2 ? 2 : (item >= base1 ? 1 : 0);
     const int li = item - (k == 2 ? base2 : (k == 1 ? base1 : 0));
@@ -1357,6 +1397,7 @@ __global__ void __launch_bounds__(128)
       if (threadIdx.x == 0) {
         const int prev = atomicAdd(&counters[rd.mseg * nh + hs], 1);
         s_last = (prev == rd.nruns - 1) ? 1 : 0;
+        if (s_last) counters[rd.mseg * nh + hs] = 0;   // every run is in: back to the plan's zero
         __threadfence();
       }
       __syncthreads();
@@ -1622,7 +1663,8 @@ cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, cons
 }
 
 // One reduce over the sorted problems in `sl` (all with p's T, H and dtype).
-cudaError_t launch_reduce(const vce_problem& p, const EmbSlots& sl, const void* dE, cudaStream_t st) {
+cudaError_t launch_reduce(const vce_problem& p, const EmbSlots& sl, const void* dE, int32_t* status,
+                          cudaStream_t st) {
   const BwdLayout L = bwd_layout(p);
   const DevInfo di = current_device_info();
   const int grid = di.num_sms * 8;
@@ -1638,51 +1680,74 @@ cudaError_t launch_reduce(const vce_problem& p, const EmbSlots& sl, const void* 
   if (p.dtype == VCE_BF16)
     e = launch_dependent(stream ? embed_reduce_kernel<uint16_t, true> : embed_reduce_kernel<uint16_t, false>,
                          dim3(grid), dim3(128), 0, st, sl, static_cast<const uint16_t*>(dE), static_cast<int>(p.H),
-                         L.nh, nh_magic, static_cast<int>(p.T));
+                         L.nh, nh_magic, static_cast<int>(p.T), status);
   else
     e = launch_dependent(stream ? embed_reduce_kernel<float, true> : embed_reduce_kernel<float, false>, dim3(grid),
                          dim3(128), 0, st, sl, static_cast<const float*>(dE), static_cast<int>(p.H), L.nh, nh_magic,
-                         static_cast<int>(p.T));
+                         static_cast<int>(p.T), status);
   note_launch(VCE_K_EMBED_REDUCE, st);
   return e;
 }
 
 }  // namespace
 
-cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* ids, float* const* dW,
-                                   void* const* ws, int n, const void* dE, cudaStream_t st) {
+// The plans of n problems: one header-zeroing launch (for the bucketed
+// sorts), then one sort per problem.
+cudaError_t launch_embed_bwd_plan_multi(const vce_problem* ps, const int64_t* const* ids, void* const* ws, int n,
+                                        cudaStream_t st) {
   if (n < 1 || n > kMaxSlots) return cudaErrorInvalidValue;
   if (ps[0].T == 0) return cudaSuccess;
   const DevInfo di = current_device_info();
   SortPlan plan[kMaxSlots];
   int32_t* zero[kMaxSlots] = {nullptr, nullptr, nullptr};
   bool any_bucketed = false;
-  EmbSlots sl{};
-  sl.n = n;
   for (int k = 0; k < n; ++k) {
     cudaError_t err = cudaSuccess;
     plan[k] = plan_sort(ps[k], di.num_sms, &err);
     if (err != cudaSuccess) return err;
-    sl.s[k] = emb_slot(ps[k], ws[k], dW[k]);
     if (plan[k].path == SortPath::kCount || plan[k].path == SortPath::kBucket) {
-      zero[k] = sl.s[k].hdr;
+      zero[k] = emb_slot(ps[k], ws[k], nullptr).hdr;
       any_bucketed = true;
     }
   }
   if (any_bucketed) {
-    embed_hdr_zero_kernel<<<1, 32, 0, st>>>(zero[0], zero[1], zero[2]);
+    embed_hdr_zero_kernel<<<1, 64, 0, st>>>(zero[0], zero[1], zero[2]);
     note_launch(VCE_K_EMBED_HDR, st);
     if (cudaError_t e = cudaGetLastError()) return e;
   }
   for (int k = 0; k < n; ++k)
     if (cudaError_t e = launch_sort(ps[k], ids[k], ws[k], plan[k], st)) return e;
-  return launch_reduce(ps[0], sl, dE, st);
+  return cudaSuccess;
+}
+
+cudaError_t launch_embed_bwd_apply_multi(const vce_problem* ps, float* const* dW, void* const* ws, int n,
+                                         const void* dE, int32_t* status, cudaStream_t st) {
+  if (n < 1 || n > kMaxSlots) return cudaErrorInvalidValue;
+  if (ps[0].T == 0) return cudaSuccess;
+  EmbSlots sl{};
+  sl.n = n;
+  for (int k = 0; k < n; ++k) sl.s[k] = emb_slot(ps[k], ws[k], dW[k]);
+  return launch_reduce(ps[0], sl, dE, status, st);
+}
+
+cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* ids, float* const* dW,
+                                   void* const* ws, int n, const void* dE, int32_t* status, cudaStream_t st) {
+  if (cudaError_t e = launch_embed_bwd_plan_multi(ps, ids, ws, n, st)) return e;
+  return launch_embed_bwd_apply_multi(ps, dW, ws, n, dE, status, st);
 }
 
 cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const void* dE, float* dW, void* ws,
                              int32_t* status, cudaStream_t st) {
-  (void)status;
-  return launch_embed_bwd_multi(&p, &ids, &dW, &ws, 1, dE, st);
+  return launch_embed_bwd_multi(&p, &ids, &dW, &ws, 1, dE, status, st);
+}
+
+cudaError_t launch_embed_bwd_plan(const vce_problem& p, const int64_t* ids, void* ws, cudaStream_t st) {
+  return launch_embed_bwd_plan_multi(&p, &ids, &ws, 1, st);
+}
+
+cudaError_t launch_embed_bwd_apply(const vce_problem& p, const void* dE, float* dW, void* ws, int32_t* status,
+                                   cudaStream_t st) {
+  return launch_embed_bwd_apply_multi(&p, &dW, &ws, 1, dE, status, st);
 }
 
 }  // namespace vce

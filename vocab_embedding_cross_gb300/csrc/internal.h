@@ -131,13 +131,19 @@ cudaError_t launch_embed_fwd(const vce_problem& p, const int64_t* ids, const voi
 size_t embed_bwd_ws_bytes(const vce_problem& p);
 // False when the embedding backward's work items would not fit in 32 bits.
 bool embed_bwd_supported(const vce_problem& p);
+// The backward is a plan (the sort of the ids into runs, kept in the
+// workspace) followed by its application to dE. launch_embed_bwd does both;
+// the apply leaves the plan unchanged, so it can be applied again.
 cudaError_t launch_embed_bwd(const vce_problem& p, const int64_t* ids, const void* dE, float* dW, void* ws,
                              int32_t* status, cudaStream_t st);
+cudaError_t launch_embed_bwd_plan(const vce_problem& p, const int64_t* ids, void* ws, cudaStream_t st);
+cudaError_t launch_embed_bwd_apply(const vce_problem& p, const void* dE, float* dW, void* ws, int32_t* status,
+                                   cudaStream_t st);
 // n (1 to 3) backward problems with the same T, H and dtype and the same dE,
 // each with its own ids, dW and workspace (embed_bwd_ws_bytes of it): one
 // header-zeroing launch, one sort per problem, one reduce over all of them.
 cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* ids, float* const* dW,
-                                   void* const* ws, int n, const void* dE, cudaStream_t st);
+                                   void* const* ws, int n, const void* dE, int32_t* status, cudaStream_t st);
 
 // Merge of the forward partials into lse, per-token loss and the mean. The
 // forward kernel before it zeroes `counter` (the merge's last-block counter).

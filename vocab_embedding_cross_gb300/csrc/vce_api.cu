@@ -352,6 +352,31 @@ vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* d
   return cuda_status(launch_embed_bwd(*p, ids, dE, dW, ws, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+vce_status vce_embed_bwd_plan(const vce_problem* p, const int64_t* ids, void* ws, size_t ws_bytes,
+                              int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (p->T == 0) return VCE_OK;
+  if (!ids) return VCE_ERR_ARG;
+  if (!aligned(ids, 8)) return VCE_ERR_UNSUPPORTED;
+  if (!embed_bwd_supported(*p)) return VCE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < embed_bwd_ws_bytes(*p)) return VCE_ERR_WORKSPACE;
+  return cuda_status(launch_embed_bwd_plan(*p, ids, ws, static_cast<cudaStream_t>(stream)));
+}
+
+vce_status vce_embed_bwd_apply(const vce_problem* p, const void* dE, float* dW, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, void* stream) {
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (p->T == 0) return VCE_OK;
+  if (!dE || !dW) return VCE_ERR_ARG;
+  if (!aligned(dE, 16) || !aligned(dW, 16)) return VCE_ERR_UNSUPPORTED;
+  if (!embed_bwd_supported(*p)) return VCE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < embed_bwd_ws_bytes(*p)) return VCE_ERR_WORKSPACE;
+  return cuda_status(launch_embed_bwd_apply(*p, dE, dW, ws, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 vce_status vce_loss_fwd(const vce_problem* p, const void* h, const void* W, const int64_t* targets, float* loss,
                         float* lse, float* token_loss, int32_t* target_owner, int32_t* max_owner, void* ws,
                         size_t ws_bytes, int32_t* dev_status, void* stream) {
@@ -641,7 +666,7 @@ vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const v
     pws[n] = pws[2];
     ++n;
   }
-  return cuda_status(launch_embed_bwd_multi(ps, pid, pdw, pws, n, dE, st));
+  return cuda_status(launch_embed_bwd_multi(ps, pid, pdw, pws, n, dE, dev_status, st));
 }
 
 vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* stream) {
