@@ -672,7 +672,9 @@ def run_ngram(args, vce, D, I, wl, d, p, W, dE, stream, peaks):
     """vce_ngram_embed_fwd / _bwd on the main workload's ids (4 sequences of
     2048) with two hashed tables of 2^18 rows: time per call and GB/s of the
     algorithmic bytes (ids, distinct rows read, E written; dE read once per
-    table, touched rows read-modify-written in fp32)."""
+    table, touched rows read-modify-written in fp32). The backward is also
+    timed in its two parts: the plan (vce_ngram_embed_bwd_plan) and its
+    application (vce_ngram_embed_bwd_apply), which moves all of its bytes."""
     import torch
     M, L = I.NGRAM_ROWS, I.NGRAM_SEQ_LEN
     T, H = wl.T, wl.H
@@ -711,6 +713,10 @@ def run_ngram(args, vce, D, I, wl, d, p, W, dE, stream, peaks):
     f_ms = timed(lambda: vce.vce_ngram_embed_fwd(p, ids, W, T2, M, T3, M, E, seq_len=L, dev_status=st, stream=sp), n)
     b_ms = timed(lambda: vce.vce_ngram_embed_bwd(p, ids, dE, dW, dT2, M, dT3, M, ws, seq_len=L, dev_status=st,
                                                  stream=sp), n)
+    # the backward split at its plan (row indices and the three sorts), then
+    # the application alone (the workspace keeps the plan of these ids)
+    pl_ms = timed(lambda: vce.vce_ngram_embed_bwd_plan(p, ids, M, M, ws, seq_len=L, dev_status=st, stream=sp), n)
+    a_ms = timed(lambda: vce.vce_ngram_embed_bwd_apply(p, dE, dW, dT2, M, dT3, M, ws, dev_status=st, stream=sp), n)
     assert int(st.item()) == 0, vce.status_str(int(st.item()))
     del T2, T3, dT2, dT3, dW, ws
     torch.cuda.empty_cache()
@@ -719,7 +725,10 @@ def run_ngram(args, vce, D, I, wl, d, p, W, dE, stream, peaks):
             "fwd_GBps": round(fwd_bytes / (f_ms / 1e3) / 1e9, 1),
             "fwd_frac": round(fwd_bytes / (f_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
             "bwd_us": round(b_ms * 1e3, 2), "bwd_GBps": round(bwd_bytes / (b_ms / 1e3) / 1e9, 1),
-            "bwd_frac": round(bwd_bytes / (b_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
+            "bwd_frac": round(bwd_bytes / (b_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "bwd_plan_us": round(pl_ms * 1e3, 2),
+            "bwd_apply_us": round(a_ms * 1e3, 2), "bwd_apply_GBps": round(bwd_bytes / (a_ms / 1e3) / 1e9, 1),
+            "bwd_apply_frac": round(bwd_bytes / (a_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
 
 
 def run_sampled(args, vce, D, I, stream, peaks, full_loss_tok_s):

@@ -354,6 +354,24 @@ vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const v
                                int32_t* dev_status, void* stream);
 
 /*
+ * vce_ngram_embed_bwd in two parts, as vce_embed_bwd_plan / _apply are for
+ * the token table: the plan (the tables' row indices and the sort of every
+ * table's (row, t) pairs) depends on the ids alone; the application adds dE
+ * into dW, dT2 and dT3 by it, with the bits of vce_ngram_embed_bwd, and leaves
+ * the plan unchanged. vce_ngram_embed_bwd also leaves its plan in `ws`. The
+ * application must pass the p, M2 and M3 of the plan; a table whose part of
+ * the workspace holds no plan of this T, column count and row count adds
+ * nothing to any table and reports VCE_ERR_ARG to dev_status. Workspace:
+ * vce_ngram_workspace_size(p) bytes for both.
+ */
+vce_status vce_ngram_embed_bwd_plan(const vce_problem* p, const int64_t* ids, int64_t M2, int64_t M3,
+                                    int64_t seq_len, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                    void* stream);
+vce_status vce_ngram_embed_bwd_apply(const vce_problem* p, const void* dE, float* dW, float* dT2, int64_t M2,
+                                     float* dT3, int64_t M3, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                     void* stream);
+
+/*
  * Loss forward without a caller workspace. The method's pages have no
  * counterpart to this call; it exists for callers that cannot allocate device
  * memory (a plugin inside a framework that owns all device memory and hands it

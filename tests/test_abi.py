@@ -87,6 +87,16 @@ def test_null_pointers_rejected(L):
     assert L.vce_embed_bwd_plan(ctypes.byref(p), None, 0x4000, 1 << 30, None, None) == vce.VCE_ERR_ARG
     assert L.vce_embed_bwd_apply(ctypes.byref(p), None, 0x2000, 0x4000, 1 << 30, None, None) == vce.VCE_ERR_ARG
     assert L.vce_embed_bwd_apply(ctypes.byref(p), 0x2000, None, 0x4000, 1 << 30, None, None) == vce.VCE_ERR_ARG
+    assert L.vce_ngram_embed_bwd_plan(ctypes.byref(p), None, 64, 64, 0, 0x4000, 1 << 30, None, None) == \
+        vce.VCE_ERR_ARG
+    assert L.vce_ngram_embed_bwd_plan(ctypes.byref(p), 0x1000, -1, 64, 0, 0x4000, 1 << 30, None, None) == \
+        vce.VCE_ERR_ARG
+    assert L.vce_ngram_embed_bwd_plan(ctypes.byref(p), 0x1000, 64, 64, -1, 0x4000, 1 << 30, None, None) == \
+        vce.VCE_ERR_ARG                            # negative sequence length
+    assert L.vce_ngram_embed_bwd_apply(ctypes.byref(p), 0x2000, 0x3000, None, 64, None, 0, 0x4000, 1 << 30,
+                                       None, None) == vce.VCE_ERR_ARG   # a 2-gram table without its gradient
+    assert L.vce_ngram_embed_bwd_apply(ctypes.byref(p), None, 0x3000, None, 0, None, 0, 0x4000, 1 << 30,
+                                       None, None) == vce.VCE_ERR_ARG
     # an empty batch has nothing to plan or apply
     p0 = P(T=0)
     assert L.vce_embed_bwd_plan(ctypes.byref(p0), None, None, 0, None, None) == vce.VCE_OK
@@ -156,6 +166,11 @@ def test_workspace_too_small_rejected_on_host(L):
     assert L.vce_embed_bwd_apply(ctypes.byref(p), 0x2000, 0x3000, None, need, None, None) == vce.VCE_ERR_WORKSPACE
     assert L.vce_embed_bwd_apply(ctypes.byref(p), 0x2008, 0x3000, 0x4000, need, None, None) == \
         vce.VCE_ERR_UNSUPPORTED                    # dE not 16-byte aligned
+    ng = vce.vce_ngram_workspace_size(p)
+    assert L.vce_ngram_embed_bwd_plan(ctypes.byref(p), 0x1000, 64, 64, 0, 0x4000, ng - 1, None, None) == \
+        vce.VCE_ERR_WORKSPACE
+    assert L.vce_ngram_embed_bwd_apply(ctypes.byref(p), 0x2000, 0x3000, 0x5000, 64, 0x6000, 64, 0x4010, ng,
+                                       None, None) == vce.VCE_ERR_WORKSPACE
 
 
 def test_sampled_candidates_rejected_on_host(L):

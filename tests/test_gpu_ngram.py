@@ -123,3 +123,54 @@ def test_ngram_qwen3_full_size():
     want = _replays(wl, ids, d["dE"], M, M, L, zeros)
     for g, w in zip(got, want):
         assert np.array_equal(g.view(np.uint32), w.view(np.uint32))
+
+
+@pytest.mark.parametrize("T,H,V_real,Vp,M2,M3,seq_len", [
+    (300, 128, 1000, 1024, 613, 1024, 50),
+    (129, 64, 1000, 1024, 0, 97, 16),                 # 2-gram table left out
+    (12000, 16, 5000, 5056, 613, 1 << 18, 3000),     # three clustered counting sorts
+])
+def test_ngram_plan_then_apply(T, H, V_real, Vp, M2, M3, seq_len):
+    """The backward split at its plan: the tables' row indices and sorts made
+    from the ids alone, then applied to dE twice (each time the bits of the
+    replay, the second on top of the first); a plan of another batch size
+    adds nothing to any table and reports VCE_ERR_ARG."""
+    wl, d, _, _ = _case("bf16", T, H, V_real, Vp, M2, M3, seed=90 + T)
+    ids = d["ids"]
+    p = R.prob(wl)
+    rng = np.random.default_rng(10)
+    inits = [rng.standard_normal((wl.Vp, wl.H)).astype(np.float32),
+             rng.standard_normal((max(M2, 1), wl.H)).astype(np.float32),
+             rng.standard_normal((max(M3, 1), wl.H)).astype(np.float32)]
+    dW = torch.from_numpy(inits[0].copy()).cuda()
+    dT2 = torch.from_numpy(inits[1].copy()).cuda() if M2 else None
+    dT3 = torch.from_numpy(inits[2].copy()).cuda() if M3 else None
+    ws = D.workspace(R.vce.vce_ngram_workspace_size(p))
+    st = R.status_word()
+    R.vce.vce_ngram_embed_bwd_plan(p, torch.from_numpy(ids).cuda(), M2, M3, ws, seq_len=seq_len, dev_status=st)
+    dE_d = D.to_device(d["dE"])
+    want = inits
+    for _ in range(2):
+        R.vce.vce_ngram_embed_bwd_apply(p, dE_d, dW, dT2, M2, dT3, M3, ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        want = _replays(wl, ids, d["dE"], M2, M3, seq_len, [w if w is not None else inits[i]
+                                                               for i, w in enumerate(want)])
+        got = [x.cpu().numpy() if x is not None else None for x in (dW, dT2, dT3)]
+        for g, w in zip(got, want):
+            if g is not None:
+                assert np.array_equal(g.view(np.uint32), w.view(np.uint32))
+    # a plan of one token fewer in the same (cleared) workspace: refused, nothing
+    # added (its tables' parts of the workspace sit at other offsets, so the
+    # apply finds either no plan or the short one)
+    before = [x.clone() if x is not None else None for x in (dW, dT2, dT3)]
+    ws.zero_()
+    p_short = R.prob(wl, T=wl.T - 1)
+    R.vce.vce_ngram_embed_bwd_plan(p_short, torch.from_numpy(ids[:-1].copy()).cuda(), M2, M3, ws, seq_len=seq_len)
+    st = R.status_word()
+    R.vce.vce_ngram_embed_bwd_apply(p, dE_d, dW, dT2, M2, dT3, M3, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 1   # VCE_ERR_ARG
+    for a, b in zip((dW, dT2, dT3), before):
+        if a is not None:
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))

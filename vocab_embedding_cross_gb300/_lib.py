@@ -86,6 +86,12 @@ def lib():
         L.vce_ngram_embed_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
                                           c_int64, c_void_p, c_size_t, c_void_p, c_void_p]
         L.vce_ngram_embed_bwd.restype = c_int32
+        L.vce_ngram_embed_bwd_plan.argtypes = [P, c_void_p, c_int64, c_int64, c_int64, c_void_p, c_size_t, c_void_p,
+                                               c_void_p]
+        L.vce_ngram_embed_bwd_plan.restype = c_int32
+        L.vce_ngram_embed_bwd_apply.argtypes = [P, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
+                                                c_void_p, c_size_t, c_void_p, c_void_p]
+        L.vce_ngram_embed_bwd_apply.restype = c_int32
         L.vce_sampled_workspace_size.argtypes = [P, c_int64]
         L.vce_sampled_workspace_size.restype = c_size_t
         L.vce_sampled_loss.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_float,
@@ -248,6 +254,20 @@ def vce_ngram_embed_bwd(p, ids, dE, dW, dT2, M2, dT3, M3, ws, ws_bytes=None, seq
     _check(lib().vce_ngram_embed_bwd(ctypes.byref(p), _ptr(ids), _ptr(dE), _ptr(dW), _ptr(dT2), int(M2), _ptr(dT3),
                                      int(M3), int(seq_len), _ptr(ws), nb, _ptr(dev_status), _stream(stream)),
            "vce_ngram_embed_bwd")
+
+
+def vce_ngram_embed_bwd_plan(p, ids, M2, M3, ws, ws_bytes=None, seq_len=0, dev_status=None, stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().vce_ngram_embed_bwd_plan(ctypes.byref(p), _ptr(ids), int(M2), int(M3), int(seq_len), _ptr(ws), nb,
+                                          _ptr(dev_status), _stream(stream)), "vce_ngram_embed_bwd_plan")
+
+
+def vce_ngram_embed_bwd_apply(p, dE, dW, dT2, M2, dT3, M3, ws, ws_bytes=None, dev_status=None,
+                              stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().vce_ngram_embed_bwd_apply(ctypes.byref(p), _ptr(dE), _ptr(dW), _ptr(dT2), int(M2), _ptr(dT3),
+                                           int(M3), _ptr(ws), nb, _ptr(dev_status), _stream(stream)),
+           "vce_ngram_embed_bwd_apply")
 
 
 def vce_embed_bwd_chunk() -> int:

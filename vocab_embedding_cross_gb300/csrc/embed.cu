@@ -106,16 +106,18 @@ struct __align__(16) RunDesc {
 };
 
 // The workspace header (16 words). The sorts claim space with atomic
-// additions on words 0-5; the reduce hands out items from word 6; words 8-10
-// describe the plan (its T, its column slices per row and a marker), so that
-// applying a plan made for another shape, or a workspace that holds none, is
-// refused on the device.
-constexpr int kHdrItem = 6, kHdrPlanT = 8, kHdrPlanNh = 9, kHdrPlanMark = 10;
+// additions on words 0-5; the reduce hands out items from word 6; words 8-11
+// describe the plan (its T, its column slices per row, a marker and the number
+// of rows its ids index), so that applying a plan made for another shape, or a
+// workspace that holds none, is refused on the device before any row is
+// touched.
+constexpr int kHdrItem = 6, kHdrPlanT = 8, kHdrPlanNh = 9, kHdrPlanMark = 10, kHdrPlanRows = 11;
 constexpr int32_t kPlanMark = 0x4E414C50;   // "PLAN"
 
-__device__ __forceinline__ void plan_seal(int32_t* hdr, int T, int nh) {
+__device__ __forceinline__ void plan_seal(int32_t* hdr, int T, int nh, int64_t V_real) {
   hdr[kHdrPlanT] = T;
   hdr[kHdrPlanNh] = nh;
+  hdr[kHdrPlanRows] = static_cast<int32_t>(V_real);
   hdr[kHdrPlanMark] = kPlanMark;
 }
 
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kSortThreads, 1)
     hdr[4] = n_runs - (nseg - n_multi);
     hdr[5] = 0;
     hdr[kHdrItem] = 0;   // the reduce's item counter
-    plan_seal(hdr, T, nh);
+    plan_seal(hdr, T, nh, V_real);
   }
 }
 
@@ -590,7 +592,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   grid_dep_wait();
   int tb = 0;
   if (tid == 0 && m > 0) tb = atomicAdd(&hdr[0], m);
-  if (tid == 0 && b == 0) plan_seal(hdr, T, nh);
+  if (tid == 0 && b == 0) plan_seal(hdr, T, nh, V_real);
 
   // Phase B: stable LSD radix passes over the id / NB bits.
   const int kpw = ((m + kBktWarps - 1) / kBktWarps + 31) & ~31;
@@ -882,7 +884,7 @@ __global__ void __launch_bounds__(kSortThreads, 1)
   if (tid == 0) {
     hdr[0] = n;
     hdr[2] = nseg;
-    plan_seal(hdr, static_cast<int>(T), nh);
+    plan_seal(hdr, static_cast<int>(T), nh, V_real);
   }
 }
 
@@ -1136,7 +1138,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   grid_dep_wait();
   int tb = 0;
   if (tid == 0 && m > 0) tb = atomicAdd(&hdr[0], m);
-  if (tid == 0 && b == 0) plan_seal(hdr, T, nh);
+  if (tid == 0 && b == 0) plan_seal(hdr, T, nh, V_real);
   __syncthreads();
 
   // Counting warp w takes part w % (kCntWarps / CL) of segment w / (kCntWarps / CL).
@@ -1276,6 +1278,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
 // launch, their items numbered one problem after the other.
 struct EmbSlot {
   int32_t* hdr;
+  int32_t rows;   // V_real of the problem: the plan must index the same rows
   const int32_t* tsorted;
   const RunDesc* runs;
   float* dW;
@@ -1301,12 +1304,13 @@ __global__ void __launch_bounds__(128)
   __shared__ int s_next[2];
   const int lane = threadIdx.x & 31;
   grid_dep_wait();   // the sorts' headers, runs and tokens
-  // Every problem must hold a plan made for this shape (T = cap); otherwise
-  // nothing is added and the call reports VCE_ERR_ARG.
+  // Every problem must hold a plan made for this shape (T = cap, the same
+  // column slices and rows); otherwise nothing is added and the call reports
+  // VCE_ERR_ARG.
   bool planned = true;
   for (int k = 0; k < sl.n; ++k)
     planned = planned && sl.s[k].hdr[kHdrPlanMark] == kPlanMark && sl.s[k].hdr[kHdrPlanT] == cap &&
-              sl.s[k].hdr[kHdrPlanNh] == nh;
+              sl.s[k].hdr[kHdrPlanNh] == nh && sl.s[k].hdr[kHdrPlanRows] == sl.s[k].rows;
   if (!planned) {
     if (blockIdx.x == 0 && threadIdx.x == 0 && status) atomicCAS(status, 0, static_cast<int>(VCE_ERR_ARG));
     return;
@@ -1481,6 +1485,7 @@ EmbSlot emb_slot(const vce_problem& p, void* ws, float* dW) {
   char* b = static_cast<char*>(ws);
   EmbSlot sl;
   sl.hdr = reinterpret_cast<int32_t*>(b + L.hdr);
+  sl.rows = static_cast<int32_t>(p.V_real);
   sl.tsorted = reinterpret_cast<const int32_t*>(b + L.tsorted);
   sl.runs = reinterpret_cast<const RunDesc*>(b + L.runs);
   sl.dW = dW;

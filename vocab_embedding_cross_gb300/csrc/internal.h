@@ -144,6 +144,12 @@ cudaError_t launch_embed_bwd_apply(const vce_problem& p, const void* dE, float* 
 // header-zeroing launch, one sort per problem, one reduce over all of them.
 cudaError_t launch_embed_bwd_multi(const vce_problem* ps, const int64_t* const* ids, float* const* dW,
                                    void* const* ws, int n, const void* dE, int32_t* status, cudaStream_t st);
+// The same in its two parts: the plans of the n problems (one zeroing launch,
+// one sort each), and one reduce that applies them all to dE.
+cudaError_t launch_embed_bwd_plan_multi(const vce_problem* ps, const int64_t* const* ids, void* const* ws, int n,
+                                        cudaStream_t st);
+cudaError_t launch_embed_bwd_apply_multi(const vce_problem* ps, float* const* dW, void* const* ws, int n,
+                                         const void* dE, int32_t* status, cudaStream_t st);
 
 // Merge of the forward partials into lse, per-token loss and the mean. The
 // forward kernel before it zeroes `counter` (the merge's last-block counter).

@@ -629,6 +629,68 @@ size_t vce_ngram_workspace_size(const vce_problem* p) {
   return 2 * align_up(sizeof(int64_t) * static_cast<size_t>(p->T), kWsAlign) + 3 * embed_bwd_ws_bytes(*p);
 }
 
+namespace {
+// The n-gram backward's problems: the token table, then the 2-gram and 3-gram
+// tables that are present, each with its row indices and its part of the
+// workspace (the two row-index arrays, then one embedding-backward workspace
+// per table).
+struct NgramBwd {
+  vce_problem ps[3];
+  const int64_t* pid[3];
+  float* pdw[3];
+  void* pws[3];
+  int n;
+  int64_t* idx2;
+  int64_t* idx3;
+};
+NgramBwd ngram_bwd(const vce_problem& p, const int64_t* ids, float* dW, float* dT2, int64_t M2, float* dT3,
+                   int64_t M3, void* ws) {
+  NgramBwd g{};
+  char* b = static_cast<char*>(ws);
+  const size_t ids_bytes = align_up(sizeof(int64_t) * static_cast<size_t>(p.T), kWsAlign);
+  const size_t ews_bytes = embed_bwd_ws_bytes(p);
+  g.idx2 = reinterpret_cast<int64_t*>(b);
+  g.idx3 = reinterpret_cast<int64_t*>(b + ids_bytes);
+  g.ps[0] = p;
+  g.pid[0] = ids;
+  g.pdw[0] = dW;
+  g.pws[0] = b + 2 * ids_bytes;
+  g.n = 1;
+  if (M2 > 0) {
+    g.ps[g.n] = ngram_table_problem(p, M2);
+    g.pid[g.n] = g.idx2;
+    g.pdw[g.n] = dT2;
+    g.pws[g.n] = b + 2 * ids_bytes + ews_bytes;
+    ++g.n;
+  }
+  if (M3 > 0) {
+    g.ps[g.n] = ngram_table_problem(p, M3);
+    g.pid[g.n] = g.idx3;
+    g.pdw[g.n] = dT3;
+    g.pws[g.n] = b + 2 * ids_bytes + 2 * ews_bytes;
+    ++g.n;
+  }
+  return g;
+}
+
+// Row indices of the present tables, then their plans.
+cudaError_t ngram_plan(const vce_problem& p, const int64_t* ids, int64_t M2, int64_t M3, int64_t seq_len,
+                       const NgramBwd& g, cudaStream_t st) {
+  if (M2 > 0)
+    if (cudaError_t e = launch_ngram_hash(ids, p.T, 2, p.V_real, M2, seq_len, g.idx2, st)) return e;
+  if (M3 > 0)
+    if (cudaError_t e = launch_ngram_hash(ids, p.T, 3, p.V_real, M3, seq_len, g.idx3, st)) return e;
+  return launch_embed_bwd_plan_multi(g.ps, g.pid, g.pws, g.n, st);
+}
+
+// The backward's size and workspace rules (after check_problem, for T > 0).
+vce_status ngram_bwd_check(const vce_problem* p, const void* ws, size_t ws_bytes) {
+  if (!embed_bwd_supported(*p)) return VCE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < vce_ngram_workspace_size(p)) return VCE_ERR_WORKSPACE;
+  return VCE_OK;
+}
+}  // namespace
+
 vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const void* dE, float* dW, float* dT2,
                                int64_t M2, float* dT3, int64_t M3, int64_t seq_len, void* ws, size_t ws_bytes,
                                int32_t* dev_status, void* stream) {
@@ -639,34 +701,43 @@ vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const v
   if (!ids || !dE || !dW) return VCE_ERR_ARG;
   if (!aligned(ids, 8) || !aligned(dE, 16) || !aligned(dW, 16) || !aligned(dT2, 16) || !aligned(dT3, 16))
     return VCE_ERR_UNSUPPORTED;
-  if (!embed_bwd_supported(*p)) return VCE_ERR_UNSUPPORTED;
-  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < vce_ngram_workspace_size(p)) return VCE_ERR_WORKSPACE;
+  if ((s = ngram_bwd_check(p, ws, ws_bytes)) != VCE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  char* b = static_cast<char*>(ws);
-  const size_t ids_bytes = align_up(sizeof(int64_t) * static_cast<size_t>(p->T), kWsAlign);
-  int64_t* idx2 = reinterpret_cast<int64_t*>(b);
-  int64_t* idx3 = reinterpret_cast<int64_t*>(b + ids_bytes);
-  const size_t ews_bytes = embed_bwd_ws_bytes(*p);
-  // The row indices first; then the three tables' backward problems are
-  // sorted one after the other and reduced in one launch.
-  vce_problem ps[3] = {*p, ngram_table_problem(*p, M2 > 0 ? M2 : 1), ngram_table_problem(*p, M3 > 0 ? M3 : 1)};
-  const int64_t* pid[3] = {ids, idx2, idx3};
-  float* pdw[3] = {dW, dT2, dT3};
-  void* pws[3] = {b + 2 * ids_bytes, b + 2 * ids_bytes + ews_bytes, b + 2 * ids_bytes + 2 * ews_bytes};
-  int n = 1;
-  if (M2 > 0) {
-    if (cudaError_t e = launch_ngram_hash(ids, p->T, 2, p->V_real, M2, seq_len, idx2, st)) return cuda_status(e);
-    ++n;
-  }
-  if (M3 > 0) {
-    if (cudaError_t e = launch_ngram_hash(ids, p->T, 3, p->V_real, M3, seq_len, idx3, st)) return cuda_status(e);
-    ps[n] = ps[2];
-    pid[n] = idx3;
-    pdw[n] = dT3;
-    pws[n] = pws[2];
-    ++n;
-  }
-  return cuda_status(launch_embed_bwd_multi(ps, pid, pdw, pws, n, dE, dev_status, st));
+  // The row indices first; then the tables' backward problems are sorted one
+  // after the other and reduced in one launch.
+  const NgramBwd g = ngram_bwd(*p, ids, dW, dT2, M2, dT3, M3, ws);
+  if (cudaError_t e = ngram_plan(*p, ids, M2, M3, seq_len, g, st)) return cuda_status(e);
+  return cuda_status(launch_embed_bwd_apply_multi(g.ps, g.pdw, g.pws, g.n, dE, dev_status, st));
+}
+
+vce_status vce_ngram_embed_bwd_plan(const vce_problem* p, const int64_t* ids, int64_t M2, int64_t M3,
+                                    int64_t seq_len, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  const int64_t lim = int64_t(1) << 31;
+  if (M2 < 0 || M2 >= lim || M3 < 0 || M3 >= lim || seq_len < 0) return VCE_ERR_ARG;
+  if (p->T == 0) return VCE_OK;
+  if (!ids) return VCE_ERR_ARG;
+  if (!aligned(ids, 8)) return VCE_ERR_UNSUPPORTED;
+  if ((s = ngram_bwd_check(p, ws, ws_bytes)) != VCE_OK) return s;
+  const NgramBwd g = ngram_bwd(*p, ids, nullptr, nullptr, M2, nullptr, M3, ws);
+  return cuda_status(ngram_plan(*p, ids, M2, M3, seq_len, g, static_cast<cudaStream_t>(stream)));
+}
+
+vce_status vce_ngram_embed_bwd_apply(const vce_problem* p, const void* dE, float* dW, float* dT2, int64_t M2,
+                                     float* dT3, int64_t M3, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                     void* stream) {
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (!ngram_tables_ok(M2, dT2, M3, dT3)) return VCE_ERR_ARG;
+  if (p->T == 0) return VCE_OK;
+  if (!dE || !dW) return VCE_ERR_ARG;
+  if (!aligned(dE, 16) || !aligned(dW, 16) || !aligned(dT2, 16) || !aligned(dT3, 16)) return VCE_ERR_UNSUPPORTED;
+  if ((s = ngram_bwd_check(p, ws, ws_bytes)) != VCE_OK) return s;
+  const NgramBwd g = ngram_bwd(*p, nullptr, dW, dT2, M2, dT3, M3, ws);
+  return cuda_status(
+      launch_embed_bwd_apply_multi(g.ps, g.pdw, g.pws, g.n, dE, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 vce_status vce_wait_selftest(uint64_t limit_ns, int32_t* dev_status, void* stream) {
