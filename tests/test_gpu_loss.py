@@ -248,11 +248,12 @@ def test_loss_gptoss_full():
 
 def test_qwen3_tied_pipeline_full():
     """The Qwen3-like tied step at full size (T=8192, H=2048, V=151936, S=8),
-    run as one pipeline on one W and one fp32 dW, with the tied flag set:
-    embedding lookup of the input ids, loss forward, loss backward adding the
-    head's gradient into dW, embedding backward adding the input gradient into
-    the same dW ("Vocabulary shards", paragraph 2: one logical parameter, all
-    contributions combined). Checked against the oracle: the lookup bit for
+    run as one pipeline on one W and one fp32 dW, with the tied flag set and
+    in the order the benchmark runs it: embedding lookup of the input ids and
+    the embedding backward's plan, loss forward, loss backward adding the
+    head's gradient into dW, and the plan's application adding the input
+    gradient into the same dW ("Vocabulary shards", paragraph 2: one logical
+    parameter, all contributions combined). Checked against the oracle: the lookup bit for
     bit; the loss scalar, every lse and every token loss; the head's dW rows of
     the most frequent (Zipf head) ids, random ids and the last id; the
     embedding's contribution to every touched row; and the combined rows."""
@@ -263,9 +264,12 @@ def test_qwen3_tied_pipeline_full():
     tol = TOL["bf16"]
     rng = np.random.default_rng(1)
     W_d, h_d, dE_d = D.to_device(W), D.to_device(h), D.to_device(dE)
-    # 1. lookup
+    # 1. lookup, and the embedding backward's plan while the ids are at hand
     E = R.embed_fwd(wl, W_d, ids, maps=False)["E"]
     assert np.array_equal(E, O.embed_forward(ids, W, wl.V_real))
+    p = R.prob(wl)
+    ws_e = D.workspace(R.vce.vce_workspace_size(p, R.vce.VCE_OP_EMBED_BWD))
+    R.vce.vce_embed_bwd_plan(p, torch.from_numpy(ids).cuda(), ws_e)
     # 2. loss forward
     out = R.loss_fwd(wl, h_d, W_d, y)
     assert out["status"] == 0
@@ -279,8 +283,11 @@ def test_qwen3_tied_pipeline_full():
     touched = np.unique(ids[(ids >= 0) & (ids < wl.V_real)])
     touched_d = torch.from_numpy(touched).cuda()
     head_touched = dW.index_select(0, touched_d).double()
-    # 4. embedding backward into the same dW
-    assert R.embed_bwd(wl, ids, dE_d, dW) == 0
+    # 4. the embedding backward (the plan applied to dE) into the same dW
+    st_e = R.status_word()
+    R.vce.vce_embed_bwd_apply(p, dE_d, dW, ws_e, dev_status=st_e)
+    torch.cuda.synchronize()
+    assert int(st_e.item()) == 0
     _check_sampled_rows(wl, d, out, dH, tol, rng)
     ref_head = _check_full_batch(wl, d, out, head_rows, vs, tol)
     ref_embed = O.embed_backward(ids, dE, wl.V_real, wl.Vp)
