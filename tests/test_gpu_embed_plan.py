@@ -151,3 +151,26 @@ def test_apply_repeated_in_a_graph():
         ref = O.embed_backward_replay_f32(ids, dE32, wl.V_real, CHUNK, ref)
         rows = dW_d.index_select(0, uniq_d).cpu().numpy()
         assert np.array_equal(_bits(rows), _bits(ref[uniq]))
+
+
+def test_plan_then_apply_f32():
+    """The fp32 reduce by a plan: the tiny fp32 case (T=64, H=64, ids mixing
+    real, padded-row, padding and out-of-range values), bit-exact against the
+    replay, twice on the same plan."""
+    wl = I.WORKLOADS["tiny_f32"]
+    d = I.make_all(wl, ("ids", "dE"))
+    ids, dE = d["ids"], d["dE"]
+    p = R.prob(wl)
+    ws = D.workspace(R.vce.vce_workspace_size(p, R.vce.VCE_OP_EMBED_BWD))
+    st = R.status_word()
+    R.vce.vce_embed_bwd_plan(p, torch.from_numpy(ids).cuda(), ws, dev_status=st)
+    dW0 = np.random.default_rng(47).standard_normal((wl.Vp, wl.H)).astype(np.float32)
+    dW_d = torch.from_numpy(dW0.copy()).cuda()
+    dE_d = torch.from_numpy(dE).cuda()
+    ref = dW0
+    for _ in range(2):
+        R.vce.vce_embed_bwd_apply(p, dE_d, dW_d, ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ref = O.embed_backward_replay_f32(ids, dE, wl.V_real, CHUNK, ref)
+        assert np.array_equal(_bits(dW_d.cpu().numpy()), _bits(ref))
