@@ -76,8 +76,8 @@ def arm_config(workload: str, world: int) -> dict:
     from vocab_embedding_cross_gb300 import inputs as I
     wl = I.WORKLOADS[workload]
     return {"workload": f"{workload}: T={wl.T} H={wl.H} V_real={wl.V_real} Vp={wl.Vp} S={wl.S} tied={wl.tied}",
-            "step": "embed_fwd + embed_bwd_plan (the ids' sort) + loss_fwd + loss_bwd (writes the tied dW) + "
-                    "embed_bwd_apply (adds into it)",
+            "step": "embed_fwd_plan (the lookup, beside the sort of the ids for the backward) + loss_fwd + "
+                    "loss_bwd (writes the tied dW) + embed_bwd_apply (adds into it)",
             "l2": "inputs larger than L2 (W 622 MB, G chunks of 1.25 GB); no extra flush",
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
@@ -207,10 +207,10 @@ def run_ours(args):
     sp = stream.cuda_stream
 
     # The embedding backward's plan (the sort of the ids) is made at the lookup,
-    # where the ids are known; the backward then only applies it to dE.
+    # where the ids are known, beside the lookup's row copies; the backward
+    # then only applies it to dE.
     def step_ops():
-        vce.vce_embed_fwd(p, ids, W, E, dev_status=st, stream=sp)
-        vce.vce_embed_bwd_plan(p, ids, ws_e, dev_status=st, stream=sp)
+        vce.vce_embed_fwd_plan(p, ids, W, E, ws_e, dev_status=st, stream=sp)
         vce.vce_loss_fwd(p, h, W, y, loss, lse, ws=ws_f, dev_status=st, stream=sp)
         vce.vce_loss_bwd(p_head, h, W, y, lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp)
         vce.vce_embed_bwd_apply(p, dE, dW, ws_e, dev_status=st, stream=sp)
@@ -591,9 +591,11 @@ def run_embedding(args, vce, D, I, stream, peaks, name):
 
     `bwd_*` is the one-call backward (vce_embed_bwd: the sort of the ids, then
     the addition of dE into dW); `bwd_plan_us` the sort alone
-    (vce_embed_bwd_plan); `bwd_apply_*` the addition by a plan made earlier
-    (vce_embed_bwd_apply), which is all the backward runs once the plan is
-    made at the lookup, and which moves all of the backward's bytes."""
+    (vce_embed_bwd_plan); `gather_with_plan_*` the lookup with the plan made
+    beside it (vce_embed_fwd_plan), credited with the lookup's bytes;
+    `bwd_apply_*` the addition by a plan made earlier (vce_embed_bwd_apply),
+    which is all the backward runs once the plan is made at the lookup, and
+    which moves all of the backward's bytes."""
     import torch
     wl = I.WORKLOADS[name]
     d = I.make_all(wl, ("W", "ids", "dE"))
@@ -636,12 +638,15 @@ def run_embedding(args, vce, D, I, stream, peaks, name):
     bwd = lambda: vce.vce_embed_bwd(p, ids, dE, dW, ws, dev_status=st, stream=sp)
     plan = lambda: vce.vce_embed_bwd_plan(p, ids, ws, dev_status=st, stream=sp)
     apply = lambda: vce.vce_embed_bwd_apply(p, dE, dW, ws, dev_status=st, stream=sp)
+    fwd_plan = lambda: vce.vce_embed_fwd_plan(p, ids, W, E, ws, dev_status=st, stream=sp)
     g_ms, b_ms = timed(fwd, n), timed(bwd, n)
     g_dirty, b_dirty = timed(fwd, n, clean_l2=False), timed(bwd, n, clean_l2=False)
-    # The backward split at its plan: the sort of the ids alone, then the
-    # application of the plan to dE (the workspace holds the plan of these ids,
-    # and every application leaves it in place).
+    # The backward split at its plan: the sort of the ids alone, the lookup
+    # with the plan made beside it, then the application of the plan to dE (the
+    # workspace holds the plan of these ids, and every application leaves it in
+    # place).
     plan_ms = timed(plan, n)
+    gp_ms = timed(fwd_plan, n)
     a_ms, a_dirty = timed(apply, n), timed(apply, n, clean_l2=False)
     assert int(st.item()) == 0, vce.status_str(int(st.item()))
     del W, dE, E, dW, ws, flush, clean
@@ -658,6 +663,7 @@ def run_embedding(args, vce, D, I, stream, peaks, name):
             "gather_us_dirty_l2": round(g_dirty * 1e3, 2), "gather_frac_dirty_l2": frac(gather_bytes, g_dirty),
             "bwd_us_dirty_l2": round(b_dirty * 1e3, 2), "bwd_frac_dirty_l2": frac(bwd_bytes, b_dirty),
             "bwd_plan_us": round(plan_ms * 1e3, 2),
+            "gather_with_plan_us": round(gp_ms * 1e3, 2), "gather_with_plan_frac": frac(gather_bytes, gp_ms),
             "bwd_apply_us": round(a_ms * 1e3, 2), "bwd_apply_GBps": round(bwd_bytes / (a_ms / 1e3) / 1e9, 1),
             "bwd_apply_frac": frac(bwd_bytes, a_ms),
             "bwd_apply_us_dirty_l2": round(a_dirty * 1e3, 2), "bwd_apply_frac_dirty_l2": frac(bwd_bytes, a_dirty),
@@ -826,8 +832,7 @@ def run_e2e(args, vce, D, d, p, p_head, W, E, loss, lse, dH, dW, st, ws_f, ws_b,
         b = i % 2
         stream.wait_event(ready[b])
         x = dev[b]
-        vce.vce_embed_fwd(p, x["ids"], W, E, dev_status=st, stream=sp)
-        vce.vce_embed_bwd_plan(p, x["ids"], ws_e, dev_status=st, stream=sp)
+        vce.vce_embed_fwd_plan(p, x["ids"], W, E, ws_e, dev_status=st, stream=sp)
         vce.vce_loss_fwd(p, x["h"], W, x["targets"], loss, lse, ws=ws_f, dev_status=st, stream=sp)
         vce.vce_loss_bwd(p_head, x["h"], W, x["targets"], lse, 1.0, dH, dW, ws_b, dev_status=st, stream=sp)
         vce.vce_embed_bwd_apply(p, x["dE"], dW, ws_e, dev_status=st, stream=sp)

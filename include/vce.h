@@ -187,6 +187,19 @@ vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* d
  */
 vce_status vce_embed_bwd_plan(const vce_problem* p, const int64_t* ids, void* ws,
                               size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * The lookup and the backward's plan in one call: the results of
+ * vce_embed_fwd (E, owner, local) and of vce_embed_bwd_plan (the plan in
+ * `ws`) for the same ids. The plan's sort reads only the ids and moves almost
+ * no memory, so the lookup's row copies run beside it, on the SMs the sort
+ * leaves free, instead of after it. The call completes, for any later work on
+ * `stream`, only when both have. Arguments as in the two calls;
+ * `dev_status` is unused and may be NULL.
+ */
+vce_status vce_embed_fwd_plan(const vce_problem* p, const int64_t* ids, const void* W,
+                              void* E, int32_t* owner, int32_t* local, void* ws,
+                              size_t ws_bytes, int32_t* dev_status, void* stream);
 vce_status vce_embed_bwd_apply(const vce_problem* p, const void* dE, float* dW,
                                void* ws, size_t ws_bytes, int32_t* dev_status,
                                void* stream);

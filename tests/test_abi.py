@@ -70,6 +70,7 @@ def test_bad_problem_rejected_on_host(L, kw, code):
     assert vce.vce_workspace_size(p, vce.VCE_OP_LOSS_FWD) == vce.SIZE_MAX
     for fn, args in ((L.vce_embed_fwd, (None,) * 7), (L.vce_embed_bwd, (None, None, None, None, 0, None, None)),
                      (L.vce_embed_bwd_plan, (None, None, 0, None, None)),
+                     (L.vce_embed_fwd_plan, (None,) * 6 + (0, None, None)),
                      (L.vce_embed_bwd_apply, (None, None, None, 0, None, None)),
                      (L.vce_loss_fwd, (None,) * 9 + (0, None, None)),
                      (L.vce_loss_bwd, (None, None, None, None, 1.0, None, None, None, 0, None, None))):
@@ -158,6 +159,12 @@ def test_workspace_too_small_rejected_on_host(L):
     assert L.vce_embed_bwd(ctypes.byref(p), 0x1000, 0x2000, 0x3000, 0x4010, need, None, None) == \
         vce.VCE_ERR_WORKSPACE                      # misaligned workspace
     # the plan and its application use the same workspace size and alignment
+    assert L.vce_embed_fwd_plan(ctypes.byref(p), 0x1000, 0x2000, 0x3000, None, None, 0x4000, need - 1, None,
+                                None) == vce.VCE_ERR_WORKSPACE
+    assert L.vce_embed_fwd_plan(ctypes.byref(p), 0x1000, 0x2008, 0x3000, None, None, 0x4000, need, None,
+                                None) == vce.VCE_ERR_UNSUPPORTED   # W not 16-byte aligned
+    assert L.vce_embed_fwd_plan(ctypes.byref(p), 0x1000, None, 0x3000, None, None, 0x4000, need, None,
+                                None) == vce.VCE_ERR_ARG
     assert L.vce_embed_bwd_plan(ctypes.byref(p), 0x1000, 0x4000, need - 1, None, None) == vce.VCE_ERR_WORKSPACE
     assert L.vce_embed_bwd_plan(ctypes.byref(p), 0x1000, 0x4010, need, None, None) == vce.VCE_ERR_WORKSPACE
     assert L.vce_embed_bwd_plan(ctypes.byref(p), 0x1000, None, need, None, None) == vce.VCE_ERR_WORKSPACE

@@ -174,3 +174,32 @@ def test_plan_then_apply_f32():
         assert int(st.item()) == 0
         ref = O.embed_backward_replay_f32(ids, dE, wl.V_real, CHUNK, ref)
         assert np.array_equal(_bits(dW_d.cpu().numpy()), _bits(ref))
+
+
+@pytest.mark.parametrize("case", SHAPES, ids=lambda c: "T{T}_H{H}_V{V_real}".format(**c))
+def test_lookup_with_plan(case):
+    """vce_embed_fwd_plan: the lookup bit-exact (with the ownership maps), and
+    the plan it leaves applied to dE bit-exact against the replay, on every
+    sort path; the call ordered before later work on its stream."""
+    wl, ids, dE1, _ = _inputs(case, 48)
+    W = I.make_W(wl)
+    p = R.prob(wl)
+    ws = D.workspace(R.vce.vce_workspace_size(p, R.vce.VCE_OP_EMBED_BWD))
+    st = R.status_word()
+    E = torch.full((wl.T, wl.H), 7, dtype=torch.bfloat16, device="cuda")
+    owner = torch.full((wl.T,), -7, dtype=torch.int32, device="cuda")
+    local = torch.full((wl.T,), -7, dtype=torch.int32, device="cuda")
+    W_d = D.to_device(W)
+    dW_d = torch.zeros((wl.Vp, wl.H), dtype=torch.float32, device="cuda")
+    # the apply is queued right behind the lookup: it must find the plan complete
+    R.vce.vce_embed_fwd_plan(p, torch.from_numpy(ids).cuda(), W_d, E, ws, owner=owner, local=local, dev_status=st)
+    R.vce.vce_embed_bwd_apply(p, D.to_device(dE1), dW_d, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(D.to_host_bits(E), O.embed_forward(ids, W, wl.V_real))
+    _, own, loc = O.ownership(ids, wl.V_real, wl.Vp, wl.S)
+    assert np.array_equal(owner.cpu().numpy(), own.astype(np.int32))
+    assert np.array_equal(local.cpu().numpy(), loc.astype(np.int32))
+    ref = O.embed_backward_replay_f32(ids, I.bf16_to_f32(dE1), wl.V_real, CHUNK,
+                                      np.zeros((wl.Vp, wl.H), np.float32))
+    assert np.array_equal(_bits(dW_d.cpu().numpy()), _bits(ref))

@@ -64,6 +64,9 @@ def lib():
         L.vce_embed_bwd_plan.restype = c_int32
         L.vce_embed_bwd_apply.argtypes = [P, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
         L.vce_embed_bwd_apply.restype = c_int32
+        L.vce_embed_fwd_plan.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                         c_void_p, c_void_p]
+        L.vce_embed_fwd_plan.restype = c_int32
         L.vce_loss_fwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]
         L.vce_loss_fwd.restype = c_int32
@@ -180,6 +183,13 @@ def vce_embed_bwd_plan(p, ids, ws, ws_bytes=None, dev_status=None, stream=None) 
     nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
     _check(lib().vce_embed_bwd_plan(ctypes.byref(p), _ptr(ids), _ptr(ws), nb, _ptr(dev_status), _stream(stream)),
            "vce_embed_bwd_plan")
+
+
+def vce_embed_fwd_plan(p, ids, W, E, ws, owner=None, local=None, ws_bytes=None, dev_status=None,
+                       stream=None) -> None:
+    nb = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(lib().vce_embed_fwd_plan(ctypes.byref(p), _ptr(ids), _ptr(W), _ptr(E), _ptr(owner), _ptr(local),
+                                    _ptr(ws), nb, _ptr(dev_status), _stream(stream)), "vce_embed_fwd_plan")
 
 
 def vce_embed_bwd_apply(p, dE, dW, ws, ws_bytes=None, dev_status=None, stream=None) -> None:

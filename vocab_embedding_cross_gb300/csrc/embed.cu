@@ -38,10 +38,19 @@ namespace {
 // ---------------------------------------------------------------------------
 constexpr int kGatherWarps = 8;
 
+// BESIDE_PLAN: launched as a dependent of the backward's plan (the sort), which
+// it does not read, so that it runs beside the sort on the SMs the sort leaves
+// free. Its last CTA waits for the sort to end before exiting, so the lookup
+// completes only after the plan does and a kernel that waits for the lookup
+// also sees the plan.
+template <bool BESIDE_PLAN>
 __global__ void __launch_bounds__(kGatherWarps * 32)
     embed_gather_kernel(const int64_t* __restrict__ ids, const uint4* __restrict__ W, uint4* __restrict__ E,
                         int32_t* __restrict__ owner, int32_t* __restrict__ local, int64_t T, int64_t Vp,
                         int64_t V_real, int32_t S, int row_vecs) {
+  if constexpr (BESIDE_PLAN) {
+    if (blockIdx.x == gridDim.x - 1) grid_dep_wait();
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kGatherWarps + warp;
   if (t >= T) return;
@@ -1465,11 +1474,25 @@ cudaError_t launch_embed_fwd(const vce_problem& p, const int64_t* ids, const voi
   const int esize = p.dtype == VCE_BF16 ? 2 : 4;
   const int row_vecs = static_cast<int>(p.H * esize / 16);
   const int64_t blocks = ceil_div(p.T, kGatherWarps);
-  embed_gather_kernel<<<static_cast<unsigned>(blocks), kGatherWarps * 32, 0, st>>>(
+  embed_gather_kernel<false><<<static_cast<unsigned>(blocks), kGatherWarps * 32, 0, st>>>(
       ids, static_cast<const uint4*>(W), static_cast<uint4*>(E), owner, local, p.T, p.Vp, p.V_real, p.S,
       row_vecs);
   note_launch(VCE_K_EMBED_GATHER, st);
   return cudaGetLastError();
+}
+
+cudaError_t launch_embed_fwd_plan(const vce_problem& p, const int64_t* ids, const void* W, void* E, int32_t* owner,
+                                  int32_t* local, void* ws, cudaStream_t st) {
+  if (p.T == 0) return cudaSuccess;
+  if (cudaError_t e = launch_embed_bwd_plan(p, ids, ws, st)) return e;
+  const int esize = p.dtype == VCE_BF16 ? 2 : 4;
+  const int row_vecs = static_cast<int>(p.H * esize / 16);
+  const int64_t blocks = ceil_div(p.T, kGatherWarps);
+  const cudaError_t e = launch_dependent(embed_gather_kernel<true>, dim3(static_cast<unsigned>(blocks)),
+                                         dim3(kGatherWarps * 32), 0, st, ids, static_cast<const uint4*>(W),
+                                         static_cast<uint4*>(E), owner, local, p.T, p.Vp, p.V_real, p.S, row_vecs);
+  note_launch(VCE_K_EMBED_GATHER, st);
+  return e;
 }
 
 size_t embed_bwd_ws_bytes(const vce_problem& p) { return bwd_layout(p).total; }

@@ -127,6 +127,10 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int 
 // ---------------------------------------------------------------------------
 cudaError_t launch_embed_fwd(const vce_problem& p, const int64_t* ids, const void* W, void* E, int32_t* owner,
                              int32_t* local, cudaStream_t st);
+// The lookup and the embedding backward's plan in one sequence: the plan's
+// launches first, then the lookup as their dependent, running beside the sort.
+cudaError_t launch_embed_fwd_plan(const vce_problem& p, const int64_t* ids, const void* W, void* E, int32_t* owner,
+                                  int32_t* local, void* ws, cudaStream_t st);
 
 size_t embed_bwd_ws_bytes(const vce_problem& p);
 // False when the embedding backward's work items would not fit in 32 bits.

@@ -340,6 +340,20 @@ vce_status vce_embed_fwd(const vce_problem* p, const int64_t* ids, const void* W
   return cuda_status(launch_embed_fwd(*p, ids, W, E, owner, local, static_cast<cudaStream_t>(stream)));
 }
 
+vce_status vce_embed_fwd_plan(const vce_problem* p, const int64_t* ids, const void* W, void* E, int32_t* owner,
+                              int32_t* local, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  vce_status s = check_problem(p);
+  if (s != VCE_OK) return s;
+  if (p->T == 0) return VCE_OK;
+  if (!ids || !W || !E) return VCE_ERR_ARG;
+  if (!aligned(ids, 8) || !aligned(W, 16) || !aligned(E, 16) || !aligned(owner, 4) || !aligned(local, 4))
+    return VCE_ERR_UNSUPPORTED;
+  if (!embed_bwd_supported(*p)) return VCE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, kWsAlign) || ws_bytes < embed_bwd_ws_bytes(*p)) return VCE_ERR_WORKSPACE;
+  return cuda_status(launch_embed_fwd_plan(*p, ids, W, E, owner, local, ws, static_cast<cudaStream_t>(stream)));
+}
+
 vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* dE, float* dW, void* ws,
                          size_t ws_bytes, int32_t* dev_status, void* stream) {
   vce_status s = check_problem(p);
