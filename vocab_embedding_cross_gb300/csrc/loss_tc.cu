@@ -729,18 +729,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             reg_fence(x1);
             if (bb == 1) release(acc);
             const int64_t vc0 = vt0 + bb * 64;
+            // The chunk's real columns [0, nval) and the target's column jy in
+            // it (-1 when elsewhere), fixed for the chunk: the loop below
+            // compares only 32-bit column indices. A row without a valid
+            // target has no real column and no target column.
+            const int64_t nv64 = row_ok ? a.pd.V_real - vc0 : 0;
+            const int nval = nv64 >= 64 ? 64 : (nv64 <= 0 ? 0 : static_cast<int>(nv64));
+            const int64_t jy64 = y - vc0;
+            const int jy = (row_ok && jy64 >= 0 && jy64 < 64) ? static_cast<int>(jy64) : -1;
 #pragma unroll
             for (int j = 0; j < 64; j += 2) {
               const uint32_t xa = j < 32 ? x0[j] : x1[j - 32];
               const uint32_t xb = j < 32 ? x0[j + 1] : x1[j - 31];
               float g0 = 0.0f, g1 = 0.0f;
-              if (row_ok) {
-                const int64_t v = vc0 + j;
-                if (v < a.pd.V_real) g0 = ex2_approx(fmaf(__uint_as_float(xa), kLog2e, -lseL)) * scale;
-                if (v + 1 < a.pd.V_real) g1 = ex2_approx(fmaf(__uint_as_float(xb), kLog2e, -lseL)) * scale;
-                if (v == y) g0 -= scale;
-                if (v + 1 == y) g1 -= scale;
-              }
+              if (j < nval) g0 = ex2_approx(fmaf(__uint_as_float(xa), kLog2e, -lseL)) * scale;
+              if (j + 1 < nval) g1 = ex2_approx(fmaf(__uint_as_float(xb), kLog2e, -lseL)) * scale;
+              if (j == jy) g0 -= scale;
+              if (j + 1 == jy) g1 -= scale;
               w[j / 2] = pack_bf16x2(g0, g1);
             }
             store_box(w, col0 + bb * 64, orow);
