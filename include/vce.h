@@ -189,7 +189,8 @@ vce_status vce_embed_bwd_plan(const vce_problem* p, const int64_t* ids, void* ws
                               size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
- * The lookup and the backward's plan in one call: the results of
+ * The lookup and the backward's plan in one call [VS p.1-2; TP Embedding]:
+ * the results of
  * vce_embed_fwd (E, owner, local) and of vce_embed_bwd_plan (the plan in
  * `ws`) for the same ids. The plan's sort reads only the ids and moves almost
  * no memory, so the lookup's row copies run beside it, on the SMs the sort
@@ -367,8 +368,9 @@ vce_status vce_ngram_embed_bwd(const vce_problem* p, const int64_t* ids, const v
                                int32_t* dev_status, void* stream);
 
 /*
- * vce_ngram_embed_bwd in two parts, as vce_embed_bwd_plan / _apply are for
- * the token table: the plan (the tables' row indices and the sort of every
+ * vce_ngram_embed_bwd in two parts ["Sampled Softmax with Over-Tokenized
+ * Transformer", Setup; VS p.2], as vce_embed_bwd_plan / _apply are for the
+ * token table: the plan (the tables' row indices and the sort of every
  * table's (row, t) pairs) depends on the ids alone; the application adds dE
  * into dW, dT2 and dT3 by it, with the bits of vce_ngram_embed_bwd, and leaves
  * the plan unchanged. vce_ngram_embed_bwd also leaves its plan in `ws`. The
