@@ -190,9 +190,8 @@ vce_status vce_embed_bwd_plan(const vce_problem* p, const int64_t* ids, void* ws
 
 /*
  * The lookup and the backward's plan in one call [VS p.1-2; TP Embedding]:
- * the results of
- * vce_embed_fwd (E, owner, local) and of vce_embed_bwd_plan (the plan in
- * `ws`) for the same ids. The plan's sort reads only the ids and moves almost
+ * the results of vce_embed_fwd (E, owner, local) and of vce_embed_bwd_plan
+ * (the plan in `ws`) for the same ids. The plan's sort reads only the ids and moves almost
  * no memory, so the lookup's row copies run beside it, on the SMs the sort
  * leaves free, instead of after it. The call completes, for any later work on
  * `stream`, only when both have. Arguments as in the two calls;
