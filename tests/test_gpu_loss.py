@@ -249,8 +249,8 @@ def test_loss_gptoss_full():
 def test_qwen3_tied_pipeline_full():
     """The Qwen3-like tied step at full size (T=8192, H=2048, V=151936, S=8),
     run as one pipeline on one W and one fp32 dW, with the tied flag set and
-    in the order the benchmark runs it: embedding lookup of the input ids and
-    the embedding backward's plan, loss forward, loss backward adding the
+    in the order the benchmark runs it: embedding lookup of the input ids with
+    the embedding backward's plan made beside it, loss forward, loss backward adding the
     head's gradient into dW, and the plan's application adding the input
     gradient into the same dW ("Vocabulary shards", paragraph 2: one logical
     parameter, all contributions combined). Checked against the oracle: the lookup bit for
@@ -264,12 +264,13 @@ def test_qwen3_tied_pipeline_full():
     tol = TOL["bf16"]
     rng = np.random.default_rng(1)
     W_d, h_d, dE_d = D.to_device(W), D.to_device(h), D.to_device(dE)
-    # 1. lookup, and the embedding backward's plan while the ids are at hand
-    E = R.embed_fwd(wl, W_d, ids, maps=False)["E"]
-    assert np.array_equal(E, O.embed_forward(ids, W, wl.V_real))
+    # 1. lookup, with the embedding backward's plan made beside it
     p = R.prob(wl)
     ws_e = D.workspace(R.vce.vce_workspace_size(p, R.vce.VCE_OP_EMBED_BWD))
-    R.vce.vce_embed_bwd_plan(p, torch.from_numpy(ids).cuda(), ws_e)
+    E_d = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    R.vce.vce_embed_fwd_plan(p, torch.from_numpy(ids).cuda(), W_d, E_d, ws_e)
+    torch.cuda.synchronize()
+    assert np.array_equal(D.to_host_bits(E_d), O.embed_forward(ids, W, wl.V_real))
     # 2. loss forward
     out = R.loss_fwd(wl, h_d, W_d, y)
     assert out["status"] == 0
