@@ -12,10 +12,12 @@ from vocab_embedding_cross_gb300 import inputs as I
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("dtype,split", [("bf16", False), ("f32", False), ("bf16", True), ("f32", True)])
+@pytest.mark.parametrize("dtype,split", [("bf16", None), ("f32", None), ("bf16", "plan"), ("f32", "plan"),
+                                         ("bf16", "lookup_plan"), ("f32", "lookup_plan")])
 def test_step_in_a_cuda_graph(dtype, split):
-    """split: the embedding backward as its plan (after the lookup) and the
-    plan's application, the order bench.py runs."""
+    """split: the embedding backward as its plan (made after the lookup, or
+    beside it by vce_embed_fwd_plan, the order bench.py runs) and the plan's
+    application."""
     wl = I.custom("graph_step", T=1000, H=256, V_real=5000, Vp=5056, S=8, dtype=dtype, seed=90, tied=True,
                   ignore_frac=0.05, pad_id_frac=0.02, oor_id_frac=0.02)
     d = I.make_all(wl)
@@ -36,8 +38,11 @@ def test_step_in_a_cuda_graph(dtype, split):
 
     def step():
         dW.zero_()
-        vce.vce_embed_fwd(p, ids, W, E, dev_status=st)
-        if split:
+        if split == "lookup_plan":
+            vce.vce_embed_fwd_plan(p, ids, W, E, ws_e, dev_status=st)
+        else:
+            vce.vce_embed_fwd(p, ids, W, E, dev_status=st)
+        if split == "plan":
             vce.vce_embed_bwd_plan(p, ids, ws_e, dev_status=st)
         vce.vce_loss_fwd(p, h, W, y, loss, lse, ws=ws_f, dev_status=st)
         vce.vce_loss_bwd(p, h, W, y, lse, 1.0, dH, dW, ws_b, dev_status=st)
