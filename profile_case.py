@@ -1,13 +1,14 @@
 """Small, self-contained invocations of the library for a profiler.
 
     python profile_case.py loss    [--workload NAME] [--tokens T] [--iters N]
-    python profile_case.py embed   [--workload NAME] [--iters N]
+    python profile_case.py embed   [--workload NAME] [--iters N] [--split]
     python profile_case.py sampled [--tokens T] [--iters N]
 
 `loss` runs the loss forward and backward on a named workload's shapes
 (default the Qwen3-like H=2048, V=151936, S=8, tied dW), with T tokens or the
 workload's own; `embed` runs the embedding lookup and its backward on a named
-workload; `sampled` runs vce_sampled_loss (P=8192) with T tokens (default
+workload (with --split: the lookup with the backward's plan made beside it,
+then the plan's application); `sampled` runs vce_sampled_loss (P=8192) with T tokens (default
 2048). Inputs are the seeded synthetic ones of `inputs.py`. Each case checks
 the device status word and exits non-zero on any error, so that a profiler is
 only pointed at a command that has already run cleanly.
@@ -62,8 +63,12 @@ def _embed(args):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = D.workspace(vce.vce_workspace_size(p, vce.VCE_OP_EMBED_BWD))
     for _ in range(args.iters):
-        vce.vce_embed_fwd(p, ids, W, E, dev_status=st)
-        vce.vce_embed_bwd(p, ids, dE, dW, ws, dev_status=st)
+        if args.split:   # the lookup with the backward's plan beside it, then the plan's application
+            vce.vce_embed_fwd_plan(p, ids, W, E, ws, dev_status=st)
+            vce.vce_embed_bwd_apply(p, dE, dW, ws, dev_status=st)
+        else:
+            vce.vce_embed_fwd(p, ids, W, E, dev_status=st)
+            vce.vce_embed_bwd(p, ids, dE, dW, ws, dev_status=st)
     torch.cuda.synchronize()
     return int(st.item()), "embedding ok"
 
@@ -96,6 +101,8 @@ def main(argv=None) -> int:
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--workload", default="qwen3_tied")
     ap.add_argument("--iters", type=int, default=2)
+    ap.add_argument("--split", action="store_true",
+                    help="embed: vce_embed_fwd_plan and vce_embed_bwd_apply instead of the lookup and the one-call backward")
     args = ap.parse_args(argv)
     status, msg = {"loss": _loss, "embed": _embed, "sampled": _sampled}[args.case](args)
     print(f"{args.case}: status {status} ({vce.status_str(status)}); {msg}")
