@@ -1,6 +1,7 @@
 """Seeded random shapes against the oracle: the whole path (lookup, loss
 forward and backward, embedding backward, greedy argmax) on problem sizes drawn
-from a fixed generator.
+from a fixed generator; every other case runs the embedding backward as a plan
+made beside the lookup and its application.
 
 T, H, V_real, the padding to Vp, S and the ignored fraction are drawn so that
 shard bounds, forward units, token blocks and vocabulary tiles fall at
@@ -52,8 +53,18 @@ def test_random_shape(case):
     tol = TOL[wl.dtype]
     d = I.make_all(wl, ("W", "h", "targets", "ids", "dE"))
     h_d, W_d = D.to_device(d["h"]), D.to_device(d["W"])
-    # lookup, bit for bit
-    got = R.embed_fwd(wl, W_d, d["ids"])
+    # lookup, bit for bit; every other case makes the embedding backward's plan
+    # beside it and applies the plan below, the others use the one-call backward
+    split = case["seed"] % 2 == 1
+    p = R.prob(wl)
+    if split:
+        ws_e = D.workspace(R.vce.vce_workspace_size(p, R.vce.VCE_OP_EMBED_BWD))
+        E = torch.empty((wl.T, wl.H), dtype=W_d.dtype, device="cuda")
+        R.vce.vce_embed_fwd_plan(p, torch.from_numpy(d["ids"]).cuda(), W_d, E, ws_e)
+        torch.cuda.synchronize()
+        got = {"E": D.to_host_bits(E)}
+    else:
+        got = R.embed_fwd(wl, W_d, d["ids"])
     assert np.array_equal(got["E"], O.embed_forward(d["ids"], d["W"], wl.V_real))
     # loss forward
     out = R.loss_fwd(wl, h_d, W_d, d["targets"], maps=False)
@@ -71,11 +82,16 @@ def test_random_shape(case):
     assert np.all(dWn[wl.V_real:] == 0)
     # embedding backward into that dW, bit for bit against the fp32 replay
     dE32 = I.bf16_to_f32(d["dE"]) if wl.dtype == "bf16" else d["dE"]
-    assert R.embed_bwd(wl, d["ids"], D.to_device(d["dE"]), dW) == 0
+    if split:
+        st_e = R.status_word()
+        R.vce.vce_embed_bwd_apply(p, D.to_device(d["dE"]), dW, ws_e, dev_status=st_e)
+        torch.cuda.synchronize()
+        assert int(st_e.item()) == 0
+    else:
+        assert R.embed_bwd(wl, d["ids"], D.to_device(d["dE"]), dW) == 0
     want = O.embed_backward_replay_f32(d["ids"], dE32, wl.V_real, CHUNK, dWn)
     assert np.array_equal(dW.cpu().numpy().view(np.uint32), want.view(np.uint32))
     # greedy argmax: a valid class whose logit is the maximum within the logits' rounding
-    p = R.prob(wl)
     arg = torch.empty(wl.T, dtype=torch.int64, device="cuda")
     ws = D.workspace(max(R.vce.vce_workspace_size(p, R.vce.VCE_OP_GREEDY_ARGMAX), 256))
     R.vce.vce_greedy_argmax(p, h_d, W_d, arg, ws=ws)
