@@ -21,7 +21,7 @@ namespace {
 
 // 16 MiB of scratch, reserved on every GPU that loads the library until the
 // process exits. Enough for the forward of T = 8192 tokens over a 151936-entry
-// vocabulary in 8 shards (about 5.3 MB) or T = 16384 over 201088 (about 13.7 MB).
+// vocabulary in 8 shards (about 5.3 MB) or T = 16384 over 201088 at H = 2048 (about 13.7 MB).
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
