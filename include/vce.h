@@ -180,29 +180,30 @@ vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* d
  * and leaves the plan unchanged: the same plan can be applied to another dE
  * or again. `p` must have the T, H and dtype the plan was made with; ids are
  * not passed again, and the caller must keep the plan's ids and workspace
- * together. A workspace that holds no plan, or one made for another T or
- * column count, adds nothing and reports VCE_ERR_ARG to dev_status. Two calls
+ * together. A workspace that holds no plan, or one made for another T,
+ * column count or V_real, adds nothing and reports VCE_ERR_ARG to dev_status
+ * (H and dtype enter through the column count). Two calls
  * on the same workspace must not overlap on the GPU (they share the plan's
  * counters).
  */
 vce_status vce_embed_bwd_plan(const vce_problem* p, const int64_t* ids, void* ws,
                               size_t ws_bytes, int32_t* dev_status, void* stream);
+vce_status vce_embed_bwd_apply(const vce_problem* p, const void* dE, float* dW,
+                               void* ws, size_t ws_bytes, int32_t* dev_status,
+                               void* stream);
 
 /*
  * The lookup and the backward's plan in one call [VS p.1-2; TP Embedding]:
  * the results of vce_embed_fwd (E, owner, local) and of vce_embed_bwd_plan
- * (the plan in `ws`) for the same ids. The plan's sort reads only the ids and moves almost
- * no memory, so the lookup's row copies run beside it, on the SMs the sort
- * leaves free, instead of after it. The call completes, for any later work on
- * `stream`, only when both have. Arguments as in the two calls;
+ * (the plan in `ws`) for the same ids. The plan's sort reads only the ids and
+ * moves almost no memory, so the lookup's row copies run beside it, on the
+ * SMs the sort leaves free, instead of after it. The call completes, for any
+ * later work on `stream`, only when both have. Arguments as in the two calls;
  * `dev_status` is unused and may be NULL.
  */
 vce_status vce_embed_fwd_plan(const vce_problem* p, const int64_t* ids, const void* W,
                               void* E, int32_t* owner, int32_t* local, void* ws,
                               size_t ws_bytes, int32_t* dev_status, void* stream);
-vce_status vce_embed_bwd_apply(const vce_problem* p, const void* dE, float* dW,
-                               void* ws, size_t ws_bytes, int32_t* dev_status,
-                               void* stream);
 
 /*
  * Globally normalised cross-entropy, forward [VS p.3-5; PAD s.5; SPN p.3].
