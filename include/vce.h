@@ -155,6 +155,12 @@ vce_status vce_embed_fwd(const vce_problem* p, const int64_t* ids, const void* W
  * (VCE_K_EMBED_SORT). The environment variable VCE_EMBED_SORT_CLUSTER, read
  * at each call, overrides the choice: 1 for the clusters whenever the bucketed
  * counting sort runs, 0 for never.
+ * Nor does the width of the column slices that the additions are cut into.
+ * The runs of ids with more than one run are added in slices half as wide
+ * when T * H * sizeof(dE element) is at most 64 MB (there the hottest id's
+ * chain of dependent loads sets the call's time), else in the full width; the
+ * environment variable VCE_EMBED_NARROW, read at each call, forces the half
+ * width (1) or the full one (0). A plan records the width it was made for.
  * The call is vce_embed_bwd_plan followed by vce_embed_bwd_apply on the same
  * workspace, and it leaves the plan of `ids` there.
  * Workspace: vce_workspace_size(p, VCE_OP_EMBED_BWD) bytes.
@@ -182,7 +188,9 @@ vce_status vce_embed_bwd(const vce_problem* p, const int64_t* ids, const void* d
  * not passed again, and the caller must keep the plan's ids and workspace
  * together. A workspace that holds no plan, or one made for another T,
  * column count or V_real, adds nothing and reports VCE_ERR_ARG to dev_status
- * (H and dtype enter through the column count). Two calls
+ * (the column count is that of the multi-run ids' slices: H, dtype and the
+ * slice width enter through it, so a plan made under another
+ * VCE_EMBED_NARROW setting can be refused). Two calls
  * on the same workspace must not overlap on the GPU (they share the plan's
  * counters).
  */

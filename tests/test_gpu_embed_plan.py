@@ -203,3 +203,72 @@ def test_lookup_with_plan(case):
     ref = O.embed_backward_replay_f32(ids, I.bf16_to_f32(dE1), wl.V_real, CHUNK,
                                       np.zeros((wl.Vp, wl.H), np.float32))
     assert np.array_equal(_bits(dW_d.cpu().numpy()), _bits(ref))
+
+
+# Multi-run ids' items in narrow column slices (half a wide slice) or wide
+# ones: both give the replay's bits, on each sort path, with slices that end
+# inside a row (H = 1288 bf16: 2 wide and 3 narrow slices; H = 520: 1 and 2).
+NARROW_CASES = [dict(T=2049, H=1288, V_real=151936, Vp=151936, S=8, dtype="bf16"),
+                dict(T=16384, H=1288, V_real=201088, Vp=201088, S=8, dtype="bf16"),
+                dict(T=5000, H=64, V_real=1048000, Vp=1048064, S=8, dtype="bf16"),
+                dict(T=20000, H=520, V_real=1000, Vp=1024, S=4, dtype="bf16"),
+                dict(T=3000, H=260, V_real=5000, Vp=5056, S=4, dtype="f32")]
+
+
+@pytest.mark.parametrize("narrow", ["0", "1"])
+@pytest.mark.parametrize("case", NARROW_CASES, ids=lambda c: "T{T}_H{H}_V{V_real}_{dtype}".format(**c))
+def test_narrow_and_wide_slices(case, narrow, monkeypatch):
+    """VCE_EMBED_NARROW forces the multi-run ids' column slices: the one-call
+    backward and a plan applied once are bit-exact against the replay either
+    way."""
+    monkeypatch.setenv("VCE_EMBED_NARROW", narrow)
+    c = dict(case)
+    dtype = c.pop("dtype")
+    wl = I.custom(dtype=dtype, pad_id_frac=0.03, oor_id_frac=0.02, seed=60, **c)
+    d = I.make_all(wl, ("ids", "dE"))
+    ids = d["ids"].copy()
+    ids[: wl.T // 5] = 7                       # one id over many runs
+    ids[wl.T // 5: wl.T // 5 + 40] = 9         # an id of two runs
+    ids = np.random.default_rng(61).permutation(ids)
+    dE = d["dE"]
+    dE32 = I.bf16_to_f32(dE) if dtype == "bf16" else dE
+    p = R.prob(wl)
+    ws = D.workspace(R.vce.vce_workspace_size(p, R.vce.VCE_OP_EMBED_BWD))
+    st = R.status_word()
+    ids_d, dE_d = torch.from_numpy(ids).cuda(), D.to_device(dE)
+    dW0 = np.random.default_rng(62).standard_normal((wl.Vp, wl.H)).astype(np.float32)
+    ref = O.embed_backward_replay_f32(ids, dE32, wl.V_real, CHUNK, dW0)
+    dW_d = torch.from_numpy(dW0.copy()).cuda()
+    R.vce.vce_embed_bwd(p, ids_d, dE_d, dW_d, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(_bits(dW_d.cpu().numpy()), _bits(ref))
+    dW_d.copy_(torch.from_numpy(dW0))
+    R.vce.vce_embed_bwd_plan(p, ids_d, ws, dev_status=st)
+    R.vce.vce_embed_bwd_apply(p, dE_d, dW_d, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(_bits(dW_d.cpu().numpy()), _bits(ref))
+
+
+def test_plan_of_other_slices_refused(monkeypatch):
+    """A plan records its multi-run ids' slice count: one made with narrow
+    slices (3 at H = 1288) is refused by an application with wide ones (2),
+    which adds nothing and reports VCE_ERR_ARG."""
+    wl = I.custom(T=2049, H=1288, V_real=151936, Vp=151936, S=8, dtype="bf16", seed=63)
+    d = I.make_all(wl, ("ids", "dE"))
+    ids = d["ids"].copy()
+    ids[:300] = 11
+    p = R.prob(wl)
+    ws = D.workspace(R.vce.vce_workspace_size(p, R.vce.VCE_OP_EMBED_BWD))
+    st = R.status_word()
+    ids_d = torch.from_numpy(ids).cuda()
+    monkeypatch.setenv("VCE_EMBED_NARROW", "1")
+    R.vce.vce_embed_bwd_plan(p, ids_d, ws, dev_status=st)
+    monkeypatch.setenv("VCE_EMBED_NARROW", "0")
+    dW0 = np.random.default_rng(64).standard_normal((wl.Vp, wl.H)).astype(np.float32)
+    dW_d = torch.from_numpy(dW0.copy()).cuda()
+    R.vce.vce_embed_bwd_apply(p, D.to_device(d["dE"]), dW_d, ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == ERR_ARG
+    assert np.array_equal(_bits(dW_d.cpu().numpy()), _bits(dW0))

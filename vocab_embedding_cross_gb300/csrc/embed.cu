@@ -26,6 +26,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -123,9 +124,9 @@ struct __align__(16) RunDesc {
 constexpr int kHdrItem = 6, kHdrPlanT = 8, kHdrPlanNh = 9, kHdrPlanMark = 10, kHdrPlanRows = 11;
 constexpr int32_t kPlanMark = 0x4E414C50;   // "PLAN"
 
-__device__ __forceinline__ void plan_seal(int32_t* hdr, int T, int nh, int64_t V_real) {
+__device__ __forceinline__ void plan_seal(int32_t* hdr, int T, int nhm, int64_t V_real) {
   hdr[kHdrPlanT] = T;
-  hdr[kHdrPlanNh] = nh;
+  hdr[kHdrPlanNh] = nhm;
   hdr[kHdrPlanRows] = static_cast<int32_t>(V_real);
   hdr[kHdrPlanMark] = kPlanMark;
 }
@@ -133,7 +134,8 @@ __device__ __forceinline__ void plan_seal(int32_t* hdr, int T, int nh, int64_t V
 struct BwdLayout {
   size_t hdr, keys_a, keys_b, seg_start, tsorted, runs, counters, partials, total;
   int64_t n_counters, n_slots;
-  int nh;
+  int nh;    // wide column slices per row: the items of single-run ids
+  int nhm;   // narrow column slices (half as wide): the items and counters of multi-run ids
 };
 
 int cols_per_item(int esize) { return 128 * (16 / esize); }
@@ -143,7 +145,8 @@ BwdLayout bwd_layout(const vce_problem& p) {
   const int64_t T = p.T;
   const int esize = p.dtype == VCE_BF16 ? 2 : 4;
   L.nh = static_cast<int>(ceil_div(p.H, cols_per_item(esize)));
-  L.n_counters = (T / (kEmbedBwdChunk + 1) + 2) * L.nh;
+  L.nhm = static_cast<int>(ceil_div(p.H, cols_per_item(esize) / 2));
+  L.n_counters = (T / (kEmbedBwdChunk + 1) + 2) * L.nhm;
   L.n_slots = 2 * T / kEmbedBwdChunk + 2;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -230,9 +233,11 @@ __device__ __forceinline__ uint64_t block_excl_scan64(uint64_t v, uint64_t* sh_w
 // Runs of kEmbedBwdChunk tokens for the segments [s0, s0 + per_thread) of one
 // thread (all threads together cover [0, nseg) in order); slots for multi-run
 // ids. seg[s] is the sorted position where segment s starts (segment s ends at
-// seg[s + 1], the last one at n); id_of(s) gives its id.
+// seg[s + 1], the last one at n); id_of(s) gives its id. As in the bucketed
+// sorts, the runs of multi-run ids go to the front of the run list (at their
+// slot's index) and single runs to its back (from index cap - 1 down).
 template <typename SegAt, typename IdOf>
-__device__ __forceinline__ void build_runs(SegAt seg, int nseg, int n, int per_thread, int nh, IdOf id_of,
+__device__ __forceinline__ void build_runs(SegAt seg, int nseg, int n, int cap, int per_thread, int nhm, IdOf id_of,
                                            int* sh_warp, int32_t* hdr, RunDesc* runs, int32_t* counters) {
   const int s0 = threadIdx.x * per_thread;
   int my_runs = 0, my_multi = 0, my_slots = 0;
@@ -249,9 +254,10 @@ __device__ __forceinline__ void build_runs(SegAt seg, int nseg, int n, int per_t
     }
   }
   int t_runs, t_multi, t_slots;
-  int r0 = block_excl_scan(my_runs, sh_warp, &t_runs);
+  block_excl_scan(my_runs, sh_warp, &t_runs);
   int m0 = block_excl_scan(my_multi, sh_warp, &t_multi);
   int q0 = block_excl_scan(my_slots, sh_warp, &t_slots);
+  int sb = min(s0, nseg) - m0;   // single-run segments before this thread's
   for (int j = 0; j < per_thread; ++j) {
     const int s = s0 + j;
     if (s >= nseg) break;
@@ -269,27 +275,29 @@ __device__ __forceinline__ void build_runs(SegAt seg, int nseg, int n, int per_t
       r.nruns = nr;
       r.first_slot = multi ? q0 : -1;
       r.pad = 0;
-      runs[r0 + k] = r;
+      // multi-run ids' runs at the front (index = slot), single runs at the back
+      runs[multi ? q0 + k : cap - 1 - sb] = r;
     }
     if (multi) {
-      for (int hh = 0; hh < nh; ++hh) counters[m0 * nh + hh] = 0;
+      for (int hh = 0; hh < nhm; ++hh) counters[m0 * nhm + hh] = 0;
       m0 += 1;
       q0 += nr;
+    } else {
+      sb += 1;
     }
-    r0 += nr;
   }
   if (threadIdx.x == 0) {
-    hdr[1] = t_runs;
+    hdr[1] = t_slots;   // runs at the front
     hdr[3] = t_multi;
     hdr[4] = t_slots;
-    hdr[5] = 0;
+    hdr[5] = nseg - t_multi;   // single runs at the back
     hdr[kHdrItem] = 0;   // the reduce's item counter
   }
 }
 
 // Shared-memory variant: keys (id << tbits) | t in 32 bits, T <= kSmemSortMax.
 __global__ void __launch_bounds__(kSortThreads, 1)
-    embed_sort_smem_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int idbits, int nh,
+    embed_sort_smem_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int idbits, int nhm,
                            int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
   extern __shared__ __align__(16) uint32_t smem_keys[];
   uint32_t* ka = smem_keys;
@@ -438,7 +446,8 @@ __global__ void __launch_bounds__(kSortThreads, 1)
   // Phase 3: runs of kEmbedBwdChunk tokens. Warp w takes segments
   // [w*spw, (w+1)*spw), one per lane per round; a block scan of the warps'
   // (runs, multi-run segments) totals gives each segment its first run and
-  // first partial slot, and the lane holding a segment writes its runs.
+  // first partial slot, and the lane holding a segment writes its runs: a
+  // multi-run id's at the front of the list, a single run at its back.
   auto seg_end = [&](int sg) { return sg + 1 < nseg ? seg[pad32(sg + 1)] : n; };
   const int spw = ((nseg + kSortWarps - 1) / kSortWarps + 31) & ~31;
   int wpacked = 0;   // (runs << 16) | multi-run segments, over this warp's segments
@@ -489,21 +498,23 @@ __global__ void __launch_bounds__(kSortThreads, 1)
         rd.nruns = nr;
         rd.first_slot = multi ? q0 : -1;
         rd.pad = 0;
-        runs[rb + k] = rd;
+        // multi-run ids' runs at the front (index = slot), single runs at the
+        // back (sg - mb single segments before this one)
+        runs[multi ? q0 + k : T - 1 - (sg - mb)] = rd;
       }
       if (multi)
-        for (int hh = 0; hh < nh; ++hh) counters[mb * nh + hh] = 0;
+        for (int hh = 0; hh < nhm; ++hh) counters[mb * nhm + hh] = 0;
     }
   }
   if (tid == 0) {
     hdr[0] = n;
-    hdr[1] = n_runs;
+    hdr[1] = n_runs - (nseg - n_multi);   // runs at the front: the slots
     hdr[2] = nseg;
     hdr[3] = n_multi;
     hdr[4] = n_runs - (nseg - n_multi);
-    hdr[5] = 0;
+    hdr[5] = nseg - n_multi;              // single runs at the back
     hdr[kHdrItem] = 0;   // the reduce's item counter
-    plan_seal(hdr, T, nh, V_real);
+    plan_seal(hdr, T, nhm, V_real);
   }
 }
 
@@ -538,7 +549,7 @@ size_t bucket_sort_smem(int64_t T) {   // two key buffers, 16-bit ranks (whole w
 }
 
 __global__ void __launch_bounds__(kBktThreads, 1)
-    embed_sort_bucket_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int qbits, int nh,
+    embed_sort_bucket_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int qbits, int nhm,
                              uint32_t nb_magic, int32_t* hdr, int32_t* tsorted, RunDesc* runs,
                              int32_t* counters) {
   extern __shared__ __align__(16) uint32_t bsm[];
@@ -601,7 +612,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   grid_dep_wait();
   int tb = 0;
   if (tid == 0 && m > 0) tb = atomicAdd(&hdr[0], m);
-  if (tid == 0 && b == 0) plan_seal(hdr, T, nh, V_real);
+  if (tid == 0 && b == 0) plan_seal(hdr, T, nhm, V_real);
 
   // Phase B: stable LSD radix passes over the id / NB bits.
   const int kpw = ((m + kBktWarps - 1) / kBktWarps + 31) & ~31;
@@ -753,14 +764,14 @@ __global__ void __launch_bounds__(kBktThreads, 1)
         runs[multi ? sbase + q0 + k : T - 1 - (bbase + (sg - mb))] = rd;
       }
       if (multi)
-        for (int hh = 0; hh < nh; ++hh) counters[(mbase + mb) * nh + hh] = 0;
+        for (int hh = 0; hh < nhm; ++hh) counters[(mbase + mb) * nhm + hh] = 0;
     }
   }
 }
 
 // Workspace variant: 64-bit keys (id << 32) | t, any T.
 __global__ void __launch_bounds__(kSortThreads, 1)
-    embed_sort_kernel(const int64_t* __restrict__ ids, int64_t T, int64_t V_real, int nh, int32_t* hdr,
+    embed_sort_kernel(const int64_t* __restrict__ ids, int64_t T, int64_t V_real, int nhm, int32_t* hdr,
                       uint64_t* keys_a, uint64_t* keys_b, int32_t* seg_start, int32_t* tsorted, RunDesc* runs,
                       int32_t* counters) {
   __shared__ int sh_warp[33];
@@ -888,18 +899,19 @@ __global__ void __launch_bounds__(kSortThreads, 1)
   __syncthreads();
   auto id_of = [&](int sg) { return static_cast<int>(seg_ids[sg]); };
   auto seg_at = [&](int sg) { return seg_start[sg]; };
-  build_runs(seg_at, nseg, n, (nseg + kSortThreads - 1) / kSortThreads, nh, id_of, sh_warp, hdr, runs,
+  build_runs(seg_at, nseg, n, static_cast<int>(T), (nseg + kSortThreads - 1) / kSortThreads, nhm, id_of, sh_warp, hdr, runs,
              counters);
   if (tid == 0) {
     hdr[0] = n;
     hdr[2] = nseg;
-    plan_seal(hdr, static_cast<int>(T), nh, V_real);
+    plan_seal(hdr, static_cast<int>(T), nhm, V_real);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Backward, step 2: persistent segmented reduction. Work item = (run, column
-// slice of 128 threads x 16 bytes).
+// slice): 128 threads x 16 bytes for the run of a single-run id, 128 threads x
+// 8 bytes for a run of a multi-run id.
 // ---------------------------------------------------------------------------
 template <typename TE>
 __device__ __forceinline__ void widen(const uint4& v, float (&o)[16 / sizeof(TE)]);
@@ -920,22 +932,38 @@ __device__ __forceinline__ void widen<float>(const uint4& v, float (&o)[4]) {
   o[3] = __uint_as_float(v.w);
 }
 
+// 8 bytes of dE (four bf16 or two fp32 values), widened.
+template <typename TE>
+__device__ __forceinline__ void widen(const uint2& v, float (&o)[8 / sizeof(TE)]);
+template <>
+__device__ __forceinline__ void widen<uint16_t>(const uint2& v, float (&o)[4]) {
+  o[0] = __uint_as_float(v.x << 16);
+  o[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  o[2] = __uint_as_float(v.y << 16);
+  o[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+template <>
+__device__ __forceinline__ void widen<float>(const uint2& v, float (&o)[2]) {
+  o[0] = __uint_as_float(v.x);
+  o[1] = __uint_as_float(v.y);
+}
+
 // acc += dE rows t_p, t_{p+1}, ..., t_{p+N-1} (this thread's 16-byte column
 // chunk), the N loads issued before the first add, the adds in token order.
 // Token t_j is lane j's my_t. Straight-line code for each N, so a short run
 // issues only its own loads and adds.
-template <int N, typename TE, bool STREAM>
+template <int N, typename TE, bool STREAM, typename LT = uint4>
 __device__ __forceinline__ void add_rows(const TE* __restrict__ dE, int64_t H, int col, int my_t, int p, bool active,
-                                         float (&acc)[16 / sizeof(TE)]) {
-  constexpr int VEC = 16 / sizeof(TE);
-  uint4 v[N];
+                                         float (&acc)[sizeof(LT) / sizeof(TE)]) {
+  constexpr int VEC = sizeof(LT) / sizeof(TE);
+  LT v[N];
 #pragma unroll
   for (int k = 0; k < N; ++k) {
     const int t = __shfl_sync(0xffffffffu, my_t, (p + k) & 31);
-    v[k] = make_uint4(0, 0, 0, 0);
+    v[k] = LT{};
     // With one problem dE is read once: streaming loads (evict first) keep the
     // L2 for the dW rows. The n-gram tables read dE once each, from L2.
-    const uint4* src = reinterpret_cast<const uint4*>(dE + static_cast<int64_t>(t) * H + col);
+    const LT* src = reinterpret_cast<const LT*>(dE + static_cast<int64_t>(t) * H + col);
     if (active) v[k] = STREAM ? __ldcs(src) : __ldg(src);
   }
 #pragma unroll
@@ -1017,7 +1045,7 @@ __device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.a
 // the sort stable exactly as with one contiguous key array.
 template <int ROUNDS, int CL>
 __global__ void __launch_bounds__(kBktThreads, 1)
-    embed_sort_count_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int nq, int nh,
+    embed_sort_count_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int nq, int nhm,
                             uint32_t nb_magic, int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
   static_assert(CL >= 1 && CL <= 8 && kCntWarps % CL == 0, "counting warps split evenly over the segments");
   extern __shared__ __align__(16) uint32_t csm[];
@@ -1147,7 +1175,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   grid_dep_wait();
   int tb = 0;
   if (tid == 0 && m > 0) tb = atomicAdd(&hdr[0], m);
-  if (tid == 0 && b == 0) plan_seal(hdr, T, nh, V_real);
+  if (tid == 0 && b == 0) plan_seal(hdr, T, nhm, V_real);
   __syncthreads();
 
   // Counting warp w takes part w % (kCntWarps / CL) of segment w / (kCntWarps / CL).
@@ -1278,7 +1306,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
     rd.pad = 0;
     runs[multi ? sbase + first + k : T - 1 - (bbase + (p_seg - p_multi))] = rd;
     if (multi && k == 0)
-      for (int hh = 0; hh < nh; ++hh) counters[(mbase + p_multi) * nh + hh] = 0;
+      for (int hh = 0; hh < nhm; ++hh) counters[(mbase + p_multi) * nhm + hh] = 0;
   }
 }
 
@@ -1299,6 +1327,128 @@ struct EmbSlots {
   EmbSlot s[kMaxSlots];
   int n;
 };
+
+// PV consecutive fp32 values of a row (16-byte aligned for PV >= 4, 8-byte for
+// PV = 2), loaded and stored as vectors; cg = at L2.
+template <int PV>
+struct FRow;
+template <>
+struct FRow<4> {
+  __device__ static void ld_cg(const float* p, float (&o)[4]) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  }
+  __device__ static void ld(const float* p, float (&o)[4]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  }
+  __device__ static void st_cg(float* p, const float (&o)[4]) {
+    __stcg(reinterpret_cast<float4*>(p), make_float4(o[0], o[1], o[2], o[3]));
+  }
+  __device__ static void st(float* p, const float (&o)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
+  }
+};
+template <>
+struct FRow<2> {
+  __device__ static void ld_cg(const float* p, float (&o)[2]) {
+    const float2 a = __ldcg(reinterpret_cast<const float2*>(p));
+    o[0] = a.x; o[1] = a.y;
+  }
+  __device__ static void ld(const float* p, float (&o)[2]) {
+    const float2 a = *reinterpret_cast<const float2*>(p);
+    o[0] = a.x; o[1] = a.y;
+  }
+  __device__ static void st_cg(float* p, const float (&o)[2]) { __stcg(reinterpret_cast<float2*>(p), make_float2(o[0], o[1])); }
+  __device__ static void st(float* p, const float (&o)[2]) { *reinterpret_cast<float2*>(p) = make_float2(o[0], o[1]); }
+};
+
+// The end of one run of a multi-run id over one column slice, its sum in
+// token order in hand (PV values per thread): the sum goes to the run's
+// partial slot; the last of the id's runs to finish then adds the id's run
+// sums left to right into its dW row, loading kAhead of them at a time so that
+// a hot id's combine waits for about nruns / kAhead round trips, not nruns.
+template <int PV, int kAhead>
+__device__ __forceinline__ void multi_run_finish(const float (&acc)[PV], int H, int col, bool active,
+                                                 const RunDesc& rd, float* __restrict__ dW, float* partials,
+                                                 int32_t* ctr, int* s_last) {
+  if (active) FRow<PV>::st_cg(partials + static_cast<int64_t>(rd.slot) * H + col, acc);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(ctr, 1);
+    *s_last = (prev == rd.nruns - 1) ? 1 : 0;
+    if (*s_last) *ctr = 0;   // every run is in: back to the plan's zero
+    __threadfence();
+  }
+  __syncthreads();
+  if (*s_last && active) {
+    float tot[PV];
+    FRow<PV>::ld_cg(partials + static_cast<int64_t>(rd.first_slot) * H + col, tot);
+    for (int j0 = 1; j0 < rd.nruns; j0 += kAhead) {
+      float a[kAhead][PV];
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k) {
+        const int j = min(j0 + k, rd.nruns - 1);   // past the end: a valid slot, not added
+        FRow<PV>::ld_cg(partials + static_cast<int64_t>(rd.first_slot + j) * H + col, a[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k)
+        if (j0 + k < rd.nruns) {
+#pragma unroll
+          for (int e = 0; e < PV; ++e) tot[e] = tot[e] + a[k][e];
+        }
+    }
+    float* row = dW + static_cast<int64_t>(rd.id) * H + col;
+    float w[PV];
+    FRow<PV>::ld(row, w);
+#pragma unroll
+    for (int e = 0; e < PV; ++e) w[e] = w[e] + tot[e];
+    FRow<PV>::st(row, w);
+  }
+}
+
+// A narrow item: one run of a multi-run id over half a wide slice's columns,
+// 8 bytes of dE per thread. A multi-run id's runs hold 32 tokens (all but its
+// last), and its last run to finish combines all of its run sums: both steps
+// wait on loads in flight. In the registers of a wide item (16 bytes per
+// thread, 8 rows and 4 run sums ahead), a narrow one keeps 16 rows and 8 run
+// sums ahead: the hottest id of a Zipf batch (35 runs at 8192 tokens) waits
+// for 2 rounds of row loads instead of 4 and 5 rounds of run sums instead of
+// 9, at the price of twice as many items for the multi-run ids. The additions
+// and their order are those of a wide item.
+template <typename TE, bool STREAM>
+__device__ __forceinline__ void reduce_multi_run_narrow(const TE* __restrict__ dE, int H, int col, bool active,
+                                                        const RunDesc& rd, int my_t, float* __restrict__ dW,
+                                                        float* partials, int32_t* ctr, int* s_last) {
+  constexpr int PV = 8 / sizeof(TE);
+  constexpr int U = 16;   // rows loaded ahead of the sequential adds
+  const int len = rd.end - rd.start;   // <= 32
+  float acc[PV];
+#pragma unroll
+  for (int e = 0; e < PV; ++e) acc[e] = 0.0f;
+  for (int p = 0; p < len; p += U) {   // tokens in ascending t, one add each
+    switch (len - p < U ? len - p : U) {
+      case 1: add_rows<1, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 2: add_rows<2, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 3: add_rows<3, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 4: add_rows<4, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 5: add_rows<5, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 6: add_rows<6, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 7: add_rows<7, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 8: add_rows<8, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 9: add_rows<9, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 10: add_rows<10, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 11: add_rows<11, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 12: add_rows<12, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 13: add_rows<13, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 14: add_rows<14, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      case 15: add_rows<15, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+      default: add_rows<U, TE, STREAM, uint2>(dE, H, col, my_t, p, active, acc); break;
+    }
+  }
+  multi_run_finish<PV, 8>(acc, H, col, active, rd, dW, partials, ctr, s_last);
+}
 
 // STREAM: dE is read once (one problem), with evict-first loads.
 template <typename TE, bool STREAM>
@@ -1466,6 +1616,132 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+
+// The reduce with narrow items for the multi-run ids (reduce_multi_run_narrow).
+// Items of problem k: first the runs of its multi-run ids (the front of its
+// run list), each in nhf narrow column slices, then its single runs (the back
+// of the list), each in nh wide slices, as in embed_reduce_kernel.
+template <typename TE, bool STREAM>
+__global__ void __launch_bounds__(128, 8)   // eight resident CTAs per SM: at most 64 registers
+    embed_reduce_narrow_kernel(const __grid_constant__ EmbSlots sl, const TE* __restrict__ dE, int H, int nh,
+                               uint32_t nh_magic, int nhf, uint32_t nhf_magic, int cap, int32_t* status) {
+  constexpr int VEC = 16 / sizeof(TE);
+  constexpr int NQ = VEC / 4;
+  constexpr int U = 8;   // rows loaded ahead of the sequential adds
+  __shared__ int s_last;
+  __shared__ int s_next[2];
+  const int lane = threadIdx.x & 31;
+  grid_dep_wait();   // the sorts' headers, runs and tokens
+  // Every problem must hold a plan made for this shape (T = cap, the same
+  // column slices of multi-run ids and rows); otherwise nothing is added and
+  // the call reports VCE_ERR_ARG.
+  bool planned = true;
+  for (int k = 0; k < sl.n; ++k)
+    planned = planned && sl.s[k].hdr[kHdrPlanMark] == kPlanMark && sl.s[k].hdr[kHdrPlanT] == cap &&
+              sl.s[k].hdr[kHdrPlanNh] == nhf && sl.s[k].hdr[kHdrPlanRows] == sl.s[k].rows;
+  if (!planned) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && status) atomicCAS(status, 0, static_cast<int>(VCE_ERR_ARG));
+    return;
+  }
+  // In each problem, runs [0, n_front) sit at the front of the list, the other
+  // n_back at its end (indices cap-1, cap-2, ...). Problem k's items are
+  // [base_k, base_k+1).
+  const int nf0 = sl.s[0].hdr[1];
+  const int nf1 = sl.n > 1 ? sl.s[1].hdr[1] : 0;
+  const int nf2 = sl.n > 2 ? sl.s[2].hdr[1] : 0;
+  const int base1 = nf0 * nhf + sl.s[0].hdr[5] * nh;
+  const int base2 = base1 + (sl.n > 1 ? nf1 * nhf + sl.s[1].hdr[5] * nh : 0);
+  const int n_items = base2 + (sl.n > 2 ? nf2 * nhf + sl.s[2].hdr[5] * nh : 0);
+  // Items are handed out in order: the first one per CTA by its index, the
+  // rest from a counter in the first problem's header (zeroed before this
+  // kernel), claimed one item ahead so that the claim's round trip overlaps
+  // the current item.
+  int32_t* item_ctr = sl.s[0].hdr + kHdrItem;
+  int it = 0;
+  for (int item = blockIdx.x; item < n_items; ++it) {
+    int next = 0;
+    if (threadIdx.x == 0) {
+      // One claim per item in all: the claim that draws n_items - 1 is the
+      // last one, and puts the counter back to zero for the plan's next use.
+      const int prev = atomicAdd(item_ctr, 1);
+      if (prev == n_items - 1) atomicExch(item_ctr, 0);
+      next = prev + static_cast<int>(gridDim.x);
+    }
+    // this item's problem (a uniform choice among at most three)
+    const int k = item >= base2 ? 2 : (item >= base1 ? 1 : 0);
+    const int li = item - (k == 2 ? base2 : (k == 1 ? base1 : 0));
+    const int n_front = k == 2 ? nf2 : (k == 1 ? nf1 : nf0);
+    const RunDesc* __restrict__ runs = k == 2 ? sl.s[2].runs : (k == 1 ? sl.s[1].runs : sl.s[0].runs);
+    const int32_t* __restrict__ tsorted = k == 2 ? sl.s[2].tsorted : (k == 1 ? sl.s[1].tsorted : sl.s[0].tsorted);
+    float* __restrict__ dW = k == 2 ? sl.s[2].dW : (k == 1 ? sl.s[1].dW : sl.s[0].dW);
+    // li / nhf and li / nh by a multiply-high when the host found it exact for
+    // every item
+    const int n_fi = n_front * nhf;
+    const bool front = li < n_fi;
+    int r, hs;
+    if (front) {
+      r = nhf_magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(li), nhf_magic)) : li / nhf;
+      hs = li - r * nhf;
+    } else {
+      const int lw = li - n_fi;
+      const int rb = nh_magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(lw), nh_magic)) : lw / nh;
+      hs = lw - rb * nh;
+      r = n_front + rb;
+    }
+    const RunDesc rd = runs[r < n_front ? r : cap - 1 - (r - n_front)];
+    const int len = rd.end - rd.start;   // <= 32
+    // the run's token indices, one per lane, broadcast below
+    const int my_t = lane < len ? tsorted[rd.start + lane] : 0;
+    if (front && (rd.slot < 0 || rd.mseg < 0)) {
+      // Only multi-run ids' runs sit at the front of a plan's list.
+      if (threadIdx.x == 0 && status) atomicCAS(status, 0, static_cast<int>(VCE_ERR_ARG));
+    } else if (front) {
+      float* partials = k == 2 ? sl.s[2].partials : (k == 1 ? sl.s[1].partials : sl.s[0].partials);
+      int32_t* ctr = (k == 2 ? sl.s[2].counters : (k == 1 ? sl.s[1].counters : sl.s[0].counters)) + rd.mseg * nhf + hs;
+      const int col = hs * 64 * VEC + static_cast<int>(threadIdx.x) * (VEC / 2);
+      reduce_multi_run_narrow<TE, STREAM>(dE, H, col, col < H, rd, my_t, dW, partials, ctr, &s_last);
+    } else {
+      // A single-run id: its sum is added straight into its dW row.
+      const int col = hs * 128 * VEC + static_cast<int>(threadIdx.x) * VEC;
+      const bool active = col < H;
+      float4* row = reinterpret_cast<float4*>(dW + static_cast<int64_t>(rd.id) * H + col);
+      float4 w[NQ];
+      if (active) {   // fetch the row now, add once the sum is ready
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) w[q] = __ldcg(row + q);   // at L2: the row is not read again here
+      }
+      float acc[VEC];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+      for (int p = 0; p < len; p += U) {   // tokens in ascending t, one add each
+        switch (len - p < U ? len - p : U) {
+          case 1: add_rows<1, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+          case 2: add_rows<2, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+          case 3: add_rows<3, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+          case 4: add_rows<4, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+          case 5: add_rows<5, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+          case 6: add_rows<6, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+          case 7: add_rows<7, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+          default: add_rows<U, TE, STREAM>(dE, H, col, my_t, p, active, acc); break;
+        }
+      }
+      if (active) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          w[q].x = w[q].x + acc[4 * q + 0];
+          w[q].y = w[q].y + acc[4 * q + 1];
+          w[q].z = w[q].z + acc[4 * q + 2];
+          w[q].w = w[q].w + acc[4 * q + 3];
+          row[q] = w[q];
+        }
+      }
+    }
+    if (threadIdx.x == 0) s_next[it & 1] = next;
+    __syncthreads();
+    item = s_next[it & 1];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_embed_fwd(const vce_problem& p, const int64_t* ids, const void* W, void* E, int32_t* owner,
@@ -1497,8 +1773,8 @@ cudaError_t launch_embed_fwd_plan(const vce_problem& p, const int64_t* ids, cons
 
 size_t embed_bwd_ws_bytes(const vce_problem& p) { return bwd_layout(p).total; }
 
-bool embed_bwd_supported(const vce_problem& p) {   // the reduce numbers its items (<= T * nh) in 32 bits
-  return static_cast<int64_t>(p.T) * bwd_layout(p).nh < (int64_t(1) << 31);
+bool embed_bwd_supported(const vce_problem& p) {   // the reduce numbers its items (<= T * nhm) in 32 bits
+  return static_cast<int64_t>(p.T) * bwd_layout(p).nhm < (int64_t(1) << 31);
 }
 
 namespace {
@@ -1603,9 +1879,33 @@ SortPlan plan_sort(const vce_problem& p, int num_sms, cudaError_t* err) {
   return {sort_path(p, nb, 1), nb, 1};
 }
 
+// The column slices of multi-run ids' items. Narrow ones (half a wide slice)
+// when one problem's dE is at most 64 MB: there the call's time is set by the
+// hottest id's chain of dependent loads (its run's rows, then its run sums),
+// which narrow items halve; on larger problems the call is bound by HBM and
+// the extra items cost more than the shorter chain saves (measured on GB300:
+// 8192 x 2048 tokens x columns 26.6 -> 22.5 us, 16384 x 3072 38.9 -> 41.0 us).
+// VCE_EMBED_NARROW=1 or =0 in the environment forces or forbids them. The
+// plan and its application must agree: the plan records the slice count.
+struct FrontSlices {
+  int nhf;
+  bool narrow;
+};
+constexpr int64_t kNarrowMaxBytes = int64_t(64) << 20;
+FrontSlices front_slices(const vce_problem& p, int n_problems) {
+  const BwdLayout L = bwd_layout(p);
+  const char* env = std::getenv("VCE_EMBED_NARROW");
+  const bool set = env && (env[0] == '0' || env[0] == '1') && env[1] == 0;
+  const int64_t esize = p.dtype == VCE_BF16 ? 2 : 4;
+  const bool narrow = set ? env[0] == '1' : (n_problems == 1 && p.T * p.H * esize <= kNarrowMaxBytes);
+  return narrow ? FrontSlices{L.nhm, true} : FrontSlices{L.nh, false};
+}
+
 // Sorts one problem's valid (id, t) pairs into its workspace and builds its
-// runs. A bucketed sort needs its header zeroed by the kernel before it.
-cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, const SortPlan& plan, cudaStream_t st) {
+// runs, with counters for nhf column slices per multi-run id. A bucketed sort
+// needs its header zeroed by the kernel before it.
+cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, const SortPlan& plan, int nhf,
+                        cudaStream_t st) {
   const SortPath path = plan.path;
   const int nb = plan.nb;
   const BwdLayout L = bwd_layout(p);
@@ -1657,7 +1957,7 @@ cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, cons
     cfg.attrs = attr;
     cfg.numAttrs = plan.cl > 1 ? 2 : 1;
     if (cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ids, static_cast<int>(p.T), p.V_real, tbits,
-                                           static_cast<int>(nq), L.nh, nb_magic, hdr, tsorted, runs, counters))
+                                           static_cast<int>(nq), nhf, nb_magic, hdr, tsorted, runs, counters))
       return e;
   } else if (path == SortPath::kBucket) {
     static std::atomic<uint64_t> configured{0};
@@ -1668,7 +1968,7 @@ cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, cons
       mark_device_done(configured);
     }
     if (cudaError_t e = launch_dependent(embed_sort_bucket_kernel, dim3(nb), dim3(kBktThreads), bucket_sort_smem(p.T),
-                                         st, ids, static_cast<int>(p.T), p.V_real, tbits, qbits, L.nh, nb_magic, hdr,
+                                         st, ids, static_cast<int>(p.T), p.V_real, tbits, qbits, nhf, nb_magic, hdr,
                                          tsorted, runs, counters))
       return e;
   } else if (path == SortPath::kSmem) {
@@ -1680,10 +1980,10 @@ cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, cons
       mark_device_done(configured);
     }
     embed_sort_smem_kernel<<<1, kSortThreads, kSmemSortBytes, st>>>(ids, static_cast<int>(p.T), p.V_real, tbits,
-                                                                    bit_width(p.V_real), L.nh, hdr, tsorted, runs,
+                                                                    bit_width(p.V_real), nhf, hdr, tsorted, runs,
                                                                     counters);
   } else {
-    embed_sort_kernel<<<1, kSortThreads, 0, st>>>(ids, p.T, p.V_real, L.nh, hdr, ka, kb, seg, tsorted, runs,
+    embed_sort_kernel<<<1, kSortThreads, 0, st>>>(ids, p.T, p.V_real, nhf, hdr, ka, kb, seg, tsorted, runs,
                                                   counters);
   }
   note_launch(path == SortPath::kCount && plan.cl > 1 ? VCE_K_EMBED_SORT_CLUSTER : VCE_K_EMBED_SORT, st);
@@ -1696,23 +1996,38 @@ cudaError_t launch_reduce(const vce_problem& p, const EmbSlots& sl, const void* 
   const BwdLayout L = bwd_layout(p);
   const DevInfo di = current_device_info();
   const int grid = di.num_sms * 8;
-  // Items of one problem number at most T * nh (a run per token at most); the
-  // multiply-high gives item / nh exactly for items below 2^32 / nh.
-  const uint64_t max_items = static_cast<uint64_t>(p.T) * static_cast<uint64_t>(L.nh);
-  const uint32_t nh_magic = (L.nh > 1 && max_items * static_cast<uint64_t>(L.nh) < (uint64_t(1) << 32))
-                                ? 0xFFFFFFFFu / static_cast<uint32_t>(L.nh) + 1u
-                                : 0u;
+  // Items of one problem number at most T * nhm (a run per token at most); the
+  // multiply-high gives item / d exactly for items below 2^32 / d.
+  const uint64_t max_items = static_cast<uint64_t>(p.T) * static_cast<uint64_t>(L.nhm);
+  auto magic = [&](int d) -> uint32_t {
+    return (d > 1 && max_items * static_cast<uint64_t>(d) < (uint64_t(1) << 32))
+               ? 0xFFFFFFFFu / static_cast<uint32_t>(d) + 1u
+               : 0u;
+  };
+  const FrontSlices fs = front_slices(p, sl.n);
+  const uint32_t nh_magic = magic(L.nh), nhf_magic = magic(fs.nhf);
   // One problem reads dE once; the n-gram tables read it once each.
   const bool stream = sl.n == 1;
+  const int H = static_cast<int>(p.H), cap = static_cast<int>(p.T);
   cudaError_t e;
-  if (p.dtype == VCE_BF16)
-    e = launch_dependent(stream ? embed_reduce_kernel<uint16_t, true> : embed_reduce_kernel<uint16_t, false>,
-                         dim3(grid), dim3(128), 0, st, sl, static_cast<const uint16_t*>(dE), static_cast<int>(p.H),
-                         L.nh, nh_magic, static_cast<int>(p.T), status);
-  else
-    e = launch_dependent(stream ? embed_reduce_kernel<float, true> : embed_reduce_kernel<float, false>, dim3(grid),
-                         dim3(128), 0, st, sl, static_cast<const float*>(dE), static_cast<int>(p.H), L.nh, nh_magic,
-                         static_cast<int>(p.T), status);
+  if (p.dtype == VCE_BF16) {
+    const uint16_t* d = static_cast<const uint16_t*>(dE);
+    if (fs.narrow)
+      e = launch_dependent(
+          stream ? embed_reduce_narrow_kernel<uint16_t, true> : embed_reduce_narrow_kernel<uint16_t, false>,
+          dim3(grid), dim3(128), 0, st, sl, d, H, L.nh, nh_magic, fs.nhf, nhf_magic, cap, status);
+    else
+      e = launch_dependent(stream ? embed_reduce_kernel<uint16_t, true> : embed_reduce_kernel<uint16_t, false>,
+                           dim3(grid), dim3(128), 0, st, sl, d, H, L.nh, nh_magic, cap, status);
+  } else {
+    const float* d = static_cast<const float*>(dE);
+    if (fs.narrow)
+      e = launch_dependent(stream ? embed_reduce_narrow_kernel<float, true> : embed_reduce_narrow_kernel<float, false>,
+                           dim3(grid), dim3(128), 0, st, sl, d, H, L.nh, nh_magic, fs.nhf, nhf_magic, cap, status);
+    else
+      e = launch_dependent(stream ? embed_reduce_kernel<float, true> : embed_reduce_kernel<float, false>, dim3(grid),
+                           dim3(128), 0, st, sl, d, H, L.nh, nh_magic, cap, status);
+  }
   note_launch(VCE_K_EMBED_REDUCE, st);
   return e;
 }
@@ -1744,7 +2059,7 @@ cudaError_t launch_embed_bwd_plan_multi(const vce_problem* ps, const int64_t* co
     if (cudaError_t e = cudaGetLastError()) return e;
   }
   for (int k = 0; k < n; ++k)
-    if (cudaError_t e = launch_sort(ps[k], ids[k], ws[k], plan[k], st)) return e;
+    if (cudaError_t e = launch_sort(ps[k], ids[k], ws[k], plan[k], front_slices(ps[k], n).nhf, st)) return e;
   return cudaSuccess;
 }
 
