@@ -117,10 +117,10 @@ struct __align__(16) RunDesc {
 
 // The workspace header (16 words). The sorts claim space with atomic
 // additions on words 0-5; the reduce hands out items from word 6; words 8-11
-// describe the plan (its T, its column slices per row, a marker and the number
-// of rows its ids index), so that applying a plan made for another shape, or a
-// workspace that holds none, is refused on the device before any row is
-// touched.
+// describe the plan (its T, the column slices per row of its multi-run ids'
+// counters, a marker and the number of rows its ids index), so that applying
+// a plan made for another shape or slice width, or a workspace that holds
+// none, is refused on the device before any row is touched.
 constexpr int kHdrItem = 6, kHdrPlanT = 8, kHdrPlanNh = 9, kHdrPlanMark = 10, kHdrPlanRows = 11;
 constexpr int32_t kPlanMark = 0x4E414C50;   // "PLAN"
 
