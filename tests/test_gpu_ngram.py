@@ -174,3 +174,24 @@ def test_ngram_plan_then_apply(T, H, V_real, Vp, M2, M3, seq_len):
     for a, b in zip((dW, dT2, dT3), before):
         if a is not None:
             assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("narrow", ["0", "1"])
+def test_ngram_bwd_narrow_and_wide_slices(narrow, monkeypatch):
+    """The three tables' reduce with the multi-run ids' column slices forced
+    narrow or wide (VCE_EMBED_NARROW; by default the three-table reduce keeps
+    them wide): bit-exact against the replays either way, with slices that end
+    inside a row (H = 1288)."""
+    monkeypatch.setenv("VCE_EMBED_NARROW", narrow)
+    T, H, V_real, Vp, M2, M3, seq_len = 3000, 1288, 5000, 5056, 613, 1024, 0
+    wl, d, _, _ = _case("bf16", T, H, V_real, Vp, M2, M3, seed=95)
+    ids = d["ids"].copy()
+    ids[100:700] = ids[99]                   # a long run of one id: multi-run rows in every table
+    rng = np.random.default_rng(11)
+    inits = [rng.standard_normal((wl.Vp, wl.H)).astype(np.float32),
+             rng.standard_normal((M2, wl.H)).astype(np.float32),
+             rng.standard_normal((M3, wl.H)).astype(np.float32)]
+    got = _bwd(wl, ids, d["dE"], M2, M3, seq_len, inits)
+    want = _replays(wl, ids, d["dE"], M2, M3, seq_len, inits)
+    for g, w in zip(got, want):
+        assert np.array_equal(g.view(np.uint32), w.view(np.uint32))

@@ -1757,10 +1757,22 @@ cudaError_t launch_embed_fwd(const vce_problem& p, const int64_t* ids, const voi
   return cudaGetLastError();
 }
 
+namespace {
+cudaError_t plan_multi(const vce_problem* ps, const int64_t* const* ids, void* const* ws, int n, int max_nb,
+                       cudaStream_t st);
+}  // namespace
+
+// Beside the lookup, a sort without clusters (T <= 8192) takes at most 64 SMs:
+// its 1024-thread CTAs hold nearly all of an SM's registers, so each SM it
+// takes runs no lookup rows until it exits (measured on GB300, 8192 x 2048
+// Qwen3-like ids: the lookup with the plan 18.4 -> 16.4 us with 64 buckets).
+// Alone, the plan keeps one bucket per SM, its fastest grid.
+constexpr int kBesideLookupBuckets = 64;
+
 cudaError_t launch_embed_fwd_plan(const vce_problem& p, const int64_t* ids, const void* W, void* E, int32_t* owner,
                                   int32_t* local, void* ws, cudaStream_t st) {
   if (p.T == 0) return cudaSuccess;
-  if (cudaError_t e = launch_embed_bwd_plan(p, ids, ws, st)) return e;
+  if (cudaError_t e = plan_multi(&p, &ids, &ws, 1, kBesideLookupBuckets, st)) return e;
   const int esize = p.dtype == VCE_BF16 ? 2 : 4;
   const int row_vecs = static_cast<int>(p.H * esize / 16);
   const int64_t blocks = ceil_div(p.T, kGatherWarps);
@@ -1868,14 +1880,15 @@ int cluster_sort_buckets(cudaError_t* err) {
 // (16 rounds per warp): measured on GB300, about 3 us less for 16384 tokens
 // and about 1 us more for 8192. VCE_EMBED_SORT_CLUSTER=1 in the environment
 // takes it whenever the counting sort runs, =0 never.
-SortPlan plan_sort(const vce_problem& p, int num_sms, cudaError_t* err) {
+SortPlan plan_sort(const vce_problem& p, int num_sms, int max_nb, cudaError_t* err) {
   const char* env = std::getenv("VCE_EMBED_SORT_CLUSTER");
   const bool set = env && (env[0] == '0' || env[0] == '1') && env[1] == 0;
   const bool allow = set ? env[0] == '1' : p.T > 8192;
   const int nbc = cluster_sort_buckets(err);
   if (allow && nbc >= 2 * kSortCluster && sort_path(p, nbc, kSortCluster) == SortPath::kCount)
     return {SortPath::kCount, nbc, kSortCluster};
-  const int nb = num_sms > 0 ? num_sms : 1;
+  int nb = num_sms > 0 ? num_sms : 1;
+  if (max_nb > 0 && nb > max_nb) nb = max_nb;
   return {sort_path(p, nb, 1), nb, 1};
 }
 
@@ -2034,10 +2047,15 @@ cudaError_t launch_reduce(const vce_problem& p, const EmbSlots& sl, const void* 
 
 }  // namespace
 
+namespace {
+
 // The plans of n problems: one header-zeroing launch (for the bucketed
-// sorts), then one sort per problem.
-cudaError_t launch_embed_bwd_plan_multi(const vce_problem* ps, const int64_t* const* ids, void* const* ws, int n,
-                                        cudaStream_t st) {
+// sorts), then one sort per problem, its one-CTA-per-bucket grid capped at
+// max_nb buckets when it runs without clusters (0: one bucket per SM). Any
+// bucket count gives the same plan up to the order of the runs in the list,
+// and the same results.
+cudaError_t plan_multi(const vce_problem* ps, const int64_t* const* ids, void* const* ws, int n, int max_nb,
+                       cudaStream_t st) {
   if (n < 1 || n > kMaxSlots) return cudaErrorInvalidValue;
   if (ps[0].T == 0) return cudaSuccess;
   const DevInfo di = current_device_info();
@@ -2046,7 +2064,7 @@ cudaError_t launch_embed_bwd_plan_multi(const vce_problem* ps, const int64_t* co
   bool any_bucketed = false;
   for (int k = 0; k < n; ++k) {
     cudaError_t err = cudaSuccess;
-    plan[k] = plan_sort(ps[k], di.num_sms, &err);
+    plan[k] = plan_sort(ps[k], di.num_sms, max_nb, &err);
     if (err != cudaSuccess) return err;
     if (plan[k].path == SortPath::kCount || plan[k].path == SortPath::kBucket) {
       zero[k] = emb_slot(ps[k], ws[k], nullptr).hdr;
@@ -2061,6 +2079,13 @@ cudaError_t launch_embed_bwd_plan_multi(const vce_problem* ps, const int64_t* co
   for (int k = 0; k < n; ++k)
     if (cudaError_t e = launch_sort(ps[k], ids[k], ws[k], plan[k], front_slices(ps[k], n).nhf, st)) return e;
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_embed_bwd_plan_multi(const vce_problem* ps, const int64_t* const* ids, void* const* ws, int n,
+                                        cudaStream_t st) {
+  return plan_multi(ps, ids, ws, n, 0, st);
 }
 
 cudaError_t launch_embed_bwd_apply_multi(const vce_problem* ps, float* const* dW, void* const* ws, int n,
