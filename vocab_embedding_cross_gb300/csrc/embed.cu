@@ -1043,11 +1043,34 @@ __device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.a
 // keys in token order, and segments follow token order too. The counting
 // warps take the segments in order (kCntWarps / CL warps each), which keeps
 // the sort stable exactly as with one contiguous key array.
+//
+// One launch sorts up to three problems of the same T side by side (the
+// n-gram backward's tables): blocks [k * nb, (k + 1) * nb) sort problem k into
+// nb buckets, nb a multiple of CL so that a cluster stays within one problem.
+constexpr int kMaxSortJobs = 3;
+struct SortJobs {
+  const int64_t* ids[kMaxSortJobs];
+  int64_t V_real[kMaxSortJobs];
+  int nq[kMaxSortJobs];   // ceil(V_real / nb)
+  int32_t* hdr[kMaxSortJobs];
+  int32_t* tsorted[kMaxSortJobs];
+  RunDesc* runs[kMaxSortJobs];
+  int32_t* counters[kMaxSortJobs];
+  int nb;                 // buckets per problem
+};
+
 template <int ROUNDS, int CL>
 __global__ void __launch_bounds__(kBktThreads, 1)
-    embed_sort_count_kernel(const int64_t* __restrict__ ids, int T, int64_t V_real, int tbits, int nq, int nhm,
-                            uint32_t nb_magic, int32_t* hdr, int32_t* tsorted, RunDesc* runs, int32_t* counters) {
+    embed_sort_count_kernel(const __grid_constant__ SortJobs J, int T, int tbits, int nhm, uint32_t nb_magic) {
   static_assert(CL >= 1 && CL <= 8 && kCntWarps % CL == 0, "counting warps split evenly over the segments");
+  const int job = static_cast<int>(blockIdx.x) / J.nb;   // the same for every CTA of a cluster
+  const int64_t* __restrict__ ids = job == 2 ? J.ids[2] : (job == 1 ? J.ids[1] : J.ids[0]);
+  const int64_t V_real = job == 2 ? J.V_real[2] : (job == 1 ? J.V_real[1] : J.V_real[0]);
+  const int nq = job == 2 ? J.nq[2] : (job == 1 ? J.nq[1] : J.nq[0]);
+  int32_t* hdr = job == 2 ? J.hdr[2] : (job == 1 ? J.hdr[1] : J.hdr[0]);
+  int32_t* tsorted = job == 2 ? J.tsorted[2] : (job == 1 ? J.tsorted[1] : J.tsorted[0]);
+  RunDesc* runs = job == 2 ? J.runs[2] : (job == 1 ? J.runs[1] : J.runs[0]);
+  int32_t* counters = job == 2 ? J.counters[2] : (job == 1 ? J.counters[1] : J.counters[0]);
   extern __shared__ __align__(16) uint32_t csm[];
   const int Tc = count_seg_cap(T, CL);
   uint32_t* ka = csm;                                  // [CL][Tc] this bucket's keys, token order
@@ -1062,7 +1085,7 @@ __global__ void __launch_bounds__(kBktThreads, 1)
   __shared__ int wdc[CL > 1 ? kBktWarps * CL : 1];     // per warp and destination rank: keys sent
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
-  const uint32_t NB = gridDim.x, b = blockIdx.x;
+  const uint32_t NB = static_cast<uint32_t>(J.nb), b = blockIdx.x - static_cast<uint32_t>(job * J.nb);
 
   grid_dep_launch();   // the reduce may be scheduled from here on; it waits for this grid to end
 
@@ -1831,9 +1854,9 @@ struct SortPlan {
 constexpr int kSortCluster = 8;
 constexpr int kClusterRounds = (kSmemSortMax / kSortCluster + 1023) / 1024;   // rounds per warp at most
 
-void set_count_smem_limit(void (*k)(const int64_t*, int, int64_t, int, int, int, uint32_t, int32_t*, int32_t*,
-                                    RunDesc*, int32_t*),
-                          cudaError_t* err) {
+using CountKern = void (*)(const SortJobs, int, int, int, uint32_t);
+
+void set_count_smem_limit(CountKern k, cudaError_t* err) {
   const cudaError_t e =
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kCountSmemBudget));
   if (e != cudaSuccess && *err == cudaSuccess) *err = e;
@@ -1914,6 +1937,64 @@ FrontSlices front_slices(const vce_problem& p, int n_problems) {
   return narrow ? FrontSlices{L.nhm, true} : FrontSlices{L.nh, false};
 }
 
+// One launch of the counting sort over n problems of the same T (ps, their
+// ids and workspaces), nb buckets each, in clusters of cl CTAs (nb a multiple
+// of cl), with counters for nhf column slices per multi-run id.
+cudaError_t launch_count_sort(const vce_problem* ps, const int64_t* const* ids, void* const* ws, int n, int nb, int cl,
+                              int nhf, cudaStream_t st) {
+  if (n < 1 || n > kMaxSortJobs || nb < 2 || nb % cl != 0) return cudaErrorInvalidValue;
+  const int64_t T = ps[0].T;
+  SortJobs J{};
+  J.nb = nb;
+  size_t smem = 0;
+  for (int k = 0; k < n; ++k) {
+    const BwdLayout L = bwd_layout(ps[k]);
+    char* b = static_cast<char*>(ws[k]);
+    J.ids[k] = ids[k];
+    J.V_real[k] = ps[k].V_real;
+    J.nq[k] = static_cast<int>(ceil_div(ps[k].V_real, nb));
+    J.hdr[k] = reinterpret_cast<int32_t*>(b + L.hdr);
+    J.tsorted[k] = reinterpret_cast<int32_t*>(b + L.tsorted);
+    J.runs[k] = reinterpret_cast<RunDesc*>(b + L.runs);
+    J.counters[k] = reinterpret_cast<int32_t*>(b + L.counters);
+    const size_t sm = count_sort_smem(T, J.nq[k], cl);
+    if (sm > smem) smem = sm;
+  }
+  const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb) + 1u;   // floor((2^32 - 1) / NB) + 1
+  CountKern kern;
+  if (cl == 1) {
+    // Phase A's rounds of 32 tokens per warp: 2, 4, 8 or 16.
+    const int rounds = T <= 2048 ? 2 : T <= 4096 ? 4 : T <= 8192 ? 8 : 16;
+    kern = rounds == 2   ? embed_sort_count_kernel<2, 1>
+           : rounds == 4 ? embed_sort_count_kernel<4, 1>
+           : rounds == 8 ? embed_sort_count_kernel<8, 1>
+                         : embed_sort_count_kernel<16, 1>;
+  } else {
+    // Each rank loads a segment of Tc <= 16384 / kSortCluster tokens: up to 512 / kSortCluster rounds per warp.
+    const int tc = count_seg_cap(static_cast<int>(T), kSortCluster);
+    const int tpw = ((tc + kBktWarps - 1) / kBktWarps + 31) & ~31;
+    if (cl != kSortCluster || tpw > 32 * kClusterRounds) return cudaErrorInvalidValue;
+    kern = tpw <= 32 ? embed_sort_count_kernel<1, kSortCluster>
+           : tpw <= 64 ? embed_sort_count_kernel<2, kSortCluster>
+                       : embed_sort_count_kernel<kClusterRounds, kSortCluster>;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(n * nb));
+  cfg.blockDim = dim3(kBktThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cl;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cl > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, J, static_cast<int>(T), bit_width(T), nhf, nb_magic);
+}
+
 // Sorts one problem's valid (id, t) pairs into its workspace and builds its
 // runs, with counters for nhf column slices per multi-run id. A bucketed sort
 // needs its header zeroed by the kernel before it.
@@ -1935,43 +2016,7 @@ cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, cons
   const int64_t nq = ceil_div(p.V_real, nb);
   const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb > 1 ? nb : 2) + 1u;   // floor((2^32 - 1) / NB) + 1
   if (path == SortPath::kCount) {
-    using CountKern = void (*)(const int64_t*, int, int64_t, int, int, int, uint32_t, int32_t*, int32_t*, RunDesc*,
-                               int32_t*);
-    CountKern kern;
-    if (plan.cl == 1) {
-      // Phase A's rounds of 32 tokens per warp: 2, 4, 8 or 16.
-      const int rounds = p.T <= 2048 ? 2 : p.T <= 4096 ? 4 : p.T <= 8192 ? 8 : 16;
-      kern = rounds == 2   ? embed_sort_count_kernel<2, 1>
-             : rounds == 4 ? embed_sort_count_kernel<4, 1>
-             : rounds == 8 ? embed_sort_count_kernel<8, 1>
-                           : embed_sort_count_kernel<16, 1>;
-    } else {
-      // Each rank loads a segment of Tc <= 16384 / kSortCluster tokens: up to 512 / kSortCluster rounds per warp.
-      const int tc = count_seg_cap(static_cast<int>(p.T), kSortCluster);
-      const int tpw = ((tc + kBktWarps - 1) / kBktWarps + 31) & ~31;
-      if (tpw > 32 * kClusterRounds) return cudaErrorInvalidValue;
-      kern = tpw <= 32 ? embed_sort_count_kernel<1, kSortCluster>
-             : tpw <= 64 ? embed_sort_count_kernel<2, kSortCluster>
-                         : embed_sort_count_kernel<kClusterRounds, kSortCluster>;
-    }
-    const size_t smem = count_sort_smem(p.T, nq, plan.cl);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nb);
-    cfg.blockDim = dim3(kBktThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = plan.cl;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = plan.cl > 1 ? 2 : 1;
-    if (cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ids, static_cast<int>(p.T), p.V_real, tbits,
-                                           static_cast<int>(nq), nhf, nb_magic, hdr, tsorted, runs, counters))
-      return e;
+    if (cudaError_t e = launch_count_sort(&p, &ids, &ws, 1, nb, plan.cl, nhf, st)) return e;
   } else if (path == SortPath::kBucket) {
     static std::atomic<uint64_t> configured{0};
     if (device_pending(configured)) {
@@ -2075,6 +2120,20 @@ cudaError_t plan_multi(const vce_problem* ps, const int64_t* const* ids, void* c
     embed_hdr_zero_kernel<<<1, 64, 0, st>>>(zero[0], zero[1], zero[2]);
     note_launch(VCE_K_EMBED_HDR, st);
     if (cudaError_t e = cudaGetLastError()) return e;
+  }
+  // Problems of the same T whose sorts all take the counting path with the
+  // same cluster size (the n-gram tables) are sorted side by side by one
+  // launch, the buckets shared out among them: each sort CTA loads every id
+  // whatever its bucket count, so fewer buckets per problem cost little, while
+  // one sort after another would each take every SM for the length of a sort.
+  if (n > 1) {
+    bool joint = true;
+    for (int k = 0; k < n; ++k)
+      joint = joint && plan[k].path == SortPath::kCount && plan[k].cl == plan[0].cl && ps[k].T == ps[0].T;
+    const int cl = plan[0].cl;
+    const int nbj = ((plan[0].nb / cl) / n) * cl;
+    for (int k = 0; joint && k < n; ++k) joint = nbj >= 2 && sort_path(ps[k], nbj, cl) == SortPath::kCount;
+    if (joint) return launch_count_sort(ps, ids, ws, n, nbj, cl, front_slices(ps[0], n).nhf, st);
   }
   for (int k = 0; k < n; ++k)
     if (cudaError_t e = launch_sort(ps[k], ids[k], ws[k], plan[k], front_slices(ps[k], n).nhf, st)) return e;

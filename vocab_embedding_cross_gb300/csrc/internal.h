@@ -207,6 +207,9 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, int32_t* status, cudaStream_
 // Hashed n-gram embeddings.
 cudaError_t launch_ngram_hash(const int64_t* ids, int64_t T, int n, int64_t V, int64_t M, int64_t seq_len,
                               int64_t* out, cudaStream_t st);
+// The 2-gram and 3-gram row indices (M2, M3 > 0) in one launch.
+cudaError_t launch_ngram_hash_pair(const int64_t* ids, int64_t T, int64_t V, int64_t M2, int64_t M3, int64_t seq_len,
+                                   int64_t* out2, int64_t* out3, cudaStream_t st);
 cudaError_t launch_ngram_embed_fwd(const vce_problem& p, const int64_t* ids, const void* W, const void* T2,
                                    int64_t M2, const void* T3, int64_t M3, int64_t seq_len, void* E,
                                    cudaStream_t st);

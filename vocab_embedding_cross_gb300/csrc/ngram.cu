@@ -48,6 +48,17 @@ __global__ void __launch_bounds__(256) ngram_hash_kernel(const int64_t* __restri
     out[t] = ngram_index(ids, t, n, V, M, seq_len);
 }
 
+// Both tables' row indices in one launch (the backward's plan needs both).
+__global__ void __launch_bounds__(256) ngram_hash_pair_kernel(const int64_t* __restrict__ ids, int64_t T, int64_t V,
+                                                              int64_t M2, int64_t M3, int64_t seq_len,
+                                                              int64_t* __restrict__ out2, int64_t* __restrict__ out3) {
+  for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < T;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    out2[t] = ngram_index(ids, t, 2, V, M2, seq_len);
+    out3[t] = ngram_index(ids, t, 3, V, M3, seq_len);
+  }
+}
+
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -115,6 +126,17 @@ cudaError_t launch_ngram_hash(const int64_t* ids, int64_t T, int n, int64_t V, i
   int64_t blocks = ceil_div(T, 256);
   if (blocks > di.num_sms * 8) blocks = di.num_sms * 8;
   ngram_hash_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(ids, T, n, V, M, seq_len, out);
+  note_launch(VCE_K_NGRAM_HASH, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ngram_hash_pair(const int64_t* ids, int64_t T, int64_t V, int64_t M2, int64_t M3, int64_t seq_len,
+                                   int64_t* out2, int64_t* out3, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const DevInfo di = current_device_info();
+  int64_t blocks = ceil_div(T, 256);
+  if (blocks > di.num_sms * 8) blocks = di.num_sms * 8;
+  ngram_hash_pair_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(ids, T, V, M2, M3, seq_len, out2, out3);
   note_launch(VCE_K_NGRAM_HASH, st);
   return cudaGetLastError();
 }

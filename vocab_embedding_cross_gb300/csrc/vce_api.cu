@@ -690,10 +690,13 @@ NgramBwd ngram_bwd(const vce_problem& p, const int64_t* ids, float* dW, float* d
 // Row indices of the present tables, then their plans.
 cudaError_t ngram_plan(const vce_problem& p, const int64_t* ids, int64_t M2, int64_t M3, int64_t seq_len,
                        const NgramBwd& g, cudaStream_t st) {
-  if (M2 > 0)
+  if (M2 > 0 && M3 > 0) {
+    if (cudaError_t e = launch_ngram_hash_pair(ids, p.T, p.V_real, M2, M3, seq_len, g.idx2, g.idx3, st)) return e;
+  } else if (M2 > 0) {
     if (cudaError_t e = launch_ngram_hash(ids, p.T, 2, p.V_real, M2, seq_len, g.idx2, st)) return e;
-  if (M3 > 0)
+  } else if (M3 > 0) {
     if (cudaError_t e = launch_ngram_hash(ids, p.T, 3, p.V_real, M3, seq_len, g.idx3, st)) return e;
+  }
   return launch_embed_bwd_plan_multi(g.ps, g.pid, g.pws, g.n, st);
 }
 
