@@ -2013,7 +2013,6 @@ cudaError_t launch_sort(const vce_problem& p, const int64_t* ids, void* ws, cons
   int32_t* counters = reinterpret_cast<int32_t*>(b + L.counters);
   const int tbits = bit_width(p.T);
   const int qbits = bit_width(ceil_div(p.V_real, nb));
-  const int64_t nq = ceil_div(p.V_real, nb);
   const uint32_t nb_magic = 0xFFFFFFFFu / static_cast<uint32_t>(nb > 1 ? nb : 2) + 1u;   // floor((2^32 - 1) / NB) + 1
   if (path == SortPath::kCount) {
     if (cudaError_t e = launch_count_sort(&p, &ids, &ws, 1, nb, plan.cl, nhf, st)) return e;
