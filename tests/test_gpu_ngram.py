@@ -88,6 +88,8 @@ def _replays(wl, ids, dE, M2, M3, seq_len, inits):
     ("bf16", 700, 8, 1000, 1024, 613, 1 << 21, 0),     # the 3-gram table sorted by radix buckets, the others counted
     ("bf16", 20000, 8, 1000, 1024, 613, 1024, 0),      # T above the shared-memory sorts: every table in the workspace
     ("bf16", 12000, 16, 5000, 5056, 613, 1 << 18, 3000),  # 8192 < T <= 16384: three clustered counting sorts
+    ("bf16", 12000, 16, 5000, 5056, 613, 1024, 3000),     # the same, small enough to run side by side in one launch
+    ("f32", 3000, 12, 700, 704, 97, 131, 0),              # fp32, the three counting sorts side by side
 ])
 def test_ngram_fwd_bwd_exact(dtype, T, H, V_real, Vp, M2, M3, seq_len):
     wl, d, T2, T3 = _case(dtype, T, H, V_real, Vp, M2, M3, seed=71 + T)
