@@ -2094,7 +2094,8 @@ cudaError_t launch_reduce(const vce_problem& p, const EmbSlots& sl, const void* 
 namespace {
 
 // The plans of n problems: one header-zeroing launch (for the bucketed
-// sorts), then one sort per problem, its one-CTA-per-bucket grid capped at
+// sorts), then the sorts (side by side in one launch where they allow it,
+// below; else one per problem), a one-CTA-per-bucket grid capped at
 // max_nb buckets when it runs without clusters (0: one bucket per SM). Any
 // bucket count gives the same plan up to the order of the runs in the list,
 // and the same results.
