@@ -9,12 +9,14 @@
 //   2. scan the words' popcounts: the distinct targets in ascending order and
 //      the rank of each (its word's prefix plus the bits below it);
 //   3. pos[t] = rank of targets[t];
-//   4. negatives in draw order, 1024 draws per round: a draw is kept when it is
-//      in [0, V_real), its bit is clear (not a target, not an earlier
-//      negative) and no earlier draw of the same round has the same value (a
-//      shared-memory hash table keeps the smallest index per value); the kept
-//      draws are ranked by a block scan and their bits set before the next
-//      round. Rounds stop once the list holds P entries.
+//   4. negatives in draw order, 4096 draws per round (four consecutive draws
+//      per thread): a draw is kept when it is in [0, V_real), its bit is clear
+//      (not a target, not an earlier negative) and no earlier draw of the same
+//      round has the same value (a shared-memory hash table keeps the smallest
+//      index per value); the kept draws are ranked by a block scan and their
+//      bits set before the next round. Rounds stop once the list holds P
+//      entries. The kept draws are the first occurrences of their values, so
+//      the list does not depend on the round size.
 // Every step is a fixed function of the inputs, so the list is deterministic.
 //
 // dW scatter: candidates are distinct by construction, so each candidate row
@@ -31,8 +33,11 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kHashSlots = 2 * kThreads;
-constexpr size_t kCandSmemBudget = 200 * 1024;   // bitmap + word prefixes held in shared memory up to this
+constexpr int kDrawsPerThread = 4;
+constexpr int kRoundDraws = kThreads * kDrawsPerThread;
+constexpr int kHashSlots = 2 * kRoundDraws;
+constexpr size_t kHashBytes = 2 * sizeof(int32_t) * kHashSlots;   // keys and smallest indices, dynamic shared memory
+constexpr size_t kCandSmemBudget = 200 * 1024;   // hash table + bitmap + word prefixes held in shared memory up to this
 
 // Exclusive block scan of one int per thread; *total gets the sum.
 __device__ __forceinline__ int block_excl_scan(int v, int* sh_warp, int* total) {
@@ -64,8 +69,9 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sh_warp, int* total) 
 }
 
 __device__ __forceinline__ uint32_t hash_slot(int32_t d) {
-  return (static_cast<uint32_t>(d) * 2654435761u) >> (32 - 11);   // 11 bits: kHashSlots = 2048
+  return (static_cast<uint32_t>(d) * 2654435761u) >> (32 - 13);   // 13 bits: kHashSlots = 8192
 }
+static_assert(kHashSlots == 8192, "hash_slot takes 13 bits");
 
 __global__ void __launch_bounds__(kThreads, 1)
     sampled_cand_kernel(const int64_t* __restrict__ targets, int32_t T, int32_t V_real, int64_t ignore_index,
@@ -74,22 +80,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         int32_t* __restrict__ n_unique, int32_t* status) {
   extern __shared__ __align__(16) uint32_t dsm[];
   __shared__ int sh_warp[33];
-  __shared__ int32_t hkey[kHashSlots];
-  __shared__ int32_t hidx[kHashSlots];
+  int32_t* hkey = reinterpret_cast<int32_t*>(dsm);
+  int32_t* hidx = hkey + kHashSlots;
   const int tid = threadIdx.x;
   const int NW = (V_real + 31) >> 5;
-  uint32_t* bits = use_smem ? dsm : g_bits;
-  int32_t* wpre = use_smem ? reinterpret_cast<int32_t*>(dsm + NW) : g_wpre;
+  uint32_t* bits = use_smem ? dsm + 2 * kHashSlots : g_bits;
+  int32_t* wpre = use_smem ? reinterpret_cast<int32_t*>(dsm + 2 * kHashSlots + NW) : g_wpre;
 
   for (int w = tid; w < NW; w += kThreads) bits[w] = 0u;
   __syncthreads();
   bool bad = false;
-  for (int t = tid; t < T; t += kThreads) {
-    const int64_t y = targets[t];
-    if (y >= 0 && y < V_real)
-      atomicOr(&bits[y >> 5], 1u << (y & 31));
-    else if (y != ignore_index)
-      bad = true;
+  // Targets kBatch per thread at a time, every load issued before the first
+  // use, so a thread waits for one round trip per batch, not per target.
+  constexpr int kBatch = 8;
+  for (int t0 = 0; t0 < T; t0 += kThreads * kBatch) {
+    int64_t yv[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int t = t0 + j * kThreads + tid;
+      yv[j] = t < T ? targets[t] : ignore_index;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t y = yv[j];
+      if (y >= 0 && y < V_real) {
+        // a hot target's bit is set once; later copies find it set and skip
+        // the atomic, which would queue behind the others on one word
+        const uint32_t m = 1u << (y & 31);
+        if (!(bits[y >> 5] & m)) atomicOr(&bits[y >> 5], m);
+      } else if (y != ignore_index) {
+        bad = true;
+      }
+    }
   }
   if (bad && status) atomicCAS(status, 0, static_cast<int>(VCE_ERR_BAD_INDEX));
   __syncthreads();
@@ -126,46 +148,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       cand[k++] = static_cast<int64_t>(w) * 32 + bit;
     }
   }
-  // Each target's position.
-  for (int t = tid; t < T; t += kThreads) {
-    const int64_t y = targets[t];
-    int64_t q = ignore_index;
-    if (y >= 0 && y < V_real) {
-      const int w = static_cast<int>(y >> 5);
-      q = wpre[w] + __popc(bits[w] & ((1u << (y & 31)) - 1u));
+  // Each target's position, the targets loaded in batches as above.
+  for (int t0 = 0; t0 < T; t0 += kThreads * kBatch) {
+    int64_t yv[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int t = t0 + j * kThreads + tid;
+      yv[j] = t < T ? targets[t] : ignore_index;
     }
-    pos[t] = q;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int t = t0 + j * kThreads + tid;
+      const int64_t y = yv[j];
+      int64_t q = ignore_index;
+      if (y >= 0 && y < V_real) {
+        const int w = static_cast<int>(y >> 5);
+        q = wpre[w] + __popc(bits[w] & ((1u << (y & 31)) - 1u));
+      }
+      if (t < T) pos[t] = q;
+    }
   }
 
-  // Negatives in draw order, a round of kThreads draws at a time.
+  // Negatives in draw order, a round of kRoundDraws draws at a time; thread
+  // tid takes the round's draws [tid * R, tid * R + R), so the block scan of
+  // the threads' kept counts ranks the kept draws in draw order.
+  constexpr int R = kDrawsPerThread;
   int have = nu;
-  for (int64_t r0 = 0; r0 < n_draws && have < P; r0 += kThreads) {
+  for (int64_t r0 = 0; r0 < n_draws && have < P; r0 += kRoundDraws) {
     for (int s = tid; s < kHashSlots; s += kThreads) {
       hkey[s] = -1;
       hidx[s] = INT_MAX;
     }
     __syncthreads();
-    const int64_t i = r0 + tid;
-    const int64_t d64 = i < n_draws ? draws[i] : -1;
-    const int32_t d = static_cast<int32_t>(d64);
-    bool ok = d64 >= 0 && d64 < V_real && !((bits[d >> 5] >> (d & 31)) & 1u);
-    uint32_t slot = 0;
-    if (ok) {
-      slot = hash_slot(d);
-      for (int probe = 0; probe < kHashSlots; ++probe) {   // at most kThreads keys in 2*kThreads slots
-        const int32_t k = atomicCAS(&hkey[slot], -1, d);
-        if (k == -1 || k == d) break;
-        slot = (slot + 1) & (kHashSlots - 1);
+    int32_t d[R];
+    bool ok[R];
+    uint32_t slot[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int64_t i = r0 + static_cast<int64_t>(tid) * R + j;
+      const int64_t d64 = i < n_draws ? draws[i] : -1;
+      d[j] = static_cast<int32_t>(d64);
+      ok[j] = d64 >= 0 && d64 < V_real;
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      ok[j] = ok[j] && !((bits[d[j] >> 5] >> (d[j] & 31)) & 1u);
+      slot[j] = 0;
+      if (ok[j]) {
+        uint32_t sl = hash_slot(d[j]);
+        for (int probe = 0; probe < kHashSlots; ++probe) {   // at most kRoundDraws keys in 2*kRoundDraws slots
+          const int32_t k = atomicCAS(&hkey[sl], -1, d[j]);
+          if (k == -1 || k == d[j]) break;
+          sl = (sl + 1) & (kHashSlots - 1);
+        }
+        slot[j] = sl;
+        atomicMin(&hidx[sl], tid * R + j);
       }
-      atomicMin(&hidx[slot], tid);
     }
     __syncthreads();
-    ok = ok && hidx[slot] == tid;   // the first draw of this value in the round
+    int mine = 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      ok[j] = ok[j] && hidx[slot[j]] == tid * R + j;   // the first draw of this value in the round
+      mine += ok[j] ? 1 : 0;
+    }
     int kept;
-    const int q = block_excl_scan(ok ? 1 : 0, sh_warp, &kept);
-    if (ok) {
-      if (have + q < P) cand[have + q] = d;
-      atomicOr(&bits[d >> 5], 1u << (d & 31));
+    int q = block_excl_scan(mine, sh_warp, &kept);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      if (ok[j]) {
+        if (have + q < P) cand[have + q] = d[j];
+        atomicOr(&bits[d[j] >> 5], 1u << (d[j] & 31));
+        ++q;
+      }
     }
     have += kept;
     __syncthreads();
@@ -224,10 +279,10 @@ cudaError_t launch_sampled_candidates(const vce_problem& p, const int64_t* targe
                                       int64_t n_draws, int64_t P, int64_t* cand, int64_t* pos, int32_t* n_unique,
                                       void* ws, int32_t* status, cudaStream_t st) {
   const size_t table = cand_table_bytes(p.V_real);
-  const bool use_smem = table <= kCandSmemBudget;
-  const size_t smem = use_smem ? table : 0;
+  const bool use_smem = kHashBytes + table <= kCandSmemBudget;
+  const size_t smem = kHashBytes + (use_smem ? table : 0);
   static std::atomic<uint64_t> configured{0};
-  if (use_smem && device_pending(configured)) {
+  if (device_pending(configured)) {
     cudaError_t e = cudaFuncSetAttribute(sampled_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kCandSmemBudget));
     if (e != cudaSuccess) return e;
